@@ -1,0 +1,233 @@
+"""Python binding of ``libflash_mca.so`` -- the FLASH mixed-chunk attention
+forward core on GB300 (sm_103a).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+kernels behind the C ABI declared in ``include/flash_mca.h``; the functions
+here take torch tensors (device memory, streams) and pass raw pointers and
+sizes to the entry points of the same names.  There is no CPU fallback: if the
+shared library is missing or fails to load, importing this package raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _buildlib as _build
+
+__all__ = [
+    "FMCA_OK", "FMCA_ERR_INVALID_ARG", "FMCA_ERR_SHAPE", "FMCA_ERR_UNSUPPORTED", "FMCA_ERR_ALIGN",
+    "FMCA_ERR_WORKSPACE", "FMCA_ERR_CUDA", "FMCA_ERR_TIMEOUT", "FMCA_F32", "FMCA_BF16",
+    "FMCA_PATH_AUTO", "FMCA_PATH_SIMT", "FMCA_PATH_TCGEN05", "FmcaError", "lib", "library_path",
+    "flash_mca_workspace_bytes", "flash_mca_forward", "flash_mca_forward_path",
+    "flash_mca_forward_timed",
+    "flash_mca_auto_path", "flash_mca_launch_count", "flash_mca_host_arena_bytes",
+    "flash_mca_forward_host", "flash_mca_device_status", "flash_mca_selftest_timeout",
+    "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
+]
+
+FMCA_OK, FMCA_ERR_INVALID_ARG, FMCA_ERR_SHAPE, FMCA_ERR_UNSUPPORTED = 0, 1, 2, 3
+FMCA_ERR_ALIGN, FMCA_ERR_WORKSPACE, FMCA_ERR_CUDA, FMCA_ERR_TIMEOUT = 4, 5, 6, 7
+FMCA_F32, FMCA_BF16 = 0, 1
+FMCA_PATH_AUTO, FMCA_PATH_SIMT, FMCA_PATH_TCGEN05 = 0, 1, 2
+
+library_path = _build.LIB
+
+# Build (or rebuild, when a source is newer) the in-tree library; without it
+# the package does not import -- there is no CPU fallback.
+try:
+    _build.build()
+except Exception as exc:  # nvcc missing or the build failed
+    if not os.path.exists(library_path):
+        raise ImportError(f"{library_path} is missing and could not be built: {exc}") from exc
+    raise ImportError(f"{library_path} is out of date and could not be rebuilt: {exc}") from exc
+lib = ctypes.CDLL(library_path)
+
+_vp, _sz, _i32, _cp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c_char_p
+_int = ctypes.c_int
+_fwd_args = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _i32, _vp, _sz]
+
+# (name, restype, argtypes) for every symbol the header declares
+_SIGNATURES = [
+    ("flash_mca_workspace_bytes", _sz, [_int] * 6 + [_i32]),
+    ("flash_mca_forward", _i32, _fwd_args + [_vp]),
+    ("flash_mca_forward_path", _i32, _fwd_args + [_i32, _vp]),
+    ("flash_mca_forward_timed", _i32, _fwd_args + [_i32, ctypes.POINTER(_vp), _int, _vp]),
+    ("flash_mca_auto_path", _int, [_int] * 6 + [_i32]),
+    ("flash_mca_launch_count", _int, [_int] * 6 + [_i32, _i32]),
+    ("flash_mca_host_arena_bytes", _sz, [_int] * 6 + [_i32]),
+    ("flash_mca_forward_host", _i32, _fwd_args + [_vp]),
+    ("flash_mca_device_status", _i32, [_vp, ctypes.POINTER(_i32)]),
+    ("flash_mca_selftest_timeout", _i32, [_int, _vp]),
+    ("flash_mca_status_string", _cp, [_i32]),
+    ("flash_mca_version", _cp, []),
+]
+EXPORTED_SYMBOLS = [name for name, _, _ in _SIGNATURES]
+for _name, _res, _args in _SIGNATURES:
+    _f = getattr(lib, _name)
+    _f.restype = _res
+    _f.argtypes = _args
+
+
+class FmcaError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = int(status)
+        msg = lib.flash_mca_status_string(self.status).decode()
+        super().__init__(f"{what}: {msg}" if what else msg)
+
+
+def _check(status: int, what: str) -> None:
+    if status != FMCA_OK:
+        raise FmcaError(status, what)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return FMCA_BF16
+    if t.dtype == torch.float32:
+        return FMCA_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: use torch.bfloat16 or torch.float32")
+
+
+def _stream_ptr(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def flash_mca_status_string(status: int) -> str:
+    return lib.flash_mca_status_string(int(status)).decode()
+
+
+def flash_mca_version() -> str:
+    return lib.flash_mca_version().decode()
+
+
+def flash_mca_workspace_bytes(B: int, n: int, s: int, e: int, C: int, causal: bool,
+                              dtype: int) -> int:
+    return int(lib.flash_mca_workspace_bytes(B, n, s, e, C, int(bool(causal)), dtype))
+
+
+def flash_mca_host_arena_bytes(B: int, n: int, s: int, e: int, C: int, causal: bool,
+                               dtype: int) -> int:
+    return int(lib.flash_mca_host_arena_bytes(B, n, s, e, C, int(bool(causal)), dtype))
+
+
+def flash_mca_auto_path(B: int, n: int, s: int, e: int, C: int, causal: bool, dtype: int) -> int:
+    return int(lib.flash_mca_auto_path(B, n, s, e, C, int(bool(causal)), dtype))
+
+
+def flash_mca_launch_count(B: int, n: int, s: int, e: int, C: int, causal: bool, dtype: int,
+                           path: int = FMCA_PATH_AUTO) -> int:
+    return int(lib.flash_mca_launch_count(B, n, s, e, C, int(bool(causal)), dtype, path))
+
+
+def _shapes(Z: torch.Tensor, V: torch.Tensor, U: torch.Tensor):
+    if Z.dim() != 3 or V.dim() != 3 or U.dim() != 3:
+        raise ValueError("Z, V, U must be 3-D: [B, n, s], [B, n, e], [B, n, e]")
+    B, n, s = Z.shape
+    e = V.shape[2]
+    if tuple(V.shape) != (B, n, e) or tuple(U.shape) != (B, n, e):
+        raise ValueError("V and U must be [B, n, e] with Z [B, n, s]")
+    return B, n, s, e
+
+
+def flash_mca_forward_path(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
+                           path: int = FMCA_PATH_AUTO, stream=None) -> None:
+    """Queue the forward pass on ``stream`` (default: torch's current stream)
+    with an explicit kernel path; all tensors are CUDA tensors the caller
+    owns."""
+    B, n, s, e = _shapes(Z, V, U)
+    for name, t in (("Z", Z), ("V", V), ("U", U), ("O", O), ("gamma", gamma), ("beta", beta),
+                    ("workspace", workspace)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if gamma.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("gamma and beta must be float32 [4, s]")
+    if tuple(gamma.shape) != (4, s) or tuple(beta.shape) != (4, s):
+        raise ValueError("gamma and beta must be [4, s]")
+    dt = _dtype_code(Z)
+    if V.dtype != Z.dtype or U.dtype != Z.dtype or O.dtype != Z.dtype:
+        raise TypeError("Z, V, U and O must share one dtype")
+    if tuple(O.shape) != (B, n, e):
+        raise ValueError("O must be [B, n, e]")
+    ws_bytes = workspace.numel() * workspace.element_size()
+    st = lib.flash_mca_forward_path(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
+                                    beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C),
+                                    int(bool(causal)), dt, workspace.data_ptr(), ws_bytes, path,
+                                    _stream_ptr(stream))
+    _check(st, "flash_mca_forward_path")
+
+
+def flash_mca_forward_timed(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
+                            events, path: int = FMCA_PATH_AUTO, stream=None) -> None:
+    """``flash_mca_forward_path`` recording ``events`` (torch.cuda.Event
+    objects, launch count + 1 of them) before the first kernel and after each
+    kernel on ``stream``."""
+    B, n, s, e = _shapes(Z, V, U)
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    for ev in events:
+        ev.record(stream)  # materialises the CUDA event handle
+    handles = (_vp * len(events))(*[ev.cuda_event for ev in events])
+    dt = _dtype_code(Z)
+    st = lib.flash_mca_forward_timed(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
+                                     beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C),
+                                     int(bool(causal)), dt, workspace.data_ptr(),
+                                     workspace.numel() * workspace.element_size(), path, handles,
+                                     len(events), _stream_ptr(stream))
+    _check(st, "flash_mca_forward_timed")
+
+
+def flash_mca_forward(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
+                      stream=None) -> None:
+    """The C entry point of the same name (kernel path chosen automatically)."""
+    flash_mca_forward_path(Z, V, U, gamma, beta, O, C, causal, workspace, FMCA_PATH_AUTO, stream)
+
+
+def flash_mca_forward_host(Z, V, U, gamma, beta, O, C: int, causal: bool, arena,
+                           stream=None) -> None:
+    """End-to-end call on HOST tensors (ideally pinned): copies in, computes,
+    copies O back and waits.  ``arena`` is a CUDA byte buffer of at least
+    ``flash_mca_host_arena_bytes`` bytes."""
+    B, n, s, e = _shapes(Z, V, U)
+    for name, t in (("Z", Z), ("V", V), ("U", U), ("O", O), ("gamma", gamma), ("beta", beta)):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous host tensor")
+    if not arena.is_cuda:
+        raise ValueError("arena must be a CUDA tensor")
+    dt = _dtype_code(Z)
+    st = lib.flash_mca_forward_host(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
+                                    beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C),
+                                    int(bool(causal)), dt, arena.data_ptr(),
+                                    arena.numel() * arena.element_size(), _stream_ptr(stream))
+    _check(st, "flash_mca_forward_host")
+
+
+def flash_mca_device_status(stream=None) -> tuple[int, int]:
+    """(status, where) recorded by the kernels since the last read; clears it."""
+    where = _i32(0)
+    st = lib.flash_mca_device_status(_stream_ptr(stream), ctypes.byref(where))
+    return int(st), int(where.value)
+
+
+def flash_mca_selftest_timeout(limit_us: int, stream=None) -> None:
+    _check(lib.flash_mca_selftest_timeout(int(limit_us), _stream_ptr(stream)),
+           "flash_mca_selftest_timeout")
+
+
+def forward(Z, V, U, gamma, beta, C: int, causal: bool, workspace=None, out=None,
+            path: int = FMCA_PATH_AUTO, stream=None) -> torch.Tensor:
+    """Convenience wrapper: allocates O (and the workspace, if not given) with
+    torch and calls ``flash_mca_forward_path``."""
+    B, n, s, e = _shapes(Z, V, U)
+    if out is None:
+        out = torch.empty((B, n, e), dtype=Z.dtype, device=Z.device)
+    if workspace is None:
+        nb = flash_mca_workspace_bytes(B, n, s, e, C, causal, _dtype_code(Z))
+        if nb == 0:
+            raise FmcaError(FMCA_ERR_SHAPE, "flash_mca_workspace_bytes")
+        workspace = torch.empty(nb, dtype=torch.uint8, device=Z.device)
+    flash_mca_forward_path(Z, V, U, gamma, beta, out, C, causal, workspace, path, stream)
+    return out

@@ -1,0 +1,214 @@
+// api.cpp -- the C ABI declared in include/flash_mca.h: argument checks,
+// workspace sizing, dispatch between the tensor-core and SIMT kernels, and
+// the host-buffer end-to-end entry point.  No allocation happens here.
+#include "flash_mca.h"
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "launch.h"
+
+using namespace fmca;
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+fmca_status check_sizes(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype) {
+  (void)causal;
+  if (B <= 0 || n <= 0 || s <= 0 || e <= 0 || C <= 0) return FMCA_ERR_INVALID_ARG;
+  if (dtype != FMCA_F32 && dtype != FMCA_BF16) return FMCA_ERR_INVALID_ARG;
+  if (C > n || n % C != 0) return FMCA_ERR_SHAPE;
+  if (s > 256) return FMCA_ERR_UNSUPPORTED;
+  const int64_t big = (int64_t)B * n * (s > e ? s : e);
+  if (big >= ((int64_t)1 << 31)) return FMCA_ERR_UNSUPPORTED;
+  // the state tensor [B][G][s][e] must be indexable as well
+  if ((int64_t)B * (n / C) * s * (int64_t)e >= ((int64_t)1 << 31)) return FMCA_ERR_UNSUPPORTED;
+  return FMCA_OK;
+}
+
+bool want_tc(int B, int n, int s, int e, int C, fmca_dtype dtype) {
+  return dtype == FMCA_BF16 && tc_supported(B, n, s, e, C);
+}
+
+size_t elem_size(fmca_dtype dtype) { return dtype == FMCA_BF16 ? 2 : 4; }
+
+}  // namespace
+
+extern "C" {
+
+size_t flash_mca_workspace_bytes(int B, int n, int s, int e, int C, int causal,
+                                 fmca_dtype dtype) {
+  if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
+  return workspace_bytes(B, n, s, e, C, causal);
+}
+
+int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype) {
+  if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return -1;
+  return want_tc(B, n, s, e, C, dtype) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
+}
+
+int flash_mca_launch_count(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                           fmca_path path) {
+  if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
+  if (path == FMCA_PATH_AUTO)
+    path = want_tc(B, n, s, e, C, dtype) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
+  if (path == FMCA_PATH_TCGEN05)
+    return want_tc(B, n, s, e, C, dtype) ? tc_launch_count() : 0;
+  if (path == FMCA_PATH_SIMT) return kSimtLaunches;
+  return 0;
+}
+
+fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
+                                    const float *gamma, const float *beta, void *O, int B,
+                                    int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                                    void *workspace, size_t workspace_bytes_, fmca_path path,
+                                    void *const *events, int n_events, fmca_stream_t stream) {
+  fmca_status st = check_sizes(B, n, s, e, C, causal, dtype);
+  if (st != FMCA_OK) return st;
+  if (!Z || !V || !U || !gamma || !beta || !O) return FMCA_ERR_INVALID_ARG;
+  if (path != FMCA_PATH_AUTO && path != FMCA_PATH_SIMT && path != FMCA_PATH_TCGEN05)
+    return FMCA_ERR_INVALID_ARG;
+  if (!aligned16(Z) || !aligned16(V) || !aligned16(U) || !aligned16(O) || !aligned16(gamma) ||
+      !aligned16(beta))
+    return FMCA_ERR_ALIGN;
+  if (!workspace) return FMCA_ERR_WORKSPACE;
+  if (!aligned256(workspace)) return FMCA_ERR_ALIGN;
+  if (workspace_bytes_ < workspace_bytes(B, n, s, e, C, causal)) return FMCA_ERR_WORKSPACE;
+  // O must not overlap the inputs or the workspace
+  {
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(O);
+    const uintptr_t o1 = o0 + (size_t)B * n * e * elem_size(dtype);
+    auto overlaps = [&](const void *p, size_t bytes) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + bytes;
+      return a0 < o1 && o0 < a1;
+    };
+    const size_t es = elem_size(dtype);
+    if (overlaps(Z, (size_t)B * n * s * es) || overlaps(V, (size_t)B * n * e * es) ||
+        overlaps(U, (size_t)B * n * e * es) || overlaps(workspace, workspace_bytes_))
+      return FMCA_ERR_INVALID_ARG;
+  }
+  const bool tc_ok = want_tc(B, n, s, e, C, dtype);
+  if (path == FMCA_PATH_TCGEN05 && !tc_ok) return FMCA_ERR_UNSUPPORTED;
+  const bool use_tc = (path == FMCA_PATH_TCGEN05) || (path == FMCA_PATH_AUTO && tc_ok);
+  const int nlaunch = use_tc ? tc_launch_count() : kSimtLaunches;
+  if (events != nullptr) {
+    if (n_events != nlaunch + 1) return FMCA_ERR_INVALID_ARG;
+    for (int i = 0; i < n_events; ++i)
+      if (events[i] == nullptr) return FMCA_ERR_INVALID_ARG;
+  }
+  cudaEvent_t const *ev = reinterpret_cast<cudaEvent_t const *>(events);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  int rc;
+  if (use_tc)
+    rc = launch_tc_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0, workspace, cs,
+                           ev);
+  else
+    rc = launch_simt_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0,
+                             dtype == FMCA_BF16 ? 1 : 0, workspace, cs, ev);
+  return rc == 0 ? FMCA_OK : FMCA_ERR_CUDA;
+}
+
+fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
+                                   const float *gamma, const float *beta, void *O, int B,
+                                   int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                                   void *workspace, size_t workspace_bytes_, fmca_path path,
+                                   fmca_stream_t stream) {
+  return flash_mca_forward_timed(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype,
+                                 workspace, workspace_bytes_, path, nullptr, 0, stream);
+}
+
+fmca_status flash_mca_forward(const void *Z, const void *V, const void *U, const float *gamma,
+                              const float *beta, void *O, int B, int n, int s, int e, int C,
+                              int causal, fmca_dtype dtype, void *workspace,
+                              size_t workspace_bytes_, fmca_stream_t stream) {
+  return flash_mca_forward_path(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype, workspace,
+                                workspace_bytes_, FMCA_PATH_AUTO, stream);
+}
+
+// Arena layout for the host-buffer entry point: Z | V | U | gamma | beta | O |
+// workspace, each 256-byte aligned.
+size_t flash_mca_host_arena_bytes(int B, int n, int s, int e, int C, int causal,
+                                  fmca_dtype dtype) {
+  if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
+  const size_t es = elem_size(dtype);
+  return align256((size_t)B * n * s * es) + 3 * align256((size_t)B * n * e * es) +
+         2 * align256(sizeof(float) * 4 * (size_t)s) + workspace_bytes(B, n, s, e, C, causal);
+}
+
+fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *hU,
+                                   const float *hgamma, const float *hbeta, void *hO, int B,
+                                   int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                                   void *device_arena, size_t arena_bytes,
+                                   fmca_stream_t stream) {
+  fmca_status st = check_sizes(B, n, s, e, C, causal, dtype);
+  if (st != FMCA_OK) return st;
+  if (!hZ || !hV || !hU || !hgamma || !hbeta || !hO) return FMCA_ERR_INVALID_ARG;
+  if (!device_arena) return FMCA_ERR_WORKSPACE;
+  if (!aligned256(device_arena)) return FMCA_ERR_ALIGN;
+  if (arena_bytes < flash_mca_host_arena_bytes(B, n, s, e, C, causal, dtype))
+    return FMCA_ERR_WORKSPACE;
+  const size_t es = elem_size(dtype);
+  const size_t zb = (size_t)B * n * s * es, vb = (size_t)B * n * e * es;
+  const size_t gbytes = sizeof(float) * 4 * (size_t)s;
+  char *p = static_cast<char *>(device_arena);
+  void *dZ = p;
+  p += align256(zb);
+  void *dV = p;
+  p += align256(vb);
+  void *dU = p;
+  p += align256(vb);
+  float *dg = reinterpret_cast<float *>(p);
+  p += align256(gbytes);
+  float *db = reinterpret_cast<float *>(p);
+  p += align256(gbytes);
+  void *dO = p;
+  p += align256(vb);
+  void *ws = p;
+  const size_t wsb = workspace_bytes(B, n, s, e, C, causal);
+  cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(dZ, hZ, zb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(dV, hV, vb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(dU, hU, vb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(dg, hgamma, gbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+      cudaMemcpyAsync(db, hbeta, gbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+    return FMCA_ERR_CUDA;
+  st = flash_mca_forward(dZ, dV, dU, dg, db, dO, B, n, s, e, C, causal, dtype, ws, wsb, stream);
+  if (st != FMCA_OK) return st;
+  if (cudaMemcpyAsync(hO, dO, vb, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return FMCA_ERR_CUDA;
+  if (cudaStreamSynchronize(cs) != cudaSuccess) return FMCA_ERR_CUDA;
+  return FMCA_OK;
+}
+
+fmca_status flash_mca_device_status(fmca_stream_t stream, int32_t *where) {
+  int st = read_and_clear_device_status(reinterpret_cast<cudaStream_t>(stream), where);
+  if (st < 0) return FMCA_ERR_CUDA;
+  return st;
+}
+
+fmca_status flash_mca_selftest_timeout(int limit_us, fmca_stream_t stream) {
+  if (limit_us <= 0 || limit_us > 10 * 1000 * 1000) return FMCA_ERR_INVALID_ARG;
+  return launch_timeout_selftest(limit_us, reinterpret_cast<cudaStream_t>(stream)) == 0
+             ? FMCA_OK
+             : FMCA_ERR_CUDA;
+}
+
+const char *flash_mca_status_string(fmca_status status) {
+  switch (status) {
+    case FMCA_OK: return "FMCA_OK";
+    case FMCA_ERR_INVALID_ARG: return "FMCA_ERR_INVALID_ARG: NULL pointer, non-positive size or bad enum";
+    case FMCA_ERR_SHAPE: return "FMCA_ERR_SHAPE: C must divide n and C <= n";
+    case FMCA_ERR_UNSUPPORTED: return "FMCA_ERR_UNSUPPORTED: shape outside what the kernels support";
+    case FMCA_ERR_ALIGN: return "FMCA_ERR_ALIGN: pointer not aligned (16 B data, 256 B workspace)";
+    case FMCA_ERR_WORKSPACE: return "FMCA_ERR_WORKSPACE: workspace missing or too small";
+    case FMCA_ERR_CUDA: return "FMCA_ERR_CUDA: a CUDA launch or copy failed";
+    case FMCA_ERR_TIMEOUT: return "FMCA_ERR_TIMEOUT: a bounded device-side wait ran out";
+    default: return "unknown fmca status";
+  }
+}
+
+const char *flash_mca_version(void) { return "0.1.0"; }
+
+}  // extern "C"

@@ -1,0 +1,185 @@
+/*
+ * flash_mca.h -- C ABI of the FLASH mixed-chunk attention forward core on GB300.
+ *
+ * The operation (one call = one forward pass of the attention core of a GAU
+ * layer, after its U/V/Z projections and before its W_o projection) follows
+ * "FLASH: Possibly the Most Interesting Efficient Transformer Design Recently"
+ * (kexue.fm archive 8934):
+ *
+ *   T_k = Z * gamma[k] + beta[k], k = 0..3       section "Weak Attention", eq.
+ *                                                relu-att (affine Q, K of Z) and
+ *                                                "Mixed Chunk" (four maps: quad_q,
+ *                                                quad_k, lin_q, lin_k)
+ *   chunks of C tokens, G = n / C                "Mixed Chunk", first paragraph
+ *   quad_g = relu(T0_g T1_g^T / C)^2 V_g,        "Mixed Chunk", eq. for V^quad_g;
+ *            strict upper triangle masked         masking sentence (decoder)
+ *            in causal mode
+ *   lin_g  = T2_g (sum_h T3_h^T V_h) / n         "Mixed Chunk", eq. for V^lin_g
+ *            over all chunks h (bidirectional)   (non-causal form) and its cumsum
+ *            or chunks h < g (causal)            form for a decoder
+ *   O_g    = U_g * (quad_g + lin_g)              "Mixed Chunk", eq. for O_g
+ *                                                (W_o is not applied here)
+ *
+ * Readings where the page leaves a choice: the intra-chunk scale is relu(x/C)^2
+ * (the appendix scale relu(x/n)^2 of "Weak Attention" applied to a chunk); the
+ * global normaliser is 1/n in both modes; the causal sum over chunks is
+ * exclusive (h < g), so chunk 0 has no global term; the causal mask keeps the
+ * diagonal.
+ *
+ * Layouts (all row-major, contiguous, last index fastest):
+ *   Z[B][n][s], V[B][n][e], U[B][n][e], O[B][n][e]  -- element type `dtype`
+ *   gamma[4][s], beta[4][s]                         -- float32, rows in the
+ *                                                      order quad_q, quad_k,
+ *                                                      lin_q, lin_k
+ *
+ * Ownership: every pointer is owned by the caller; the library allocates no
+ * memory.  Device pointers must stay valid until the work queued on `stream`
+ * has finished.
+ *
+ * Errors: every argument check runs on the host before anything is queued; a
+ * call that returns a status other than FMCA_OK has queued nothing, except for
+ * FMCA_ERR_CUDA (a launch or copy failed after earlier work was queued).  The
+ * kernels never trap: a bounded wait that runs out records FMCA_ERR_TIMEOUT in
+ * a device-side status word that flash_mca_device_status() returns.
+ */
+#ifndef FLASH_MCA_H
+#define FLASH_MCA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Opaque CUDA stream handle (the same object as cudaStream_t); NULL is the
+ * legacy default stream. */
+typedef struct CUstream_st *fmca_stream_t;
+
+typedef int32_t fmca_status;
+#define FMCA_OK 0
+#define FMCA_ERR_INVALID_ARG 1 /* NULL pointer, non-positive size, bad enum */
+#define FMCA_ERR_SHAPE 2       /* C does not divide n, or C > n */
+#define FMCA_ERR_UNSUPPORTED 3 /* shape outside what the kernels support */
+#define FMCA_ERR_ALIGN 4       /* a device pointer is not 16-byte aligned */
+#define FMCA_ERR_WORKSPACE 5   /* workspace NULL or smaller than required */
+#define FMCA_ERR_CUDA 6        /* a CUDA launch or copy failed */
+#define FMCA_ERR_TIMEOUT 7     /* a bounded device-side wait ran out */
+
+typedef int32_t fmca_dtype;
+#define FMCA_F32 0  /* Z, V, U, O are float32; arithmetic in fp32 FMA */
+#define FMCA_BF16 1 /* Z, V, U, O are bfloat16; tensor-core products with
+                       fp32 accumulation, output rounded to nearest even */
+
+/* Which kernels carry a call. */
+typedef int32_t fmca_path;
+#define FMCA_PATH_AUTO 0    /* tensor-core path when the shape allows it,
+                               else the SIMT path */
+#define FMCA_PATH_SIMT 1    /* CUDA-core fp32 kernels, any supported shape */
+#define FMCA_PATH_TCGEN05 2 /* tcgen05/TMEM + TMA kernels; FMCA_BF16 only,
+                               s == 128, C in {128, 256}, e % 256 == 0 */
+
+/* Supported sizes: B, n, s, e >= 1; 1 <= C <= n with n % C == 0; s <= 256;
+ * B * n * max(s, e) < 2^31.  The tensor-core path additionally needs the
+ * conditions listed at FMCA_PATH_TCGEN05. */
+
+/*
+ * Bytes of device workspace one flash_mca_forward call with these arguments
+ * needs (the per-chunk linear-attention states and their prefix sums).
+ * Returns 0 for arguments flash_mca_forward would reject.
+ */
+size_t flash_mca_workspace_bytes(int B, int n, int s, int e, int C, int causal,
+                                 fmca_dtype dtype);
+
+/*
+ * The forward pass O = U * (quad + lin) described at the top of this file.
+ *   Z, V, U, O     device pointers, 16-byte aligned, element type `dtype`;
+ *                  O must not overlap Z, V, U or the workspace.
+ *   gamma, beta    device pointers to float32 [4][s].
+ *   causal         nonzero: decoder form (masked chunk, exclusive chunk sum).
+ *   workspace      device buffer of at least flash_mca_workspace_bytes(...)
+ *                  bytes, 256-byte aligned; its contents on entry do not
+ *                  matter and are undefined on exit.
+ *   stream         work is queued on this stream; the call does not wait.
+ * Deterministic: fixed shapes and inputs give bit-identical outputs.
+ */
+fmca_status flash_mca_forward(const void *Z, const void *V, const void *U,
+                              const float *gamma, const float *beta, void *O, int B,
+                              int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                              void *workspace, size_t workspace_bytes,
+                              fmca_stream_t stream);
+
+/* flash_mca_forward with an explicit choice of kernels (FMCA_PATH_*).
+ * FMCA_PATH_TCGEN05 returns FMCA_ERR_UNSUPPORTED for shapes it does not
+ * cover instead of falling back. */
+fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
+                                   const float *gamma, const float *beta, void *O, int B,
+                                   int n, int s, int e, int C, int causal,
+                                   fmca_dtype dtype, void *workspace,
+                                   size_t workspace_bytes, fmca_path path,
+                                   fmca_stream_t stream);
+
+/* flash_mca_forward_path that also records caller-created CUDA events
+ * (cudaEvent_t handles) on `stream` around its kernels: events[0] before the
+ * first kernel and events[i] after kernel i (1-based), so `n_events` must be
+ * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
+ * stream it runs on.  Kernel order: chunk states, state scan, chunk
+ * attention (both paths). */
+fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
+                                    const float *gamma, const float *beta, void *O, int B,
+                                    int n, int s, int e, int C, int causal,
+                                    fmca_dtype dtype, void *workspace,
+                                    size_t workspace_bytes, fmca_path path,
+                                    void *const *events, int n_events,
+                                    fmca_stream_t stream);
+
+/* Which path FMCA_PATH_AUTO takes for these arguments (FMCA_PATH_SIMT or
+ * FMCA_PATH_TCGEN05), or -1 for arguments that would be rejected. */
+int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype);
+
+/* Number of kernel launches one flash_mca_forward call queues for these
+ * arguments (0 when they would be rejected). */
+int flash_mca_launch_count(int B, int n, int s, int e, int C, int causal,
+                           fmca_dtype dtype, fmca_path path);
+
+/*
+ * End-to-end variant on HOST buffers: copies Z, V, U, gamma, beta from host
+ * memory into `device_arena`, runs flash_mca_forward on `stream`, copies O
+ * back to host memory and waits for the stream before returning, so hO is
+ * ready on return.  Host buffers should be page-locked for the copies to run
+ * at full speed (pageable memory works, more slowly).
+ *   device_arena   caller-owned device buffer, 256-byte aligned, of at least
+ *                  flash_mca_host_arena_bytes(...) bytes; it holds the device
+ *                  copies of the inputs and output and the workspace.
+ */
+size_t flash_mca_host_arena_bytes(int B, int n, int s, int e, int C, int causal,
+                                  fmca_dtype dtype);
+fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *hU,
+                                   const float *hgamma, const float *hbeta, void *hO,
+                                   int B, int n, int s, int e, int C, int causal,
+                                   fmca_dtype dtype, void *device_arena,
+                                   size_t arena_bytes, fmca_stream_t stream);
+
+/* Status recorded by the kernels on the current device since the last call of
+ * this function (FMCA_OK or FMCA_ERR_TIMEOUT); waits for `stream`, then
+ * clears the record.  *where (if not NULL) receives a code naming the wait
+ * that ran out (0 when none did). */
+fmca_status flash_mca_device_status(fmca_stream_t stream, int32_t *where);
+
+/* Queues one kernel whose single bounded wait can never be satisfied; with a
+ * limit of `limit_us` microseconds it gives up, records FMCA_ERR_TIMEOUT and
+ * returns, leaving the context usable.  Exercises the timeout path of the
+ * kernels' waits without faulting or hanging the GPU. */
+fmca_status flash_mca_selftest_timeout(int limit_us, fmca_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char *flash_mca_status_string(fmca_status status);
+
+/* Library version, e.g. "0.1.0". */
+const char *flash_mca_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLASH_MCA_H */

@@ -1,8 +1,6 @@
 import os
 import sys
 
-import pytest
-
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
@@ -10,10 +8,9 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (GB300, sm_103a)")
-
-
-def pytest_collection_modifyitems(config, items):
-    """A gpu-marked test on a machine without a GPU is an error of the
-    invocation, not something to skip silently: the CPU suite is run with
-    ``-m "not gpu"``."""
-    return None
+    # Build the in-tree CUDA library and the CPU oracle before any test module
+    # imports them (both builds are no-ops when up to date).
+    from flash_mixed_chunk_gb300 import _buildlib as _b
+    _b.build()
+    import oracle
+    oracle.build()

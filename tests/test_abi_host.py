@@ -1,0 +1,161 @@
+"""Host-side tests of the C ABI: the library loads, exports every entry point
+the header declares, sizes its workspace as documented and rejects bad
+arguments before queuing any work.  No call here reaches the GPU: every call
+with device pointers carries one argument the host checks refuse."""
+from __future__ import annotations
+
+import os
+import re
+
+import pytest
+
+import flash_mixed_chunk_gb300 as fm
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "flash_mca.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flash_mca_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    names = declared_functions()
+    for must in ("flash_mca_forward", "flash_mca_workspace_bytes", "flash_mca_status_string",
+                 "flash_mca_forward_host", "flash_mca_host_arena_bytes"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    for name in names:
+        assert hasattr(fm.lib, name), f"{name} declared in the header but not exported"
+    assert sorted(fm.EXPORTED_SYMBOLS) == names, "binding and header disagree"
+
+
+def test_library_is_in_tree_and_not_the_oracle():
+    assert os.path.dirname(fm.library_path) == os.path.join(ROOT, "flash_mixed_chunk_gb300")
+    # the product binding never imports the oracle
+    src = open(os.path.join(ROOT, "flash_mixed_chunk_gb300", "__init__.py")).read()
+    assert "oracle" not in src.replace("no CPU fallback", "")
+
+
+def test_status_strings():
+    for code in range(8):
+        sname = fm.flash_mca_status_string(code)
+        assert sname.startswith("FMCA_")
+    assert "unknown" in fm.flash_mca_status_string(99)
+    assert fm.flash_mca_version() == "0.1.0"
+
+
+@pytest.mark.parametrize("B,n,s,e,C,causal", [(2, 8192, 128, 1536, 256, 1),
+                                              (4, 4096, 128, 1536, 256, 0),
+                                              (1, 256, 32, 64, 64, 1),
+                                              (3, 96, 48, 80, 32, 0)])
+def test_workspace_bytes_formula(B, n, s, e, C, causal):
+    a = lambda x: (x + 255) // 256 * 256
+    G = n // C
+    want = a(4 * B * G * s * e) + a(4 * B * (G if causal else 1) * s * e)
+    for dt in (fm.FMCA_F32, fm.FMCA_BF16):
+        assert fm.flash_mca_workspace_bytes(B, n, s, e, C, causal, dt) == want
+
+
+def test_workspace_bytes_zero_for_rejected_shapes():
+    assert fm.flash_mca_workspace_bytes(1, 100, 32, 64, 30, 1, fm.FMCA_F32) == 0   # C !| n
+    assert fm.flash_mca_workspace_bytes(1, 64, 32, 64, 128, 1, fm.FMCA_F32) == 0   # C > n
+    assert fm.flash_mca_workspace_bytes(0, 64, 32, 64, 64, 1, fm.FMCA_F32) == 0
+    assert fm.flash_mca_workspace_bytes(1, 64, 512, 64, 64, 1, fm.FMCA_F32) == 0   # s > 256
+    assert fm.flash_mca_workspace_bytes(1, 64, 32, 64, 64, 1, 7) == 0              # bad dtype
+
+
+def test_auto_path_choice():
+    bf, f32 = fm.FMCA_BF16, fm.FMCA_F32
+    assert fm.flash_mca_auto_path(2, 8192, 128, 1536, 256, 1, bf) == fm.FMCA_PATH_TCGEN05
+    assert fm.flash_mca_auto_path(1, 32768, 128, 2048, 256, 1, bf) == fm.FMCA_PATH_TCGEN05
+    assert fm.flash_mca_auto_path(1, 256, 128, 256, 128, 0, bf) == fm.FMCA_PATH_TCGEN05
+    assert fm.flash_mca_auto_path(2, 8192, 128, 1536, 256, 1, f32) == fm.FMCA_PATH_SIMT
+    assert fm.flash_mca_auto_path(1, 256, 32, 64, 64, 1, f32) == fm.FMCA_PATH_SIMT
+    assert fm.flash_mca_auto_path(1, 512, 64, 256, 256, 1, bf) == fm.FMCA_PATH_SIMT   # s != 128
+    assert fm.flash_mca_auto_path(1, 512, 128, 320, 256, 1, bf) == fm.FMCA_PATH_SIMT  # e % 256
+    assert fm.flash_mca_auto_path(1, 512, 128, 256, 64, 1, bf) == fm.FMCA_PATH_SIMT   # C = 64
+    assert fm.flash_mca_auto_path(1, 500, 128, 256, 64, 1, bf) == -1
+
+
+def test_launch_counts():
+    bf = fm.FMCA_BF16
+    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 3
+    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
+    assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
+    assert fm.flash_mca_launch_count(1, 500, 128, 256, 64, 1, bf) == 0
+
+
+# A fake device address: aligned, never dereferenced (each call below fails a
+# host check first).
+P = 0x7F0000000000
+BIG = 1 << 40
+
+
+def fwd(**kw):
+    args = dict(Z=P, V=P + 0x10000000, U=P + 0x20000000, g=P + 0x30000000, b=P + 0x30001000,
+                O=P + 0x40000000, B=1, n=256, s=32, e=64, C=64, causal=1, dt=fm.FMCA_F32,
+                ws=P + 0x50000000, wsb=BIG, path=fm.FMCA_PATH_AUTO)
+    args.update(kw)
+    return fm.lib.flash_mca_forward_path(args["Z"], args["V"], args["U"], args["g"], args["b"],
+                                         args["O"], args["B"], args["n"], args["s"], args["e"],
+                                         args["C"], args["causal"], args["dt"], args["ws"],
+                                         args["wsb"], args["path"], None)
+
+
+def test_validation_codes():
+    assert fwd(C=60) == fm.FMCA_ERR_SHAPE
+    assert fwd(C=512) == fm.FMCA_ERR_SHAPE
+    assert fwd(B=0) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(e=-1) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(dt=5) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(path=9) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(Z=0) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(O=0) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(g=0) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(s=300) == fm.FMCA_ERR_UNSUPPORTED
+    assert fwd(V=P + 0x10000008) == fm.FMCA_ERR_ALIGN
+    assert fwd(O=P + 0x40000004) == fm.FMCA_ERR_ALIGN
+    assert fwd(ws=0) == fm.FMCA_ERR_WORKSPACE
+    assert fwd(ws=P + 0x50000010) == fm.FMCA_ERR_ALIGN
+    assert fwd(wsb=100) == fm.FMCA_ERR_WORKSPACE
+    # O overlapping an input or the workspace
+    assert fwd(O=P + 0x10000000) == fm.FMCA_ERR_INVALID_ARG
+    assert fwd(O=P + 0x50000000) == fm.FMCA_ERR_INVALID_ARG
+    # explicit tensor-core path on a shape it does not cover: no fallback
+    assert fwd(path=fm.FMCA_PATH_TCGEN05) == fm.FMCA_ERR_UNSUPPORTED
+    assert fwd(dt=fm.FMCA_BF16, s=64, e=256, n=512, C=256,
+               path=fm.FMCA_PATH_TCGEN05) == fm.FMCA_ERR_UNSUPPORTED
+
+
+def test_host_entry_validation():
+    f = fm.lib.flash_mca_forward_host
+    good = dict(B=1, n=256, s=32, e=64, C=64, causal=1, dt=fm.FMCA_F32)
+    need = fm.flash_mca_host_arena_bytes(1, 256, 32, 64, 64, 1, fm.FMCA_F32)
+    assert need > fm.flash_mca_workspace_bytes(1, 256, 32, 64, 64, 1, fm.FMCA_F32)
+    h = P  # host pointers are never touched either
+    assert f(h, h, h, h, h, h, 1, 256, 32, 64, 60, 1, fm.FMCA_F32, P, need, None) == fm.FMCA_ERR_SHAPE
+    assert f(0, h, h, h, h, h, 1, 256, 32, 64, 64, 1, fm.FMCA_F32, P, need, None) == fm.FMCA_ERR_INVALID_ARG
+    assert f(h, h, h, h, h, h, 1, 256, 32, 64, 64, 1, fm.FMCA_F32, 0, need, None) == fm.FMCA_ERR_WORKSPACE
+    assert f(h, h, h, h, h, h, 1, 256, 32, 64, 64, 1, fm.FMCA_F32, P, need - 1, None) == fm.FMCA_ERR_WORKSPACE
+    assert f(h, h, h, h, h, h, 1, 256, 32, 64, 64, 1, fm.FMCA_F32, P + 16, need, None) == fm.FMCA_ERR_ALIGN
+
+
+def test_selftest_rejects_bad_limits():
+    assert fm.lib.flash_mca_selftest_timeout(0, None) == fm.FMCA_ERR_INVALID_ARG
+    assert fm.lib.flash_mca_selftest_timeout(20_000_000, None) == fm.FMCA_ERR_INVALID_ARG
+
+
+def test_python_binding_rejects_bad_tensors():
+    import torch
+    Z = torch.zeros(1, 256, 32)
+    V = torch.zeros(1, 256, 64)
+    with pytest.raises(ValueError):
+        fm.flash_mca_forward(Z, V, V, torch.zeros(4, 32), torch.zeros(4, 32), V, 64, True, Z)
+    with pytest.raises(ValueError):
+        fm.forward(Z[0], V, V, torch.zeros(4, 32), torch.zeros(4, 32), 64, True)
