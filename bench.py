@@ -1,0 +1,429 @@
+"""Benchmark of the FLASH mixed-chunk attention forward core on GB300.
+
+One step = one forward pass of the whole core (chunk states, chunk-axis scan,
+chunk attention with the U gate) over one batch of synthetic input, through
+the C ABI.  Default workload: the long causal shape (B=2, n=8192, C=256,
+s=128, e=1536, bf16 I/O, fp32 accumulation).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME]
+
+Prints one JSON line (rank 0).  Our arm: `value` is tokens/s over K steps with
+inputs resident in HBM, timed with CUDA events on the launching stream between
+a barrier + synchronize on both sides (max over ranks); per-kernel durations
+come from events the library records between its kernels.  Inputs and outputs
+rotate over three buffer sets, each larger than L2 (129 MB), so no step reads
+what the previous step left in L2.  `e2e` is the same metric through the
+host-buffer entry point (pinned host memory, copies in and out inside the
+timed region).  The reference arm (--impl reference) times the fp64 CPU
+oracle on the host cores on bounded samples of the same workload.
+
+Multi-GPU: the workload is a batch of independent sequences, so N ranks run N
+independent replicas (one per GPU, weak scaling) with no collective on the
+data path; only the timing uses a barrier and a max-reduction.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import mca_inputs  # noqa: E402
+
+METRIC = "mixed-chunk attn fwd tokens/s and TFLOP/s at 1 GB300; % of bf16 tensor peak"
+PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+DOMINANT_KERNEL = "tc_chunk_attn"
+
+
+# ---------------------------------------------------------------- work accounting
+def algorithmic_flops(w) -> float:
+    """Per forward pass: per chunk 2*P*(s+e) for the intra-chunk scores and
+    relu^2-weighted values over the P unmasked (query, key) pairs, plus
+    4*C*s*e for the chunk state and the global term."""
+    P = w.C * (w.C + 1) // 2 if w.causal else w.C * w.C
+    per_chunk = 2.0 * P * (w.s + w.e) + 4.0 * w.C * w.s * w.e
+    return per_chunk * w.B * w.G
+
+
+def algorithmic_bytes(w) -> float:
+    """Compulsory HBM traffic of one pass: read Z, V, U once, write O once."""
+    es = 2 if w.dtype == "bf16" else 4
+    return float(w.B * w.n * (w.s + 3 * w.e) * es)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+
+
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    for f in ("tc.cu", "ptx.cuh"):
+        with open(os.path.join(ROOT, "flash_mixed_chunk_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    sha = kernel_source_sha()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(tok.split("=", 1) for tok in line.split() if "=" in tok)
+        if (kv.get("kernel") == kernel and kv.get("workload") == workload
+                and kv.get("source_sha") == sha):
+            return float(kv["dram_bytes_per_launch"])
+    return None
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples (every 50 ms) of SM clock and throttle reasons."""
+
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0: float, t1: float):
+        rows = [s for t, s in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not rows:  # timed region shorter than the sampling period
+            near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
+            rows = [s for _, s in near[:2]]
+            window = "nearest"
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            parts = [p.strip() for p in r.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+def oracle_sample_rate(w, inputs64, gamma, beta, budget_s: float):
+    """Time the oracle on a bounded sample of the workload: the outputs of the
+    first m chunks of batch element 0 (in causal mode they need only chunks
+    < m; otherwise all chunks), with m grown up to the whole sequence, then the
+    whole workload (every batch element) repeated, until one measurement takes
+    about `budget_s`.  Returns (tokens/s, seconds, description, threads)."""
+    import oracle
+    Z, V, U = inputs64
+    m = 1
+    while True:
+        rows = np.arange(m * w.C, dtype=np.int64)
+        t = time.perf_counter()
+        oracle.rows(Z, V, U, gamma, beta, w.C, w.causal, rows)
+        dt = time.perf_counter() - t
+        if dt >= budget_s:
+            return m * w.C / dt, dt, f"outputs of the first {m} chunk(s) of batch element 0", \
+                oracle.max_threads()
+        if m >= w.G:
+            break
+        m = min(w.G, max(m + 1, int(m * budget_s / max(dt, 1e-3))))
+    reps = 0
+    t = time.perf_counter()
+    while True:
+        oracle.forward(Z, V, U, gamma, beta, w.C, w.causal)
+        reps += 1
+        dt = time.perf_counter() - t
+        if dt >= budget_s:
+            break
+    return reps * w.B * w.n / dt, dt, f"{reps} full forward pass(es) of all {w.B} batch " \
+        "element(s)", oracle.max_threads()
+
+
+def run_reference(args, w):
+    """Reference arm: the fp64 CPU oracle as it stands, on host cores."""
+    import oracle
+    oracle.build()
+    seed = mca_inputs.WORKLOAD_ORDER.index(w.name) + 1
+    Z, V, U, gamma, beta = mca_inputs.workload_inputs(w, seed)
+    inputs64 = tuple(x.to(torch.float64).numpy() for x in (Z, V, U))
+    g64, b64 = gamma.double().numpy(), beta.double().numpy()
+    # size each step so that warm-up + steps stay within about two minutes
+    per_step = max(0.05, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    # each step: the outputs of the first m chunks of batch element 0, m sized
+    # so that one step takes about `per_step` seconds (at most the sequence)
+    m = 1
+    while True:
+        rows = np.arange(m * w.C, dtype=np.int64)
+        t = time.perf_counter()
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows)
+        dt = time.perf_counter() - t
+        if dt >= per_step or m >= w.G:
+            break
+        m = min(w.G, max(m + 1, int(m * per_step / max(dt, 1e-3))))
+    threads = oracle.max_threads()
+    for _ in range(args.warmup):
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows)
+    dt = time.perf_counter() - t
+    value = args.steps * m * w.C / dt
+    sample = (f"outputs of the first {m} chunk(s) of batch element 0 of {w.name} per step "
+              f"({m * w.C} tokens; fp64 oracle, OpenMP)")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": config_of(w),
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def config_of(w):
+    return {"workload": w.name, "B": w.B, "n": w.n, "C": w.C, "G": w.G, "s": w.s, "e": w.e,
+            "causal": w.causal, "io_dtype": w.dtype, "accumulate": "fp32",
+            "l2": "inputs larger than L2, 3 rotating buffer sets",
+            "parallelism": "replicas (one independent problem per GPU)"}
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, w, rank, world, device):
+    import flash_mixed_chunk_gb300 as fm
+
+    torch.cuda.set_device(device)
+    seed = mca_inputs.WORKLOAD_ORDER.index(w.name) + 1
+    Zc, Vc, Uc, gc, bc = mca_inputs.workload_inputs(w, seed)
+    dt_code = fm.FMCA_BF16 if w.dtype == "bf16" else fm.FMCA_F32
+    path = fm.flash_mca_auto_path(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code)
+    nl = fm.flash_mca_launch_count(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code)
+    sets = []
+    for _ in range(3):
+        sets.append(dict(Z=Zc.to(device), V=Vc.to(device), U=Uc.to(device),
+                         O=torch.empty((w.B, w.n, w.e), dtype=Zc.dtype, device=device)))
+    gd, bd = gc.to(device), bc.to(device)
+    ws = torch.empty(fm.flash_mca_workspace_bytes(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(i, events=None):
+        s = sets[i % 3]
+        if events is None:
+            fm.flash_mca_forward(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws, stream)
+        else:
+            fm.flash_mca_forward_timed(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws,
+                                       events, fm.FMCA_PATH_AUTO, stream)
+
+    sampler = ClockSampler(torch.cuda.current_device() if device.index is None else device.index)
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(device)
+    st, where = fm.flash_mca_device_status()
+    if st != fm.FMCA_OK:
+        raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
+
+    # ---- timed region: exactly K steps
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(nl + 1)]
+              for _ in range(args.steps)]
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    for evs in events:  # create the CUDA event handles outside the timed region
+        for ev in evs:
+            ev.record(stream)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    wall0 = time.time()
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(i, events[i])
+    t_end.record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    sampler.stop()
+    st, where = fm.flash_mca_device_status()
+    if st != fm.FMCA_OK:
+        raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
+    ms = t_start.elapsed_time(t_end)
+    per_kernel_ms = [statistics.fmean(ev[k].elapsed_time(ev[k + 1]) for ev in events)
+                     for k in range(nl)]
+    if world > 1:
+        tt = torch.tensor([ms], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+
+    # ---- end to end through the host-buffer entry point
+    pin = [t.pin_memory() for t in (Zc, Vc, Uc, gc, bc)]
+    Oh = torch.empty((w.B, w.n, w.e), dtype=Zc.dtype).pin_memory()
+    arena = torch.empty(fm.flash_mca_host_arena_bytes(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code),
+                        dtype=torch.uint8, device=device)
+    k_e2e = max(3, min(args.steps, 200))
+    for _ in range(3):
+        fm.flash_mca_forward_host(*pin, Oh, w.C, w.causal, arena, stream)
+    if world > 1:
+        torch.distributed.barrier()
+    t = time.perf_counter()
+    for _ in range(k_e2e):
+        fm.flash_mca_forward_host(*pin, Oh, w.C, w.causal, arena, stream)
+    e2e_s = time.perf_counter() - t
+    if world > 1:
+        tt = torch.tensor([e2e_s], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        e2e_s = float(tt.item())
+    h2d = sum(t.numel() * t.element_size() for t in pin)
+    d2h = Oh.numel() * Oh.element_size()
+
+    if rank != 0:
+        return
+    peaks, peak_kind = load_peaks()
+    tokens = w.B * w.n
+    value = world * tokens * args.steps / (ms / 1e3)
+    flops = algorithmic_flops(w)
+    tflops = world * flops * args.steps / (ms / 1e3) / 1e12
+    kernel_names = (["tc_chunk_state", "tc_state_scan", "tc_chunk_attn"]
+                    if path == fm.FMCA_PATH_TCGEN05 else
+                    ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"])
+    kernels = {name: {"ms": per_kernel_ms[i], "share": per_kernel_ms[i] / sum(per_kernel_ms)}
+               for i, name in enumerate(kernel_names)}
+    dom = max(kernels, key=lambda k: kernels[k]["ms"])
+    dom_ms = kernels[dom]["ms"]
+    achieved = algorithmic_bytes(w) / (dom_ms / 1e3) / 1e9
+    hbm_peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    bf16_peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    traffic = profiled_traffic(dom, w.name)
+
+    # ---- CPU baseline: the oracle as it stands, bounded sample, host cores
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        inputs64 = tuple(x.to(torch.float64).numpy() for x in (Zc, Vc, Uc))
+        rate, dt, what, threads = oracle_sample_rate(w, inputs64, gc.double().numpy(),
+                                                     bc.double().numpy(), args.cpu_budget)
+        cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+               "sample": f"{what} of {w.name} ({dt:.1f} s; fp64 oracle, OpenMP)"}
+
+    clocks = sampler.summary(wall0, wall1)
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
+        "config": config_of(w),
+        "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / bf16_peak,
+        "hbm_gbs_step": world * algorithmic_bytes(w) * args.steps / (ms / 1e3) / 1e9,
+        "path": "tcgen05" if path == fm.FMCA_PATH_TCGEN05 else "simt",
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
+                     "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
+                     "algorithmic_bytes_per_launch": algorithmic_bytes(w),
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * tokens * k_e2e / e2e_s, "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e},
+        "gpu_launches": nl * args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="long_causal", choices=list(mca_inputs.WORKLOADS))
+    ap.add_argument("--cpu-budget", type=float, default=10.0,
+                    help="seconds of oracle work for the CPU baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = mca_inputs.WORKLOADS[args.workload]
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        if rank == 0:
+            run_reference(args, w)
+        return
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    device = torch.device("cuda", local)
+    try:
+        run_ours(args, w, rank, world, device)
+    finally:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -164,12 +164,14 @@ def flash_mca_forward_timed(Z, V, U, gamma, beta, O, C: int, causal: bool, works
                             events, path: int = FMCA_PATH_AUTO, stream=None) -> None:
     """``flash_mca_forward_path`` recording ``events`` (torch.cuda.Event
     objects, launch count + 1 of them) before the first kernel and after each
-    kernel on ``stream``."""
+    kernel on ``stream``.  torch creates an event's CUDA handle on its first
+    record; events without a handle yet are recorded once here to create it."""
     B, n, s, e = _shapes(Z, V, U)
     if stream is None:
         stream = torch.cuda.current_stream()
     for ev in events:
-        ev.record(stream)  # materialises the CUDA event handle
+        if not ev.cuda_event:
+            ev.record(stream)
     handles = (_vp * len(events))(*[ev.cuda_event for ev in events])
     dt = _dtype_code(Z)
     st = lib.flash_mca_forward_timed(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),

@@ -306,16 +306,24 @@ __global__ void __launch_bounds__(256)
 //   [0,   64K)  Z tile of the chunk's keys, K-major (atom a = s cols 64a..64a+63
 //               at a*32K, 256 rows x 128 B); turned into T1 in place; after the
 //               score MMA it holds P (bf16 [128 rows][keys], key atom k at k*16K)
-//   [64K, 96K)  T0 rows (2 atoms x 16K)
+//   [64K, 96K)  T0 rows (2 atoms x 16K); after the score MMA: ring B, 2 slots
+//               of U / O tiles (128 rows x 64 e, 16 KB)
 //   [96K,128K)  T2 rows (2 atoms x 16K)
-//   [128K, 224K) ring of 3 x 32 KB slots: V stages (64 keys x 256 e), state
-//               prefix stages (64 s rows x 256 e), U/O stages (128 rows x 128 e)
-constexpr int ATTN_NSLOT = 3;
-constexpr uint32_t ATTN_SLOT = 32768;
+//   [128K, 224K) ring A, 3 x 32 KB slots: V stages (64 keys x 256 e) and state
+//               prefix stages (64 s rows x 256 e)
+// Each ring has exactly one consumer (ring A: the MMA warp; ring B: the
+// epilogue warps), so a consumer never waits on a slot whose previous phase
+// belongs to another consumer.
+constexpr int RING_A = 3;
+constexpr uint32_t SLOT_A = 32768;
+constexpr int RING_B = 2;
+constexpr uint32_t SLOT_B = 16384;
 constexpr uint32_t OFF_T0 = 65536, OFF_T2 = 98304, OFF_RING = 131072;
-constexpr uint32_t ATTN_SMEM = OFF_RING + ATTN_NSLOT * ATTN_SLOT + 1024;
+constexpr uint32_t OFF_RING_B = OFF_T0;
+constexpr uint32_t ATTN_SMEM = OFF_RING + RING_A * SLOT_A + 1024;
 constexpr int ATTN_THREADS = 192;
 static_assert(ATTN_SMEM + 512 <= 232448, "tc_chunk_attn exceeds 227 KB of shared memory");
+static_assert(RING_B * SLOT_B <= OFF_T2 - OFF_T0, "ring B must fit in the T0 region");
 
 __global__ void __launch_bounds__(ATTN_THREADS, 1)
     tc_chunk_attn(const __grid_constant__ CUtensorMap mapZ,   // box {64, 128}
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[ATTN_NSLOT], empty[ATTN_NSLOT];
+  __shared__ __align__(8) uint64_t fullA[RING_A], emptyA[RING_A], fullB[RING_B], emptyB[RING_B];
   __shared__ __align__(8) uint64_t zfull, tready, sfull, pready, acc_full[2], acc_empty[2];
   __shared__ __align__(8) uint64_t mma_done;
   __shared__ uint32_t tmem_base;
@@ -345,12 +353,17 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   const int nkv = keys_n / KEY_STAGE;  // V stages per e tile
   const int chunk_row = b * n + g * C;
   const int prow = (causal ? bg : b) * S_DIM;  // first row of this chunk's prefix in [.., e]
-  const int items_per_et = nkv + 2 + 2;        // V stages, 2 prefix stages, 2 U stages
+  const int a_per_et = nkv + 2;                // ring A items per e tile: V stages, 2 prefix stages
+  constexpr int B_PER_ET = E_TILE / 64;        // ring B items per e tile: U quarters
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < ATTN_NSLOT; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int i = 0; i < RING_A; ++i) {
+      mbar_init(&fullA[i], 1);
+      mbar_init(&emptyA[i], 1);
+    }
+    for (int i = 0; i < RING_B; ++i) {
+      mbar_init(&fullB[i], 1);
+      mbar_init(&emptyB[i], 1);
     }
     mbar_init(&zfull, 1);
     mbar_init(&tready, 1);
@@ -374,7 +387,8 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
   uint8_t *zt = smem;
   uint8_t *t0 = smem + OFF_T0;
   uint8_t *t2 = smem + OFF_T2;
-  uint8_t *ring = smem + OFF_RING;
+  uint8_t *ringA = smem + OFF_RING;
+  uint8_t *ringB = smem + OFF_RING_B;
 
   if (warp == 0) {
     // =========================== TMA producer
@@ -387,38 +401,52 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       for (int kh = 0; kh < keys_n / 128; ++kh)
         for (int a = 0; a < 2; ++a)
           tma_load_2d(zt + a * 32768 + kh * 16384, &mapZ, &zfull, 64 * a, chunk_row + 128 * kh);
-      int item = 0;
+      int ia = 0, ib = 0;
       bool ok = true;
       for (int et = 0; et < n_et && ok; ++et) {
         const int e0 = (eg * n_et + et) * E_TILE;
-        for (int k = 0; k < items_per_et; ++k, ++item) {
-          const int slot = item % ATTN_NSLOT;
-          if (item >= ATTN_NSLOT &&
-              !mbar_wait(&empty[slot], ((item / ATTN_NSLOT) - 1) & 1, kWaitLimitNs)) {
+        for (int k = 0; k < a_per_et; ++k, ++ia) {
+          const int slot = ia % RING_A;
+          if (ia >= RING_A &&
+              !mbar_wait(&emptyA[slot], ((ia / RING_A) - 1) & 1, kWaitLimitNs)) {
             record_timeout(201);
             ok = false;
             break;
           }
-          uint8_t *dst = ring + slot * ATTN_SLOT;
-          mbar_arrive_expect_tx(&full[slot], ATTN_SLOT);
+          uint8_t *dst = ringA + slot * SLOT_A;
+          mbar_arrive_expect_tx(&fullA[slot], SLOT_A);
           if (k < nkv) {  // V keys [64k, 64k+64) x e cols [e0, e0+256)
             const int y = chunk_row + k * KEY_STAGE;
-            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * 8192, &mapV, &full[slot], e0 + 64 * i, y);
-          } else if (k < nkv + 2) {  // prefix rows [64q, 64q+64) x [e0, e0+256)
+            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * 8192, &mapV, &fullA[slot], e0 + 64 * i, y);
+          } else {  // prefix rows [64q, 64q+64) x [e0, e0+256)
             const int y = prow + (k - nkv) * KEY_STAGE;
-            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * 8192, &mapP, &full[slot], e0 + 64 * i, y);
-          } else {  // U rows of the tile x e cols [e0 + 128h, +128)
-            const int h = k - nkv - 2;
-            const int y = chunk_row + rt * 128;
-            for (int i = 0; i < 2; ++i)
-              tma_load_2d(dst + i * 16384, &mapU, &full[slot], e0 + 128 * h + 64 * i, y);
+            for (int i = 0; i < 4; ++i) tma_load_2d(dst + i * 8192, &mapP, &fullA[slot], e0 + 64 * i, y);
           }
         }
+        if (!ok) break;
+        // ring B lives over T0, which is free once the score MMA has retired
+        if (et == 0 && !mbar_wait(&sfull, 0, kWaitLimitNs)) {
+          record_timeout(204);
+          ok = false;
+          break;
+        }
+        for (int q = 0; q < B_PER_ET; ++q, ++ib) {
+          const int slot = ib % RING_B;
+          if (ib >= RING_B &&
+              !mbar_wait(&emptyB[slot], ((ib / RING_B) - 1) & 1, kWaitLimitNs)) {
+            record_timeout(205);
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&fullB[slot], SLOT_B);
+          tma_load_2d(ringB + slot * SLOT_B, &mapU, &fullB[slot], e0 + 64 * q, chunk_row + rt * 128);
+        }
       }
-      // drain: the last stage issued in each slot has landed
-      for (int q = (item > ATTN_NSLOT ? item - ATTN_NSLOT : 0); q < item; ++q)
-        if (!mbar_wait(&full[q % ATTN_NSLOT], (q / ATTN_NSLOT) & 1, kWaitLimitNs))
-          record_timeout(202);
+      // drain: the last load issued into every slot has landed
+      for (int q = (ia > RING_A ? ia - RING_A : 0); q < ia; ++q)
+        if (!mbar_wait(&fullA[q % RING_A], (q / RING_A) & 1, kWaitLimitNs)) record_timeout(202);
+      for (int q = (ib > RING_B ? ib - RING_B : 0); q < ib; ++q)
+        if (!mbar_wait(&fullB[q % RING_B], (q / RING_B) & 1, kWaitLimitNs)) record_timeout(206);
       if (!mbar_wait(&zfull, 0, kWaitLimitNs)) record_timeout(203);
     }
   } else if (warp == 1) {
@@ -443,7 +471,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       // acc[rows][256 e] = P * V (A K-major, B MN-major) + T2 * Pg (same)
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, E_TILE, false, true);
       const uint32_t pbase = smem_u32(zt), t2base = smem_u32(t2);
-      int item = 0;
+      int ia = 0;
       for (int et = 0; et < n_et && ok; ++et) {
         const int buf = (et & 1) ? 0 : 1;  // tile 0 -> cols 256.., tile 1 -> cols 0..
         const int use = et >> 1;
@@ -454,15 +482,15 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         }
         tc_fence_after();
         const uint32_t dcol = tbase + (buf ? 256u : 0u);
-        for (int k = 0; k < nkv + 2; ++k, ++item) {
-          const int slot = item % ATTN_NSLOT;
-          if (!mbar_wait(&full[slot], (item / ATTN_NSLOT) & 1, kWaitLimitNs)) {
+        for (int k = 0; k < a_per_et; ++k, ++ia) {
+          const int slot = ia % RING_A;
+          if (!mbar_wait(&fullA[slot], (ia / RING_A) & 1, kWaitLimitNs)) {
             record_timeout(214);
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t sb = smem_u32(ring + slot * ATTN_SLOT);
+          const uint32_t sb = smem_u32(ringA + slot * SLOT_A);
           for (int kk = 0; kk < 4; ++kk) {
             const uint64_t bd = smem_desc_sw128(sb + kk * 2048, 8192, 1024);
             uint64_t ad;
@@ -472,11 +500,10 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
               ad = smem_desc_sw128(t2base + (k - nkv) * 16384 + kk * 32, 16, 1024);
             mma_bf16_ss(dcol, ad, bd, idesc_o, (k | kk) != 0);
           }
-          mma_commit(&empty[slot]);
+          mma_commit(&emptyA[slot]);
         }
         if (!ok) break;
         mma_commit(&acc_full[buf]);
-        item += 2;  // the two U stages belong to the epilogue
       }
       // every MMA has finished before TMEM is released
       mma_commit(&mma_done);
@@ -538,6 +565,7 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
       fence_proxy_async_smem();
       named_bar_sync(1, 128);
       if (mt == 0) mbar_arrive(&tready);
+      __syncwarp();
     }
     // ---- P = relu(S / C)^2 (masked) as bf16 over the Z tile
     if (ok) {
@@ -579,37 +607,36 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
         if (ok) mbar_arrive(&pready);
         else record_timeout(222);
       }
+      __syncwarp();
     }
-    // ---- epilogue per e tile: O = U * acc, written over the U stage, TMA store
-    int item = 0;
+    // ---- epilogue per e tile: O = U * acc in ring B, TMA store per 64 columns
+    int ib = 0;
     for (int et = 0; et < n_et && ok; ++et) {
       const int e0 = (eg * n_et + et) * E_TILE;
       const int buf = (et & 1) ? 0 : 1;
       const int use = et >> 1;
-      item += nkv + 2;
       const bool acc_ok = mbar_wait(&acc_full[buf], use & 1, kWaitLimitNs);
       if (acc_ok) tc_fence_after();
       const uint32_t dcol = tbase + (buf ? 256u : 0u) + ((uint32_t)(quad * 32) << 16);
-      for (int h = 0; h < 2; ++h, ++item) {
-        const int slot = item % ATTN_NSLOT;
-        got = acc_ok && mbar_wait(&full[slot], (item / ATTN_NSLOT) & 1, kWaitLimitNs);
-        uint8_t *us = ring + slot * ATTN_SLOT;
+      for (int q = 0; q < B_PER_ET; ++q, ++ib) {
+        const int slot = ib % RING_B;
+        got = acc_ok && mbar_wait(&fullB[slot], (ib / RING_B) & 1, kWaitLimitNs);
+        uint8_t *us = ringB + slot * SLOT_B;
         if (got) {
-          for (int c4 = 0; c4 < 4; ++c4) {
+          for (int c2 = 0; c2 < 2; ++c2) {
             uint32_t r[32];
-            tmem_ld32(dcol + h * 128 + c4 * 32, r);
+            tmem_ld32(dcol + q * 64 + c2 * 32, r);
             tmem_ld_wait();
-            uint8_t *ubox = us + (c4 >> 1) * 16384;
-            const uint32_t byte0 = (c4 & 1) * 64;
+            const uint32_t byte0 = c2 * 64;
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint4 *ptr = reinterpret_cast<uint4 *>(ubox + sw128_offset(row, byte0 + 16 * q));
+            for (int j4 = 0; j4 < 4; ++j4) {
+              uint4 *ptr = reinterpret_cast<uint4 *>(us + sw128_offset(row, byte0 + 16 * j4));
               const uint4 uv = *ptr;
               const uint32_t w[4] = {uv.x, uv.y, uv.z, uv.w};
               uint32_t o[4];
 #pragma unroll
               for (int i = 0; i < 4; ++i) {
-                const int j = 8 * q + 2 * i;
+                const int j = 8 * j4 + 2 * i;
                 o[i] = pack_bf16x2(bf16_lo(w[i]) * __uint_as_float(r[j]),
                                    bf16_hi(w[i]) * __uint_as_float(r[j + 1]));
               }
@@ -624,17 +651,18 @@ __global__ void __launch_bounds__(ATTN_THREADS, 1)
           break;
         }
         if (mt == 0) {
-          const int y = chunk_row + rt * 128;
-          for (int i = 0; i < 2; ++i) tma_store_2d(&mapO, us + i * 16384, e0 + 128 * h + 64 * i, y);
+          tma_store_2d(&mapO, us, e0 + 64 * q, chunk_row + rt * 128);
           bulk_commit_group();
           bulk_wait_group_read<0>();
-          mbar_arrive(&empty[slot]);
+          mbar_arrive(&emptyB[slot]);
         }
+        __syncwarp();
       }
       if (!ok) break;
       tc_fence_before();
       named_bar_sync(1, 128);
       if (mt == 0) mbar_arrive(&acc_empty[buf]);
+      __syncwarp();
     }
     if (mt == 0) bulk_wait_group<0>();
   }
