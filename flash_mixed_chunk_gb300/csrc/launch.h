@@ -11,20 +11,33 @@ namespace fmca {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace layout (both paths):
-//   [0, align256(B*G*s*e*4))          per-chunk states, fp32 [B][G][s][e]
-//   [that, + B*Gp*s*e*4)              state prefix sums / n, Gp = G (causal)
-//                                     or 1 (bidirectional); fp32 on the SIMT
-//                                     path, bf16 on the tensor-core path
-inline size_t workspace_bytes(int B, int n, int s, int e, int C, int causal) {
+// Workspace layout (byte offsets, each region 256-byte aligned):
+//   states  per-chunk states, fp32 [B][G][s][e]
+//   prefix  state prefix sums / n, Gp = G (causal) or 1 (bidirectional) chunks
+//           of [s][e]; fp32 on the SIMT path, bf16 on the tensor-core path
+//   scores  intra-chunk relu^2 weights, bf16 [B*n][C] (tensor-core path)
+//   lin_q   T2 = Z*gamma2 + beta2, bf16 [B*n][s] (tensor-core path)
+//   sched   work counter of the persistent attention kernel (tensor-core path)
+struct WorkspaceLayout {
+  size_t states, prefix, scores, lin_q, sched, total;
+};
+inline WorkspaceLayout workspace_layout(int B, int n, int s, int e, int C, int causal) {
   const size_t G = (size_t)(n / C);
   const size_t se = (size_t)s * (size_t)e;
   const size_t Gp = causal ? G : 1;
-  return align256(sizeof(float) * (size_t)B * G * se) +
-         align256(sizeof(float) * (size_t)B * Gp * se);
+  WorkspaceLayout L;
+  L.states = 0;
+  L.prefix = L.states + align256(sizeof(float) * (size_t)B * G * se);
+  L.scores = L.prefix + align256(sizeof(float) * (size_t)B * Gp * se);
+  L.lin_q = L.scores + align256(2 * (size_t)B * n * (size_t)C);
+  L.sched = L.lin_q + align256(2 * (size_t)B * n * (size_t)s);
+  L.total = L.sched + 256;
+  return L;
+}
+inline size_t workspace_bytes(int B, int n, int s, int e, int C, int causal) {
+  return workspace_layout(B, n, s, e, C, causal).total;
 }
 
-// Both return 0 on success, nonzero when a launch failed.
 // `events` (may be NULL) holds launch-count + 1 cudaEvent_t handles recorded
 // before the first kernel and after each kernel.
 int launch_simt_forward(const void *Z, const void *V, const void *U, const float *gamma,

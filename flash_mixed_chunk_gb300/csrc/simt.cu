@@ -259,11 +259,9 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
                         const float *beta, void *O, int B, int n, int s, int e, int C,
                         int causal, int dtype_bf16, void *workspace, cudaStream_t stream,
                         cudaEvent_t const *events) {
-  const int G = n / C;
-  const size_t se = (size_t)s * e;
-  float *states = static_cast<float *>(workspace);
-  float *prefix = reinterpret_cast<float *>(static_cast<char *>(workspace) +
-                                            align256(sizeof(float) * (size_t)B * G * se));
+  const WorkspaceLayout L = workspace_layout(B, n, s, e, C, causal);
+  float *states = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.states);
+  float *prefix = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.prefix);
   if (dtype_bf16)
     return launch_simt_impl<__nv_bfloat16>(Z, V, U, gamma, beta, O, B, n, s, e, C, causal,
                                            states, prefix, stream, events);

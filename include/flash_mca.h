@@ -85,7 +85,8 @@ typedef int32_t fmca_path;
 
 /*
  * Bytes of device workspace one flash_mca_forward call with these arguments
- * needs (the per-chunk linear-attention states and their prefix sums).
+ * needs: the per-chunk linear-attention states and their prefix sums, and
+ * (tensor-core path) the bf16 intra-chunk relu^2 weights and lin_q rows.
  * Returns 0 for arguments flash_mca_forward would reject.
  */
 size_t flash_mca_workspace_bytes(int B, int n, int s, int e, int C, int causal,
@@ -123,8 +124,9 @@ fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
  * (cudaEvent_t handles) on `stream` around its kernels: events[0] before the
  * first kernel and events[i] after kernel i (1-based), so `n_events` must be
  * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
- * stream it runs on.  Kernel order: chunk states, state scan, chunk
- * attention (both paths). */
+ * stream it runs on.  Kernel order: tensor-core path -- chunk scores,
+ * chunk states, state scan, chunk attention; SIMT path -- chunk states,
+ * state scan, chunk output. */
 fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     const float *gamma, const float *beta, void *O, int B,
                                     int n, int s, int e, int C, int causal,

@@ -57,7 +57,8 @@ def test_status_strings():
 def test_workspace_bytes_formula(B, n, s, e, C, causal):
     a = lambda x: (x + 255) // 256 * 256
     G = n // C
-    want = a(4 * B * G * s * e) + a(4 * B * (G if causal else 1) * s * e)
+    want = (a(4 * B * G * s * e) + a(4 * B * (G if causal else 1) * s * e)
+            + a(2 * B * n * C) + a(2 * B * n * s) + 256)
     for dt in (fm.FMCA_F32, fm.FMCA_BF16):
         assert fm.flash_mca_workspace_bytes(B, n, s, e, C, causal, dt) == want
 
@@ -85,7 +86,7 @@ def test_auto_path_choice():
 
 def test_launch_counts():
     bf = fm.FMCA_BF16
-    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 3
+    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 4
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
     assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
     assert fm.flash_mca_launch_count(1, 500, 128, 256, 64, 1, bf) == 0
