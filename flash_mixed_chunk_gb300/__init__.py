@@ -23,7 +23,8 @@ __all__ = [
     "flash_mca_workspace_bytes", "flash_mca_forward", "flash_mca_forward_path",
     "flash_mca_forward_timed",
     "flash_mca_auto_path", "flash_mca_launch_count", "flash_mca_host_arena_bytes",
-    "flash_mca_forward_host", "flash_mca_device_status", "flash_mca_selftest_timeout",
+    "flash_mca_forward_host", "flash_mca_forward_noalloc", "flash_mca_device_status",
+    "flash_mca_selftest_timeout", "FMCA_NOALLOC_SCRATCH_BYTES",
     "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
 ]
 
@@ -31,6 +32,7 @@ FMCA_OK, FMCA_ERR_INVALID_ARG, FMCA_ERR_SHAPE, FMCA_ERR_UNSUPPORTED = 0, 1, 2, 3
 FMCA_ERR_ALIGN, FMCA_ERR_WORKSPACE, FMCA_ERR_CUDA, FMCA_ERR_TIMEOUT = 4, 5, 6, 7
 FMCA_F32, FMCA_BF16 = 0, 1
 FMCA_PATH_AUTO, FMCA_PATH_SIMT, FMCA_PATH_TCGEN05 = 0, 1, 2
+FMCA_NOALLOC_SCRATCH_BYTES = 64 << 20  # size of the fixed scratch of flash_mca_forward_noalloc
 
 library_path = _build.LIB
 
@@ -58,6 +60,7 @@ _SIGNATURES = [
     ("flash_mca_launch_count", _int, [_int] * 6 + [_i32, _i32]),
     ("flash_mca_host_arena_bytes", _sz, [_int] * 6 + [_i32]),
     ("flash_mca_forward_host", _i32, _fwd_args + [_vp]),
+    ("flash_mca_forward_noalloc", _i32, _fwd_args[:13] + [_vp]),
     ("flash_mca_device_status", _i32, [_vp, ctypes.POINTER(_i32)]),
     ("flash_mca_selftest_timeout", _i32, [_int, _vp]),
     ("flash_mca_status_string", _cp, [_i32]),
@@ -205,6 +208,19 @@ def flash_mca_forward_host(Z, V, U, gamma, beta, O, C: int, causal: bool, arena,
                                     int(bool(causal)), dt, arena.data_ptr(),
                                     arena.numel() * arena.element_size(), _stream_ptr(stream))
     _check(st, "flash_mca_forward_host")
+
+
+def flash_mca_forward_noalloc(Z, V, U, gamma, beta, O, C: int, causal: bool,
+                              stream=None) -> None:
+    """The C entry point of the same name: the forward pass with its scratch
+    in a fixed array inside the library, for callers that cannot allocate
+    device memory (see include/flash_mca.h).  Only the output is passed."""
+    B, n, s, e = _shapes(Z, V, U)
+    dt = _dtype_code(Z)
+    st = lib.flash_mca_forward_noalloc(Z.data_ptr(), V.data_ptr(), U.data_ptr(),
+                                       gamma.data_ptr(), beta.data_ptr(), O.data_ptr(), B, n, s,
+                                       e, int(C), int(bool(causal)), dt, _stream_ptr(stream))
+    _check(st, "flash_mca_forward_noalloc")
 
 
 def flash_mca_device_status(stream=None) -> tuple[int, int]:

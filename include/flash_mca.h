@@ -162,6 +162,36 @@ fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *h
                                    fmca_dtype dtype, void *device_arena,
                                    size_t arena_bytes, fmca_stream_t stream);
 
+/*
+ * flash_mca_forward without a caller-provided workspace, for callers that
+ * cannot allocate device memory: code running inside a host framework that
+ * owns all device memory and only lends out the tensors it manages, code that
+ * must not call cudaMalloc (an allocation lock held elsewhere, or a hard rule
+ * against failing half-way on an out-of-memory error).  The computation has no
+ * counterpart on the pages: it is the same forward pass, only the scratch
+ * comes from a fixed array inside the library.
+ *
+ * The scratch is one array of FMCA_NOALLOC_SCRATCH_BYTES compiled into the
+ * library; a GPU keeps it until the process exits once this entry point has
+ * run there.  Problems whose workspace (flash_mca_workspace_bytes) exceeds it
+ * are rejected with FMCA_ERR_WORKSPACE; the long_causal-sized problems (B=2,
+ * n=8192, e=1536) need more and must use flash_mca_forward.  Only the
+ * tensor-core path is available (FMCA_BF16, s == 128, C in {128, 256},
+ * e % 256 == 0); other shapes return FMCA_ERR_UNSUPPORTED.
+ *
+ * The first call on a device looks up the array's device address on that
+ * device (the current one); make that first call before any CUDA stream
+ * capture begins.  All calls on a device share the array: calls whose work
+ * overlaps on the GPU (different streams) race and give wrong results; calls
+ * queued on one stream are ordered.  The call allocates nothing, queues its
+ * kernels on `stream` and does not wait.  Arguments as for flash_mca_forward.
+ */
+#define FMCA_NOALLOC_SCRATCH_BYTES ((size_t)64 << 20) /* 64 MiB */
+fmca_status flash_mca_forward_noalloc(const void *Z, const void *V, const void *U,
+                                      const float *gamma, const float *beta, void *O,
+                                      int B, int n, int s, int e, int C, int causal,
+                                      fmca_dtype dtype, fmca_stream_t stream);
+
 /* Status recorded by the kernels on the current device since the last call of
  * this function (FMCA_OK or FMCA_ERR_TIMEOUT); waits for `stream`, then
  * clears the record.  *where (if not NULL) receives a code naming the wait
