@@ -108,7 +108,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   const int Gp = causal ? G : 1;
   const WorkspaceLayout L = workspace_layout(B, n, s, e, C, causal);
   char *ws = static_cast<char *>(workspace);
-  float *states = reinterpret_cast<float *>(ws + L.states);
+  __nv_bfloat16 *states = reinterpret_cast<__nv_bfloat16 *>(ws + L.states);
   __nv_bfloat16 *prefix = reinterpret_cast<__nv_bfloat16 *>(ws + L.prefix);
   void *pw = ws + L.scores;
   void *t2 = ws + L.lin_q;
@@ -135,20 +135,23 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     attrs = true;
   }
   if (!record_event(events, 0, stream)) return 1;
-  tc_chunk_scores<<<B * G * R, SC_THREADS, SC_SMEM, stream>>>(mZ, mPw, mT2, gamma, beta, n, C, G,
-                                                              causal);
+  // sched[0]: work counter of tc_chunk_state (zeroed by tc_chunk_scores);
+  // sched[1]: work counter of tc_chunk_attn (zeroed by tc_state_scan)
+  tc_chunk_scores<<<B * G * R, SC_THREADS, SC_SMEM, stream>>>(mZ, mPw, mT2, gamma, beta, sched, n,
+                                                              C, G, causal);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
-  tc_chunk_state<<<B * G * (e / E_TILE), STATE_THREADS, STATE_SMEM, stream>>>(
-      mZs, mVs, gamma, beta, states, n, e, C, G);
+  const int st_units = B * G * (e / E_TILE);
+  tc_chunk_state<<<st_units < num_sms() ? st_units : num_sms(), STATE_THREADS, STATE_SMEM, stream>>>(
+      mZs, mVs, gamma, beta, states, sched, n, e, C, G, st_units);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 2, stream)) return 1;
   const int64_t lanes = (int64_t)B * se / 8;
   tc_state_scan<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(
-      states, prefix, B, G, se, 1.0f / (float)n, causal, sched);
+      states, prefix, B, G, se, 1.0f / (float)n, causal, sched + 1);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 3, stream)) return 1;
   const int n_units = B * G * R * (e / E_TILE);
   const int grid = n_units < num_sms() ? n_units : num_sms();
-  tc_chunk_attn<<<grid, AT_THREADS, AT_SMEM, stream>>>(mPw, mT2, mV, mS, mU, mO, sched, n, e, C, G,
-                                                       causal, n_units);
+  tc_chunk_attn<<<grid, AT_THREADS, AT_SMEM, stream>>>(mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C,
+                                                       G, causal, n_units);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 4, stream)) return 1;
   return 0;
 }

@@ -26,8 +26,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1)
     tc_chunk_scores(const __grid_constant__ CUtensorMap mapZ,   // Z [B*n][s], box {64,128}
                     const __grid_constant__ CUtensorMap mapPw,  // P [B*n][C], box {64,128}
                     const __grid_constant__ CUtensorMap mapT2,  // T2 [B*n][s], box {64,128}
-                    const float *__restrict__ gamma, const float *__restrict__ beta, int n,
-                    int C, int G, int causal) {
+                    const float *__restrict__ gamma, const float *__restrict__ beta,
+                    unsigned int *__restrict__ state_sched, int n, int C, int G, int causal) {
+  // the state kernel that follows on the stream hands out work from here
+  if (blockIdx.x == 0 && threadIdx.x == 0) *state_sched = 0u;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

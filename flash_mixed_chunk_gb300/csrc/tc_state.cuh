@@ -1,5 +1,8 @@
 // tc_state.cuh -- per-chunk linear-attention states and their chunk-axis
-// prefix (included by tc.cu; device code of the tensor-core path).
+// prefix ("FLASH: Possibly the Most Interesting Efficient Transformer Design
+// Recently", section "Mixed Chunk": the summands K^lin_h^T V_h of V-hat^lin_g
+// and their sum over all chunks, or cumsum over the chunks before g for a
+// decoder).  Device code of the tensor-core path, included by tc.cu.
 #pragma once
 
 #include "tc_common.cuh"
@@ -8,56 +11,66 @@ namespace fmca {
 namespace {
 
 // =====================================================================
-// tc_chunk_state: one CTA per (b, g, 256-column slice of e)
+// tc_chunk_state: state_h = T3_h^T V_h, T3 = Z * gamma3 + beta3
 // =====================================================================
-// shared memory: NSLOT_STATE slots of [Z: 64 keys x 128 s (2 boxes of 8 KB)]
-//                                   + [V: 64 keys x 256 e (4 boxes of 8 KB)]
-constexpr int STATE_NSLOT = 2;
-constexpr uint32_t STATE_Z_BYTES = KEY_STAGE * S_DIM * 2;      // 16 KB
-constexpr uint32_t STATE_V_BYTES = KEY_STAGE * E_TILE * 2;     // 32 KB
-constexpr uint32_t STATE_SLOT = STATE_Z_BYTES + STATE_V_BYTES; // 48 KB
-constexpr uint32_t STATE_SMEM = STATE_NSLOT * STATE_SLOT + 1024;
-constexpr int STATE_THREADS = 192;  // warp0 TMA, warp1 MMA, warps 2-5 math
+// Persistent: one CTA per SM takes units (chunk h, 256-column slice of e)
+// from a counter (zeroed by tc_chunk_scores, which runs first).  A unit
+// streams C/64 items [Z: 64 keys x 128 s (16 KB) | V: 64 keys x 256 e (32 KB)]
+// through a four-slot ring.  Four transform warps turn each item's Z part into
+// T3 in place; the MMA warp accumulates D[s][e] = T3^T V over the unit's keys
+// in TMEM (A = the T3 tile as an MN-major operand, B = the V tile, both
+// MN-major); four epilogue warps write D to the workspace as bf16.  The
+// accumulator is double-buffered so a unit's epilogue overlaps the next
+// unit's MMAs.  Each barrier has a single consumer.
+constexpr int ST_RING = 4;
+constexpr uint32_t ST_Z_BYTES = KEY_STAGE * S_DIM * 2;   // 16 KB
+constexpr uint32_t ST_SLOT = ST_Z_BYTES + KEY_STAGE * E_TILE * 2;  // 48 KB
+constexpr uint32_t STATE_SMEM = ST_RING * ST_SLOT + 1024;
+constexpr int ST_QUEUE = 2;
+// warp 0: scheduler + TMA; warp 1: MMA; warps 2-5: T3 transform;
+// warps 6-9: epilogue
+constexpr int STATE_THREADS = 320;
+static_assert(STATE_SMEM + 1024 <= 232448, "tc_chunk_state exceeds 227 KB of shared memory");
 
 __global__ void __launch_bounds__(STATE_THREADS, 1)
-    tc_chunk_state(const __grid_constant__ CUtensorMap mapZ,   // box {64, 64}
-                   const __grid_constant__ CUtensorMap mapV,   // box {64, 64}
+    tc_chunk_state(const __grid_constant__ CUtensorMap mapZ,   // Z [B*n][s], box {64, 64}
+                   const __grid_constant__ CUtensorMap mapV,   // V [B*n][e], box {64, 64}
                    const float *__restrict__ gamma, const float *__restrict__ beta,
-                   float *__restrict__ states, int n, int e, int C, int G) {
+                   __nv_bfloat16 *__restrict__ states, unsigned int *__restrict__ sched, int n,
+                   int e, int C, int G, int n_units) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  __shared__ __align__(8) uint64_t full[STATE_NSLOT], tready[STATE_NSLOT], empty[STATE_NSLOT];
-  __shared__ __align__(8) uint64_t dfull, mma_done;
+  __shared__ __align__(8) uint64_t full[ST_RING], tready[ST_RING], empty[ST_RING];
+  __shared__ __align__(8) uint64_t q_full[ST_QUEUE], q_empty[ST_QUEUE];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
+  __shared__ int q_unit[ST_QUEUE], acc_unit[2], slot_valid[ST_RING];
   __shared__ uint32_t tmem_base;
-  __shared__ float g3[S_DIM], b3[S_DIM];
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_es = e / E_TILE;
-  const int es = blockIdx.x % n_es;
-  const int bg = blockIdx.x / n_es;
-  const int b = bg / G, g = bg % G;
-  const int e0 = es * E_TILE;
-  const int row0 = b * n + g * C;
   const int nstage = C / KEY_STAGE;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < STATE_NSLOT; ++i) {
+    for (int i = 0; i < ST_RING; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&tready[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&dfull, 1);
+    for (int i = 0; i < ST_QUEUE; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 2);  // tcgen05.commit + the MMA thread's arrive
+      mbar_init(&acc_empty[i], 1);
+    }
     mbar_init(&mma_done, 1);
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base, 256);
+    tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
-  }
-  for (int i = threadIdx.x; i < S_DIM; i += STATE_THREADS) {
-    g3[i] = gamma[3 * S_DIM + i];
-    b3[i] = beta[3 * S_DIM + i];
   }
   tc_fence_before();
   __syncthreads();
@@ -65,190 +78,243 @@ __global__ void __launch_bounds__(STATE_THREADS, 1)
   const uint32_t tbase = tmem_base;
 
   if (warp == 0) {
-    // ---------------- TMA producer
+    // =========================== scheduler + TMA producer
     if (lane == 0) {
       tma_prefetch_desc(&mapZ);
       tma_prefetch_desc(&mapV);
-      int issued = 0;
-      for (int q = 0; q < nstage; ++q) {
-        const int slot = q % STATE_NSLOT;
-        if (q >= STATE_NSLOT) {
-          if (!mbar_wait(&empty[slot], ((q / STATE_NSLOT) - 1) & 1, kWaitLimitNs)) {
-            record_timeout(101);
+      int it = 0;
+      bool ok = true, ended = false;
+      for (int i = 0; ok; ++i) {
+        const int u = (int)atomicAdd(sched, 1u);
+        const int uu = u < n_units ? u : -1;
+        const int qs = i % ST_QUEUE;
+        if (i >= ST_QUEUE && !mbar_wait(&q_empty[qs], ((i / ST_QUEUE) - 1) & 1, kWaitLimitNs)) {
+          record_timeout(500);
+          break;
+        }
+        q_unit[qs] = uu;
+        mbar_arrive(&q_full[qs]);
+        // one more ring item than real work: an empty one tells the
+        // transform warps that the stream has ended
+        const int es = uu < 0 ? 0 : uu % n_es;
+        const int hb = uu < 0 ? 0 : uu / n_es;  // b*G + h
+        const int row0 = (hb / G) * n + (hb % G) * C;
+        const int items = uu < 0 ? 1 : nstage;
+        for (int k = 0; k < items; ++k, ++it) {
+          const int slot = it % ST_RING;
+          if (it >= ST_RING &&
+              !mbar_wait(&empty[slot], ((it / ST_RING) - 1) & 1, kWaitLimitNs)) {
+            record_timeout(501);
+            ok = false;
             break;
           }
+          if (uu < 0) {
+            slot_valid[slot] = 0;
+            mbar_arrive(&full[slot]);
+            ended = true;
+            break;
+          }
+          slot_valid[slot] = 1;
+          uint8_t *sz = smem + slot * ST_SLOT;
+          mbar_arrive_expect_tx(&full[slot], ST_SLOT);
+          const int y = row0 + k * KEY_STAGE;
+          tma_load_2d(sz, &mapZ, &full[slot], 0, y);
+          tma_load_2d(sz + 8192, &mapZ, &full[slot], 64, y);
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(sz + ST_Z_BYTES + j * 8192, &mapV, &full[slot], es * E_TILE + 64 * j, y);
         }
-        uint8_t *sz = smem + slot * STATE_SLOT;
-        uint8_t *sv = sz + STATE_Z_BYTES;
-        mbar_arrive_expect_tx(&full[slot], STATE_SLOT);
-        const int y = row0 + q * KEY_STAGE;
-        tma_load_2d(sz, &mapZ, &full[slot], 0, y);
-        tma_load_2d(sz + 8192, &mapZ, &full[slot], 64, y);
-        for (int i = 0; i < 4; ++i) tma_load_2d(sv + i * 8192, &mapV, &full[slot], e0 + 64 * i, y);
-        issued = q + 1;
+        if (uu < 0) break;
       }
-      // drain: every issued stage has landed before this CTA may exit
-      for (int q = (issued > STATE_NSLOT ? issued - STATE_NSLOT : 0); q < issued; ++q)
-        if (!mbar_wait(&full[q % STATE_NSLOT], (q / STATE_NSLOT) & 1, kWaitLimitNs))
-          record_timeout(102);
+      // After a normal end the transform warps have waited on every item, so
+      // every copy has landed.  After a timeout, wait (bounded) for the last
+      // copy issued into each slot.  (Not after a normal end: the end marker
+      // moved one slot's barrier a phase further.)
+      if (!ended)
+        for (int q = (it > ST_RING ? it - ST_RING : 0); q < it; ++q)
+          if (!mbar_wait(&full[q % ST_RING], (q / ST_RING) & 1, kWaitLimitNs)) record_timeout(502);
     }
   } else if (warp == 1) {
-    // ---------------- MMA issuer
+    // =========================== MMA issuer
     if (lane == 0) {
-      // D_h^T[e][s] += V^T[e][k] * T3[k][s]   (A: V tile, MN-major;
-      // B: T3 tile, MN-major), M = 128 (e), N = 128 (s), K = 16 keys per op.
-      constexpr uint32_t idesc = idesc_bf16_f32(128, 128, true, true);
+      // D[s][e] += T3^T[s][k] V[k][e]: M = 128 (s), N = 256 (e), K = 16 keys per op
+      constexpr uint32_t idesc = idesc_bf16_f32(128, E_TILE, true, true);
+      int it = 0, j = 0;
       bool ok = true;
-      for (int q = 0; q < nstage && ok; ++q) {
-        const int slot = q % STATE_NSLOT;
-        if (!mbar_wait(&tready[slot], (q / STATE_NSLOT) & 1, kWaitLimitNs)) {
-          record_timeout(103);
+      for (;; ++j) {
+        const int qs = j % ST_QUEUE;
+        if (!mbar_wait(&q_full[qs], (j / ST_QUEUE) & 1, kWaitLimitNs)) {
+          record_timeout(510);
           ok = false;
           break;
         }
-        tc_fence_after();
-        const uint32_t sz = smem_u32(smem + slot * STATE_SLOT);
-        const uint32_t sv = sz + STATE_Z_BYTES;
-        for (int kk = 0; kk < KEY_STAGE / 16; ++kk) {
-          const uint64_t bdesc = smem_desc_sw128(sz + kk * 2048, 8192, 1024);
-          for (int h = 0; h < 2; ++h) {
-            const uint64_t adesc = smem_desc_sw128(sv + h * 16384 + kk * 2048, 8192, 1024);
-            mma_bf16_ss(tbase + h * 128, adesc, bdesc, idesc, (q | kk) != 0);
-          }
+        const int u = q_unit[qs];
+        mbar_arrive(&q_empty[qs]);
+        const int buf = j & 1, use = j >> 1;
+        if (use >= 1 && !mbar_wait(&acc_empty[buf], (use - 1) & 1, kWaitLimitNs)) {
+          record_timeout(511);
+          ok = false;
+          break;
         }
-        mma_commit(&empty[slot]);
-      }
-      mma_commit(&dfull);
-      // every MMA has finished before TMEM is released
-      mma_commit(&mma_done);
-      if (!mbar_wait(&mma_done, 0, kWaitLimitNs)) record_timeout(106);
-    }
-  } else {
-    // ---------------- math warps: T3 in place, then the epilogue
-    const int mt = threadIdx.x - 64;  // 0..127
-    bool ok = true;
-    for (int q = 0; q < nstage; ++q) {
-      const int slot = q % STATE_NSLOT;
-      const bool got = mbar_wait(&full[slot], (q / STATE_NSLOT) & 1, kWaitLimitNs);
-      if (got) {
-        uint8_t *sz = smem + slot * STATE_SLOT;
-        // 2 boxes x 64 rows x 8 chunks of 16 B = 1024 chunks
-        for (int x = mt; x < 1024; x += 128) {
-          const int box = x >> 9, r = (x >> 3) & 63, p = x & 7;
-          uint4 *ptr = reinterpret_cast<uint4 *>(sz + box * 8192 + r * 128 + p * 16);
-          uint4 v = *ptr;
-          const int c = box * 64 + ((p ^ (r & 7)) << 3);
-          uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            float lo = bf16_lo(w[i]) * g3[c + 2 * i] + b3[c + 2 * i];
-            float hi = bf16_hi(w[i]) * g3[c + 2 * i + 1] + b3[c + 2 * i + 1];
-            w[i] = pack_bf16x2(lo, hi);
+        if (u < 0) break;
+        tc_fence_after();
+        const uint32_t dcol = tbase + (uint32_t)buf * 256u;
+        for (int k = 0; k < nstage; ++k, ++it) {
+          const int slot = it % ST_RING;
+          if (!mbar_wait(&tready[slot], (it / ST_RING) & 1, kWaitLimitNs)) {
+            record_timeout(512);
+            ok = false;
+            break;
           }
-          *ptr = make_uint4(w[0], w[1], w[2], w[3]);
+          tc_fence_after();
+          const uint32_t sz = smem_u32(smem + slot * ST_SLOT);
+#pragma unroll
+          for (int kk = 0; kk < KEY_STAGE / 16; ++kk) {
+            const uint64_t ad = smem_desc_sw128(sz + kk * 2048, 8192, 1024);
+            const uint64_t bd = smem_desc_sw128(sz + ST_Z_BYTES + kk * 2048, 8192, 1024);
+            mma_bf16_ss(dcol, ad, bd, idesc, (k | kk) != 0);
+          }
+          mma_commit(&empty[slot]);
+        }
+        if (!ok) break;
+        acc_unit[buf] = u;
+        mbar_arrive(&acc_full[buf]);
+        mma_commit(&acc_full[buf]);
+      }
+      if (ok) {
+        const int buf = j & 1;
+        acc_unit[buf] = -1;
+        mbar_arrive(&acc_full[buf]);
+        mma_commit(&acc_full[buf]);
+      }
+      mma_commit(&mma_done);
+      if (!mbar_wait(&mma_done, 0, kWaitLimitNs)) record_timeout(513);
+    }
+  } else if (warp < 6) {
+    // =========================== T3 transform warps (128 threads)
+    const int mt = threadIdx.x - 64;
+    // chunk x = mt + 128 i of a Z stage: box i / 4, row (mt / 8 + 16 i) % 64,
+    // physical 16-byte chunk mt % 8, i.e. logical columns 64 box + cl .. + 7
+    const int p = mt & 7, rb = mt >> 3;
+    const int cl = (p ^ (rb & 7)) << 3;
+    float g3[2][8], b3[2][8];
+#pragma unroll
+    for (int bx = 0; bx < 2; ++bx) {
+      load8(gamma + 3 * S_DIM + bx * 64 + cl, g3[bx]);
+      load8(beta + 3 * S_DIM + bx * 64 + cl, b3[bx]);
+    }
+    for (int it = 0;; ++it) {
+      const int slot = it % ST_RING;
+      const bool got = mbar_wait(&full[slot], (it / ST_RING) & 1, kWaitLimitNs);
+      const bool valid = got && slot_valid[slot] != 0;
+      if (valid) {
+        uint8_t *sz = smem + slot * ST_SLOT;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int bx = i >> 2, r = (rb + 16 * i) & 63;
+          uint4 *ptr = reinterpret_cast<uint4 *>(sz + bx * 8192 + r * 128 + p * 16);
+          *ptr = affine8(*ptr, g3[bx], b3[bx]);
         }
         fence_proxy_async_smem();
       }
-      ok = named_bar_and(1, 128, got);
-      if (!ok) {
-        if (mt == 0) record_timeout(104);
+      if (!named_bar_and(1, 128, valid)) {
+        if (!got && mt == 0) record_timeout(520);
         break;
       }
       if (mt == 0) mbar_arrive(&tready[slot]);
+      __syncwarp();
     }
-    // epilogue: thread = e row of D^T, 2 halves x 4 chunks of 32 s columns
-    if (ok && mbar_wait(&dfull, 0, kWaitLimitNs)) {
-      tc_fence_after();
-      const int quad = warp & 3;
-      const int e_idx = e0 + quad * 32 + lane;
-      float *dst = states + (size_t)bg * S_DIM * e;
-      for (int h = 0; h < 2; ++h) {
-        for (int c = 0; c < S_DIM / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tbase + ((uint32_t)(quad * 32) << 16) + h * 128 + c * 32, r);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            dst[(size_t)(c * 32 + i) * e + e_idx + h * 128] = __uint_as_float(r[i]);
-        }
+  } else {
+    // =========================== epilogue warps (128 threads)
+    const int mt = threadIdx.x - 192;
+    const int quad = warp & 3;
+    const int srow = quad * 32 + lane;  // accumulator row = state row s
+    for (int j = 0;; ++j) {
+      const int buf = j & 1, use = j >> 1;
+      const bool got = mbar_wait(&acc_full[buf], use & 1, kWaitLimitNs);
+      const int u = got ? acc_unit[buf] : -1;
+      if (!named_bar_and(2, 128, u >= 0)) {
+        if (!got && mt == 0) record_timeout(530);
+        break;
       }
-    } else if (ok) {
-      record_timeout(105);
+      tc_fence_after();
+      const int es = u % n_es, hb = u / n_es;
+      __nv_bfloat16 *dst = states + ((size_t)hb * S_DIM + srow) * e + es * E_TILE;
+      const uint32_t dcol = tbase + (uint32_t)buf * 256u + ((uint32_t)(quad * 32) << 16);
+#pragma unroll 1
+      for (int c = 0; c < E_TILE / 32; ++c) {
+        uint32_t r[32];
+        tmem_ld32(dcol + c * 32, r);
+        tmem_ld_wait();
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
+                             pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
+                             pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
+                             pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+      }
+      tc_fence_before();
+      named_bar_sync(2, 128);
+      if (mt == 0) mbar_arrive(&acc_empty[buf]);
+      __syncwarp();
     }
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) tmem_dealloc(tbase, 256);
+  if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
 // =====================================================================
-// tc_state_scan: prefix (or total) over chunks, scaled by 1/n, to bf16
+// tc_state_scan: prefix (or total) over chunks of the bf16 states, in fp32,
+// scaled by 1/n and rounded to bf16; also zeroes the attention kernel's work
+// counter (it runs right after on the same stream)
 // =====================================================================
 __global__ void __launch_bounds__(256)
-    tc_state_scan(const float *__restrict__ S, __nv_bfloat16 *__restrict__ P, int B, int G,
-                  int64_t se, float inv_n, int causal, unsigned int *__restrict__ sched) {
-  // the attention kernel that follows on the stream hands out work from here
+    tc_state_scan(const __nv_bfloat16 *__restrict__ S, __nv_bfloat16 *__restrict__ P, int B,
+                  int G, int64_t se, float inv_n, int causal, unsigned int *__restrict__ sched) {
   if (blockIdx.x == 0 && threadIdx.x == 0) *sched = 0u;
   const int64_t per_b = se / 8;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * per_b) return;
   const int64_t b = t / per_b, x = (t % per_b) * 8;
-  const float *src = S + b * G * se + x;
+  const __nv_bfloat16 *src = S + b * G * se + x;
+  __nv_bfloat16 *dst = P + (causal ? b * G * se : b * se) + x;
   float run[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) run[i] = 0.f;
-  constexpr int U = 4;
-  if (causal) {
-    __nv_bfloat16 *dst = P + b * G * se + x;
-    for (int g0 = 0; g0 < G; g0 += U) {
-      float4 v[U][2];
+  constexpr int U = 8;
+  for (int g0 = 0; g0 < G; g0 += U) {
+    uint4 v[U];
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (g0 + u < G) {
-          const float4 *p4 = reinterpret_cast<const float4 *>(src + (int64_t)(g0 + u) * se);
-          v[u][0] = __ldcs(p4);
-          v[u][1] = __ldcs(p4 + 1);
-        }
-      }
+    for (int u = 0; u < U; ++u)
+      if (g0 + u < G) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)(g0 + u) * se));
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (g0 + u < G) {
+    for (int u = 0; u < U; ++u) {
+      if (g0 + u < G) {
+        if (causal) {
           uint4 o;
           o.x = pack_bf16x2(run[0] * inv_n, run[1] * inv_n);
           o.y = pack_bf16x2(run[2] * inv_n, run[3] * inv_n);
           o.z = pack_bf16x2(run[4] * inv_n, run[5] * inv_n);
           o.w = pack_bf16x2(run[6] * inv_n, run[7] * inv_n);
           *reinterpret_cast<uint4 *>(dst + (int64_t)(g0 + u) * se) = o;
-          run[0] += v[u][0].x; run[1] += v[u][0].y; run[2] += v[u][0].z; run[3] += v[u][0].w;
-          run[4] += v[u][1].x; run[5] += v[u][1].y; run[6] += v[u][1].z; run[7] += v[u][1].w;
+        }
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          run[2 * i] += bf16_lo(w[i]);
+          run[2 * i + 1] += bf16_hi(w[i]);
         }
       }
     }
-  } else {
-    for (int g0 = 0; g0 < G; g0 += U) {
-      float4 v[U][2];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (g0 + u < G) {
-          const float4 *p4 = reinterpret_cast<const float4 *>(src + (int64_t)(g0 + u) * se);
-          v[u][0] = __ldcs(p4);
-          v[u][1] = __ldcs(p4 + 1);
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        if (g0 + u < G) {
-          run[0] += v[u][0].x; run[1] += v[u][0].y; run[2] += v[u][0].z; run[3] += v[u][0].w;
-          run[4] += v[u][1].x; run[5] += v[u][1].y; run[6] += v[u][1].z; run[7] += v[u][1].w;
-        }
-      }
-    }
+  }
+  if (!causal) {
     uint4 o;
     o.x = pack_bf16x2(run[0] * inv_n, run[1] * inv_n);
     o.y = pack_bf16x2(run[2] * inv_n, run[3] * inv_n);
     o.z = pack_bf16x2(run[4] * inv_n, run[5] * inv_n);
     o.w = pack_bf16x2(run[6] * inv_n, run[7] * inv_n);
-    *reinterpret_cast<uint4 *>(P + b * se + x) = o;
+    *reinterpret_cast<uint4 *>(dst) = o;
   }
 }
 
