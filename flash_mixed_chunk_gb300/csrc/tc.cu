@@ -114,9 +114,10 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   void *t2 = ws + L.lin_q;
   unsigned int *sched = reinterpret_cast<unsigned int *>(ws + L.sched);
 
-  CUtensorMap mZs, mVs, mZ, mPw, mT2, mV, mS, mU, mO;
+  CUtensorMap mZs, mVs, mSt, mZ, mPw, mT2, mV, mS, mU, mO;
   const uint64_t rows = (uint64_t)B * n;
   if (!make_map_bf16(&mZs, Z, s, rows, 64, 64) || !make_map_bf16(&mVs, V, e, rows, 64, 64) ||
+      !make_map_bf16(&mSt, states, e, (uint64_t)B * G * s, 64, 128) ||
       !make_map_bf16(&mZ, Z, s, rows, 64, 128) || !make_map_bf16(&mPw, pw, C, rows, 64, 128) ||
       !make_map_bf16(&mT2, t2, s, rows, 64, 128) || !make_map_bf16(&mV, V, e, rows, 64, 64) ||
       !make_map_bf16(&mS, prefix, e, (uint64_t)B * Gp * s, 64, 64) ||
@@ -142,7 +143,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
   const int st_units = B * G * (e / E_TILE);
   tc_chunk_state<<<st_units < num_sms() ? st_units : num_sms(), STATE_THREADS, STATE_SMEM, stream>>>(
-      mZs, mVs, gamma, beta, states, sched, n, e, C, G, st_units);
+      mZs, mVs, mSt, gamma, beta, sched, n, e, C, G, st_units);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 2, stream)) return 1;
   const int64_t lanes = (int64_t)B * se / 8;
   tc_state_scan<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(

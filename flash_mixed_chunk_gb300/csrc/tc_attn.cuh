@@ -11,9 +11,10 @@
 // A unit is (chunk, 128-row tile, 256-column e tile); it streams
 //   nkv items  (P rows x 64 keys [16 KB], V 64 keys x 256 e [32 KB])
 //   2 items    (T2 rows x 64 s [16 KB], prefix 64 s rows x 256 e [32 KB])
-// through ring A (the MMA warp's only input: every operand is used once per
-// unit, so nothing stays resident across units), and its U tile in four
-// 64-column quarters through ring B (the epilogue's input, turned into O in
+// through ring A (three slots; the MMA warp's only input: every operand is
+// used once per unit, so nothing stays resident across units), and its U tile
+// in four 64-column quarters through ring B (four slots, so a unit's U tile
+// can be in flight while the previous unit's epilogue runs; turned into O in
 // place and stored with TMA).  The accumulator is double-buffered in TMEM, so
 // the epilogue of one unit overlaps the MMAs of the next.
 #pragma once
@@ -23,10 +24,10 @@
 namespace fmca {
 namespace {
 
-constexpr int AT_RING_A = 4;
+constexpr int AT_RING_A = 3;
 constexpr uint32_t AT_A_BYTES = 16384;               // A operand part of an item
 constexpr uint32_t AT_SLOT_A = AT_A_BYTES + 32768;   // + B operand part
-constexpr int AT_RING_B = 2;
+constexpr int AT_RING_B = 4;
 constexpr uint32_t AT_SLOT_B = 16384;
 constexpr int AT_QUEUE = 2;                          // unit-id queue depth
 constexpr uint32_t AT_OFF_B = AT_RING_A * AT_SLOT_A;
@@ -125,9 +126,13 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tma_prefetch_desc(&mapS);
       int ia = 0;
       bool ok = true;
+      // the next unit is fetched one unit ahead, so the atomic's latency
+      // overlaps the current unit's copies
+      int u_next = (int)atomicAdd(sched, 1u);
       for (int i = 0; ok; ++i) {
-        const int u = (int)atomicAdd(sched, 1u);
+        const int u = u_next;
         const int uu = u < n_units ? u : -1;
+        if (uu >= 0) u_next = (int)atomicAdd(sched, 1u);
         // hand the unit to the MMA warp and to the ring B producer
         const int qs = i % AT_QUEUE;
         if (i >= AT_QUEUE) {

@@ -19,13 +19,17 @@ namespace {
 // through a four-slot ring.  Four transform warps turn each item's Z part into
 // T3 in place; the MMA warp accumulates D[s][e] = T3^T V over the unit's keys
 // in TMEM (A = the T3 tile as an MN-major operand, B = the V tile, both
-// MN-major); four epilogue warps write D to the workspace as bf16.  The
-// accumulator is double-buffered so a unit's epilogue overlaps the next
-// unit's MMAs.  Each barrier has a single consumer.
+// MN-major); four epilogue warps round D to bf16 into a swizzled staging tile
+// that a TMA store writes to the workspace.  The accumulator is
+// double-buffered so a unit's epilogue overlaps the next unit's MMAs.  Each
+// barrier has a single consumer.
 constexpr int ST_RING = 4;
 constexpr uint32_t ST_Z_BYTES = KEY_STAGE * S_DIM * 2;   // 16 KB
 constexpr uint32_t ST_SLOT = ST_Z_BYTES + KEY_STAGE * E_TILE * 2;  // 48 KB
-constexpr uint32_t STATE_SMEM = ST_RING * ST_SLOT + 1024;
+constexpr int ST_STAGE_BUFS = 2;                         // epilogue staging buffers
+constexpr uint32_t ST_STAGE_BYTES = 128 * 64 * 2;        // [128 s][64 e] bf16, 16 KB
+constexpr uint32_t ST_OFF_STAGE = ST_RING * ST_SLOT;
+constexpr uint32_t STATE_SMEM = ST_OFF_STAGE + ST_STAGE_BUFS * ST_STAGE_BYTES + 1024;
 constexpr int ST_QUEUE = 2;
 // warp 0: scheduler + TMA; warp 1: MMA; warps 2-5: T3 transform;
 // warps 6-9: epilogue
@@ -35,9 +39,9 @@ static_assert(STATE_SMEM + 1024 <= 232448, "tc_chunk_state exceeds 227 KB of sha
 __global__ void __launch_bounds__(STATE_THREADS, 1)
     tc_chunk_state(const __grid_constant__ CUtensorMap mapZ,   // Z [B*n][s], box {64, 64}
                    const __grid_constant__ CUtensorMap mapV,   // V [B*n][e], box {64, 64}
+                   const __grid_constant__ CUtensorMap mapSt,  // states [B*G*s][e], box {64, 128}
                    const float *__restrict__ gamma, const float *__restrict__ beta,
-                   __nv_bfloat16 *__restrict__ states, unsigned int *__restrict__ sched, int n,
-                   int e, int C, int G, int n_units) {
+                   unsigned int *__restrict__ sched, int n, int e, int C, int G, int n_units) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -84,9 +88,13 @@ __global__ void __launch_bounds__(STATE_THREADS, 1)
       tma_prefetch_desc(&mapV);
       int it = 0;
       bool ok = true, ended = false;
+      // the next unit is fetched one unit ahead, so the atomic's latency
+      // overlaps the current unit's copies
+      int u_next = (int)atomicAdd(sched, 1u);
       for (int i = 0; ok; ++i) {
-        const int u = (int)atomicAdd(sched, 1u);
+        const int u = u_next;
         const int uu = u < n_units ? u : -1;
+        if (uu >= 0) u_next = (int)atomicAdd(sched, 1u);
         const int qs = i % ST_QUEUE;
         if (i >= ST_QUEUE && !mbar_wait(&q_empty[qs], ((i / ST_QUEUE) - 1) & 1, kWaitLimitNs)) {
           record_timeout(500);
@@ -228,6 +236,8 @@ __global__ void __launch_bounds__(STATE_THREADS, 1)
     const int mt = threadIdx.x - 192;
     const int quad = warp & 3;
     const int srow = quad * 32 + lane;  // accumulator row = state row s
+    uint8_t *stage = smem + ST_OFF_STAGE;
+    int nst = 0;  // staging tiles written so far
     for (int j = 0;; ++j) {
       const int buf = j & 1, use = j >> 1;
       const bool got = mbar_wait(&acc_full[buf], use & 1, kWaitLimitNs);
@@ -238,26 +248,40 @@ __global__ void __launch_bounds__(STATE_THREADS, 1)
       }
       tc_fence_after();
       const int es = u % n_es, hb = u / n_es;
-      __nv_bfloat16 *dst = states + ((size_t)hb * S_DIM + srow) * e + es * E_TILE;
       const uint32_t dcol = tbase + (uint32_t)buf * 256u + ((uint32_t)(quad * 32) << 16);
-#pragma unroll 1
-      for (int c = 0; c < E_TILE / 32; ++c) {
-        uint32_t r[32];
-        tmem_ld32(dcol + c * 32, r);
+      for (int q = 0; q < E_TILE / 64; ++q, ++nst) {
+        uint8_t *sb = stage + (nst % ST_STAGE_BUFS) * ST_STAGE_BYTES;
+        // the TMA store that last read this staging tile has finished reading it
+        if (mt == 0 && nst >= ST_STAGE_BUFS) bulk_wait_group_read<ST_STAGE_BUFS - 1>();
+        named_bar_sync(2, 128);
+        uint32_t r[2][32];
+        tmem_ld32(dcol + q * 64, r[0]);
+        tmem_ld32(dcol + q * 64 + 32, r[1]);
         tmem_ld_wait();
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
-          d4[q] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * q]), __uint_as_float(r[8 * q + 1])),
-                             pack_bf16x2(__uint_as_float(r[8 * q + 2]), __uint_as_float(r[8 * q + 3])),
-                             pack_bf16x2(__uint_as_float(r[8 * q + 4]), __uint_as_float(r[8 * q + 5])),
-                             pack_bf16x2(__uint_as_float(r[8 * q + 6]), __uint_as_float(r[8 * q + 7])));
+        for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const uint32_t *v = r[c2] + 8 * j4;
+            *reinterpret_cast<uint4 *>(sb + sw128_offset(srow, c2 * 64 + 16 * j4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                           pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                           pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+          }
+        fence_proxy_async_smem();
+        if (q == E_TILE / 64 - 1) tc_fence_before();
+        named_bar_sync(2, 128);
+        if (mt == 0) {
+          tma_store_2d(&mapSt, sb, es * E_TILE + 64 * q, hb * S_DIM);
+          bulk_commit_group();
+          // every epilogue thread has read this unit's accumulator
+          if (q == E_TILE / 64 - 1) mbar_arrive(&acc_empty[buf]);
+        }
+        __syncwarp();
       }
-      tc_fence_before();
-      named_bar_sync(2, 128);
-      if (mt == 0) mbar_arrive(&acc_empty[buf]);
-      __syncwarp();
     }
+    if (mt == 0) bulk_wait_group<0>();
   }
   tc_fence_before();
   __syncthreads();
