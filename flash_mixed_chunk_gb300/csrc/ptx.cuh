@@ -120,6 +120,12 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Drop a 128-byte line from L2 without writing it back (its contents become
+// undefined); for scratch that no one reads again.
+__device__ __forceinline__ void discard_l2_line(const void *p) {
+  asm volatile("discard.global.L2 [%0], 128;" ::"l"(p) : "memory");
+}
+
 // Generic-proxy writes to shared memory -> visible to the async proxy
 // (tensor cores, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

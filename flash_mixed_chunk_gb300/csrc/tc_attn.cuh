@@ -275,6 +275,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     int ib = 0;
+    // Each O store is committed as its own bulk group; a U slot is released
+    // once the store after it has been issued (wait_group.read 1), so the
+    // store's shared-memory read overlaps the next quarter's work.
     for (int j = 0;; ++j) {
       const int buf = j & 1, use = j >> 1;
       const bool acc_ok = mbar_wait(&acc_full[buf], use & 1, kWaitLimitNs);
@@ -325,8 +328,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (mt == 0) {
           tma_store_2d(&mapO, us, a.e0 + 64 * q, a.row0);
           bulk_commit_group();
-          bulk_wait_group_read<0>();
-          mbar_arrive(&emptyB[slot]);
+          if (ib > 0) {
+            bulk_wait_group_read<1>();  // the previous quarter's store has read its slot
+            mbar_arrive(&emptyB[(ib - 1) % AT_RING_B]);
+          }
           // all 128 threads have read this unit's accumulator
           if (q == E_TILE / 64 - 1) mbar_arrive(&acc_empty[buf]);
         }
@@ -334,7 +339,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       }
       if (!ok) break;
     }
-    if (mt == 0) bulk_wait_group<0>();
+    if (mt == 0) {
+      bulk_wait_group<0>();
+      if (ib > 0) mbar_arrive(&emptyB[(ib - 1) % AT_RING_B]);  // nobody waits on it; keeps the count even
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -291,7 +291,8 @@ __global__ void __launch_bounds__(STATE_THREADS, 1)
 // =====================================================================
 // tc_state_scan: prefix (or total) over chunks of the bf16 states, in fp32,
 // scaled by 1/n and rounded to bf16; also zeroes the attention kernel's work
-// counter (it runs right after on the same stream)
+// counter (it runs right after on the same stream).  The thread count is a
+// multiple of 32 for every shape this path takes (B * s * e / 8).
 // =====================================================================
 __global__ void __launch_bounds__(256)
     tc_state_scan(const __nv_bfloat16 *__restrict__ S, __nv_bfloat16 *__restrict__ P, int B,
@@ -330,6 +331,15 @@ __global__ void __launch_bounds__(256)
           run[2 * i + 1] += bf16_hi(w[i]);
         }
       }
+    }
+    // The states are dead once read: drop their lines from L2 so they are
+    // never written back (eight lanes share a 128-byte line; every lane's
+    // load has returned once the sums above used it).
+    __syncwarp();
+    if ((x & 63) == 0) {
+#pragma unroll
+      for (int u = 0; u < U; ++u)
+        if (g0 + u < G) discard_l2_line(src + (int64_t)(g0 + u) * se);
     }
   }
   if (!causal) {
