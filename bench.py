@@ -345,7 +345,7 @@ def run_ours(args, w, rank, world, device):
     value = world * tokens * args.steps / (ms / 1e3)
     flops = algorithmic_flops(w)
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
-    kernel_names = (["tc_chunk_scores", "tc_chunk_state", "tc_state_scan", "tc_chunk_attn"]
+    kernel_names = (["tc_chunk_prep", "tc_state_scan", "tc_chunk_attn"]
                     if path == fm.FMCA_PATH_TCGEN05 else
                     ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"])
     kernels = {name: {"ms": per_kernel_ms[i], "share": per_kernel_ms[i] / sum(per_kernel_ms)}

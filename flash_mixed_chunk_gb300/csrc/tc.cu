@@ -2,17 +2,17 @@
 // (sm_103a: tcgen05 MMA into TMEM, TMA-staged 128-byte-swizzled bf16 tiles,
 // mbarrier pipelines) for bf16 I/O, s = 128, C in {128, 256}, e % 256 == 0.
 //
-// Four kernels per call ("FLASH: Possibly the Most Interesting Efficient
-// Transformer Design Recently", sections "Weak Attention" and "Mixed Chunk"):
+// Per call: one memset of the two work counters and three kernels
+// ("FLASH: Possibly the Most Interesting Efficient Transformer Design
+// Recently", sections "Weak Attention" and "Mixed Chunk"):
 //
-//   tc_chunk_scores  P = relu(T0 T1^T / C)^2 (masked) and T2 = Z*gamma2+beta2
-//                    per (chunk, 128-row tile), to the workspace in bf16
-//   tc_chunk_state   state_g = T3_g^T V_g per chunk and 256-column slice of e,
-//                    fp32 [B][G][s][e] (T3 formed in shared memory)
+//   tc_chunk_prep    state_g = T3_g^T V_g per chunk and 256-column slice of e
+//                    (bf16), P = relu(T0 T1^T / C)^2 (masked) and T2 rows
+//                    (bf16), as one persistent stream of work units
 //   tc_state_scan    exclusive prefix over chunks (causal) or total
 //                    (bidirectional) of the states, times 1/n, to bf16
 //   tc_chunk_attn    O = U * (P V_g + T2 prefix_g) per (chunk, row tile,
-//                    e tiles), both products accumulated in TMEM
+//                    e tile), both products accumulated in TMEM
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -25,8 +25,8 @@
 #include "ptx.cuh"
 
 #include "tc_common.cuh"
-#include "tc_scores.cuh"
-#include "tc_state.cuh"
+#include "tc_prep.cuh"
+#include "tc_scan.cuh"
 #include "tc_attn.cuh"
 
 namespace fmca {
@@ -97,7 +97,7 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   return true;
 }
 
-int tc_launch_count() { return 4; }
+int tc_launch_count() { return 3; }
 
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
@@ -114,46 +114,45 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   void *t2 = ws + L.lin_q;
   unsigned int *sched = reinterpret_cast<unsigned int *>(ws + L.sched);
 
-  CUtensorMap mZs, mVs, mSt, mZ, mPw, mT2, mV, mS, mU, mO;
+  CUtensorMap mZ64, mZ128, mVs, mSt, mPw, mT2, mV, mS, mU, mO;
   const uint64_t rows = (uint64_t)B * n;
-  if (!make_map_bf16(&mZs, Z, s, rows, 64, 64) || !make_map_bf16(&mVs, V, e, rows, 64, 64) ||
+  if (!make_map_bf16(&mZ64, Z, s, rows, 64, 64) || !make_map_bf16(&mZ128, Z, s, rows, 64, 128) ||
+      !make_map_bf16(&mVs, V, e, rows, 64, 64) ||
       !make_map_bf16(&mSt, states, e, (uint64_t)B * G * s, 64, 128) ||
-      !make_map_bf16(&mZ, Z, s, rows, 64, 128) || !make_map_bf16(&mPw, pw, C, rows, 64, 128) ||
-      !make_map_bf16(&mT2, t2, s, rows, 64, 128) || !make_map_bf16(&mV, V, e, rows, 64, 64) ||
+      !make_map_bf16(&mPw, pw, C, rows, 64, 128) || !make_map_bf16(&mT2, t2, s, rows, 64, 128) ||
+      !make_map_bf16(&mV, V, e, rows, 64, 64) ||
       !make_map_bf16(&mS, prefix, e, (uint64_t)B * Gp * s, 64, 64) ||
       !make_map_bf16(&mU, U, e, rows, 64, 128) || !make_map_bf16(&mO, O, e, rows, 64, 128))
     return 2;
 
   static bool attrs = false;
   if (!attrs) {
-    if (cudaFuncSetAttribute(tc_chunk_scores, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SC_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_state, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)STATE_SMEM) != cudaSuccess ||
+    if (cudaFuncSetAttribute(tc_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PREP_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)AT_SMEM) != cudaSuccess)
       return 1;
     attrs = true;
   }
   if (!record_event(events, 0, stream)) return 1;
-  // sched[0]: work counter of tc_chunk_state (zeroed by tc_chunk_scores);
-  // sched[1]: work counter of tc_chunk_attn (zeroed by tc_state_scan)
-  tc_chunk_scores<<<B * G * R, SC_THREADS, SC_SMEM, stream>>>(mZ, mPw, mT2, gamma, beta, sched, n,
-                                                              C, G, causal);
+  // sched[0]: work counter of tc_chunk_prep; sched[1]: of tc_chunk_attn
+  if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
+  const int n_state = B * G * (e / E_TILE);
+  const int n_score = B * G * (causal ? R * (R + 1) : R * (C / KEY_STAGE));
+  const int n_prep = n_state + n_score;
+  tc_chunk_prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
+      mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n, e,
+      C, G, causal, n_state, n_score);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
-  const int st_units = B * G * (e / E_TILE);
-  tc_chunk_state<<<st_units < num_sms() ? st_units : num_sms(), STATE_THREADS, STATE_SMEM, stream>>>(
-      mZs, mVs, mSt, gamma, beta, sched, n, e, C, G, st_units);
-  if (cudaGetLastError() != cudaSuccess || !record_event(events, 2, stream)) return 1;
   const int64_t lanes = (int64_t)B * se / 8;
-  tc_state_scan<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(
-      states, prefix, B, G, se, 1.0f / (float)n, causal, sched + 1);
-  if (cudaGetLastError() != cudaSuccess || !record_event(events, 3, stream)) return 1;
+  tc_state_scan<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(states, prefix, B, G, se,
+                                                                     1.0f / (float)n, causal);
+  if (cudaGetLastError() != cudaSuccess || !record_event(events, 2, stream)) return 1;
   const int n_units = B * G * R * (e / E_TILE);
   const int grid = n_units < num_sms() ? n_units : num_sms();
   tc_chunk_attn<<<grid, AT_THREADS, AT_SMEM, stream>>>(mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C,
                                                        G, causal, n_units);
-  if (cudaGetLastError() != cudaSuccess || !record_event(events, 4, stream)) return 1;
+  if (cudaGetLastError() != cudaSuccess || !record_event(events, 3, stream)) return 1;
   return 0;
 }
 

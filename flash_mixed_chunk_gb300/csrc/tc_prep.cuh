@@ -1,0 +1,418 @@
+// tc_prep.cuh -- everything the output kernel needs besides the inputs, in one
+// persistent kernel ("FLASH: Possibly the Most Interesting Efficient
+// Transformer Design Recently", sections "Weak Attention" and "Mixed Chunk"):
+//
+//   state units  (chunk h, 256-column slice of e):
+//                state_h = T3_h^T V_h, T3 = Z * gamma3 + beta3, bf16 [B*G*s][e]
+//   score units  (chunk, 128-row tile, 64-key stage):
+//                P = relu(T0 T1^T / C)^2, strict upper triangle masked in causal
+//                mode, bf16 [B*n][C]; the key-stage-0 unit of each row tile also
+//                writes T2 = Z * gamma2 + beta2, bf16 [B*n][s]
+//
+// One CTA per SM takes units from a work counter (zeroed before the launch):
+// the larger state units first, the small score units last, so the score work
+// fills the state work's tail.  Every unit streams 48 KB items through one
+// four-slot ring:
+//   state item [Z: 64 keys x 128 s (16 KB) | V: 64 keys x 256 e (32 KB)]
+//   score item [Z: 128 query rows x 128 s (32 KB) | Z: 64 keys x 128 s (16 KB)]
+// Four transform warps form T3 (state) or T0, T1 and T2 (score) in place; the
+// MMA warp accumulates D = T3^T V (M = s, N = 256; both operands MN-major) or
+// S = T0 T1^T (M = 128 rows, N = 64 keys; both K-major) into one of two TMEM
+// accumulators; four epilogue warps round D (or relu(S/C)^2) to bf16 into a
+// swizzled staging tile that a TMA store writes out.  Every barrier has one
+// consumer.  Included by tc.cu.
+#pragma once
+
+#include "tc_common.cuh"
+
+namespace fmca {
+namespace {
+
+constexpr int PR_RING = 4;
+constexpr uint32_t PR_SLOT = 49152;                      // 48 KB items
+constexpr uint32_t PR_ST_Z = KEY_STAGE * S_DIM * 2;      // state: Z part, 16 KB
+constexpr uint32_t PR_SC_K = 128 * S_DIM * 2;            // score: offset of the key part
+constexpr int PR_STAGE_BUFS = 2;
+constexpr uint32_t PR_STAGE_BYTES = 128 * 64 * 2;        // [128 rows][64 cols] bf16
+constexpr uint32_t PR_OFF_STAGE = PR_RING * PR_SLOT;
+constexpr uint32_t PREP_SMEM = PR_OFF_STAGE + PR_STAGE_BUFS * PR_STAGE_BYTES + 1024;
+constexpr int PR_QUEUE = 2;
+// warp 0: scheduler + TMA; warp 1: MMA; warps 2-5: transform; warps 6-9: epilogue
+constexpr int PREP_THREADS = 320;
+static_assert(PREP_SMEM + 1024 <= 232448, "tc_chunk_prep exceeds 227 KB of shared memory");
+
+enum : int { KIND_END = 0, KIND_STATE = 1, KIND_SCORE = 2 };
+
+struct PrepUnit {
+  int kind;
+  // state: hb = b*G + h, es = 256-column slice
+  int hb, es;
+  // score: rows [row0, row0+128) of the chunk starting at crow; key stage ks
+  int crow, row0, rt, ks;
+};
+
+__device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score, int n, int e,
+                                                int C, int G, int causal) {
+  PrepUnit p;
+  p.kind = KIND_END;
+  p.hb = p.es = p.crow = p.row0 = p.rt = p.ks = 0;
+  if (u < 0) return p;
+  if (u < n_state) {
+    const int n_es = e / E_TILE;
+    p.kind = KIND_STATE;
+    p.es = u % n_es;
+    p.hb = u / n_es;
+    return p;
+  }
+  u -= n_state;
+  if (u >= n_score) return p;
+  const int R = C / ROW_TILE;
+  // causal: row tile rt covers keys [0, 128 (rt+1)); otherwise all C keys
+  const int per_chunk = causal ? R * (R + 1) : R * (C / KEY_STAGE);
+  const int bg = u / per_chunk;
+  int w = u % per_chunk;
+  int rt = 0;
+  for (;; ++rt) {
+    const int nks = (causal ? (rt + 1) * ROW_TILE : C) / KEY_STAGE;
+    if (w < nks) break;
+    w -= nks;
+  }
+  p.kind = KIND_SCORE;
+  p.crow = (bg / G) * n + (bg % G) * C;
+  p.rt = rt;
+  p.row0 = p.crow + rt * ROW_TILE;
+  p.ks = w;
+  return p;
+}
+
+__global__ void __launch_bounds__(PREP_THREADS, 1)
+    tc_chunk_prep(const __grid_constant__ CUtensorMap mapZ64,   // Z [B*n][s], box {64, 64}
+                  const __grid_constant__ CUtensorMap mapZ128,  // Z [B*n][s], box {64, 128}
+                  const __grid_constant__ CUtensorMap mapV,     // V [B*n][e], box {64, 64}
+                  const __grid_constant__ CUtensorMap mapSt,    // states [B*G*s][e], box {64, 128}
+                  const __grid_constant__ CUtensorMap mapPw,    // P [B*n][C], box {64, 128}
+                  const float *__restrict__ gamma, const float *__restrict__ beta,
+                  __nv_bfloat16 *__restrict__ t2out, unsigned int *__restrict__ sched, int n,
+                  int e, int C, int G, int causal, int n_state, int n_score) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t full[PR_RING], tready[PR_RING], empty[PR_RING];
+  __shared__ __align__(8) uint64_t q_full[PR_QUEUE], q_empty[PR_QUEUE];
+  __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
+  __shared__ int q_unit[PR_QUEUE], acc_unit[2], slot_unit[PR_RING];
+  __shared__ uint32_t tmem_base;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int n_units = n_state + n_score;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < PR_RING; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&tready[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < PR_QUEUE; ++i) {
+      mbar_init(&q_full[i], 1);
+      mbar_init(&q_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&acc_full[i], 2);  // tcgen05.commit + the MMA thread's arrive
+      mbar_init(&acc_empty[i], 1);
+    }
+    mbar_init(&mma_done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+
+  if (warp == 0) {
+    // =========================== scheduler + TMA producer
+    if (lane == 0) {
+      tma_prefetch_desc(&mapZ64);
+      tma_prefetch_desc(&mapZ128);
+      tma_prefetch_desc(&mapV);
+      int it = 0;
+      bool ok = true, ended = false;
+      // the next unit is fetched one unit ahead, so the atomic's latency
+      // overlaps the current unit's copies
+      int u_next = (int)atomicAdd(sched, 1u);
+      for (int i = 0; ok; ++i) {
+        const int uu = u_next < n_units ? u_next : -1;
+        if (uu >= 0) u_next = (int)atomicAdd(sched, 1u);
+        const int qs = i % PR_QUEUE;
+        if (i >= PR_QUEUE && !mbar_wait(&q_empty[qs], ((i / PR_QUEUE) - 1) & 1, kWaitLimitNs)) {
+          record_timeout(500);
+          break;
+        }
+        q_unit[qs] = uu;
+        mbar_arrive(&q_full[qs]);
+        const PrepUnit p = decode_prep(uu, n_state, n_score, n, e, C, G, causal);
+        // state: C/64 items; score: 1 item; end: one empty item that tells the
+        // transform warps the stream is over
+        const int items = p.kind == KIND_STATE ? C / KEY_STAGE : 1;
+        for (int k = 0; k < items; ++k, ++it) {
+          const int slot = it % PR_RING;
+          if (it >= PR_RING && !mbar_wait(&empty[slot], ((it / PR_RING) - 1) & 1, kWaitLimitNs)) {
+            record_timeout(501);
+            ok = false;
+            break;
+          }
+          slot_unit[slot] = uu;
+          if (p.kind == KIND_END) {
+            mbar_arrive(&full[slot]);
+            ended = true;
+            break;
+          }
+          uint8_t *sz = smem + slot * PR_SLOT;
+          mbar_arrive_expect_tx(&full[slot], PR_SLOT);
+          if (p.kind == KIND_STATE) {
+            const int y = (p.hb / G) * n + (p.hb % G) * C + k * KEY_STAGE;
+            tma_load_2d(sz, &mapZ64, &full[slot], 0, y);
+            tma_load_2d(sz + 8192, &mapZ64, &full[slot], 64, y);
+            for (int j = 0; j < 4; ++j)
+              tma_load_2d(sz + PR_ST_Z + j * 8192, &mapV, &full[slot], p.es * E_TILE + 64 * j, y);
+          } else {
+            tma_load_2d(sz, &mapZ128, &full[slot], 0, p.row0);
+            tma_load_2d(sz + 16384, &mapZ128, &full[slot], 64, p.row0);
+            const int y = p.crow + p.ks * KEY_STAGE;
+            tma_load_2d(sz + PR_SC_K, &mapZ64, &full[slot], 0, y);
+            tma_load_2d(sz + PR_SC_K + 8192, &mapZ64, &full[slot], 64, y);
+          }
+        }
+        if (ended) break;
+      }
+      // After a normal end the transform warps have waited on every item, so
+      // every copy has landed; after a timeout, wait (bounded) for the last
+      // copy issued into each slot.
+      if (!ended)
+        for (int q = (it > PR_RING ? it - PR_RING : 0); q < it; ++q)
+          if (!mbar_wait(&full[q % PR_RING], (q / PR_RING) & 1, kWaitLimitNs)) record_timeout(502);
+    }
+  } else if (warp == 1) {
+    // =========================== MMA issuer
+    if (lane == 0) {
+      // state: D[s][e] += T3^T[s][k] V[k][e], M = 128 (s), N = 256, MN-major A and B
+      constexpr uint32_t idesc_st = idesc_bf16_f32(128, E_TILE, true, true);
+      // score: S[rows][keys] = T0 T1^T, M = 128, N = 64, K-major A and B
+      constexpr uint32_t idesc_sc = idesc_bf16_f32(128, KEY_STAGE, false, false);
+      int it = 0, j = 0;
+      bool ok = true;
+      for (;; ++j) {
+        const int qs = j % PR_QUEUE;
+        if (!mbar_wait(&q_full[qs], (j / PR_QUEUE) & 1, kWaitLimitNs)) {
+          record_timeout(510);
+          ok = false;
+          break;
+        }
+        const int u = q_unit[qs];
+        mbar_arrive(&q_empty[qs]);
+        const int buf = j & 1, use = j >> 1;
+        if (use >= 1 && !mbar_wait(&acc_empty[buf], (use - 1) & 1, kWaitLimitNs)) {
+          record_timeout(511);
+          ok = false;
+          break;
+        }
+        if (u < 0) break;
+        tc_fence_after();
+        const PrepUnit p = decode_prep(u, n_state, n_score, n, e, C, G, causal);
+        const uint32_t dcol = tbase + (uint32_t)buf * 256u;
+        const int items = p.kind == KIND_STATE ? C / KEY_STAGE : 1;
+        for (int k = 0; k < items; ++k, ++it) {
+          const int slot = it % PR_RING;
+          if (!mbar_wait(&tready[slot], (it / PR_RING) & 1, kWaitLimitNs)) {
+            record_timeout(512);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sz = smem_u32(smem + slot * PR_SLOT);
+          if (p.kind == KIND_STATE) {
+#pragma unroll
+            for (int kk = 0; kk < KEY_STAGE / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(sz + kk * 2048, 8192, 1024);
+              const uint64_t bd = smem_desc_sw128(sz + PR_ST_Z + kk * 2048, 8192, 1024);
+              mma_bf16_ss(dcol, ad, bd, idesc_st, (k | kk) != 0);
+            }
+          } else {
+#pragma unroll
+            for (int kk = 0; kk < S_DIM / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(sz + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd =
+                  smem_desc_sw128(sz + PR_SC_K + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+              mma_bf16_ss(dcol, ad, bd, idesc_sc, kk != 0);
+            }
+          }
+          mma_commit(&empty[slot]);
+        }
+        if (!ok) break;
+        acc_unit[buf] = u;
+        mbar_arrive(&acc_full[buf]);
+        mma_commit(&acc_full[buf]);
+      }
+      if (ok) {
+        const int buf = j & 1;
+        acc_unit[buf] = -1;
+        mbar_arrive(&acc_full[buf]);
+        mma_commit(&acc_full[buf]);
+      }
+      mma_commit(&mma_done);
+      if (!mbar_wait(&mma_done, 0, kWaitLimitNs)) record_timeout(513);
+    }
+  } else if (warp < 6) {
+    // =========================== transform warps (128 threads)
+    const int mt = threadIdx.x - 64;
+    // Every 16-byte chunk this thread touches (in any part of an item) sits at
+    // physical chunk position p = mt % 8 of rows r with r % 8 = (mt / 8) % 8,
+    // i.e. logical columns a*64 + cl .. + 7 for the two 64-column atoms a.
+    const int p = mt & 7, rb = mt >> 3;
+    const int cl = (p ^ (rb & 7)) << 3;
+    // lin_k's gamma/beta (state items) stay in registers; quad_q, quad_k and
+    // lin_q's (score items, fewer) are re-read from L1 per item
+    float g3[2][8], b3[2][8];
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      load8(gamma + 3 * S_DIM + a * 64 + cl, g3[a]);
+      load8(beta + 3 * S_DIM + a * 64 + cl, b3[a]);
+    }
+    for (int it = 0;; ++it) {
+      const int slot = it % PR_RING;
+      const bool got = mbar_wait(&full[slot], (it / PR_RING) & 1, kWaitLimitNs);
+      const PrepUnit pu =
+          decode_prep(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
+      uint8_t *sz = smem + slot * PR_SLOT;
+      if (pu.kind == KIND_STATE) {
+        // T3 in place over the Z part: 2 boxes x 64 rows x 8 chunks
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int a = i >> 2, r = (rb + 16 * i) & 63;
+          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 8192 + r * 128 + p * 16);
+          *ptr = affine8(*ptr, g3[a], b3[a]);
+        }
+        fence_proxy_async_smem();
+      } else if (pu.kind == KIND_SCORE) {
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          float g[8], b[8], g2[8], b2[8];
+          load8(gamma + a * 64 + cl, g);
+          load8(beta + a * 64 + cl, b);
+          if (pu.ks == 0) {
+            load8(gamma + 2 * S_DIM + a * 64 + cl, g2);
+            load8(beta + 2 * S_DIM + a * 64 + cl, b2);
+          }
+          // query rows of atom a: T0 in place; T2 to global from the same Z
+          // values (once per row tile, by its key-stage-0 unit)
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = rb + 16 * i;
+            uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 16384 + r * 128 + p * 16);
+            const uint4 z = *ptr;
+            if (pu.ks == 0)
+              *reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + a * 64 + cl) =
+                  affine8(z, g2, b2);
+            *ptr = affine8(z, g, b);
+          }
+          // keys of atom a: T1 in place
+          load8(gamma + S_DIM + a * 64 + cl, g);
+          load8(beta + S_DIM + a * 64 + cl, b);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int r = rb + 16 * i;
+            uint4 *ptr = reinterpret_cast<uint4 *>(sz + PR_SC_K + a * 8192 + r * 128 + p * 16);
+            *ptr = affine8(*ptr, g, b);
+          }
+        }
+        fence_proxy_async_smem();
+      }
+      const bool valid = pu.kind != KIND_END;
+      if (!named_bar_and(1, 128, valid)) {
+        if (!got && mt == 0) record_timeout(520);
+        break;
+      }
+      if (mt == 0) mbar_arrive(&tready[slot]);
+      __syncwarp();
+    }
+  } else {
+    // =========================== epilogue warps (128 threads)
+    const int mt = threadIdx.x - 192;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // accumulator row (state row s or query row)
+    uint8_t *stage = smem + PR_OFF_STAGE;
+    const float inv_c = 1.0f / (float)C;
+    int nst = 0;  // staging tiles written so far
+    for (int j = 0;; ++j) {
+      const int buf = j & 1, use = j >> 1;
+      const bool got = mbar_wait(&acc_full[buf], use & 1, kWaitLimitNs);
+      const int u = got ? acc_unit[buf] : -1;
+      if (!named_bar_and(2, 128, u >= 0)) {
+        if (!got && mt == 0) record_timeout(530);
+        break;
+      }
+      tc_fence_after();
+      const PrepUnit p = decode_prep(u, n_state, n_score, n, e, C, G, causal);
+      const uint32_t dcol = tbase + (uint32_t)buf * 256u + ((uint32_t)(quad * 32) << 16);
+      const int nq = p.kind == KIND_STATE ? E_TILE / 64 : 1;
+      for (int q = 0; q < nq; ++q, ++nst) {
+        uint8_t *sb = stage + (nst % PR_STAGE_BUFS) * PR_STAGE_BYTES;
+        // the TMA store that last read this staging tile has finished reading it
+        if (mt == 0 && nst >= PR_STAGE_BUFS) bulk_wait_group_read<PR_STAGE_BUFS - 1>();
+        named_bar_sync(2, 128);
+        uint32_t r[2][32];
+        tmem_ld32(dcol + q * 64, r[0]);
+        tmem_ld32(dcol + q * 64 + 32, r[1]);
+        tmem_ld_wait();
+        if (p.kind == KIND_SCORE) {
+          // relu(S / C)^2; causal: key position > query position -> 0
+          const int qpos = p.rt * ROW_TILE + row;
+          const int kbase = p.ks * KEY_STAGE;
+#pragma unroll
+          for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              float x = fmaxf(__uint_as_float(r[c2][i]) * inv_c, 0.f);
+              x = x * x;
+              if (causal && kbase + c2 * 32 + i > qpos) x = 0.f;
+              r[c2][i] = __float_as_uint(x);
+            }
+        }
+#pragma unroll
+        for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+          for (int j4 = 0; j4 < 4; ++j4) {
+            const uint32_t *v = r[c2] + 8 * j4;
+            *reinterpret_cast<uint4 *>(sb + sw128_offset(row, c2 * 64 + 16 * j4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                           pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                           pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
+          }
+        fence_proxy_async_smem();
+        if (q == nq - 1) tc_fence_before();
+        named_bar_sync(2, 128);
+        if (mt == 0) {
+          if (p.kind == KIND_STATE)
+            tma_store_2d(&mapSt, sb, p.es * E_TILE + 64 * q, p.hb * S_DIM);
+          else
+            tma_store_2d(&mapPw, sb, p.ks * KEY_STAGE, p.row0);
+          bulk_commit_group();
+          // every epilogue thread has read this unit's accumulator
+          if (q == nq - 1) mbar_arrive(&acc_empty[buf]);
+        }
+        __syncwarp();
+      }
+    }
+    if (mt == 0) bulk_wait_group<0>();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+}  // namespace fmca

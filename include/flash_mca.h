@@ -124,9 +124,10 @@ fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
  * (cudaEvent_t handles) on `stream` around its kernels: events[0] before the
  * first kernel and events[i] after kernel i (1-based), so `n_events` must be
  * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
- * stream it runs on.  Kernel order: tensor-core path -- chunk scores,
- * chunk states, state scan, chunk attention; SIMT path -- chunk states,
- * state scan, chunk output. */
+ * stream it runs on.  Kernel order: tensor-core path -- chunk preparation
+ * (states, relu^2 weights, lin_q rows; events[0] is recorded before the
+ * reset of its work counters), state scan, chunk attention; SIMT path --
+ * chunk states, state scan, chunk output. */
 fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     const float *gamma, const float *beta, void *O, int B,
                                     int n, int s, int e, int C, int causal,

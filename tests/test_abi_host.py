@@ -86,7 +86,7 @@ def test_auto_path_choice():
 
 def test_launch_counts():
     bf = fm.FMCA_BF16
-    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 4
+    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 3
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
     assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
     assert fm.flash_mca_launch_count(1, 500, 128, 256, 64, 1, bf) == 0
