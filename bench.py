@@ -75,10 +75,14 @@ def load_peaks():
 
 
 def kernel_source_sha() -> str:
+    """Hash of the tensor-core kernel sources (tc*.cu, tc*.cuh, ptx.cuh)."""
+    csrc = os.path.join(ROOT, "flash_mixed_chunk_gb300", "csrc")
     h = hashlib.sha256()
-    for f in ("tc.cu", "ptx.cuh"):
-        with open(os.path.join(ROOT, "flash_mixed_chunk_gb300", "csrc", f), "rb") as fh:
-            h.update(fh.read())
+    for f in sorted(os.listdir(csrc)):
+        if (f.startswith("tc") and f.endswith((".cu", ".cuh"))) or f == "ptx.cuh":
+            with open(os.path.join(csrc, f), "rb") as fh:
+                h.update(f.encode())
+                h.update(fh.read())
     return h.hexdigest()[:16]
 
 
