@@ -10,8 +10,8 @@
 //                writes T2 = Z * gamma2 + beta2, bf16 [B*n][s]
 //
 // One CTA per SM takes units from a work counter (zeroed before the launch):
-// the larger state units first, the small score units last, so the score work
-// fills the state work's tail.  Every unit streams 48 KB items through one
+// the small, latency-bound score units first, so that their chains overlap
+// the state units streaming behind them, then the state units.  Every unit streams 48 KB items through one
 // four-slot ring:
 //   state item [Z: 64 keys x 128 s (16 KB) | V: 64 keys x 256 e (32 KB)]
 //   score item [Z: 128 query rows x 128 s (32 KB) | Z: 64 keys x 128 s (16 KB)]
@@ -56,16 +56,15 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
   PrepUnit p;
   p.kind = KIND_END;
   p.hb = p.es = p.crow = p.row0 = p.rt = p.ks = 0;
-  if (u < 0) return p;
-  if (u < n_state) {
+  if (u < 0 || u >= n_state + n_score) return p;
+  if (u >= n_score) {
+    u -= n_score;
     const int n_es = e / E_TILE;
     p.kind = KIND_STATE;
     p.es = u % n_es;
     p.hb = u / n_es;
     return p;
   }
-  u -= n_state;
-  if (u >= n_score) return p;
   const int R = C / ROW_TILE;
   // causal: row tile rt covers keys [0, 128 (rt+1)); otherwise all C keys
   const int per_chunk = causal ? R * (R + 1) : R * (C / KEY_STAGE);
