@@ -120,6 +120,16 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Programmatic dependent launch: let the next kernel on the stream start
+// launching, and (in that kernel) wait until every prerequisite grid has
+// completed and its memory is visible.
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Drop a 128-byte line from L2 without writing it back (its contents become
 // undefined); for scratch that no one reads again.
 __device__ __forceinline__ void discard_l2_line(const void *p) {

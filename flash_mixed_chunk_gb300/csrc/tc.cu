@@ -144,15 +144,33 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
       mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n, e,
       C, G, causal, n_state, n_score);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
+  // The scan and the attention kernel are launched as programmatic dependents
+  // of the kernel before them: each may start launching (and run its
+  // prologue) while its predecessor drains, and waits (griddepcontrol.wait)
+  // for it to complete before reading what it wrote.
+  cudaLaunchAttribute pdl[1];
+  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  pdl[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.stream = stream;
+  cfg.attrs = pdl;
+  cfg.numAttrs = 1;
   const int64_t lanes = (int64_t)B * se / 8;
-  tc_state_scan<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(states, prefix, B, G, se,
-                                                                     1.0f / (float)n, causal);
-  if (cudaGetLastError() != cudaSuccess || !record_event(events, 2, stream)) return 1;
+  cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
+  cfg.blockDim = dim3(256);
+  cfg.dynamicSmemBytes = 0;
+  if (cudaLaunchKernelEx(&cfg, tc_state_scan, (const __nv_bfloat16 *)states, prefix, B, G, se,
+                         1.0f / (float)n, causal) != cudaSuccess ||
+      !record_event(events, 2, stream))
+    return 1;
   const int n_units = B * G * R * (e / E_TILE);
-  const int grid = n_units < num_sms() ? n_units : num_sms();
-  tc_chunk_attn<<<grid, AT_THREADS, AT_SMEM, stream>>>(mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C,
-                                                       G, causal, n_units);
-  if (cudaGetLastError() != cudaSuccess || !record_event(events, 3, stream)) return 1;
+  cfg.gridDim = dim3(n_units < num_sms() ? n_units : num_sms());
+  cfg.blockDim = dim3(AT_THREADS);
+  cfg.dynamicSmemBytes = AT_SMEM;
+  if (cudaLaunchKernelEx(&cfg, tc_chunk_attn, mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C, G,
+                         causal, n_units) != cudaSuccess ||
+      !record_event(events, 3, stream))
+    return 1;
   return 0;
 }
 

@@ -116,6 +116,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t tbase = tmem_base;
   uint8_t *ringA = smem;
   uint8_t *ringB = smem + AT_OFF_B;
+  // launched as a dependent of the scan: everything above overlapped its
+  // tail; nothing below reads the workspace before the scan has finished
+  griddep_wait();
 
   if (warp == 0) {
     // =========================== scheduler + ring A producer

@@ -104,6 +104,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_units = n_state + n_score;
+  // the scan kernel may start launching now; it waits for this grid to finish
+  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < PR_RING; ++i) {

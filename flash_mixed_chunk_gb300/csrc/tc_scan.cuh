@@ -18,6 +18,10 @@ namespace {
 __global__ void __launch_bounds__(256)
     tc_state_scan(const __nv_bfloat16 *__restrict__ S, __nv_bfloat16 *__restrict__ P, int B,
                   int G, int64_t se, float inv_n, int causal) {
+  // launched as a dependent of the prep kernel: wait for its states; let the
+  // attention kernel start launching (it waits for this grid in turn)
+  griddep_wait();
+  griddep_launch_dependents();
   const int64_t per_b = se / 8;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * per_b) return;
