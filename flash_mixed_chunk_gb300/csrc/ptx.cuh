@@ -96,6 +96,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
       "r"(x), "r"(y), "r"(smem_u32(src))
       : "memory");
 }
+// Same with an L2 cache-policy hint.
+__device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, const void *src,
+                                                  int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(smem_u32(src)), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

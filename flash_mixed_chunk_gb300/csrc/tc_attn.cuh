@@ -133,8 +133,11 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       // overlaps the current unit's copies
       int u_next = (int)atomicAdd(sched, 1u);
       for (int i = 0; ok; ++i) {
+        // units are taken last chunk first: the prep kernel streamed V in
+        // chunk order, so the chunks it read last are the likeliest to still
+        // be in L2 (and the longer causal row tiles go before the short ones)
         const int u = u_next;
-        const int uu = u < n_units ? u : -1;
+        const int uu = u < n_units ? n_units - 1 - u : -1;
         if (uu >= 0) u_next = (int)atomicAdd(sched, 1u);
         // hand the unit to the MMA warp and to the ring B producer
         const int qs = i % AT_QUEUE;
@@ -184,6 +187,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     // =========================== ring B producer (U tiles)
     if (lane == 0) {
       tma_prefetch_desc(&mapU);
+      // U is read once: keep it from displacing V and the workspace in L2
+      const uint64_t stream_policy = policy_evict_first();
       int ib = 0;
       bool ok = true;
       for (int i = 0; ok; ++i) {
@@ -205,7 +210,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             break;
           }
           mbar_arrive_expect_tx(&fullB[slot], AT_SLOT_B);
-          tma_load_2d(ringB + slot * AT_SLOT_B, &mapU, &fullB[slot], a.e0 + 64 * q, a.row0);
+          tma_load_2d_hint(ringB + slot * AT_SLOT_B, &mapU, &fullB[slot], a.e0 + 64 * q, a.row0,
+                           stream_policy);
         }
       }
       for (int q = (ib > AT_RING_B ? ib - AT_RING_B : 0); q < ib; ++q)
@@ -278,6 +284,8 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     int ib = 0;
+    // O is written once and read by nobody here: first out of L2
+    const uint64_t out_policy = policy_evict_first();
     // Each O store is committed as its own bulk group; a U slot is released
     // once the store after it has been issued (wait_group.read 1), so the
     // store's shared-memory read overlaps the next quarter's work.
@@ -329,7 +337,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
           break;
         }
         if (mt == 0) {
-          tma_store_2d(&mapO, us, a.e0 + 64 * q, a.row0);
+          tma_store_2d_hint(&mapO, us, a.e0 + 64 * q, a.row0, out_policy);
           bulk_commit_group();
           if (ib > 0) {
             bulk_wait_group_read<1>();  // the previous quarter's store has read its slot
