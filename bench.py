@@ -48,6 +48,36 @@ PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 DOMINANT_KERNEL = "tc_chunk_attn"
 
 
+# ---------------------------------------------------------------- ranks
+def rank_seed(seed: int, rank: int) -> int:
+    """Input seed of one rank: every rank runs its own independent problem
+    (another batch of sequences); rank 0 keeps the workload's own seed."""
+    return seed + 1000 * rank
+
+
+def reduce_max(x: float, device) -> float:
+    """Max of `x` over the ranks of the default process group (x itself
+    without one): the job's time is its slowest rank's."""
+    dist = torch.distributed
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    tt = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def barrier():
+    dist = torch.distributed
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def whole_job_rate(world: int, units_per_rank_step: float, steps: int, max_seconds: float) -> float:
+    """Units per second of the whole job: every rank processed its own
+    units_per_rank_step each step, over the slowest rank's time."""
+    return world * units_per_rank_step * steps / max_seconds
+
+
 # ---------------------------------------------------------------- work accounting
 def algorithmic_flops(w) -> float:
     """Per forward pass: per chunk 2*P*(s+e) for the intra-chunk scores and
@@ -258,7 +288,7 @@ def run_ours(args, w, rank, world, device):
     import flash_mixed_chunk_gb300 as fm
 
     torch.cuda.set_device(device)
-    seed = mca_inputs.WORKLOAD_ORDER.index(w.name) + 1
+    seed = rank_seed(mca_inputs.WORKLOAD_ORDER.index(w.name) + 1, rank)
     Zc, Vc, Uc, gc, bc = mca_inputs.workload_inputs(w, seed)
     dt_code = fm.FMCA_BF16 if w.dtype == "bf16" else fm.FMCA_F32
     path = fm.flash_mca_auto_path(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code)
@@ -293,8 +323,7 @@ def run_ours(args, w, rank, world, device):
     # its kernels (the library chains them with programmatic dependent launch)
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier()
     torch.cuda.synchronize(device)
     wall0 = time.time()
     t_start.record(stream)
@@ -303,17 +332,12 @@ def run_ours(args, w, rank, world, device):
     t_end.record(stream)
     torch.cuda.synchronize(device)
     wall1 = time.time()
-    if world > 1:
-        torch.distributed.barrier()
+    barrier()
     sampler.stop()
     st, where = fm.flash_mca_device_status()
     if st != fm.FMCA_OK:
         raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
-    ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        tt = torch.tensor([ms], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = reduce_max(t_start.elapsed_time(t_end), device)
 
     # ---- second timed pass of K steps with CUDA events recorded by the library
     # before the first kernel and after each kernel (on the launching stream):
@@ -343,16 +367,11 @@ def run_ours(args, w, rank, world, device):
     k_e2e = max(3, min(args.steps, 200))
     for _ in range(3):
         fm.flash_mca_forward_host(*pin, Oh, w.C, w.causal, arena, stream)
-    if world > 1:
-        torch.distributed.barrier()
+    barrier()
     t = time.perf_counter()
     for _ in range(k_e2e):
         fm.flash_mca_forward_host(*pin, Oh, w.C, w.causal, arena, stream)
-    e2e_s = time.perf_counter() - t
-    if world > 1:
-        tt = torch.tensor([e2e_s], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(tt.item())
+    e2e_s = reduce_max(time.perf_counter() - t, device)
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = Oh.numel() * Oh.element_size()
 
@@ -360,7 +379,7 @@ def run_ours(args, w, rank, world, device):
         return
     peaks, peak_kind = load_peaks()
     tokens = w.B * w.n
-    value = world * tokens * args.steps / (ms / 1e3)
+    value = whole_job_rate(world, tokens, args.steps, ms / 1e3)
     flops = algorithmic_flops(w)
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
     kernel_names = (["tc_chunk_prep", "tc_state_scan", "tc_chunk_attn"]
@@ -404,7 +423,7 @@ def run_ours(args, w, rank, world, device):
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * tokens * k_e2e / e2e_s, "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(world, tokens, k_e2e, e2e_s), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": k_e2e},
         "gpu_launches": nl * args.steps,
         "clocks": clocks,

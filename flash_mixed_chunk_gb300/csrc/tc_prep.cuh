@@ -9,9 +9,10 @@
 //                mode, bf16 [B*n][C]; the key-stage-0 unit of each row tile also
 //                writes T2 = Z * gamma2 + beta2, bf16 [B*n][s]
 //
-// One CTA per SM takes units from a work counter (zeroed before the launch):
-// the small, latency-bound score units first, so that their chains overlap
-// the state units streaming behind them, then the state units.  Every unit streams 48 KB items through one
+// One CTA per SM: the small, latency-bound score units first, dealt
+// round-robin over the CTAs, so that their chains overlap the state units
+// streaming behind them; then the state units, from a work counter (zeroed
+// before the launch).  Every unit streams 48 KB items through one
 // four-slot ring:
 //   state item [Z: 64 keys x 128 s (16 KB) | V: 64 keys x 256 e (32 KB)]
 //   score item [Z: 128 query rows x 128 s (32 KB) | Z: 64 keys x 128 s (16 KB)]
@@ -141,12 +142,23 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
       tma_prefetch_desc(&mapV);
       int it = 0;
       bool ok = true, ended = false;
-      // the next unit is fetched one unit ahead, so the atomic's latency
-      // overlaps the current unit's copies
-      int u_next = (int)atomicAdd(sched, 1u);
+      // Score units are dealt round-robin (CTA c takes c, c + grid, ...): they
+      // come first and are short, so an atomic per unit would cost more than
+      // the unit.  State units come from the work counter, fetched one unit
+      // ahead so that the atomic's latency overlaps the current unit's copies.
+      int k_static = 0;
+      auto next_unit = [&]() -> int {
+        const int us = (int)blockIdx.x + k_static * (int)gridDim.x;
+        if (us < n_score) {
+          ++k_static;
+          return us;
+        }
+        return n_score + (int)atomicAdd(sched, 1u);
+      };
+      int u_next = next_unit();
       for (int i = 0; ok; ++i) {
         const int uu = u_next < n_units ? u_next : -1;
-        if (uu >= 0) u_next = (int)atomicAdd(sched, 1u);
+        if (uu >= 0) u_next = next_unit();
         const int qs = i % PR_QUEUE;
         if (i >= PR_QUEUE && !mbar_wait(&q_empty[qs], ((i / PR_QUEUE) - 1) & 1, kWaitLimitNs)) {
           record_timeout(500);
@@ -269,19 +281,22 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
   } else if (warp < 6) {
     // =========================== transform warps (128 threads)
     const int mt = threadIdx.x - 64;
-    // Every 16-byte chunk this thread touches (in any part of an item) sits at
-    // physical chunk position p = mt % 8 of rows r with r % 8 = (mt / 8) % 8,
-    // i.e. logical columns a*64 + cl .. + 7 for the two 64-column atoms a.
-    const int p = mt & 7, rb = mt >> 3;
-    const int cl = (p ^ (rb & 7)) << 3;
-    // lin_k's gamma/beta (state items) stay in registers; quad_q, quad_k and
-    // lin_q's (score items, fewer) are re-read from L1 per item
-    float g3[2][8], b3[2][8];
-#pragma unroll
-    for (int a = 0; a < 2; ++a) {
-      load8(gamma + 3 * S_DIM + a * 64 + cl, g3[a]);
-      load8(beta + 3 * S_DIM + a * 64 + cl, b3[a]);
-    }
+    // Thread mt owns physical 16-byte chunk p = mt % 8 of the rows r with
+    // r % 8 = (mt / 8) % 8 in 64-column atom a = mt / 64 of every operand box:
+    // under the 128-byte swizzle those are logical columns a*64 + cl .. + 7 in
+    // every such row, so the thread needs gamma/beta of only those 8 columns
+    // for each of the four transforms, kept in registers for the whole kernel.
+    const int a = mt >> 6, p = mt & 7, rb = (mt >> 3) & 7;
+    const int cl = a * 64 + ((p ^ rb) << 3);
+    float g0[8], b0[8], g1[8], b1[8], g2[8], b2[8], g3[8], b3[8];
+    load8(gamma + cl, g0);
+    load8(beta + cl, b0);
+    load8(gamma + S_DIM + cl, g1);
+    load8(beta + S_DIM + cl, b1);
+    load8(gamma + 2 * S_DIM + cl, g2);
+    load8(beta + 2 * S_DIM + cl, b2);
+    load8(gamma + 3 * S_DIM + cl, g3);
+    load8(beta + 3 * S_DIM + cl, b3);
     for (int it = 0;; ++it) {
       const int slot = it % PR_RING;
       const bool got = mbar_wait(&full[slot], (it / PR_RING) & 1, kWaitLimitNs);
@@ -289,45 +304,32 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
           decode_prep(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
       uint8_t *sz = smem + slot * PR_SLOT;
       if (pu.kind == KIND_STATE) {
-        // T3 in place over the Z part: 2 boxes x 64 rows x 8 chunks
+        // T3 in place over the Z part (atom a: 64 key rows)
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          const int a = i >> 2, r = (rb + 16 * i) & 63;
-          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 8192 + r * 128 + p * 16);
-          *ptr = affine8(*ptr, g3[a], b3[a]);
+          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 8192 + (rb + 8 * i) * 128 + p * 16);
+          *ptr = affine8(*ptr, g3, b3);
         }
         fence_proxy_async_smem();
       } else if (pu.kind == KIND_SCORE) {
+        // query rows (atom a: 128 rows): T0 in place; T2 to global from the
+        // same Z values, once per row tile (by its key-stage-0 unit)
 #pragma unroll
-        for (int a = 0; a < 2; ++a) {
-          float g[8], b[8], g2[8], b2[8];
-          load8(gamma + a * 64 + cl, g);
-          load8(beta + a * 64 + cl, b);
-          if (pu.ks == 0) {
-            load8(gamma + 2 * S_DIM + a * 64 + cl, g2);
-            load8(beta + 2 * S_DIM + a * 64 + cl, b2);
-          }
-          // query rows of atom a: T0 in place; T2 to global from the same Z
-          // values (once per row tile, by its key-stage-0 unit)
+        for (int i = 0; i < 16; ++i) {
+          const int r = rb + 8 * i;
+          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 16384 + r * 128 + p * 16);
+          const uint4 z = *ptr;
+          if (pu.ks == 0)
+            *reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + cl) =
+                affine8(z, g2, b2);
+          *ptr = affine8(z, g0, b0);
+        }
+        // keys (atom a: 64 rows): T1 in place
 #pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = rb + 16 * i;
-            uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 16384 + r * 128 + p * 16);
-            const uint4 z = *ptr;
-            if (pu.ks == 0)
-              *reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + a * 64 + cl) =
-                  affine8(z, g2, b2);
-            *ptr = affine8(z, g, b);
-          }
-          // keys of atom a: T1 in place
-          load8(gamma + S_DIM + a * 64 + cl, g);
-          load8(beta + S_DIM + a * 64 + cl, b);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int r = rb + 16 * i;
-            uint4 *ptr = reinterpret_cast<uint4 *>(sz + PR_SC_K + a * 8192 + r * 128 + p * 16);
-            *ptr = affine8(*ptr, g, b);
-          }
+        for (int i = 0; i < 8; ++i) {
+          uint4 *ptr =
+              reinterpret_cast<uint4 *>(sz + PR_SC_K + a * 8192 + (rb + 8 * i) * 128 + p * 16);
+          *ptr = affine8(*ptr, g1, b1);
         }
         fence_proxy_async_smem();
       }
