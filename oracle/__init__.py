@@ -52,6 +52,13 @@ def _load():
             lib.mca_oracle_rows.argtypes = [d, d, d, d, d, i, i, i, i, i, i, i,
                                             ctypes.POINTER(ctypes.c_int64), d, i]
             lib.mca_oracle_rows.restype = i
+            lib.mca_oracle_forward_ex.argtypes = [d, d, d, d, d, d, i, i, i, i, i, i,
+                                                  ctypes.c_double, i, i]
+            lib.mca_oracle_forward_ex.restype = i
+            lib.mca_oracle_rows_ex.argtypes = [d, d, d, d, d, i, i, i, i, i, i,
+                                               ctypes.c_double, i, i,
+                                               ctypes.POINTER(ctypes.c_int64), d, i]
+            lib.mca_oracle_rows_ex.restype = i
             lib.mca_oracle_max_threads.argtypes = []
             lib.mca_oracle_max_threads.restype = i
             _lib = lib
@@ -76,8 +83,19 @@ def max_threads() -> int:
     return int(_load().mca_oracle_max_threads())
 
 
-def forward(Z, V, U, gamma, beta, C: int, causal: bool, nthreads: int = 0) -> np.ndarray:
-    """O[B, n, e] in fp64 for Z[B, n, s], V/U[B, n, e], gamma/beta[4, s]."""
+# Global-term divisors of the variants (see the top of mca_oracle.c).
+LIN_NORM_N = 0         # 1/n
+LIN_NORM_SUMMED = 1    # 1/(tokens the sum covers): g*C for causal chunk g, n otherwise
+LIN_NORM_POSITION = 2  # 1/(t+1) for the token at position t
+
+
+def forward(Z, V, U, gamma, beta, C: int, causal: bool, nthreads: int = 0,
+            quad_scale: float | None = None, lin_norm: int | None = None) -> np.ndarray:
+    """O[B, n, e] in fp64 for Z[B, n, s], V/U[B, n, e], gamma/beta[4, s].
+
+    With ``quad_scale`` or ``lin_norm`` given, the variant form: intra-chunk
+    weights quad_scale * relu(q . k)^2 (default 1/C^2, i.e. relu(x/C)^2) and
+    the global-term divisor ``lin_norm`` (LIN_NORM_*)."""
     Z, V, U, gamma, beta = (_f64(t) for t in (Z, V, U, gamma, beta))
     B, n, s = Z.shape
     e = V.shape[2]
@@ -86,25 +104,41 @@ def forward(Z, V, U, gamma, beta, C: int, causal: bool, nthreads: int = 0) -> np
     if gamma.shape != (4, s) or beta.shape != (4, s):
         raise ValueError("gamma and beta must be [4, s]")
     O = np.zeros((B, n, e), dtype=np.float64)
-    rc = _load().mca_oracle_forward(_ptr(Z), _ptr(V), _ptr(U), _ptr(gamma), _ptr(beta),
-                                    _ptr(O), B, n, s, e, int(C), int(bool(causal)),
-                                    int(nthreads))
+    if quad_scale is None and lin_norm is None:
+        rc = _load().mca_oracle_forward(_ptr(Z), _ptr(V), _ptr(U), _ptr(gamma), _ptr(beta),
+                                        _ptr(O), B, n, s, e, int(C), int(bool(causal)),
+                                        int(nthreads))
+    else:
+        qs = 1.0 / (float(C) * float(C)) if quad_scale is None else float(quad_scale)
+        rc = _load().mca_oracle_forward_ex(_ptr(Z), _ptr(V), _ptr(U), _ptr(gamma),
+                                           _ptr(beta), _ptr(O), B, n, s, e, int(C),
+                                           int(bool(causal)), qs, int(lin_norm or 0),
+                                           int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return O
 
 
-def rows(Z, V, U, gamma, beta, C: int, causal: bool, row_ids, nthreads: int = 0) -> np.ndarray:
-    """O at selected flat token indices ``row_ids`` (b*n + t): array [len, e]."""
+def rows(Z, V, U, gamma, beta, C: int, causal: bool, row_ids, nthreads: int = 0,
+         quad_scale: float | None = None, lin_norm: int | None = None) -> np.ndarray:
+    """O at selected flat token indices ``row_ids`` (b*n + t): array [len, e]
+    (variant arguments as for ``forward``)."""
     Z, V, U, gamma, beta = (_f64(t) for t in (Z, V, U, gamma, beta))
     B, n, s = Z.shape
     e = V.shape[2]
     ids = np.ascontiguousarray(np.asarray(row_ids, dtype=np.int64).reshape(-1))
     out = np.zeros((ids.size, e), dtype=np.float64)
-    rc = _load().mca_oracle_rows(_ptr(Z), _ptr(V), _ptr(U), _ptr(gamma), _ptr(beta),
-                                 B, n, s, e, int(C), int(bool(causal)), int(ids.size),
-                                 ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)),
-                                 _ptr(out), int(nthreads))
+    idp = ids.ctypes.data_as(ctypes.POINTER(ctypes.c_int64))
+    if quad_scale is None and lin_norm is None:
+        rc = _load().mca_oracle_rows(_ptr(Z), _ptr(V), _ptr(U), _ptr(gamma), _ptr(beta),
+                                     B, n, s, e, int(C), int(bool(causal)), int(ids.size),
+                                     idp, _ptr(out), int(nthreads))
+    else:
+        qs = 1.0 / (float(C) * float(C)) if quad_scale is None else float(quad_scale)
+        rc = _load().mca_oracle_rows_ex(_ptr(Z), _ptr(V), _ptr(U), _ptr(gamma), _ptr(beta),
+                                        B, n, s, e, int(C), int(bool(causal)), qs,
+                                        int(lin_norm or 0), int(ids.size), idp, _ptr(out),
+                                        int(nthreads))
     if rc != 0:
         raise ValueError(f"oracle rejected the arguments (code {rc})")
     return out

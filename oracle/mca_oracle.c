@@ -42,12 +42,30 @@
  *      -- same page, "Mixed Chunk", final equation for O_g (W_o is applied
  *         outside this core).
  *
+ * Variants (the *_ex entry points), for where the page's own formulas differ
+ * from the reading above ("Mixed Chunk", the equations for V-hat^quad_g and
+ * the decoder form of V-hat^lin_g; "Extended Thoughts", the remark on the
+ * decoder's normalisation factor):
+ *   quad_scale  the weight is quad_scale * relu(T_0[i] . T_1[j])^2; the page's
+ *               1/(cs) relu^2(Q K^T) is quad_scale = 1/(C s), and the default
+ *               relu(x / C)^2 above is quad_scale = 1/C^2.
+ *   lin_norm    0: the global term is divided by n (as above);
+ *               1: by the number of tokens its sum covers -- g*C for chunk g
+ *                  (counted from 0) in causal mode, which is the decoder
+ *                  equation's 1/((g-1)c) with chunks counted from 1, and n
+ *                  otherwise; chunk 0's causal sum is empty, so its term is 0;
+ *               2: by t+1 for the token at position t (counted from 0) of its
+ *                  sequence, i.e. by its position counted from 1 ("the sum of
+ *                  the first t items should be divided by t").
+ *
  * All arithmetic is fp64.  Arrays are row-major and contiguous:
  *   Z[B][n][s], V[B][n][e], U[B][n][e], gamma[4][s], beta[4][s], O[B][n][e].
  *
  * Return codes: 0 ok, -1 bad arguments (non-positive sizes, C not dividing n,
- * NULL pointers, s > 4096), -2 out of host memory.
+ * NULL pointers, s > 4096, a negative or non-finite quad_scale, an unknown
+ * lin_norm), -2 out of host memory.
  */
+#include <math.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -121,6 +139,69 @@ static void output_row(const double *Z, const double *V, const double *U,
   for (int c = 0; c < e; ++c) out[c] *= u[c];
 }
 
+/* The variants: the divisor of the global term of token i of chunk g. */
+static double lin_factor(int lin_norm, int causal, int n, int C, int g, int i) {
+  if (lin_norm == 1) {
+    if (!causal) return 1.0 / (double)n;
+    return g > 0 ? 1.0 / ((double)g * (double)C) : 0.0; /* chunk 0: empty sum */
+  }
+  if (lin_norm == 2) return 1.0 / ((double)g * (double)C + (double)i + 1.0);
+  return 1.0 / (double)n;
+}
+
+/* output_row with the variant weight quad_scale * relu(q . k)^2 and divisor
+ * lin_factor(...). */
+static void output_row_ex(const double *Z, const double *V, const double *U,
+                          const double *gamma, const double *beta, const double *glob_state,
+                          int b, int n, int s, int e, int C, int causal, int g, int i,
+                          double quad_scale, int lin_norm, double *out, double *q0,
+                          double *k1, double *q2) {
+  int64_t row = (int64_t)b * n + (int64_t)g * C + i;
+  affine_row(Z, gamma, beta, s, row, 0, q0);
+  affine_row(Z, gamma, beta, s, row, 2, q2);
+  for (int c = 0; c < e; ++c) out[c] = 0.0;
+  int jmax = causal ? i : C - 1;
+  for (int j = 0; j <= jmax; ++j) {
+    int64_t krow = (int64_t)b * n + (int64_t)g * C + j;
+    affine_row(Z, gamma, beta, s, krow, 1, k1);
+    double r = relu(dot(q0, k1, s));
+    double w = quad_scale * r * r;
+    const double *v = V + krow * (int64_t)e;
+    for (int c = 0; c < e; ++c) out[c] += w * v[c];
+  }
+  double f = lin_factor(lin_norm, causal, n, C, g, i);
+  for (int a = 0; a < s; ++a) {
+    double qa = q2[a] * f;
+    const double *sr = glob_state + (size_t)a * e;
+    for (int c = 0; c < e; ++c) out[c] += qa * sr[c];
+  }
+  const double *u = U + row * (int64_t)e;
+  for (int c = 0; c < e; ++c) out[c] *= u[c];
+}
+
+/* Which formula a driver applies: NULL = the definition at the top. */
+struct variant {
+  double quad_scale;
+  int lin_norm;
+};
+
+static void row_of(const double *Z, const double *V, const double *U, const double *gamma,
+                   const double *beta, const double *glob_state, int b, int n, int s, int e,
+                   int C, int causal, int g, int i, const struct variant *v, double *out,
+                   double *q0, double *k1, double *q2) {
+  if (v)
+    output_row_ex(Z, V, U, gamma, beta, glob_state, b, n, s, e, C, causal, g, i,
+                  v->quad_scale, v->lin_norm, out, q0, k1, q2);
+  else
+    output_row(Z, V, U, gamma, beta, glob_state, b, n, s, e, C, causal, g, i, out, q0, k1, q2);
+}
+
+static int check_variant(double quad_scale, int lin_norm) {
+  if (!(quad_scale >= 0.0) || !isfinite(quad_scale)) return -1;
+  if (lin_norm < 0 || lin_norm > 2) return -1;
+  return 0;
+}
+
 static int check_args(const void *Z, const void *V, const void *U, const void *gamma,
                       const void *beta, int B, int n, int s, int e, int C) {
   if (!Z || !V || !U || !gamma || !beta) return -1;
@@ -131,9 +212,10 @@ static int check_args(const void *Z, const void *V, const void *U, const void *g
 }
 
 /* Whole output O[B][n][e].  nthreads <= 0 means the OpenMP default. */
-int mca_oracle_forward(const double *Z, const double *V, const double *U,
-                       const double *gamma, const double *beta, double *O, int B, int n,
-                       int s, int e, int C, int causal, int nthreads) {
+static int forward_impl(const double *Z, const double *V, const double *U,
+                        const double *gamma, const double *beta, double *O, int B, int n,
+                        int s, int e, int C, int causal, const struct variant *var,
+                        int nthreads) {
   if (check_args(Z, V, U, gamma, beta, B, n, s, e, C) || !O) return -1;
   const int G = n / C;
   const size_t se = (size_t)s * (size_t)e;
@@ -173,8 +255,8 @@ int mca_oracle_forward(const double *Z, const double *V, const double *U,
       double q0[s], k1[s], q2[s];
       for (int i = 0; i < C; ++i) {
         int64_t row = (int64_t)b * n + (int64_t)g * C + i;
-        output_row(Z, V, U, gamma, beta, glob + se * g, b, n, s, e, C, causal, g, i,
-                   O + row * (int64_t)e, q0, k1, q2);
+        row_of(Z, V, U, gamma, beta, glob + se * g, b, n, s, e, C, causal, g, i, var,
+               O + row * (int64_t)e, q0, k1, q2);
       }
     }
   }
@@ -183,15 +265,31 @@ int mca_oracle_forward(const double *Z, const double *V, const double *U,
   return 0;
 }
 
+int mca_oracle_forward(const double *Z, const double *V, const double *U,
+                       const double *gamma, const double *beta, double *O, int B, int n,
+                       int s, int e, int C, int causal, int nthreads) {
+  return forward_impl(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, NULL, nthreads);
+}
+
+/* The variants (see the top of this file). */
+int mca_oracle_forward_ex(const double *Z, const double *V, const double *U,
+                          const double *gamma, const double *beta, double *O, int B, int n,
+                          int s, int e, int C, int causal, double quad_scale, int lin_norm,
+                          int nthreads) {
+  if (check_variant(quad_scale, lin_norm)) return -1;
+  struct variant v = {quad_scale, lin_norm};
+  return forward_impl(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, &v, nthreads);
+}
+
 /* Selected output rows only.  rows[r] is a flat token index b*n + t; the
  * result for rows[r] goes to Orows[r][0..e).  Same definition as above: the
  * state sum a row reads is built from the chunk states of its own batch
  * element, chunk by chunk, up to the row's chunk (causal) or over all chunks
  * (non-causal). */
-int mca_oracle_rows(const double *Z, const double *V, const double *U,
-                    const double *gamma, const double *beta, int B, int n, int s, int e,
-                    int C, int causal, int nrows, const int64_t *rows, double *Orows,
-                    int nthreads) {
+static int rows_impl(const double *Z, const double *V, const double *U, const double *gamma,
+                     const double *beta, int B, int n, int s, int e, int C, int causal,
+                     int nrows, const int64_t *rows, double *Orows, const struct variant *var,
+                     int nthreads) {
   if (check_args(Z, V, U, gamma, beta, B, n, s, e, C) || !rows || !Orows || nrows < 0)
     return -1;
   for (int r = 0; r < nrows; ++r)
@@ -241,14 +339,32 @@ int mca_oracle_rows(const double *Z, const double *V, const double *U,
         if (rows[r] / n != b || (int)((rows[r] % n) / C) != g) continue;
         double q0[s], k1[s], q2[s];
         int i = (int)((rows[r] % n) % C);
-        output_row(Z, V, U, gamma, beta, acc, b, n, s, e, C, causal, g, i,
-                   Orows + (int64_t)r * e, q0, k1, q2);
+        row_of(Z, V, U, gamma, beta, acc, b, n, s, e, C, causal, g, i, var,
+               Orows + (int64_t)r * e, q0, k1, q2);
       }
     }
   }
   free(states);
   free(acc);
   return 0;
+}
+
+int mca_oracle_rows(const double *Z, const double *V, const double *U,
+                    const double *gamma, const double *beta, int B, int n, int s, int e,
+                    int C, int causal, int nrows, const int64_t *rows, double *Orows,
+                    int nthreads) {
+  return rows_impl(Z, V, U, gamma, beta, B, n, s, e, C, causal, nrows, rows, Orows, NULL,
+                   nthreads);
+}
+
+int mca_oracle_rows_ex(const double *Z, const double *V, const double *U,
+                       const double *gamma, const double *beta, int B, int n, int s, int e,
+                       int C, int causal, double quad_scale, int lin_norm, int nrows,
+                       const int64_t *rows, double *Orows, int nthreads) {
+  if (check_variant(quad_scale, lin_norm)) return -1;
+  struct variant v = {quad_scale, lin_norm};
+  return rows_impl(Z, V, U, gamma, beta, B, n, s, e, C, causal, nrows, rows, Orows, &v,
+                   nthreads);
 }
 
 int mca_oracle_max_threads(void) {

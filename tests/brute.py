@@ -30,7 +30,12 @@ def affine(Z, gamma, beta, k):
     return Z * gamma[k][None, None, :] + beta[k][None, None, :]
 
 
-def explicit_matrix(Z, V, U, gamma, beta, C, causal):
+def explicit_matrix(Z, V, U, gamma, beta, C, causal, quad_scale=None, lin_norm=0):
+    """O = U * (A V), A assembled entry by entry.  ``quad_scale`` (default
+    1/C^2) multiplies relu(q . k)^2; ``lin_norm`` picks the divisor of the
+    low-rank part per query row: 0 n, 1 the number of keys the row's global
+    sum covers (its count of True entries in the low-rank mask), 2 the row's
+    position counted from 1."""
     Z, V, U, gamma, beta = (np.asarray(a, dtype=np.float64) for a in (Z, V, U, gamma, beta))
     B, n, s = Z.shape
     T = [affine(Z, gamma, beta, k) for k in range(4)]
@@ -43,11 +48,24 @@ def explicit_matrix(Z, V, U, gamma, beta, C, causal):
     else:
         quad_mask = same
         lin_mask = np.ones((n, n), dtype=bool)
+    if lin_norm == 0:
+        div = np.full(n, float(n))
+    elif lin_norm == 1:
+        div = lin_mask.sum(axis=1).astype(np.float64)  # keys each row's sum covers
+    elif lin_norm == 2:
+        div = pos + 1.0
+    else:
+        raise ValueError(lin_norm)
+    inv = np.where(div > 0, 1.0 / np.maximum(div, 1.0), 0.0)
     out = np.empty_like(U)
     for b in range(B):
-        scores = T[0][b] @ T[1][b].T / C
-        A = np.where(quad_mask, np.maximum(scores, 0.0) ** 2, 0.0)
-        A = A + np.where(lin_mask, T[2][b] @ T[3][b].T / n, 0.0)
+        raw = T[0][b] @ T[1][b].T
+        if quad_scale is None:
+            quad = np.maximum(raw / C, 0.0) ** 2
+        else:
+            quad = quad_scale * np.maximum(raw, 0.0) ** 2
+        A = np.where(quad_mask, quad, 0.0)
+        A = A + np.where(lin_mask, (T[2][b] @ T[3][b].T) * inv[:, None], 0.0)
         out[b] = U[b] * (A @ V[b])
     return out
 
