@@ -239,6 +239,8 @@ def run_reference(args, w):
     Z, V, U, gamma, beta = mca_inputs.workload_inputs(w, seed)
     inputs64 = tuple(x.to(torch.float64).numpy() for x in (Z, V, U))
     g64, b64 = gamma.double().numpy(), beta.double().numpy()
+    qs, ln = variant_of(args, w)
+    variant = {} if qs is None and ln == 0 else {"quad_scale": qs, "lin_norm": ln}
     # size each step so that warm-up + steps stay within about two minutes
     per_step = max(0.05, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
     # each step: the outputs of the first m chunks of batch element 0, m sized
@@ -247,17 +249,17 @@ def run_reference(args, w):
     while True:
         rows = np.arange(m * w.C, dtype=np.int64)
         t = time.perf_counter()
-        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows)
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, **variant)
         dt = time.perf_counter() - t
         if dt >= per_step or m >= w.G:
             break
         m = min(w.G, max(m + 1, int(m * per_step / max(dt, 1e-3))))
     threads = oracle.max_threads()
     for _ in range(args.warmup):
-        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows)
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, **variant)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows)
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, **variant)
     dt = time.perf_counter() - t
     value = args.steps * m * w.C / dt
     sample = (f"outputs of the first {m} chunk(s) of batch element 0 of {w.name} per step "
@@ -267,7 +269,7 @@ def run_reference(args, w):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * dt / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, args),
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -276,11 +278,26 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-def config_of(w):
+LIN_NORMS = {"n": 0, "summed": 1, "position": 2}
+
+
+def variant_of(args, w):
+    """(quad_scale or None, lin_norm) from --quad-scale / --lin-norm; "cs" is
+    the page's 1/(C s)."""
+    qs = None
+    if args.quad_scale is not None:
+        qs = 1.0 / (w.C * w.s) if args.quad_scale == "cs" else float(args.quad_scale)
+    return qs, LIN_NORMS[args.lin_norm]
+
+
+def config_of(w, args=None):
     return {"workload": w.name, "B": w.B, "n": w.n, "C": w.C, "G": w.G, "s": w.s, "e": w.e,
             "causal": w.causal, "io_dtype": w.dtype, "accumulate": "fp32",
             "l2": "inputs larger than L2, 3 rotating buffer sets",
-            "parallelism": "replicas (one independent problem per GPU)"}
+            "parallelism": "replicas (one independent problem per GPU)",
+            **({} if args is None or (args.quad_scale is None and args.lin_norm == "n") else
+               {"quad_scale": variant_of(args, w)[0] or 1.0 / (w.C * w.C),
+                "lin_norm": args.lin_norm})}
 
 
 # ---------------------------------------------------------------- our arm
@@ -302,9 +319,14 @@ def run_ours(args, w, rank, world, device):
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
 
+    quad_scale, lin_norm = variant_of(args, w)
+
     def step(i, events=None):
         s = sets[i % 3]
-        if events is None:
+        if events is None and (quad_scale is not None or lin_norm):
+            fm.flash_mca_forward_ex(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws,
+                                    quad_scale, lin_norm, fm.FMCA_PATH_AUTO, stream)
+        elif events is None:
             fm.flash_mca_forward(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws, stream)
         else:
             fm.flash_mca_forward_timed(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws,
@@ -411,7 +433,7 @@ def run_ours(args, w, rank, world, device):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if w.dtype == "bf16" else "f32", "data": "synthetic",
-        "config": config_of(w),
+        "config": config_of(w, args),
         "tflops": tflops, "pct_bf16_peak": 100.0 * tflops / bf16_peak,
         "hbm_gbs_step": world * algorithmic_bytes(w) * args.steps / (ms / 1e3) / 1e9,
         "path": "tcgen05" if path == fm.FMCA_PATH_TCGEN05 else "simt",
@@ -441,6 +463,12 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=10.0,
                     help="seconds of oracle work for the CPU baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--quad-scale", default=None,
+                    help="intra-chunk weight scale: a number, or 'cs' for the page's 1/(C s) "
+                         "(default: 1/C^2); the headline loop then runs flash_mca_forward_ex")
+    ap.add_argument("--lin-norm", default="n", choices=list(LIN_NORMS),
+                    help="global-term divisor: n (default), summed (tokens the sum covers), "
+                         "position (t+1)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -26,12 +26,17 @@ __all__ = [
     "flash_mca_forward_host", "flash_mca_forward_noalloc", "flash_mca_device_status",
     "flash_mca_selftest_timeout", "FMCA_NOALLOC_SCRATCH_BYTES",
     "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
+    "FMCA_LIN_NORM_N", "FMCA_LIN_NORM_SUMMED", "FMCA_LIN_NORM_POSITION", "FmcaOptions",
+    "flash_mca_default_options", "flash_mca_forward_ex",
 ]
 
 FMCA_OK, FMCA_ERR_INVALID_ARG, FMCA_ERR_SHAPE, FMCA_ERR_UNSUPPORTED = 0, 1, 2, 3
 FMCA_ERR_ALIGN, FMCA_ERR_WORKSPACE, FMCA_ERR_CUDA, FMCA_ERR_TIMEOUT = 4, 5, 6, 7
 FMCA_F32, FMCA_BF16 = 0, 1
 FMCA_PATH_AUTO, FMCA_PATH_SIMT, FMCA_PATH_TCGEN05 = 0, 1, 2
+# global-term divisors of flash_mca_forward_ex: n; the tokens the sum covers;
+# the token's position counted from 1
+FMCA_LIN_NORM_N, FMCA_LIN_NORM_SUMMED, FMCA_LIN_NORM_POSITION = 0, 1, 2
 FMCA_NOALLOC_SCRATCH_BYTES = 64 << 20  # size of the fixed scratch of flash_mca_forward_noalloc
 
 library_path = _build.LIB
@@ -50,12 +55,21 @@ _vp, _sz, _i32, _cp = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int32, ctypes.c
 _int = ctypes.c_int
 _fwd_args = [_vp, _vp, _vp, _vp, _vp, _vp, _int, _int, _int, _int, _int, _int, _i32, _vp, _sz]
 
+
+class FmcaOptions(ctypes.Structure):
+    """``fmca_options`` of the header: intra-chunk weights quad_scale *
+    relu(q . k)^2 and the global-term divisor lin_norm (FMCA_LIN_NORM_*)."""
+    _fields_ = [("quad_scale", ctypes.c_float), ("lin_norm", _i32)]
+
+
 # (name, restype, argtypes) for every symbol the header declares
 _SIGNATURES = [
     ("flash_mca_workspace_bytes", _sz, [_int] * 6 + [_i32]),
     ("flash_mca_forward", _i32, _fwd_args + [_vp]),
     ("flash_mca_forward_path", _i32, _fwd_args + [_i32, _vp]),
     ("flash_mca_forward_timed", _i32, _fwd_args + [_i32, ctypes.POINTER(_vp), _int, _vp]),
+    ("flash_mca_default_options", _i32, [_int, ctypes.POINTER(FmcaOptions)]),
+    ("flash_mca_forward_ex", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions), _vp]),
     ("flash_mca_auto_path", _int, [_int] * 6 + [_i32]),
     ("flash_mca_launch_count", _int, [_int] * 6 + [_i32, _i32]),
     ("flash_mca_host_arena_bytes", _sz, [_int] * 6 + [_i32]),
@@ -136,11 +150,14 @@ def _shapes(Z: torch.Tensor, V: torch.Tensor, U: torch.Tensor):
     return B, n, s, e
 
 
-def flash_mca_forward_path(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
-                           path: int = FMCA_PATH_AUTO, stream=None) -> None:
-    """Queue the forward pass on ``stream`` (default: torch's current stream)
-    with an explicit kernel path; all tensors are CUDA tensors the caller
-    owns."""
+def flash_mca_default_options(C: int) -> FmcaOptions:
+    opts = FmcaOptions()
+    _check(lib.flash_mca_default_options(int(C), ctypes.byref(opts)), "flash_mca_default_options")
+    return opts
+
+
+def _check_device_args(Z, V, U, gamma, beta, O, workspace):
+    B, n, s, e = _shapes(Z, V, U)
     B, n, s, e = _shapes(Z, V, U)
     for name, t in (("Z", Z), ("V", V), ("U", U), ("O", O), ("gamma", gamma), ("beta", beta),
                     ("workspace", workspace)):
@@ -155,12 +172,38 @@ def flash_mca_forward_path(Z, V, U, gamma, beta, O, C: int, causal: bool, worksp
         raise TypeError("Z, V, U and O must share one dtype")
     if tuple(O.shape) != (B, n, e):
         raise ValueError("O must be [B, n, e]")
-    ws_bytes = workspace.numel() * workspace.element_size()
+    return B, n, s, e, dt, workspace.numel() * workspace.element_size()
+
+
+def flash_mca_forward_path(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
+                           path: int = FMCA_PATH_AUTO, stream=None) -> None:
+    """Queue the forward pass on ``stream`` (default: torch's current stream)
+    with an explicit kernel path; all tensors are CUDA tensors the caller
+    owns."""
+    B, n, s, e, dt, ws_bytes = _check_device_args(Z, V, U, gamma, beta, O, workspace)
     st = lib.flash_mca_forward_path(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
                                     beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C),
                                     int(bool(causal)), dt, workspace.data_ptr(), ws_bytes, path,
                                     _stream_ptr(stream))
     _check(st, "flash_mca_forward_path")
+
+
+def flash_mca_forward_ex(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
+                         quad_scale: float | None = None, lin_norm: int = FMCA_LIN_NORM_N,
+                         path: int = FMCA_PATH_AUTO, stream=None) -> None:
+    """``flash_mca_forward_path`` with the scale and normalisation variants:
+    intra-chunk weights quad_scale * relu(q . k)^2 (default 1/C^2) and the
+    global-term divisor ``lin_norm`` (FMCA_LIN_NORM_*)."""
+    B, n, s, e, dt, ws_bytes = _check_device_args(Z, V, U, gamma, beta, O, workspace)
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    opts.lin_norm = int(lin_norm)
+    st = lib.flash_mca_forward_ex(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
+                                  beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C),
+                                  int(bool(causal)), dt, workspace.data_ptr(), ws_bytes, path,
+                                  ctypes.byref(opts), _stream_ptr(stream))
+    _check(st, "flash_mca_forward_ex")
 
 
 def flash_mca_forward_timed(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
@@ -236,9 +279,10 @@ def flash_mca_selftest_timeout(limit_us: int, stream=None) -> None:
 
 
 def forward(Z, V, U, gamma, beta, C: int, causal: bool, workspace=None, out=None,
-            path: int = FMCA_PATH_AUTO, stream=None) -> torch.Tensor:
+            path: int = FMCA_PATH_AUTO, stream=None, quad_scale: float | None = None,
+            lin_norm: int = FMCA_LIN_NORM_N) -> torch.Tensor:
     """Convenience wrapper: allocates O (and the workspace, if not given) with
-    torch and calls ``flash_mca_forward_path``."""
+    torch and calls ``flash_mca_forward_ex``."""
     B, n, s, e = _shapes(Z, V, U)
     if out is None:
         out = torch.empty((B, n, e), dtype=Z.dtype, device=Z.device)
@@ -247,5 +291,6 @@ def forward(Z, V, U, gamma, beta, C: int, causal: bool, workspace=None, out=None
         if nb == 0:
             raise FmcaError(FMCA_ERR_SHAPE, "flash_mca_workspace_bytes")
         workspace = torch.empty(nb, dtype=torch.uint8, device=Z.device)
-    flash_mca_forward_path(Z, V, U, gamma, beta, out, C, causal, workspace, path, stream)
+    flash_mca_forward_ex(Z, V, U, gamma, beta, out, C, causal, workspace, quad_scale, lin_norm,
+                         path, stream)
     return out

@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdint>
 
 #include "launch.h"
@@ -35,9 +36,38 @@ bool want_tc(int B, int n, int s, int e, int C, fmca_dtype dtype) {
 
 size_t elem_size(fmca_dtype dtype) { return dtype == FMCA_BF16 ? 2 : 4; }
 
+// The kernels' form of the options: relu(x * quad_a)^2 with quad_a =
+// sqrt(quad_scale).  The defaults give exactly quad_a = 1/C.
+fmca_status to_variant(const fmca_options *opts, int C, Variant *v) {
+  *v = default_variant(C);
+  if (!opts) return FMCA_OK;
+  const float q = opts->quad_scale;
+  if (!std::isfinite(q) || q < 0.0f) return FMCA_ERR_INVALID_ARG;
+  if (opts->lin_norm != FMCA_LIN_NORM_N && opts->lin_norm != FMCA_LIN_NORM_SUMMED &&
+      opts->lin_norm != FMCA_LIN_NORM_POSITION)
+    return FMCA_ERR_INVALID_ARG;
+  const double dq = (double)q, dflt = 1.0 / ((double)C * (double)C);
+  if ((float)dflt != q) v->quad_a = (float)std::sqrt(dq);
+  v->lin_norm = opts->lin_norm;
+  return FMCA_OK;
+}
+
+fmca_status forward_impl(const void *Z, const void *V, const void *U, const float *gamma,
+                         const float *beta, void *O, int B, int n, int s, int e, int C,
+                         int causal, fmca_dtype dtype, void *workspace, size_t workspace_bytes_,
+                         fmca_path path, const fmca_options *opts, void *const *events,
+                         int n_events, fmca_stream_t stream);
+
 }  // namespace
 
 extern "C" {
+
+fmca_status flash_mca_default_options(int C, fmca_options *opts) {
+  if (C <= 0 || !opts) return FMCA_ERR_INVALID_ARG;
+  opts->quad_scale = (float)(1.0 / ((double)C * (double)C));
+  opts->lin_norm = FMCA_LIN_NORM_N;
+  return FMCA_OK;
+}
 
 size_t flash_mca_workspace_bytes(int B, int n, int s, int e, int C, int causal,
                                  fmca_dtype dtype) {
@@ -66,7 +96,32 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     int n, int s, int e, int C, int causal, fmca_dtype dtype,
                                     void *workspace, size_t workspace_bytes_, fmca_path path,
                                     void *const *events, int n_events, fmca_stream_t stream) {
+  return forward_impl(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype, workspace,
+                      workspace_bytes_, path, nullptr, events, n_events, stream);
+}
+
+fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
+                                 const float *gamma, const float *beta, void *O, int B, int n,
+                                 int s, int e, int C, int causal, fmca_dtype dtype,
+                                 void *workspace, size_t workspace_bytes_, fmca_path path,
+                                 const fmca_options *opts, fmca_stream_t stream) {
+  return forward_impl(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype, workspace,
+                      workspace_bytes_, path, opts, nullptr, 0, stream);
+}
+
+}  // extern "C"
+
+namespace {
+
+fmca_status forward_impl(const void *Z, const void *V, const void *U, const float *gamma,
+                         const float *beta, void *O, int B, int n, int s, int e, int C,
+                         int causal, fmca_dtype dtype, void *workspace, size_t workspace_bytes_,
+                         fmca_path path, const fmca_options *opts, void *const *events,
+                         int n_events, fmca_stream_t stream) {
   fmca_status st = check_sizes(B, n, s, e, C, causal, dtype);
+  if (st != FMCA_OK) return st;
+  Variant var;
+  st = to_variant(opts, C, &var);
   if (st != FMCA_OK) return st;
   if (!Z || !V || !U || !gamma || !beta || !O) return FMCA_ERR_INVALID_ARG;
   if (path != FMCA_PATH_AUTO && path != FMCA_PATH_SIMT && path != FMCA_PATH_TCGEN05)
@@ -103,13 +158,17 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   int rc;
   if (use_tc)
-    rc = launch_tc_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0, workspace, cs,
-                           ev);
+    rc = launch_tc_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0, var,
+                           workspace, cs, ev);
   else
     rc = launch_simt_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0,
-                             dtype == FMCA_BF16 ? 1 : 0, workspace, cs, ev);
+                             dtype == FMCA_BF16 ? 1 : 0, var, workspace, cs, ev);
   return rc == 0 ? FMCA_OK : FMCA_ERR_CUDA;
 }
+
+}  // namespace
+
+extern "C" {
 
 fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
                                    const float *gamma, const float *beta, void *O, int B,

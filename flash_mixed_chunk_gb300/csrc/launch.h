@@ -38,16 +38,27 @@ inline size_t workspace_bytes(int B, int n, int s, int e, int C, int causal) {
   return workspace_layout(B, n, s, e, C, causal).total;
 }
 
+// Scale and normalisation variants (flash_mca_forward_ex): intra-chunk weights
+// relu(x * quad_a)^2 (quad_a = sqrt(quad_scale); 1/C by default), global-term
+// divisor lin_norm (FMCA_LIN_NORM_*).
+struct Variant {
+  float quad_a;
+  int lin_norm;
+};
+constexpr int kLinNormN = 0, kLinNormSummed = 1, kLinNormPosition = 2;
+inline Variant default_variant(int C) { return Variant{1.0f / (float)C, kLinNormN}; }
+
 // `events` (may be NULL) holds launch-count + 1 cudaEvent_t handles recorded
 // before the first kernel and after each kernel.
 int launch_simt_forward(const void *Z, const void *V, const void *U, const float *gamma,
                         const float *beta, void *O, int B, int n, int s, int e, int C,
-                        int causal, int dtype_bf16, void *workspace, cudaStream_t stream,
-                        cudaEvent_t const *events = nullptr);
+                        int causal, int dtype_bf16, const Variant &var, void *workspace,
+                        cudaStream_t stream, cudaEvent_t const *events = nullptr);
 
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
-                      void *workspace, cudaStream_t stream, cudaEvent_t const *events = nullptr);
+                      const Variant &var, void *workspace, cudaStream_t stream,
+                      cudaEvent_t const *events = nullptr);
 
 inline bool record_event(cudaEvent_t const *events, int i, cudaStream_t stream) {
   return events == nullptr || cudaEventRecord(events[i], stream) == cudaSuccess;

@@ -82,6 +82,7 @@ extern "C" fmca_status flash_mca_forward_noalloc(const void *Z, const void *V, c
   void *scratch = scratch_on_current_device();
   if (scratch == nullptr) return FMCA_ERR_CUDA;
   const int rc = fmca::launch_tc_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0,
-                                         scratch, reinterpret_cast<cudaStream_t>(stream));
+                                         fmca::default_variant(C), scratch,
+                                         reinterpret_cast<cudaStream_t>(stream));
   return rc == 0 ? FMCA_OK : FMCA_ERR_CUDA;
 }

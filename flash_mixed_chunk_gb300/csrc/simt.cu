@@ -10,6 +10,7 @@
 //                     P   = sum_h state_h / n          (bidirectional)
 //   simt_chunk_output O_g = U_g * (relu(T0_g T1_g^T / C)^2 V_g  [masked]
 //                                  + T2_g P_g)
+// (scale and divisor as the caller's variant chooses: 1/C and n by default).
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -99,23 +100,29 @@ __global__ void __launch_bounds__(kThreads)
   }
 }
 
-// causal: P[b][g][x] = sum_{h<g} S[b][h][x] * inv_n ; else P[b][x] = sum_h S * inv_n
+// causal: P[b][g][x] = sum_{h<g} S[b][h][x] * f(g) ; else P[b][x] = sum_h S * f
+// with f the inverse of the global-term divisor: 1/n by default; 1/(g*C) for
+// causal chunk g with the tokens-summed divisor; 1 with the per-position
+// divisor (the T2 rows carry 1/(t+1) instead).
 __global__ void simt_chunk_scan(const float *__restrict__ S, float *__restrict__ P, int B, int G,
-                                int64_t se, float inv_n, int causal) {
+                                int64_t se, float inv_n, int causal, int C, int lin_norm) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * se) return;
   const int64_t b = t / se, x = t % se;
   const float *src = S + b * G * se + x;
+  const float keep = lin_norm == kLinNormPosition ? 1.0f : inv_n;
   float run = 0.f;
   if (causal) {
     float *dst = P + b * G * se + x;
     for (int g = 0; g < G; ++g) {
-      dst[(int64_t)g * se] = run * inv_n;
+      const float f = lin_norm != kLinNormSummed ? keep
+                      : (g > 0 ? 1.0f / ((float)g * (float)C) : 0.0f);
+      dst[(int64_t)g * se] = run * f;
       run += src[(int64_t)g * se];
     }
   } else {
     for (int g = 0; g < G; ++g) run += src[(int64_t)g * se];
-    P[b * se + x] = run * inv_n;
+    P[b * se + x] = run * keep;
   }
 }
 
@@ -126,7 +133,7 @@ __global__ void __launch_bounds__(kThreads)
     simt_chunk_output(const T *__restrict__ Z, const T *__restrict__ V, const T *__restrict__ U,
                       const float *__restrict__ gamma, const float *__restrict__ beta,
                       const float *__restrict__ P, T *__restrict__ O, int n, int s, int e, int C,
-                      int G, int causal) {
+                      int G, int causal, float quad_a, int lin_norm) {
   extern __shared__ float sm[];
   float *t0 = sm;                      // [32][s]  quad_q rows
   float *t2 = t0 + kRows * s;          // [32][s]  lin_q rows
@@ -140,13 +147,14 @@ __global__ void __launch_bounds__(kThreads)
   const int tid = threadIdx.x, col = tid % kCols, rbase = tid / kCols;
   const int64_t chunk0 = (int64_t)b * n + (int64_t)g * C;
   const int r0 = rb * kRows;
-  const float inv_c = 1.0f / (float)C;
 
   for (int x = tid; x < kRows * s; x += kThreads) {
     int r = x / s, a = x % s;
     float z = (r0 + r < C) ? to_f(Z[(chunk0 + r0 + r) * s + a]) : 0.f;
     t0[x] = z * gamma[a] + beta[a];
-    t2[x] = z * gamma[2 * s + a] + beta[2 * s + a];
+    // per-position divisor: the lin_q row of token t carries 1/(t+1)
+    const float w = lin_norm == kLinNormPosition ? 1.0f / (float)(g * C + r0 + r + 1) : 1.0f;
+    t2[x] = (z * gamma[2 * s + a] + beta[2 * s + a]) * w;
   }
   float acc[kPerThread];
 #pragma unroll
@@ -174,7 +182,7 @@ __global__ void __launch_bounds__(kThreads)
       float dotv = 0.f;
       const float *q = t0 + r * s, *k = t1 + j * s;
       for (int a = 0; a < s; ++a) dotv = fmaf(q[a], k[a], dotv);
-      float rl = fmaxf(dotv * inv_c, 0.f);
+      float rl = fmaxf(dotv * quad_a, 0.f);
       float wt = rl * rl;
       bool valid = (r0 + r < C) && (k0 + j < C) && (!causal || k0 + j <= r0 + r);
       w[r * (kKeys + 1) + j] = valid ? wt : 0.f;
@@ -188,7 +196,7 @@ __global__ void __launch_bounds__(kThreads)
         acc[i] = fmaf(w[(rbase + 4 * i) * (kKeys + 1) + j], vv, acc[i]);
     }
   }
-  // global linear term: T2 rows . P_g  (P_g already divided by n)
+  // global linear term: T2 rows . P_g  (P_g already scaled by the divisor)
   const float *pg = P + (int64_t)(causal ? bg : b) * s * e;
   for (int a0 = 0; a0 < s; a0 += kKeys) {
     __syncthreads();
@@ -226,7 +234,7 @@ size_t output_smem_bytes(int s) {
 template <typename T>
 int launch_simt_impl(const void *Z, const void *V, const void *U, const float *gamma,
                      const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
-                     float *states, float *prefix, cudaStream_t stream,
+                     const Variant &var, float *states, float *prefix, cudaStream_t stream,
                      cudaEvent_t const *events) {
   const int G = n / C;
   const T *z = static_cast<const T *>(Z);
@@ -240,7 +248,8 @@ int launch_simt_impl(const void *Z, const void *V, const void *U, const float *g
   const int64_t se = (int64_t)s * e;
   const int64_t lanes = (int64_t)B * se;
   simt_chunk_scan<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(states, prefix, B, G, se,
-                                                                         1.0f / (float)n, causal);
+                                                                         1.0f / (float)n, causal, C,
+                                                                         var.lin_norm);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 2, stream)) return 1;
   const size_t smem = output_smem_bytes(s);
   if (cudaFuncSetAttribute(simt_chunk_output<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -248,7 +257,7 @@ int launch_simt_impl(const void *Z, const void *V, const void *U, const float *g
     return 1;
   dim3 g3(B * G * ((C + kRows - 1) / kRows), (e + kCols - 1) / kCols);
   simt_chunk_output<T><<<g3, kThreads, smem, stream>>>(z, v, u, gamma, beta, prefix, o, n, s, e,
-                                                       C, G, causal);
+                                                       C, G, causal, var.quad_a, var.lin_norm);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 3, stream)) return 1;
   return 0;
 }
@@ -257,16 +266,16 @@ int launch_simt_impl(const void *Z, const void *V, const void *U, const float *g
 
 int launch_simt_forward(const void *Z, const void *V, const void *U, const float *gamma,
                         const float *beta, void *O, int B, int n, int s, int e, int C,
-                        int causal, int dtype_bf16, void *workspace, cudaStream_t stream,
-                        cudaEvent_t const *events) {
+                        int causal, int dtype_bf16, const Variant &var, void *workspace,
+                        cudaStream_t stream, cudaEvent_t const *events) {
   const WorkspaceLayout L = workspace_layout(B, n, s, e, C, causal);
   float *states = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.states);
   float *prefix = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.prefix);
   if (dtype_bf16)
-    return launch_simt_impl<__nv_bfloat16>(Z, V, U, gamma, beta, O, B, n, s, e, C, causal,
+    return launch_simt_impl<__nv_bfloat16>(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, var,
                                            states, prefix, stream, events);
-  return launch_simt_impl<float>(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, states, prefix,
-                                 stream, events);
+  return launch_simt_impl<float>(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, var, states,
+                                 prefix, stream, events);
 }
 
 }  // namespace fmca

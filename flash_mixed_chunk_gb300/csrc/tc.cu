@@ -101,7 +101,8 @@ int tc_launch_count() { return 3; }
 
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
-                      void *workspace, cudaStream_t stream, cudaEvent_t const *events) {
+                      const Variant &var, void *workspace, cudaStream_t stream,
+                      cudaEvent_t const *events) {
   const int G = n / C;
   const int R = C / ROW_TILE;
   const int64_t se = (int64_t)s * e;
@@ -127,7 +128,9 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
 
   static bool attrs = false;
   if (!attrs) {
-    if (cudaFuncSetAttribute(tc_chunk_prep, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(tc_chunk_prep<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)PREP_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_chunk_prep<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PREP_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)AT_SMEM) != cudaSuccess)
@@ -140,9 +143,10 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   const int n_state = B * G * (e / E_TILE);
   const int n_score = B * G * (causal ? R * (R + 1) : R * (C / KEY_STAGE));
   const int n_prep = n_state + n_score;
-  tc_chunk_prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
+  auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
+  prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
       mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n, e,
-      C, G, causal, n_state, n_score);
+      C, G, causal, n_state, n_score, var.quad_a);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
   // The scan and the attention kernel are launched as programmatic dependents
   // of the kernel before them: each may start launching (and run its
@@ -159,8 +163,11 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  if (cudaLaunchKernelEx(&cfg, tc_state_scan, (const __nv_bfloat16 *)states, prefix, B, G, se,
-                         1.0f / (float)n, causal) != cudaSuccess ||
+  auto *scan = var.lin_norm == kLinNormSummed     ? tc_state_scan<kLinNormSummed>
+               : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
+                                                  : tc_state_scan<kLinNormN>;
+  if (cudaLaunchKernelEx(&cfg, scan, (const __nv_bfloat16 *)states, prefix, B, G, se,
+                         1.0f / (float)n, causal, C) != cudaSuccess ||
       !record_event(events, 2, stream))
     return 1;
   const int n_units = B * G * R * (e / E_TILE);

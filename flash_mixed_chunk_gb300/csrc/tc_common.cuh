@@ -49,5 +49,16 @@ __device__ __forceinline__ uint4 affine8(uint4 v, const float (&g)[8], const flo
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// affine8 followed by a scale w of the 8 results, before rounding.
+__device__ __forceinline__ uint4 affine8_scaled(uint4 v, const float (&g)[8], const float (&b)[8],
+                                                float w) {
+  uint32_t x[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    x[i] = pack_bf16x2((bf16_lo(x[i]) * g[2 * i] + b[2 * i]) * w,
+                       (bf16_hi(x[i]) * g[2 * i + 1] + b[2 * i + 1]) * w);
+  return make_uint4(x[0], x[1], x[2], x[3]);
+}
+
 }  // namespace
 }  // namespace fmca

@@ -85,6 +85,10 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
   return p;
 }
 
+// BY_POSITION: the lin_q rows carry the per-position divisor 1/(t+1) of the
+// global term (a separate instantiation, so that the default one carries no
+// code for it).
+template <bool BY_POSITION>
 __global__ void __launch_bounds__(PREP_THREADS, 1)
     tc_chunk_prep(const __grid_constant__ CUtensorMap mapZ64,   // Z [B*n][s], box {64, 64}
                   const __grid_constant__ CUtensorMap mapZ128,  // Z [B*n][s], box {64, 128}
@@ -93,7 +97,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                   const __grid_constant__ CUtensorMap mapPw,    // P [B*n][C], box {64, 128}
                   const float *__restrict__ gamma, const float *__restrict__ beta,
                   __nv_bfloat16 *__restrict__ t2out, unsigned int *__restrict__ sched, int n,
-                  int e, int C, int G, int causal, int n_state, int n_score) {
+                  int e, int C, int G, int causal, int n_state, int n_score, float quad_a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -105,8 +109,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int n_units = n_state + n_score;
-  // the scan kernel may start launching now; it waits for this grid to finish
-  griddep_launch_dependents();
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < PR_RING; ++i) {
@@ -159,6 +161,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
       for (int i = 0; ok; ++i) {
         const int uu = u_next < n_units ? u_next : -1;
         if (uu >= 0) u_next = next_unit();
+        // This CTA has taken its last unit: the scan kernel may start launching
+        // once every CTA is this far (it waits for this grid to finish before
+        // reading).  Triggered no earlier, so that its blocks do not sit on the
+        // SMs beside this kernel's CTAs for their whole run.
+        if (u_next >= n_units) griddep_launch_dependents();
         const int qs = i % PR_QUEUE;
         if (i >= PR_QUEUE && !mbar_wait(&q_empty[qs], ((i / PR_QUEUE) - 1) & 1, kWaitLimitNs)) {
           record_timeout(500);
@@ -314,14 +321,19 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
       } else if (pu.kind == KIND_SCORE) {
         // query rows (atom a: 128 rows): T0 in place; T2 to global from the
         // same Z values, once per row tile (by its key-stage-0 unit)
+        const int tpos0 = BY_POSITION ? pu.row0 % n : 0;  // position of the tile's first row
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int r = rb + 8 * i;
           uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 16384 + r * 128 + p * 16);
           const uint4 z = *ptr;
-          if (pu.ks == 0)
-            *reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + cl) =
-                affine8(z, g2, b2);
+          if (pu.ks == 0) {
+            uint4 *t2p = reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + cl);
+            if (BY_POSITION)  // row t of its sequence carries 1/(t+1)
+              *t2p = affine8_scaled(z, g2, b2, 1.0f / (float)(tpos0 + r + 1));
+            else
+              *t2p = affine8(z, g2, b2);
+          }
           *ptr = affine8(z, g0, b0);
         }
         // keys (atom a: 64 rows): T1 in place
@@ -347,7 +359,6 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // accumulator row (state row s or query row)
     uint8_t *stage = smem + PR_OFF_STAGE;
-    const float inv_c = 1.0f / (float)C;
     int nst = 0;  // staging tiles written so far
     for (int j = 0;; ++j) {
       const int buf = j & 1, use = j >> 1;
@@ -371,14 +382,15 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         tmem_ld32(dcol + q * 64 + 32, r[1]);
         tmem_ld_wait();
         if (p.kind == KIND_SCORE) {
-          // relu(S / C)^2; causal: key position > query position -> 0
+          // relu(S * quad_a)^2 (quad_a = 1/C by default); causal: key position >
+          // query position -> 0
           const int qpos = p.rt * ROW_TILE + row;
           const int kbase = p.ks * KEY_STAGE;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
             for (int i = 0; i < 32; ++i) {
-              float x = fmaxf(__uint_as_float(r[c2][i]) * inv_c, 0.f);
+              float x = fmaxf(__uint_as_float(r[c2][i]) * quad_a, 0.f);
               x = x * x;
               if (causal && kbase + c2 * 32 + i > qpos) x = 0.f;
               r[c2][i] = __float_as_uint(x);

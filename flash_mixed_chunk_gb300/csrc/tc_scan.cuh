@@ -12,12 +12,17 @@ namespace {
 
 // =====================================================================
 // tc_state_scan: prefix (or total) over chunks of the bf16 states, in fp32,
-// scaled by 1/n and rounded to bf16.  The thread count is a multiple of 32
+// scaled by the global-term divisor's inverse (1/n by default; 1/(g*C) for
+// causal chunk g with the tokens-summed divisor; 1 with the per-position
+// divisor, which the T2 rows carry instead) and rounded to bf16.  The thread count is a multiple of 32
 // for every shape this path takes (B * s * e / 8).
 // =====================================================================
+// LIN_NORM: the global-term divisor (kLinNorm*), one instantiation each, so
+// that the default one is the plain 1/n scan.
+template <int LIN_NORM>
 __global__ void __launch_bounds__(256)
     tc_state_scan(const __nv_bfloat16 *__restrict__ S, __nv_bfloat16 *__restrict__ P, int B,
-                  int G, int64_t se, float inv_n, int causal) {
+                  int G, int64_t se, float inv_n, int causal, int C) {
   // launched as a dependent of the prep kernel: wait for its states; let the
   // attention kernel start launching (it waits for this grid in turn)
   griddep_wait();
@@ -31,6 +36,7 @@ __global__ void __launch_bounds__(256)
   float run[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) run[i] = 0.f;
+  const float keep = LIN_NORM == kLinNormPosition ? 1.0f : inv_n;  // all but summed+causal
   constexpr int U = 8;
   for (int g0 = 0; g0 < G; g0 += U) {
     uint4 v[U];
@@ -41,11 +47,14 @@ __global__ void __launch_bounds__(256)
     for (int u = 0; u < U; ++u) {
       if (g0 + u < G) {
         if (causal) {
+          const int g = g0 + u;
+          const float f = LIN_NORM != kLinNormSummed ? keep
+                          : (g > 0 ? 1.0f / ((float)g * (float)C) : 0.0f);
           uint4 o;
-          o.x = pack_bf16x2(run[0] * inv_n, run[1] * inv_n);
-          o.y = pack_bf16x2(run[2] * inv_n, run[3] * inv_n);
-          o.z = pack_bf16x2(run[4] * inv_n, run[5] * inv_n);
-          o.w = pack_bf16x2(run[6] * inv_n, run[7] * inv_n);
+          o.x = pack_bf16x2(run[0] * f, run[1] * f);
+          o.y = pack_bf16x2(run[2] * f, run[3] * f);
+          o.z = pack_bf16x2(run[4] * f, run[5] * f);
+          o.w = pack_bf16x2(run[6] * f, run[7] * f);
           *reinterpret_cast<uint4 *>(dst + (int64_t)(g0 + u) * se) = o;
         }
         const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
@@ -68,10 +77,10 @@ __global__ void __launch_bounds__(256)
   }
   if (!causal) {
     uint4 o;
-    o.x = pack_bf16x2(run[0] * inv_n, run[1] * inv_n);
-    o.y = pack_bf16x2(run[2] * inv_n, run[3] * inv_n);
-    o.z = pack_bf16x2(run[4] * inv_n, run[5] * inv_n);
-    o.w = pack_bf16x2(run[6] * inv_n, run[7] * inv_n);
+    o.x = pack_bf16x2(run[0] * keep, run[1] * keep);
+    o.y = pack_bf16x2(run[2] * keep, run[3] * keep);
+    o.z = pack_bf16x2(run[4] * keep, run[5] * keep);
+    o.w = pack_bf16x2(run[6] * keep, run[7] * keep);
     *reinterpret_cast<uint4 *>(dst) = o;
   }
 }

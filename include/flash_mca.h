@@ -136,6 +136,52 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     void *const *events, int n_events,
                                     fmca_stream_t stream);
 
+/*
+ * Scale and normalisation variants.  The page states some factors in more
+ * than one way; flash_mca_forward uses the readings given at the top of this
+ * file, flash_mca_forward_ex lets the caller pick:
+ *
+ *   quad_scale   intra-chunk weights are quad_scale * relu(T0_i . T1_j)^2.
+ *                "Mixed Chunk", eq. for V^quad_g, writes 1/(cs) relu^2(Q K^T):
+ *                quad_scale = 1/(C s).  The default relu(x/C)^2 (the appendix
+ *                scale of "Weak Attention" applied per chunk) is 1/C^2.
+ *                Must be finite and >= 0.
+ *   lin_norm     the divisor of the global term:
+ *     FMCA_LIN_NORM_N         n, in both modes (default; "Mixed Chunk", the
+ *                             non-causal eq.'s 1/n).
+ *     FMCA_LIN_NORM_SUMMED    the number of tokens the global sum covers: g*C
+ *                             for chunk g (counted from 0) in causal mode --
+ *                             the decoder eq.'s 1/((g-1)c) with chunks counted
+ *                             from 1 -- and n otherwise.  Chunk 0's causal sum
+ *                             is empty, so its global term is 0.
+ *     FMCA_LIN_NORM_POSITION  t+1 for the token at position t (counted from 0)
+ *                             of its sequence ("Extended Thoughts": the sum of
+ *                             the first t items should be divided by t).
+ */
+typedef int32_t fmca_lin_norm;
+#define FMCA_LIN_NORM_N 0
+#define FMCA_LIN_NORM_SUMMED 1
+#define FMCA_LIN_NORM_POSITION 2
+
+typedef struct fmca_options {
+  float quad_scale;
+  fmca_lin_norm lin_norm;
+} fmca_options;
+
+/* Fills *opts with the defaults for chunk length C (quad_scale = 1/C^2,
+ * lin_norm = FMCA_LIN_NORM_N).  FMCA_ERR_INVALID_ARG for C <= 0 or NULL. */
+fmca_status flash_mca_default_options(int C, fmca_options *opts);
+
+/* flash_mca_forward_path with the variants of `opts` (host pointer, read
+ * during the call; NULL means the defaults).  A negative or non-finite
+ * quad_scale or an unknown lin_norm returns FMCA_ERR_INVALID_ARG.  Same
+ * kernels, workspace and launch count as flash_mca_forward_path. */
+fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
+                                 const float *gamma, const float *beta, void *O, int B,
+                                 int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                                 void *workspace, size_t workspace_bytes, fmca_path path,
+                                 const fmca_options *opts, fmca_stream_t stream);
+
 /* Which path FMCA_PATH_AUTO takes for these arguments (FMCA_PATH_SIMT or
  * FMCA_PATH_TCGEN05), or -1 for arguments that would be rejected. */
 int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype);

@@ -160,3 +160,35 @@ def test_python_binding_rejects_bad_tensors():
         fm.flash_mca_forward(Z, V, V, torch.zeros(4, 32), torch.zeros(4, 32), V, 64, True, Z)
     with pytest.raises(ValueError):
         fm.forward(Z[0], V, V, torch.zeros(4, 32), torch.zeros(4, 32), 64, True)
+
+
+def fwd_ex(opts, **kw):
+    args = dict(Z=P, V=P + 0x10000000, U=P + 0x20000000, g=P + 0x30000000, b=P + 0x30001000,
+                O=P + 0x40000000, B=1, n=256, s=32, e=64, C=64, causal=1, dt=fm.FMCA_F32,
+                ws=P + 0x50000000, wsb=BIG, path=fm.FMCA_PATH_AUTO)
+    args.update(kw)
+    return fm.lib.flash_mca_forward_ex(args["Z"], args["V"], args["U"], args["g"], args["b"],
+                                       args["O"], args["B"], args["n"], args["s"], args["e"],
+                                       args["C"], args["causal"], args["dt"], args["ws"],
+                                       args["wsb"], args["path"], opts, None)
+
+
+def test_default_options():
+    import ctypes
+    o = fm.FmcaOptions()
+    assert fm.lib.flash_mca_default_options(256, ctypes.byref(o)) == fm.FMCA_OK
+    assert o.quad_scale == 1.0 / 65536.0 and o.lin_norm == fm.FMCA_LIN_NORM_N
+    assert fm.lib.flash_mca_default_options(0, ctypes.byref(o)) == fm.FMCA_ERR_INVALID_ARG
+    assert fm.lib.flash_mca_default_options(64, None) == fm.FMCA_ERR_INVALID_ARG
+
+
+def test_options_validation_codes():
+    import ctypes
+    for q, ln in ((-1.0, 0), (float("nan"), 0), (float("inf"), 0), (0.5, 3), (0.5, -1)):
+        o = fm.FmcaOptions(q, ln)
+        assert fwd_ex(ctypes.byref(o)) == fm.FMCA_ERR_INVALID_ARG, (q, ln)
+    # valid options still go through the other host checks first
+    o = fm.FmcaOptions(0.25, fm.FMCA_LIN_NORM_POSITION)
+    assert fwd_ex(ctypes.byref(o), C=60) == fm.FMCA_ERR_SHAPE
+    assert fwd_ex(ctypes.byref(o), ws=0) == fm.FMCA_ERR_WORKSPACE
+    assert fwd_ex(None, V=P + 0x10000008) == fm.FMCA_ERR_ALIGN
