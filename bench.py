@@ -300,6 +300,105 @@ def config_of(w, args=None):
                 "lin_norm": args.lin_norm})}
 
 
+# ---------------------------------------------------------------- decode
+def decode_bytes_per_token(s, e, C, i):
+    """Bytes one decode step must move per sequence at chunk index i: the
+    carried fp32 state (s x e), the i cached Z and V rows of its chunk, the
+    token's z, v, u and its output o (bf16); plus, at the chunk's last token,
+    the fold (cache read once, state read and written)."""
+    b = 4 * s * e + 2 * i * (s + e) + 2 * (s + 3 * e)
+    if i == C - 1:
+        b += 2 * C * (s + e) + 8 * s * e
+    return b
+
+
+def run_decode(args, device):
+    """Autoregressive decoding of B sequences in lockstep through
+    flash_mca_decode_step: K consecutive positions from t0 (whole chunks, so
+    every chunk index and one fold per chunk are in the timed region)."""
+    import flash_mixed_chunk_gb300 as fm
+    torch.cuda.set_device(device)
+    B, s, e, C = args.decode_batch, 128, 1536, 256
+    t0, K, W = 4 * C, 2 * C, C
+    n_norm = 16 * C
+    qs, ln = variant_of(args, mca_inputs.WORKLOADS["gau_base_causal"])
+    g = torch.Generator().manual_seed(11)
+    rows = W + K
+    z = torch.nn.functional.silu(torch.randn(rows, B, s, generator=g)).to(torch.bfloat16).to(device)
+    v = torch.nn.functional.silu(torch.randn(rows, B, e, generator=g)).to(torch.bfloat16).to(device)
+    u = torch.nn.functional.silu(torch.randn(rows, B, e, generator=g)).to(torch.bfloat16).to(device)
+    gamma = (1 + 0.1 * torch.randn(4, s, generator=g)).to(device)
+    beta = (0.1 * torch.randn(4, s, generator=g)).to(device)
+    o = torch.empty(B, e, dtype=torch.bfloat16, device=device)
+    state = torch.empty(fm.flash_mca_decode_state_bytes(B, s, e, C, fm.FMCA_BF16),
+                        dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    fm.flash_mca_decode_reset(state, B, s, e, C, fm.FMCA_BF16, stream)
+    # positions t0 - W .. t0 - 1 warm up (the state then holds earlier chunks)
+    for k in range(W):
+        fm.flash_mca_decode_step(z[k], v[k], u[k], gamma, beta, o, C, t0 - W + k, state, n_norm,
+                                 qs, ln, stream)
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    # the timed loop calls the C entry point directly (pointers prepared
+    # above), so that it measures the library, not Python argument checks
+    opts = fm.flash_mca_default_options(C)
+    if qs is not None:
+        opts.quad_scale = qs
+    opts.lin_norm = ln
+    import ctypes
+    call = fm.lib.flash_mca_decode_step
+    sp = stream.cuda_stream
+    zp = [z[W + k].data_ptr() for k in range(K)]
+    vp = [v[W + k].data_ptr() for k in range(K)]
+    up = [u[W + k].data_ptr() for k in range(K)]
+    gp, bp, op, stp, stb = gamma.data_ptr(), beta.data_ptr(), o.data_ptr(), state.data_ptr(), \
+        state.numel()
+    ob = ctypes.byref(opts)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    a.record(stream)
+    h0 = time.perf_counter()
+    for k in range(K):
+        rc = call(zp[k], vp[k], up[k], gp, bp, op, B, s, e, C, t0 + k, n_norm, fm.FMCA_BF16, ob,
+                  stp, stb, sp)
+        if rc:
+            raise RuntimeError(fm.flash_mca_status_string(rc))
+    host_us = (time.perf_counter() - h0) / K * 1e6
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.time()
+    sampler.stop()
+    st, where = fm.flash_mca_device_status()
+    if st != fm.FMCA_OK:
+        raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
+    ms = a.elapsed_time(b)
+    nbytes = B * sum(decode_bytes_per_token(s, e, C, (t0 + k) % C) for k in range(K))
+    peaks, peak_kind = load_peaks()
+    hbm_peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
+    achieved = nbytes / (ms / 1e3) / 1e9
+    folds = sum(1 for k in range(K) if (t0 + k) % C == C - 1)
+    line = {
+        "metric": "mixed-chunk attn decode tokens/s (B sequences in lockstep) at 1 GB300",
+        "value": B * K / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": K, "warmup": W,
+        "ms_per_step": ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "decode", "B": B, "s": s, "e": e, "C": C,
+                   "positions": f"{t0}..{t0 + K - 1}", "n_norm": n_norm,
+                   **({} if qs is None and ln == 0 else {"quad_scale": qs, "lin_norm": args.lin_norm})},
+        "roofline": {"bound": "hbm", "kernel": "decode step (decode_token + decode_fold)",
+                     "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "traffic": None,
+                     "algorithmic_bytes_per_step": nbytes / K,
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"},
+        "gpu_launches": K + folds,
+        "host_enqueue_us_per_step": host_us,
+        "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, w, rank, world, device):
     import flash_mixed_chunk_gb300 as fm
@@ -466,6 +565,10 @@ def main():
     ap.add_argument("--quad-scale", default=None,
                     help="intra-chunk weight scale: a number, or 'cs' for the page's 1/(C s) "
                          "(default: 1/C^2); the headline loop then runs flash_mca_forward_ex")
+    ap.add_argument("--decode", action="store_true",
+                    help="time the autoregressive decode step instead of the forward pass "
+                         "(its own JSON line)")
+    ap.add_argument("--decode-batch", type=int, default=8)
     ap.add_argument("--lin-norm", default="n", choices=list(LIN_NORMS),
                     help="global-term divisor: n (default), summed (tokens the sum covers), "
                          "position (t+1)")
@@ -477,6 +580,10 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.decode:
+        if rank == 0 and args.impl == "ours":
+            run_decode(args, torch.device("cuda", local))
+        return
     if args.impl == "reference":
         if rank == 0:
             run_reference(args, w)

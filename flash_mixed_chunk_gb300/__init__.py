@@ -27,7 +27,8 @@ __all__ = [
     "flash_mca_selftest_timeout", "FMCA_NOALLOC_SCRATCH_BYTES",
     "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
     "FMCA_LIN_NORM_N", "FMCA_LIN_NORM_SUMMED", "FMCA_LIN_NORM_POSITION", "FmcaOptions",
-    "flash_mca_default_options", "flash_mca_forward_ex",
+    "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
+    "flash_mca_decode_reset", "flash_mca_decode_step",
 ]
 
 FMCA_OK, FMCA_ERR_INVALID_ARG, FMCA_ERR_SHAPE, FMCA_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -70,6 +71,10 @@ _SIGNATURES = [
     ("flash_mca_forward_timed", _i32, _fwd_args + [_i32, ctypes.POINTER(_vp), _int, _vp]),
     ("flash_mca_default_options", _i32, [_int, ctypes.POINTER(FmcaOptions)]),
     ("flash_mca_forward_ex", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions), _vp]),
+    ("flash_mca_decode_state_bytes", _sz, [_int] * 4 + [_i32]),
+    ("flash_mca_decode_reset", _i32, [_vp, _sz] + [_int] * 4 + [_i32, _vp]),
+    ("flash_mca_decode_step", _i32, [_vp] * 6 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
+                                                             _vp, _sz, _vp]),
     ("flash_mca_auto_path", _int, [_int] * 6 + [_i32]),
     ("flash_mca_launch_count", _int, [_int] * 6 + [_i32, _i32]),
     ("flash_mca_host_arena_bytes", _sz, [_int] * 6 + [_i32]),
@@ -264,6 +269,53 @@ def flash_mca_forward_noalloc(Z, V, U, gamma, beta, O, C: int, causal: bool,
                                        gamma.data_ptr(), beta.data_ptr(), O.data_ptr(), B, n, s,
                                        e, int(C), int(bool(causal)), dt, _stream_ptr(stream))
     _check(st, "flash_mca_forward_noalloc")
+
+
+def flash_mca_decode_state_bytes(B: int, s: int, e: int, C: int, dtype: int) -> int:
+    return int(lib.flash_mca_decode_state_bytes(B, s, e, C, dtype))
+
+
+def flash_mca_decode_reset(state, B: int, s: int, e: int, C: int, dtype: int,
+                           stream=None) -> None:
+    """Clear a decode state (a CUDA byte tensor) before position 0."""
+    if not state.is_cuda:
+        raise ValueError("state must be a CUDA tensor")
+    _check(lib.flash_mca_decode_reset(state.data_ptr(), state.numel() * state.element_size(), B,
+                                      s, e, C, dtype, _stream_ptr(stream)),
+           "flash_mca_decode_reset")
+
+
+def flash_mca_decode_step(z, v, u, gamma, beta, o, C: int, t: int, state, n_norm: int = 0,
+                          quad_scale: float | None = None, lin_norm: int = FMCA_LIN_NORM_N,
+                          stream=None) -> None:
+    """One decode step for the tokens at position ``t`` of B sequences:
+    z [B, s], v, u, o [B, e] CUDA tensors; ``state`` as sized by
+    ``flash_mca_decode_state_bytes`` and cleared by ``flash_mca_decode_reset``
+    before t = 0.  ``n_norm``: the length n the default divisor uses."""
+    if z.dim() != 2 or v.dim() != 2 or u.dim() != 2 or o.dim() != 2:
+        raise ValueError("z, v, u, o must be 2-D: [B, s], [B, e], [B, e], [B, e]")
+    B, s = z.shape
+    e = v.shape[1]
+    for name, x in (("z", z), ("v", v), ("u", u), ("o", o), ("gamma", gamma), ("beta", beta),
+                    ("state", state)):
+        if not x.is_cuda or not x.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if tuple(v.shape) != (B, e) or tuple(u.shape) != (B, e) or tuple(o.shape) != (B, e):
+        raise ValueError("v, u and o must be [B, e] with z [B, s]")
+    dt = _dtype_code(z)
+    if v.dtype != z.dtype or u.dtype != z.dtype or o.dtype != z.dtype:
+        raise TypeError("z, v, u and o must share one dtype")
+    if gamma.dtype != torch.float32 or tuple(gamma.shape) != (4, s) or tuple(beta.shape) != (4, s):
+        raise ValueError("gamma and beta must be float32 [4, s]")
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    opts.lin_norm = int(lin_norm)
+    st = lib.flash_mca_decode_step(z.data_ptr(), v.data_ptr(), u.data_ptr(), gamma.data_ptr(),
+                                   beta.data_ptr(), o.data_ptr(), B, s, e, int(C), int(t),
+                                   int(n_norm), dt, ctypes.byref(opts), state.data_ptr(),
+                                   state.numel() * state.element_size(), _stream_ptr(stream))
+    _check(st, "flash_mca_decode_step")
 
 
 def flash_mca_device_status(stream=None) -> tuple[int, int]:

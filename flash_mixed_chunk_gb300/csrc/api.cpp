@@ -100,6 +100,65 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                       workspace_bytes_, path, nullptr, events, n_events, stream);
 }
 
+size_t flash_mca_decode_state_bytes(int B, int s, int e, int C, fmca_dtype dtype) {
+  if (B <= 0 || s <= 0 || e <= 0 || C <= 0) return 0;
+  if (dtype != FMCA_F32 && dtype != FMCA_BF16) return 0;
+  if (s > 256 || C > kDecodeMaxC) return 0;
+  if ((int64_t)B * s * e >= ((int64_t)1 << 31) || (int64_t)B * C * (s > e ? s : e) >= ((int64_t)1 << 31))
+    return 0;
+  return decode_state_layout(B, s, e, C, elem_size(dtype)).total;
+}
+
+fmca_status flash_mca_decode_reset(void *state, size_t state_bytes, int B, int s, int e, int C,
+                                   fmca_dtype dtype, fmca_stream_t stream) {
+  const size_t need = flash_mca_decode_state_bytes(B, s, e, C, dtype);
+  if (need == 0) return FMCA_ERR_INVALID_ARG;
+  if (!state || state_bytes < need) return FMCA_ERR_WORKSPACE;
+  if (!aligned256(state)) return FMCA_ERR_ALIGN;
+  // only the carried sum must start at zero; cache slots are written before
+  // they are read
+  const DecodeStateLayout L = decode_state_layout(B, s, e, C, elem_size(dtype));
+  return cudaMemsetAsync(state, 0, L.Zc - L.P, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? FMCA_OK
+             : FMCA_ERR_CUDA;
+}
+
+fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
+                                  const float *gamma, const float *beta, void *o, int B, int s,
+                                  int e, int C, int t, int n_norm, fmca_dtype dtype,
+                                  const fmca_options *opts, void *state, size_t state_bytes,
+                                  fmca_stream_t stream) {
+  const size_t need = flash_mca_decode_state_bytes(B, s, e, C, dtype);
+  if (need == 0 || t < 0) return FMCA_ERR_INVALID_ARG;
+  if (!z || !v || !u || !gamma || !beta || !o) return FMCA_ERR_INVALID_ARG;
+  Variant var;
+  fmca_status st = to_variant(opts, C, &var);
+  if (st != FMCA_OK) return st;
+  if (var.lin_norm == FMCA_LIN_NORM_N && n_norm <= t) return FMCA_ERR_INVALID_ARG;
+  if (!aligned16(z) || !aligned16(v) || !aligned16(u) || !aligned16(o) || !aligned16(gamma) ||
+      !aligned16(beta))
+    return FMCA_ERR_ALIGN;
+  if (!state || state_bytes < need) return FMCA_ERR_WORKSPACE;
+  if (!aligned256(state)) return FMCA_ERR_ALIGN;
+  {  // o must not overlap the inputs or the state
+    const size_t es = elem_size(dtype);
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(o), o1 = o0 + (size_t)B * e * es;
+    auto overlaps = [&](const void *p, size_t bytes) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + bytes;
+      return a0 < o1 && o0 < a1;
+    };
+    if (overlaps(z, (size_t)B * s * es) || overlaps(v, (size_t)B * e * es) ||
+        overlaps(u, (size_t)B * e * es) || overlaps(state, state_bytes))
+      return FMCA_ERR_INVALID_ARG;
+  }
+  return launch_decode_step(z, v, u, gamma, beta, o, B, s, e, C, t, n_norm,
+                            dtype == FMCA_BF16 ? 1 : 0, var, state,
+                            reinterpret_cast<cudaStream_t>(stream)) == 0
+             ? FMCA_OK
+             : FMCA_ERR_CUDA;
+}
+
 fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                                  const float *gamma, const float *beta, void *O, int B, int n,
                                  int s, int e, int C, int causal, fmca_dtype dtype,

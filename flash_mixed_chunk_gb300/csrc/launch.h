@@ -64,6 +64,30 @@ inline bool record_event(cudaEvent_t const *events, int i, cudaStream_t stream) 
   return events == nullptr || cudaEventRecord(events[i], stream) == cudaSuccess;
 }
 
+// Decode state (caller-owned, flash_mca_decode_state_bytes), each region
+// 256-byte aligned:
+//   P   fp32 [B][s][e]   sum of T3^T V over the completed chunks
+//   Zc  [B][C][s]        Z rows of the current chunk's tokens (I/O type)
+//   Vc  [B][C][e]        their V rows (I/O type)
+struct DecodeStateLayout {
+  size_t P, Zc, Vc, total;
+};
+inline DecodeStateLayout decode_state_layout(int B, int s, int e, int C, size_t elem) {
+  DecodeStateLayout L;
+  L.P = 0;
+  L.Zc = align256(sizeof(float) * (size_t)B * s * e);
+  L.Vc = L.Zc + align256(elem * (size_t)B * C * s);
+  L.total = L.Vc + align256(elem * (size_t)B * C * e);
+  return L;
+}
+constexpr int kDecodeMaxC = 1024;  // chunk length the decode kernels take
+
+// One decode step for the token at position t (launches 1 kernel, or 2 at
+// the last token of a chunk).
+int launch_decode_step(const void *z, const void *v, const void *u, const float *gamma,
+                       const float *beta, void *o, int B, int s, int e, int C, int t, int n_norm,
+                       int dtype_bf16, const Variant &var, void *state, cudaStream_t stream);
+
 // Shapes the tensor-core path covers.
 bool tc_supported(int B, int n, int s, int e, int C);
 int tc_launch_count();

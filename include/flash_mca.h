@@ -182,6 +182,45 @@ fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                                  void *workspace, size_t workspace_bytes, fmca_path path,
                                  const fmca_options *opts, fmca_stream_t stream);
 
+/*
+ * Autoregressive decoding, one token per call, in the recurrent form of the
+ * causal core ("Mixed Chunk": the decoder's masked intra-chunk term and the
+ * cumsum form of the global term; the linear-attention recurrence of
+ * "大模型训练之加速篇 -attention优化", section 1.4).  For B sequences decoded in
+ * lockstep, the token at position t (chunk g = t / C, index i = t % C) gets
+ *
+ *   o = u * ( sum_{j <= i in chunk g} quad_scale * relu(T0_t . T1_j)^2 v_j
+ *           + T2_t . (sum_{h < g} T3_h^T V_h) / d(t) )
+ *
+ * which is row t of flash_mca_forward(causal = 1) over the sequence decoded so
+ * far.  d(t) is n_norm (FMCA_LIN_NORM_N: pass the length n of the sequence
+ * whose forward pass the decode must reproduce), g*C (FMCA_LIN_NORM_SUMMED) or
+ * t+1 (FMCA_LIN_NORM_POSITION); quad_scale and lin_norm come from `opts`
+ * (NULL: the defaults).  The caller-owned device `state` carries the fp32 sum
+ * of T3^T V over completed chunks and the current chunk's Z and V rows:
+ *
+ *   flash_mca_decode_state_bytes  its size (0 for rejected sizes);
+ *   flash_mca_decode_reset        clears it before position 0 (queued on
+ *                                 `stream`);
+ *   flash_mca_decode_step         one token: z [B][s], v, u, o [B][e] device
+ *                                 arrays of `dtype`, 16-byte aligned; calls
+ *                                 must come in order t = 0, 1, 2, ... on one
+ *                                 stream (the state is not told which
+ *                                 positions it has seen).  The last token of a
+ *                                 chunk also folds the chunk into the state.
+ *
+ * Sizes: B, s, e >= 1, s <= 256, 1 <= C <= 1024, t >= 0; n_norm > t for
+ * FMCA_LIN_NORM_N (ignored otherwise).  fp32 arithmetic on the CUDA cores.
+ */
+size_t flash_mca_decode_state_bytes(int B, int s, int e, int C, fmca_dtype dtype);
+fmca_status flash_mca_decode_reset(void *state, size_t state_bytes, int B, int s, int e, int C,
+                                   fmca_dtype dtype, fmca_stream_t stream);
+fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
+                                  const float *gamma, const float *beta, void *o, int B, int s,
+                                  int e, int C, int t, int n_norm, fmca_dtype dtype,
+                                  const fmca_options *opts, void *state, size_t state_bytes,
+                                  fmca_stream_t stream);
+
 /* Which path FMCA_PATH_AUTO takes for these arguments (FMCA_PATH_SIMT or
  * FMCA_PATH_TCGEN05), or -1 for arguments that would be rejected. */
 int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype);

@@ -192,3 +192,42 @@ def test_options_validation_codes():
     assert fwd_ex(ctypes.byref(o), C=60) == fm.FMCA_ERR_SHAPE
     assert fwd_ex(ctypes.byref(o), ws=0) == fm.FMCA_ERR_WORKSPACE
     assert fwd_ex(None, V=P + 0x10000008) == fm.FMCA_ERR_ALIGN
+
+
+def test_decode_state_bytes_and_validation():
+    import ctypes
+    nb = fm.flash_mca_decode_state_bytes(2, 32, 64, 16, fm.FMCA_F32)
+    a = lambda x: (x + 255) // 256 * 256
+    assert nb == a(4 * 2 * 32 * 64) + a(4 * 2 * 16 * 32) + a(4 * 2 * 16 * 64)
+    assert fm.flash_mca_decode_state_bytes(2, 32, 64, 16, fm.FMCA_BF16) == \
+        a(4 * 2 * 32 * 64) + a(2 * 2 * 16 * 32) + a(2 * 2 * 16 * 64)
+    for bad in ((0, 32, 64, 16), (2, 300, 64, 16), (2, 32, 64, 2048), (2, 32, 0, 16)):
+        assert fm.flash_mca_decode_state_bytes(*bad, fm.FMCA_F32) == 0
+    step = fm.lib.flash_mca_decode_step
+    base = dict(z=P, v=P + 0x1000, u=P + 0x2000, g=P + 0x3000, b=P + 0x4000, o=P + 0x5000,
+                B=2, s=32, e=64, C=16, t=5, n=64, dt=fm.FMCA_F32, opts=None,
+                st=P + 0x100000, stb=nb)
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return step(d["z"], d["v"], d["u"], d["g"], d["b"], d["o"], d["B"], d["s"], d["e"], d["C"],
+                    d["t"], d["n"], d["dt"], d["opts"], d["st"], d["stb"], None)
+    assert call(t=-1) == fm.FMCA_ERR_INVALID_ARG
+    assert call(n=5) == fm.FMCA_ERR_INVALID_ARG          # n_norm must exceed t
+    assert call(C=4096) == fm.FMCA_ERR_INVALID_ARG
+    assert call(z=0) == fm.FMCA_ERR_INVALID_ARG
+    assert call(v=P + 0x1004) == fm.FMCA_ERR_ALIGN
+    assert call(stb=nb - 1) == fm.FMCA_ERR_WORKSPACE
+    assert call(st=0) == fm.FMCA_ERR_WORKSPACE
+    assert call(st=P + 0x100010) == fm.FMCA_ERR_ALIGN
+    assert call(o=P + 0x1000) == fm.FMCA_ERR_INVALID_ARG    # o overlaps v
+    o = fm.FmcaOptions(0.1, 7)
+    assert call(opts=ctypes.byref(o)) == fm.FMCA_ERR_INVALID_ARG
+    # the per-position and tokens-summed divisors do not need n_norm
+    o = fm.FmcaOptions(0.1, fm.FMCA_LIN_NORM_SUMMED)
+    assert call(opts=ctypes.byref(o), n=0, stb=0) == fm.FMCA_ERR_WORKSPACE
+    reset = fm.lib.flash_mca_decode_reset
+    assert reset(P + 0x100000, nb - 1, 2, 32, 64, 16, fm.FMCA_F32, None) == fm.FMCA_ERR_WORKSPACE
+    assert reset(P + 0x100010, nb, 2, 32, 64, 16, fm.FMCA_F32, None) == fm.FMCA_ERR_ALIGN
+    assert reset(P + 0x100000, nb, 0, 32, 64, 16, fm.FMCA_F32, None) == fm.FMCA_ERR_INVALID_ARG
