@@ -87,6 +87,7 @@ def max_threads() -> int:
 LIN_NORM_N = 0         # 1/n
 LIN_NORM_SUMMED = 1    # 1/(tokens the sum covers): g*C for causal chunk g, n otherwise
 LIN_NORM_POSITION = 2  # 1/(t+1) for the token at position t
+LIN_NORM_NONE = 3      # no global term (with C = n: FLASH-Quad)
 
 
 def forward(Z, V, U, gamma, beta, C: int, causal: bool, nthreads: int = 0,

@@ -56,7 +56,11 @@
  *                  otherwise; chunk 0's causal sum is empty, so its term is 0;
  *               2: by t+1 for the token at position t (counted from 0) of its
  *                  sequence, i.e. by its position counted from 1 ("the sum of
- *                  the first t items should be divided by t").
+ *                  the first t items should be divided by t");
+ *               3: no global term at all -- with C = n this is the
+ *                  quadratic-only model of "Weak Attention" (FLASH-Quad:
+ *                  relu(q.k / n)^2 over the whole sequence, masked for a
+ *                  decoder).
  *
  * All arithmetic is fp64.  Arrays are row-major and contiguous:
  *   Z[B][n][s], V[B][n][e], U[B][n][e], gamma[4][s], beta[4][s], O[B][n][e].
@@ -146,6 +150,7 @@ static double lin_factor(int lin_norm, int causal, int n, int C, int g, int i) {
     return g > 0 ? 1.0 / ((double)g * (double)C) : 0.0; /* chunk 0: empty sum */
   }
   if (lin_norm == 2) return 1.0 / ((double)g * (double)C + (double)i + 1.0);
+  if (lin_norm == 3) return 0.0; /* no global term */
   return 1.0 / (double)n;
 }
 
@@ -198,7 +203,7 @@ static void row_of(const double *Z, const double *V, const double *U, const doub
 
 static int check_variant(double quad_scale, int lin_norm) {
   if (!(quad_scale >= 0.0) || !isfinite(quad_scale)) return -1;
-  if (lin_norm < 0 || lin_norm > 2) return -1;
+  if (lin_norm < 0 || lin_norm > 3) return -1;
   return 0;
 }
 

@@ -133,7 +133,7 @@ def test_chunk_zero_of_the_summed_divisor_has_no_global_term():
 def test_bad_variant_arguments_are_rejected():
     args = rand_inputs(1, 4, 2, 2, seed=1)
     for kw in ({"quad_scale": -1.0}, {"quad_scale": float("nan")}, {"quad_scale": float("inf")},
-               {"lin_norm": 3}, {"lin_norm": -1}):
+               {"lin_norm": 4}, {"lin_norm": -1}):
         with pytest.raises(ValueError):
             oracle.forward(*args, C=2, causal=True, **kw)
 
@@ -209,3 +209,37 @@ def test_pins_catch_planted_mistakes_in_the_variants(tmp_path):
             assert not failed, "the pins must pass on the real oracle"
         else:
             assert failed, f"planted mistake '{name}' was not caught by the pins"
+
+
+# --------------------------------------------------------------------------
+# no global term: with C = n, the quadratic-only model (FLASH-Quad)
+# --------------------------------------------------------------------------
+NONE = oracle.LIN_NORM_NONE
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("n,s,e", [(16, 4, 3), (24, 5, 6)])
+def test_no_global_term_with_one_chunk_is_flash_quad(causal, n, s, e):
+    """"Weak Attention": O = U * relu(Q K^T / n)^2 V with Q, K affine maps of Z,
+    masked for a decoder -- brute force over the whole n x n matrix, with
+    lin_q and lin_k left non-zero (they must not contribute)."""
+    Z, V, U, gamma, beta = rand_inputs(2, n, s, e, seed=n + s)
+    got = oracle.forward(Z, V, U, gamma, beta, C=n, causal=causal, lin_norm=NONE)
+    for b in range(2):
+        T0 = Z[b] * gamma[0] + beta[0]
+        T1 = Z[b] * gamma[1] + beta[1]
+        want = U[b] * brute.full_relu2_attention(T0, T1, V[b], causal)
+        assert close(got[b], want)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_no_global_term_equals_zero_lin_maps(causal):
+    """Dropping the global term equals zeroing lin_q's affine map (T2 = 0)."""
+    Z, V, U, gamma, beta = rand_inputs(1, 20, 3, 4, seed=6)
+    a = oracle.forward(Z, V, U, gamma, beta, C=5, causal=causal, lin_norm=NONE)
+    g2, b2 = gamma.copy(), beta.copy()
+    g2[2] = 0.0
+    b2[2] = 0.0
+    b = oracle.forward(Z, V, U, g2, b2, C=5, causal=causal)
+    assert close(a, b, rtol=1e-14)
+    assert np.max(np.abs(a - oracle.forward(Z, V, U, gamma, beta, C=5, causal=causal))) > 0
