@@ -79,12 +79,13 @@ def whole_job_rate(world: int, units_per_rank_step: float, steps: int, max_secon
 
 
 # ---------------------------------------------------------------- work accounting
-def algorithmic_flops(w) -> float:
+def algorithmic_flops(w, lin_norm: int = 0) -> float:
     """Per forward pass: per chunk 2*P*(s+e) for the intra-chunk scores and
     relu^2-weighted values over the P unmasked (query, key) pairs, plus
-    4*C*s*e for the chunk state and the global term."""
+    4*C*s*e for the chunk state and the global term (none without a global
+    term)."""
     P = w.C * (w.C + 1) // 2 if w.causal else w.C * w.C
-    per_chunk = 2.0 * P * (w.s + w.e) + 4.0 * w.C * w.s * w.e
+    per_chunk = 2.0 * P * (w.s + w.e) + (0.0 if lin_norm == 3 else 4.0 * w.C * w.s * w.e)
     return per_chunk * w.B * w.G
 
 
@@ -278,7 +279,7 @@ def run_reference(args, w):
     print(json.dumps(line), flush=True)
 
 
-LIN_NORMS = {"n": 0, "summed": 1, "position": 2}
+LIN_NORMS = {"n": 0, "summed": 1, "position": 2, "none": 3}
 
 
 def variant_of(args, w):
@@ -287,7 +288,7 @@ def variant_of(args, w):
     qs = None
     if args.quad_scale is not None:
         qs = 1.0 / (w.C * w.s) if args.quad_scale == "cs" else float(args.quad_scale)
-    return qs, LIN_NORMS[args.lin_norm]
+    return qs, LIN_NORMS[args.lin_norm or w.lin_norm]
 
 
 def config_of(w, args=None):
@@ -295,9 +296,10 @@ def config_of(w, args=None):
             "causal": w.causal, "io_dtype": w.dtype, "accumulate": "fp32",
             "l2": "inputs larger than L2, 3 rotating buffer sets",
             "parallelism": "replicas (one independent problem per GPU)",
-            **({} if args is None or (args.quad_scale is None and args.lin_norm == "n") else
+            **({} if args is None or (args.quad_scale is None and
+                                      (args.lin_norm or w.lin_norm) == "n") else
                {"quad_scale": variant_of(args, w)[0] or 1.0 / (w.C * w.C),
-                "lin_norm": args.lin_norm})}
+                "lin_norm": args.lin_norm or w.lin_norm})}
 
 
 # ---------------------------------------------------------------- decode
@@ -429,7 +431,7 @@ def run_ours(args, w, rank, world, device):
             fm.flash_mca_forward(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws, stream)
         else:
             fm.flash_mca_forward_timed(s["Z"], s["V"], s["U"], gd, bd, s["O"], w.C, w.causal, ws,
-                                       events, fm.FMCA_PATH_AUTO, stream)
+                                       events, fm.FMCA_PATH_AUTO, stream, quad_scale, lin_norm)
 
     sampler = ClockSampler(torch.cuda.current_device() if device.index is None else device.index)
     sampler.start()
@@ -501,7 +503,7 @@ def run_ours(args, w, rank, world, device):
     peaks, peak_kind = load_peaks()
     tokens = w.B * w.n
     value = whole_job_rate(world, tokens, args.steps, ms / 1e3)
-    flops = algorithmic_flops(w)
+    flops = algorithmic_flops(w, lin_norm)
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
     kernel_names = (["tc_chunk_prep", "tc_state_scan", "tc_chunk_attn"]
                     if path == fm.FMCA_PATH_TCGEN05 else
@@ -569,9 +571,10 @@ def main():
                     help="time the autoregressive decode step instead of the forward pass "
                          "(its own JSON line)")
     ap.add_argument("--decode-batch", type=int, default=8)
-    ap.add_argument("--lin-norm", default="n", choices=list(LIN_NORMS),
-                    help="global-term divisor: n (default), summed (tokens the sum covers), "
-                         "position (t+1)")
+    ap.add_argument("--lin-norm", default=None, choices=list(LIN_NORMS),
+                    help="global-term divisor: n, summed (tokens the sum covers), position "
+                         "(t+1), or none (no global term; with C = n: FLASH-Quad); default: "
+                         "the workload's (n for all but flash_quad_base)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -26,7 +26,8 @@ __all__ = [
     "flash_mca_forward_host", "flash_mca_forward_noalloc", "flash_mca_device_status",
     "flash_mca_selftest_timeout", "FMCA_NOALLOC_SCRATCH_BYTES",
     "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
-    "FMCA_LIN_NORM_N", "FMCA_LIN_NORM_SUMMED", "FMCA_LIN_NORM_POSITION", "FmcaOptions",
+    "FMCA_LIN_NORM_N", "FMCA_LIN_NORM_SUMMED", "FMCA_LIN_NORM_POSITION", "FMCA_LIN_NORM_NONE",
+    "FmcaOptions",
     "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
     "flash_mca_decode_reset", "flash_mca_decode_step",
 ]
@@ -38,6 +39,7 @@ FMCA_PATH_AUTO, FMCA_PATH_SIMT, FMCA_PATH_TCGEN05 = 0, 1, 2
 # global-term divisors of flash_mca_forward_ex: n; the tokens the sum covers;
 # the token's position counted from 1
 FMCA_LIN_NORM_N, FMCA_LIN_NORM_SUMMED, FMCA_LIN_NORM_POSITION = 0, 1, 2
+FMCA_LIN_NORM_NONE = 3  # no global term (with C = n: FLASH-Quad)
 FMCA_NOALLOC_SCRATCH_BYTES = 64 << 20  # size of the fixed scratch of flash_mca_forward_noalloc
 
 library_path = _build.LIB
@@ -68,8 +70,9 @@ _SIGNATURES = [
     ("flash_mca_workspace_bytes", _sz, [_int] * 6 + [_i32]),
     ("flash_mca_forward", _i32, _fwd_args + [_vp]),
     ("flash_mca_forward_path", _i32, _fwd_args + [_i32, _vp]),
-    ("flash_mca_forward_timed", _i32, _fwd_args + [_i32, ctypes.POINTER(_vp), _int, _vp]),
     ("flash_mca_default_options", _i32, [_int, ctypes.POINTER(FmcaOptions)]),
+    ("flash_mca_forward_timed", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions),
+                                                   ctypes.POINTER(_vp), _int, _vp]),
     ("flash_mca_forward_ex", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions), _vp]),
     ("flash_mca_decode_state_bytes", _sz, [_int] * 4 + [_i32]),
     ("flash_mca_decode_reset", _i32, [_vp, _sz] + [_int] * 4 + [_i32, _vp]),
@@ -212,8 +215,10 @@ def flash_mca_forward_ex(Z, V, U, gamma, beta, O, C: int, causal: bool, workspac
 
 
 def flash_mca_forward_timed(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,
-                            events, path: int = FMCA_PATH_AUTO, stream=None) -> None:
-    """``flash_mca_forward_path`` recording ``events`` (torch.cuda.Event
+                            events, path: int = FMCA_PATH_AUTO, stream=None,
+                            quad_scale: float | None = None,
+                            lin_norm: int = FMCA_LIN_NORM_N) -> None:
+    """``flash_mca_forward_ex`` recording ``events`` (torch.cuda.Event
     objects, launch count + 1 of them) before the first kernel and after each
     kernel on ``stream``.  torch creates an event's CUDA handle on its first
     record; events without a handle yet are recorded once here to create it."""
@@ -225,11 +230,16 @@ def flash_mca_forward_timed(Z, V, U, gamma, beta, O, C: int, causal: bool, works
             ev.record(stream)
     handles = (_vp * len(events))(*[ev.cuda_event for ev in events])
     dt = _dtype_code(Z)
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    opts.lin_norm = int(lin_norm)
     st = lib.flash_mca_forward_timed(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
                                      beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C),
                                      int(bool(causal)), dt, workspace.data_ptr(),
-                                     workspace.numel() * workspace.element_size(), path, handles,
-                                     len(events), _stream_ptr(stream))
+                                     workspace.numel() * workspace.element_size(), path,
+                                     ctypes.byref(opts), handles, len(events),
+                                     _stream_ptr(stream))
     _check(st, "flash_mca_forward_timed")
 
 

@@ -44,7 +44,7 @@ fmca_status to_variant(const fmca_options *opts, int C, Variant *v) {
   const float q = opts->quad_scale;
   if (!std::isfinite(q) || q < 0.0f) return FMCA_ERR_INVALID_ARG;
   if (opts->lin_norm != FMCA_LIN_NORM_N && opts->lin_norm != FMCA_LIN_NORM_SUMMED &&
-      opts->lin_norm != FMCA_LIN_NORM_POSITION)
+      opts->lin_norm != FMCA_LIN_NORM_POSITION && opts->lin_norm != FMCA_LIN_NORM_NONE)
     return FMCA_ERR_INVALID_ARG;
   const double dq = (double)q, dflt = 1.0 / ((double)C * (double)C);
   if ((float)dflt != q) v->quad_a = (float)std::sqrt(dq);
@@ -95,9 +95,10 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     const float *gamma, const float *beta, void *O, int B,
                                     int n, int s, int e, int C, int causal, fmca_dtype dtype,
                                     void *workspace, size_t workspace_bytes_, fmca_path path,
-                                    void *const *events, int n_events, fmca_stream_t stream) {
+                                    const fmca_options *opts, void *const *events, int n_events,
+                                    fmca_stream_t stream) {
   return forward_impl(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype, workspace,
-                      workspace_bytes_, path, nullptr, events, n_events, stream);
+                      workspace_bytes_, path, opts, events, n_events, stream);
 }
 
 size_t flash_mca_decode_state_bytes(int B, int s, int e, int C, fmca_dtype dtype) {
@@ -235,7 +236,7 @@ fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
                                    void *workspace, size_t workspace_bytes_, fmca_path path,
                                    fmca_stream_t stream) {
   return flash_mca_forward_timed(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype,
-                                 workspace, workspace_bytes_, path, nullptr, 0, stream);
+                                 workspace, workspace_bytes_, path, nullptr, nullptr, 0, stream);
 }
 
 fmca_status flash_mca_forward(const void *Z, const void *V, const void *U, const float *gamma,

@@ -222,6 +222,7 @@ int launch_decode_impl(const void *z, const void *v, const void *u, const float 
     lin_f = 1.0f;
     t2_w = 1.0f / (float)(t + 1);
   }
+  if (var.lin_norm == kLinNormNone) lin_f = 0.0f;
   // block width: 32 columns while that leaves fewer than about three blocks
   // per SM, wider (fewer repeats of the key weights) beyond
   const int64_t blocks32 = (int64_t)B * ((e + 31) / 32);

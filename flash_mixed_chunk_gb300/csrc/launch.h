@@ -45,7 +45,7 @@ struct Variant {
   float quad_a;
   int lin_norm;
 };
-constexpr int kLinNormN = 0, kLinNormSummed = 1, kLinNormPosition = 2;
+constexpr int kLinNormN = 0, kLinNormSummed = 1, kLinNormPosition = 2, kLinNormNone = 3;
 inline Variant default_variant(int C) { return Variant{1.0f / (float)C, kLinNormN}; }
 
 // `events` (may be NULL) holds launch-count + 1 cudaEvent_t handles recorded

@@ -110,7 +110,7 @@ __global__ void simt_chunk_scan(const float *__restrict__ S, float *__restrict__
   if (t >= (int64_t)B * se) return;
   const int64_t b = t / se, x = t % se;
   const float *src = S + b * G * se + x;
-  const float keep = lin_norm == kLinNormPosition ? 1.0f : inv_n;
+  const float keep = lin_norm == kLinNormPosition ? 1.0f : (lin_norm == kLinNormNone ? 0.0f : inv_n);
   float run = 0.f;
   if (causal) {
     float *dst = P + b * G * se + x;

@@ -90,7 +90,7 @@ int num_sms() {
 
 bool tc_supported(int B, int n, int s, int e, int C) {
   if (s != S_DIM) return false;
-  if (C != 128 && C != 256) return false;
+  if (C % ROW_TILE) return false;  // whole 128-row tiles (C = n: FLASH-Quad)
   if (e % E_TILE) return false;
   if (n % C) return false;
   (void)B;
@@ -140,7 +140,10 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   if (!record_event(events, 0, stream)) return 1;
   // sched[0]: work counter of tc_chunk_prep; sched[1]: of tc_chunk_attn
   if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
-  const int n_state = B * G * (e / E_TILE);
+  // without a global term (FMCA_LIN_NORM_NONE) there are no chunk states, the
+  // scan has nothing to do and the attention units have no lin_q items
+  const bool no_global = var.lin_norm == kLinNormNone;
+  const int n_state = no_global ? 0 : B * G * (e / E_TILE);
   const int n_score = B * G * (causal ? R * (R + 1) : R * (C / KEY_STAGE));
   const int n_prep = n_state + n_score;
   auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
@@ -160,11 +163,12 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   const int64_t lanes = (int64_t)B * se / 8;
-  cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
+  cfg.gridDim = dim3(no_global ? 1u : (unsigned)((lanes + 255) / 256));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
   auto *scan = var.lin_norm == kLinNormSummed     ? tc_state_scan<kLinNormSummed>
                : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
+               : no_global                        ? tc_state_scan<kLinNormNone>
                                                   : tc_state_scan<kLinNormN>;
   if (cudaLaunchKernelEx(&cfg, scan, (const __nv_bfloat16 *)states, prefix, B, G, se,
                          1.0f / (float)n, causal, C) != cudaSuccess ||
@@ -175,7 +179,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   cfg.blockDim = dim3(AT_THREADS);
   cfg.dynamicSmemBytes = AT_SMEM;
   if (cudaLaunchKernelEx(&cfg, tc_chunk_attn, mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C, G,
-                         causal, n_units) != cudaSuccess ||
+                         causal, n_units, no_global ? 0 : S_DIM / KEY_STAGE) != cudaSuccess ||
       !record_event(events, 3, stream))
     return 1;
   return 0;

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
                   const __grid_constant__ CUtensorMap mapU,   // U [B*n][e], box {64,128}
                   const __grid_constant__ CUtensorMap mapO,   // O [B*n][e], box {64,128}
                   unsigned int *__restrict__ sched, int n, int e, int C, int G, int causal,
-                  int n_units) {
+                  int n_units, int lin_items) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_arrive(&qb_full[qs]);
         if (uu < 0) break;
         const AttnUnit a = decode_unit(uu, n, e, C, G, causal);
-        const int items = a.nkv + S_DIM / KEY_STAGE;
+        const int items = a.nkv + lin_items;
         for (int k = 0; k < items; ++k, ++ia) {
           const int slot = ia % AT_RING_A;
           if (ia >= AT_RING_A &&
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         if (u < 0) break;
         tc_fence_after();
         const AttnUnit a = decode_unit(u, n, e, C, G, causal);
-        const int items = a.nkv + S_DIM / KEY_STAGE;
+        const int items = a.nkv + lin_items;
         const uint32_t dcol = tbase + (uint32_t)buf * 256u;
         for (int k = 0; k < items; ++k, ++ia) {
           const int slot = ia % AT_RING_A;

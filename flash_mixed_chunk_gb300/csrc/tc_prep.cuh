@@ -70,18 +70,24 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
   // causal: row tile rt covers keys [0, 128 (rt+1)); otherwise all C keys
   const int per_chunk = causal ? R * (R + 1) : R * (C / KEY_STAGE);
   const int bg = u / per_chunk;
-  int w = u % per_chunk;
-  int rt = 0;
-  for (;; ++rt) {
-    const int nks = (causal ? (rt + 1) * ROW_TILE : C) / KEY_STAGE;
-    if (w < nks) break;
-    w -= nks;
+  const int w = u % per_chunk;
+  int rt, ks;
+  if (causal) {
+    // row tile rt has 2 (rt+1) key stages: its units are w in
+    // [rt (rt+1), (rt+1) (rt+2)) of the chunk
+    rt = (int)((sqrtf(4.0f * (float)w + 1.0f) - 1.0f) * 0.5f);
+    while (rt > 0 && rt * (rt + 1) > w) --rt;
+    while ((rt + 1) * (rt + 2) <= w) ++rt;
+    ks = w - rt * (rt + 1);
+  } else {
+    rt = w / (C / KEY_STAGE);
+    ks = w % (C / KEY_STAGE);
   }
   p.kind = KIND_SCORE;
   p.crow = (bg / G) * n + (bg % G) * C;
   p.rt = rt;
   p.row0 = p.crow + rt * ROW_TILE;
-  p.ks = w;
+  p.ks = ks;
   return p;
 }
 

@@ -27,6 +27,7 @@ __global__ void __launch_bounds__(256)
   // attention kernel start launching (it waits for this grid in turn)
   griddep_wait();
   griddep_launch_dependents();
+  if (LIN_NORM == kLinNormNone) return;  // no global term: nothing to sum
   const int64_t per_b = se / 8;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * per_b) return;

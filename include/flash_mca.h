@@ -77,7 +77,7 @@ typedef int32_t fmca_path;
                                else the SIMT path */
 #define FMCA_PATH_SIMT 1    /* CUDA-core fp32 kernels, any supported shape */
 #define FMCA_PATH_TCGEN05 2 /* tcgen05/TMEM + TMA kernels; FMCA_BF16 only,
-                               s == 128, C in {128, 256}, e % 256 == 0 */
+                               s == 128, C % 128 == 0, e % 256 == 0 */
 
 /* Supported sizes: B, n, s, e >= 1; 1 <= C <= n with n % C == 0; s <= 256;
  * B * n * max(s, e) < 2^31.  The tensor-core path additionally needs the
@@ -120,22 +120,6 @@ fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
                                    size_t workspace_bytes, fmca_path path,
                                    fmca_stream_t stream);
 
-/* flash_mca_forward_path that also records caller-created CUDA events
- * (cudaEvent_t handles) on `stream` around its kernels: events[0] before the
- * first kernel and events[i] after kernel i (1-based), so `n_events` must be
- * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
- * stream it runs on.  Kernel order: tensor-core path -- chunk preparation
- * (states, relu^2 weights, lin_q rows; events[0] is recorded before the
- * reset of its work counters), state scan, chunk attention; SIMT path --
- * chunk states, state scan, chunk output. */
-fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
-                                    const float *gamma, const float *beta, void *O, int B,
-                                    int n, int s, int e, int C, int causal,
-                                    fmca_dtype dtype, void *workspace,
-                                    size_t workspace_bytes, fmca_path path,
-                                    void *const *events, int n_events,
-                                    fmca_stream_t stream);
-
 /*
  * Scale and normalisation variants.  The page states some factors in more
  * than one way; flash_mca_forward uses the readings given at the top of this
@@ -157,11 +141,18 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
  *     FMCA_LIN_NORM_POSITION  t+1 for the token at position t (counted from 0)
  *                             of its sequence ("Extended Thoughts": the sum of
  *                             the first t items should be divided by t).
+ *     FMCA_LIN_NORM_NONE      no global term at all.  With C = n this is the
+ *                             quadratic-only model FLASH-Quad ("Weak
+ *                             Attention": relu(q.k / n)^2 attention over the
+ *                             whole sequence, the upper triangle masked for a
+ *                             decoder); the kernels then skip the chunk
+ *                             states, the scan and the global product.
  */
 typedef int32_t fmca_lin_norm;
 #define FMCA_LIN_NORM_N 0
 #define FMCA_LIN_NORM_SUMMED 1
 #define FMCA_LIN_NORM_POSITION 2
+#define FMCA_LIN_NORM_NONE 3
 
 typedef struct fmca_options {
   float quad_scale;
@@ -181,6 +172,23 @@ fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                                  int n, int s, int e, int C, int causal, fmca_dtype dtype,
                                  void *workspace, size_t workspace_bytes, fmca_path path,
                                  const fmca_options *opts, fmca_stream_t stream);
+
+/* flash_mca_forward_ex that also records caller-created CUDA events
+ * (cudaEvent_t handles) on `stream` around its kernels: events[0] before the
+ * first kernel and events[i] after kernel i (1-based), so `n_events` must be
+ * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
+ * stream it runs on.  `opts` as for flash_mca_forward_ex (NULL: defaults).
+ * Kernel order: tensor-core path -- chunk preparation (states, relu^2
+ * weights, lin_q rows; events[0] is recorded before the reset of its work
+ * counters), state scan, chunk attention; SIMT path -- chunk states, state
+ * scan, chunk output. */
+fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
+                                    const float *gamma, const float *beta, void *O, int B,
+                                    int n, int s, int e, int C, int causal,
+                                    fmca_dtype dtype, void *workspace,
+                                    size_t workspace_bytes, fmca_path path,
+                                    const fmca_options *opts, void *const *events,
+                                    int n_events, fmca_stream_t stream);
 
 /*
  * Autoregressive decoding, one token per call, in the recurrent form of the

@@ -34,6 +34,7 @@ class Workload:
     e: int
     causal: bool
     dtype: str  # "f32" or "bf16"
+    lin_norm: str = "n"  # global-term divisor: "n", "summed", "position" or "none"
 
     @property
     def G(self) -> int:
@@ -60,6 +61,10 @@ WORKLOADS = {
         Workload("bidir_mlm", B=4, n=4096, C=256, s=128, e=1536, causal=False, dtype="bf16"),
         Workload("long_causal", B=2, n=8192, C=256, s=128, e=1536, causal=True, dtype="bf16"),
         Workload("very_long_causal", B=1, n=32768, C=256, s=128, e=2048, causal=True, dtype="bf16"),
+        # the quadratic-only model (FLASH-Quad) at the pages' base scale, sequence
+        # length 1024: one chunk spanning the sequence, no global term
+        Workload("flash_quad_base", B=8, n=1024, C=1024, s=128, e=1536, causal=True,
+                 dtype="bf16", lin_norm="none"),
     ]
 }
 WORKLOAD_ORDER = list(WORKLOADS)

@@ -184,7 +184,7 @@ def test_default_options():
 
 def test_options_validation_codes():
     import ctypes
-    for q, ln in ((-1.0, 0), (float("nan"), 0), (float("inf"), 0), (0.5, 3), (0.5, -1)):
+    for q, ln in ((-1.0, 0), (float("nan"), 0), (float("inf"), 0), (0.5, 4), (0.5, -1)):
         o = fm.FmcaOptions(q, ln)
         assert fwd_ex(ctypes.byref(o)) == fm.FMCA_ERR_INVALID_ARG, (q, ln)
     # valid options still go through the other host checks first
