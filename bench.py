@@ -401,6 +401,70 @@ def run_decode(args, device):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- backward
+# fp32 CUDA-core rate of a GB300: 152 SMs x 128 FP32 lanes x 2 FLOP x 2.07 GHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def run_backward(args, w, device):
+    """The backward pass through flash_mca_backward on the workload's shape:
+    K steps of dZ, dV, dU, dgamma, dbeta for a fixed dO, inputs resident."""
+    import flash_mixed_chunk_gb300 as fm
+    torch.cuda.set_device(device)
+    seed = mca_inputs.WORKLOAD_ORDER.index(w.name) + 1
+    Z, V, U, gamma, beta = (t.to(device) for t in mca_inputs.workload_inputs(w, seed))
+    dO = torch.randn(w.B, w.n, w.e, generator=torch.Generator().manual_seed(seed + 100)).to(
+        Z.dtype).to(device)
+    qs, ln = variant_of(args, w)
+    dZ, dV, dU = torch.empty_like(Z), torch.empty_like(V), torch.empty_like(U)
+    dg = torch.empty(4, w.s, device=device)
+    db = torch.empty_like(dg)
+    ws = torch.empty(fm.flash_mca_backward_workspace_bytes(w.B, w.n, w.s, w.e, w.C, w.causal,
+                                                           fm.FMCA_BF16 if w.dtype == "bf16"
+                                                           else fm.FMCA_F32),
+                     dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step():
+        fm.flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dg, db, w.C, w.causal, ws, qs,
+                              ln, stream)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(device)
+    sampler = ClockSampler(device.index or 0)
+    sampler.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    a.record(stream)
+    for _ in range(args.steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize(device)
+    wall1 = time.time()
+    sampler.stop()
+    st, where = fm.flash_mca_device_status()
+    if st != fm.FMCA_OK:
+        raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
+    ms = a.elapsed_time(b) / args.steps
+    flops = 2.0 * algorithmic_flops(w, ln)
+    achieved = flops / (ms / 1e3) / 1e12
+    line = {
+        "metric": "mixed-chunk attn backward tokens/s at 1 GB300",
+        "value": w.B * w.n / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32 (CUDA cores; I/O " + w.dtype + ")", "data": "synthetic",
+        "config": {**config_of(w, args), "pass": "backward"},
+        "roofline": {"bound": "alu", "kernel": "whole backward (SIMT fp32)",
+                     "achieved": achieved, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / FP32_ALU_TFLOPS, "traffic": None,
+                     "algorithmic_flops_per_step": flops,
+                     "peak_source": "fp32 CUDA-core rate from unit counts and max clock"},
+        "gpu_launches": None,
+        "clocks": sampler.summary(wall0, wall1),
+    }
+    print(json.dumps(line), flush=True)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, w, rank, world, device):
     import flash_mixed_chunk_gb300 as fm
@@ -571,6 +635,8 @@ def main():
                     help="time the autoregressive decode step instead of the forward pass "
                          "(its own JSON line)")
     ap.add_argument("--decode-batch", type=int, default=8)
+    ap.add_argument("--backward", action="store_true",
+                    help="time the backward pass on the workload (its own JSON line)")
     ap.add_argument("--lin-norm", default=None, choices=list(LIN_NORMS),
                     help="global-term divisor: n, summed (tokens the sum covers), position "
                          "(t+1), or none (no global term; with C = n: FLASH-Quad); default: "
@@ -586,6 +652,10 @@ def main():
     if args.decode:
         if rank == 0 and args.impl == "ours":
             run_decode(args, torch.device("cuda", local))
+        return
+    if args.backward:
+        if rank == 0 and args.impl == "ours":
+            run_backward(args, w, torch.device("cuda", local))
         return
     if args.impl == "reference":
         if rank == 0:

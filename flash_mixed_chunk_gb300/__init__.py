@@ -29,7 +29,8 @@ __all__ = [
     "FMCA_LIN_NORM_N", "FMCA_LIN_NORM_SUMMED", "FMCA_LIN_NORM_POSITION", "FMCA_LIN_NORM_NONE",
     "FmcaOptions",
     "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
-    "flash_mca_decode_reset", "flash_mca_decode_step",
+    "flash_mca_decode_reset", "flash_mca_decode_step", "flash_mca_backward_workspace_bytes",
+    "flash_mca_backward", "backward",
 ]
 
 FMCA_OK, FMCA_ERR_INVALID_ARG, FMCA_ERR_SHAPE, FMCA_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -75,6 +76,9 @@ _SIGNATURES = [
                                                    ctypes.POINTER(_vp), _int, _vp]),
     ("flash_mca_forward_ex", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions), _vp]),
     ("flash_mca_decode_state_bytes", _sz, [_int] * 4 + [_i32]),
+    ("flash_mca_backward_workspace_bytes", _sz, [_int] * 6 + [_i32]),
+    ("flash_mca_backward", _i32, [_vp] * 11 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
+                                                          _vp, _sz, _vp]),
     ("flash_mca_decode_reset", _i32, [_vp, _sz] + [_int] * 4 + [_i32, _vp]),
     ("flash_mca_decode_step", _i32, [_vp] * 6 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
                                                              _vp, _sz, _vp]),
@@ -326,6 +330,59 @@ def flash_mca_decode_step(z, v, u, gamma, beta, o, C: int, t: int, state, n_norm
                                    int(n_norm), dt, ctypes.byref(opts), state.data_ptr(),
                                    state.numel() * state.element_size(), _stream_ptr(stream))
     _check(st, "flash_mca_decode_step")
+
+
+def flash_mca_backward_workspace_bytes(B: int, n: int, s: int, e: int, C: int, causal: bool,
+                                       dtype: int) -> int:
+    return int(lib.flash_mca_backward_workspace_bytes(B, n, s, e, C, int(bool(causal)), dtype))
+
+
+def flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, C: int,
+                       causal: bool, workspace, quad_scale: float | None = None,
+                       lin_norm: int = FMCA_LIN_NORM_N, stream=None) -> None:
+    """Gradients of sum(O * dO) into dZ, dV, dU (I/O dtype) and dgamma, dbeta
+    (float32 [4, s]); all CUDA tensors the caller owns."""
+    B, n, s, e = _shapes(Z, V, U)
+    for name, t in (("dO", dO), ("dZ", dZ), ("dV", dV), ("dU", dU), ("dgamma", dgamma),
+                    ("dbeta", dbeta), ("workspace", workspace)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    dt = _dtype_code(Z)
+    for name, t, shape in (("dO", dO, (B, n, e)), ("dZ", dZ, (B, n, s)), ("dV", dV, (B, n, e)),
+                           ("dU", dU, (B, n, e))):
+        if t.dtype != Z.dtype or tuple(t.shape) != shape:
+            raise ValueError(f"{name} must be {shape} of Z's dtype")
+    if dgamma.dtype != torch.float32 or tuple(dgamma.shape) != (4, s) or \
+            tuple(dbeta.shape) != (4, s):
+        raise ValueError("dgamma and dbeta must be float32 [4, s]")
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    opts.lin_norm = int(lin_norm)
+    st = lib.flash_mca_backward(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
+                                beta.data_ptr(), dO.data_ptr(), dZ.data_ptr(), dV.data_ptr(),
+                                dU.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(), B, n, s, e,
+                                int(C), int(bool(causal)), dt, ctypes.byref(opts),
+                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                _stream_ptr(stream))
+    _check(st, "flash_mca_backward")
+
+
+def backward(Z, V, U, gamma, beta, dO, C: int, causal: bool, quad_scale: float | None = None,
+             lin_norm: int = FMCA_LIN_NORM_N, stream=None):
+    """Convenience wrapper: allocates the outputs and the workspace with torch;
+    returns (dZ, dV, dU, dgamma, dbeta)."""
+    B, n, s, e = _shapes(Z, V, U)
+    dZ, dV, dU = torch.empty_like(Z), torch.empty_like(V), torch.empty_like(U)
+    dgamma = torch.empty((4, s), dtype=torch.float32, device=Z.device)
+    dbeta = torch.empty_like(dgamma)
+    nb = flash_mca_backward_workspace_bytes(B, n, s, e, C, causal, _dtype_code(Z))
+    if nb == 0:
+        raise FmcaError(FMCA_ERR_SHAPE, "flash_mca_backward_workspace_bytes")
+    ws = torch.empty(nb, dtype=torch.uint8, device=Z.device)
+    flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, C, causal, ws,
+                       quad_scale, lin_norm, stream)
+    return dZ, dV, dU, dgamma, dbeta
 
 
 def flash_mca_device_status(stream=None) -> tuple[int, int]:

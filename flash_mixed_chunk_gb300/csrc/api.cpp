@@ -160,6 +160,55 @@ fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
              : FMCA_ERR_CUDA;
 }
 
+size_t flash_mca_backward_workspace_bytes(int B, int n, int s, int e, int C, int causal,
+                                          fmca_dtype dtype) {
+  if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
+  return backward_layout(B, n, s, e, C, causal).total;
+}
+
+fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, const float *gamma,
+                               const float *beta, const void *dO, void *dZ, void *dV, void *dU,
+                               float *dgamma, float *dbeta, int B, int n, int s, int e, int C,
+                               int causal, fmca_dtype dtype, const fmca_options *opts,
+                               void *workspace, size_t workspace_bytes_, fmca_stream_t stream) {
+  fmca_status st = check_sizes(B, n, s, e, C, causal, dtype);
+  if (st != FMCA_OK) return st;
+  if (!Z || !V || !U || !gamma || !beta || !dO || !dZ || !dV || !dU || !dgamma || !dbeta)
+    return FMCA_ERR_INVALID_ARG;
+  Variant var;
+  st = to_variant(opts, C, &var);
+  if (st != FMCA_OK) return st;
+  const void *ptrs[] = {Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return FMCA_ERR_ALIGN;
+  if (!workspace) return FMCA_ERR_WORKSPACE;
+  if (!aligned256(workspace)) return FMCA_ERR_ALIGN;
+  if (workspace_bytes_ < backward_layout(B, n, s, e, C, causal).total) return FMCA_ERR_WORKSPACE;
+  {  // outputs must not overlap the inputs or the workspace
+    const size_t es = elem_size(dtype), zb = (size_t)B * n * s * es, vb = (size_t)B * n * e * es;
+    const size_t gb = sizeof(float) * 4 * (size_t)s;
+    struct Span { const void *p; size_t n; };
+    const Span outs[] = {{dZ, zb}, {dV, vb}, {dU, vb}, {dgamma, gb}, {dbeta, gb}};
+    const Span ins[] = {{Z, zb}, {V, vb}, {U, vb}, {dO, vb}, {gamma, gb}, {beta, gb},
+                        {workspace, workspace_bytes_}};
+    auto overlap = [](const Span &a, const Span &b) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+      return a0 < b0 + b.n && b0 < a0 + a.n;
+    };
+    for (const Span &o : outs) {
+      for (const Span &i : ins)
+        if (overlap(o, i)) return FMCA_ERR_INVALID_ARG;
+      for (const Span &o2 : outs)
+        if (&o2 != &o && overlap(o, o2)) return FMCA_ERR_INVALID_ARG;
+    }
+  }
+  return launch_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C,
+                         causal ? 1 : 0, dtype == FMCA_BF16 ? 1 : 0, var, workspace,
+                         reinterpret_cast<cudaStream_t>(stream)) == 0
+             ? FMCA_OK
+             : FMCA_ERR_CUDA;
+}
+
 fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                                  const float *gamma, const float *beta, void *O, int B, int n,
                                  int s, int e, int C, int causal, fmca_dtype dtype,

@@ -88,6 +88,40 @@ int launch_decode_step(const void *z, const void *v, const void *u, const float 
                        const float *beta, void *o, int B, int s, int e, int C, int t, int n_norm,
                        int dtype_bf16, const Variant &var, void *state, cudaStream_t stream);
 
+// Backward workspace (flash_mca_backward_workspace_bytes), fp32, each region
+// 256-byte aligned:
+//   states   [B][G][s][e]   chunk states (recomputed)
+//   prefix   [B][Gp][s][e]  their scaled prefix / total (recomputed)
+//   dprefix  [B][G][s][e]   d(prefix) per chunk, then the chunk-state gradients
+//   dY       [B*n][e]       dO * U
+//   W, dS    [B][G][C][C]   relu^2 weights and score gradients
+//   dT       [4][B*n][s]    gradients of the four affine maps
+//   part     [ceil(B*n/64)][8][s]  per-block partial sums of dgamma, dbeta
+struct BackwardLayout {
+  size_t states, prefix, dprefix, dY, W, dS, dT, part, total;
+};
+inline BackwardLayout backward_layout(int B, int n, int s, int e, int C, int causal) {
+  const size_t G = (size_t)(n / C), se = (size_t)s * (size_t)e, rows = (size_t)B * n;
+  const size_t Gp = causal ? G : 1;
+  BackwardLayout L;
+  L.states = 0;
+  L.prefix = L.states + align256(4 * (size_t)B * G * se);
+  L.dprefix = L.prefix + align256(4 * (size_t)B * Gp * se);
+  L.dY = L.dprefix + align256(4 * (size_t)B * G * se);
+  L.W = L.dY + align256(4 * rows * (size_t)e);
+  L.dS = L.W + align256(4 * (size_t)B * G * (size_t)C * (size_t)C);
+  L.dT = L.dS + align256(4 * (size_t)B * G * (size_t)C * (size_t)C);
+  L.part = L.dT + align256(4 * 4 * rows * (size_t)s);
+  L.total = L.part + align256(4 * 8 * (size_t)s * ((rows + 63) / 64));
+  return L;
+}
+
+int launch_backward(const void *Z, const void *V, const void *U, const float *gamma,
+                    const float *beta, const void *dO, void *dZ, void *dV, void *dU,
+                    float *dgamma, float *dbeta, int B, int n, int s, int e, int C, int causal,
+                    int dtype_bf16, const Variant &var, void *workspace, cudaStream_t stream);
+constexpr int kBackwardLaunches = 12;  // kernels + memsets one backward call queues (at most)
+
 // Shapes the tensor-core path covers.
 bool tc_supported(int B, int n, int s, int e, int C);
 int tc_launch_count();

@@ -137,8 +137,9 @@ __global__ void __launch_bounds__(kThreads)
   extern __shared__ float sm[];
   float *t0 = sm;                      // [32][s]  quad_q rows
   float *t2 = t0 + kRows * s;          // [32][s]  lin_q rows
-  float *t1 = t2 + kRows * s;          // [32][s]  quad_k keys
-  float *w = t1 + kKeys * s;           // [32][33] relu^2 weights
+  float *t1 = t2 + kRows * s;          // [32][s+1] quad_k keys (odd stride: the
+                                       // 32 lanes of a warp read 32 banks)
+  float *w = t1 + kKeys * (s + 1);     // [32][33] relu^2 weights
   float *vb = w + kRows * (kKeys + 1); // [32][64] V keys / P rows
   const int nrb = (C + kRows - 1) / kRows;
   const int bg = blockIdx.x / nrb, rb = blockIdx.x % nrb;
@@ -168,7 +169,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int x = tid; x < kKeys * s; x += kThreads) {
       int j = x / s, a = x % s;
       float z = (k0 + j < C) ? to_f(Z[(chunk0 + k0 + j) * s + a]) : 0.f;
-      t1[x] = z * gamma[s + a] + beta[s + a];
+      t1[j * (s + 1) + a] = z * gamma[s + a] + beta[s + a];
     }
     for (int x = tid; x < kKeys * kCols; x += kThreads) {
       int j = x / kCols, c = x % kCols;
@@ -180,7 +181,7 @@ __global__ void __launch_bounds__(kThreads)
     for (int x = tid; x < kRows * kKeys; x += kThreads) {
       int r = x / kKeys, j = x % kKeys;
       float dotv = 0.f;
-      const float *q = t0 + r * s, *k = t1 + j * s;
+      const float *q = t0 + r * s, *k = t1 + j * (s + 1);
       for (int a = 0; a < s; ++a) dotv = fmaf(q[a], k[a], dotv);
       float rl = fmaxf(dotv * quad_a, 0.f);
       float wt = rl * rl;
@@ -227,8 +228,8 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 size_t output_smem_bytes(int s) {
-  return sizeof(float) * ((size_t)kRows * s * 2 + (size_t)kKeys * s + kRows * (kKeys + 1) +
-                          kKeys * kCols);
+  return sizeof(float) * ((size_t)kRows * s * 2 + (size_t)kKeys * (s + 1) +
+                          kRows * (kKeys + 1) + kKeys * kCols);
 }
 
 template <typename T>

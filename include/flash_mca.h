@@ -229,6 +229,29 @@ fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
                                   const fmca_options *opts, void *state, size_t state_bytes,
                                   fmca_stream_t stream);
 
+/*
+ * Backward pass: gradients of sum(O * dO) for the O that flash_mca_forward_ex
+ * computes with the same arguments and options.  The pages define only the
+ * forward pass ("Mixed Chunk"); the gradient follows by calculus through the
+ * gate, the masked relu^2 chunk attention, the chunk states and their
+ * exclusive (causal) or total sum with its divisor, and the four affine maps.
+ *   Z, V, U, dO          device arrays of `dtype` (layouts as for the forward)
+ *   dZ, dV, dU           device outputs of `dtype` (overwritten)
+ *   dgamma, dbeta        device float32 [4][s] outputs (overwritten)
+ *   workspace            at least flash_mca_backward_workspace_bytes(...) bytes,
+ *                        256-byte aligned
+ * fp32 arithmetic on the CUDA cores, fixed reduction order (deterministic).
+ * Sizes as for flash_mca_forward (any supported shape, both dtypes).  The
+ * outputs must not overlap the inputs or the workspace.
+ */
+size_t flash_mca_backward_workspace_bytes(int B, int n, int s, int e, int C, int causal,
+                                          fmca_dtype dtype);
+fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, const float *gamma,
+                               const float *beta, const void *dO, void *dZ, void *dV, void *dU,
+                               float *dgamma, float *dbeta, int B, int n, int s, int e, int C,
+                               int causal, fmca_dtype dtype, const fmca_options *opts,
+                               void *workspace, size_t workspace_bytes, fmca_stream_t stream);
+
 /* Which path FMCA_PATH_AUTO takes for these arguments (FMCA_PATH_SIMT or
  * FMCA_PATH_TCGEN05), or -1 for arguments that would be rejected. */
 int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype);

@@ -231,3 +231,37 @@ def test_decode_state_bytes_and_validation():
     assert reset(P + 0x100000, nb - 1, 2, 32, 64, 16, fm.FMCA_F32, None) == fm.FMCA_ERR_WORKSPACE
     assert reset(P + 0x100010, nb, 2, 32, 64, 16, fm.FMCA_F32, None) == fm.FMCA_ERR_ALIGN
     assert reset(P + 0x100000, nb, 0, 32, 64, 16, fm.FMCA_F32, None) == fm.FMCA_ERR_INVALID_ARG
+
+
+def test_backward_workspace_and_validation():
+    nb = fm.flash_mca_backward_workspace_bytes(2, 64, 16, 32, 16, 1, fm.FMCA_F32)
+    a = lambda x: (x + 255) // 256 * 256
+    G, rows = 4, 128
+    want = (a(4 * 2 * G * 16 * 32) * 3 + a(4 * rows * 32) + 2 * a(4 * 2 * G * 16 * 16) +
+            a(4 * 4 * rows * 16) + a(4 * 8 * 16 * 2))
+    assert nb == want
+    assert fm.flash_mca_backward_workspace_bytes(2, 64, 16, 32, 60, 1, fm.FMCA_F32) == 0
+    f = fm.lib.flash_mca_backward
+    base = dict(Z=P, V=P + 0x10000, U=P + 0x20000, g=P + 0x30000, b=P + 0x31000, dO=P + 0x40000,
+                dZ=P + 0x50000, dV=P + 0x60000, dU=P + 0x70000, dg=P + 0x80000, db=P + 0x81000,
+                B=2, n=64, s=16, e=32, C=16, causal=1, dt=fm.FMCA_F32, opts=None,
+                ws=P + 0x100000, wsb=nb)
+
+    def call(**kw):
+        d = dict(base)
+        d.update(kw)
+        return f(d["Z"], d["V"], d["U"], d["g"], d["b"], d["dO"], d["dZ"], d["dV"], d["dU"],
+                 d["dg"], d["db"], d["B"], d["n"], d["s"], d["e"], d["C"], d["causal"], d["dt"],
+                 d["opts"], d["ws"], d["wsb"], None)
+    assert call(C=60) == fm.FMCA_ERR_SHAPE
+    assert call(dO=0) == fm.FMCA_ERR_INVALID_ARG
+    assert call(dg=0) == fm.FMCA_ERR_INVALID_ARG
+    assert call(dV=P + 0x60004) == fm.FMCA_ERR_ALIGN
+    assert call(ws=0) == fm.FMCA_ERR_WORKSPACE
+    assert call(wsb=nb - 1) == fm.FMCA_ERR_WORKSPACE
+    assert call(ws=P + 0x100010) == fm.FMCA_ERR_ALIGN
+    assert call(dZ=P + 0x10000) == fm.FMCA_ERR_INVALID_ARG   # dZ overlaps V
+    assert call(dU=P + 0x60000) == fm.FMCA_ERR_INVALID_ARG   # dU overlaps dV
+    import ctypes
+    o = fm.FmcaOptions(0.1, 9)
+    assert call(opts=ctypes.byref(o)) == fm.FMCA_ERR_INVALID_ARG
