@@ -465,6 +465,62 @@ def run_backward(args, w, device):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- projections
+def run_projections(args, w, device):
+    """The GAU projections around the core on the workload's token count:
+    U, V, Z = SiLU(X [W_u|W_v|W_z]) and Out = Y W_o, d = e / 2, on the tensor
+    cores; one JSON line per GEMM."""
+    import flash_mixed_chunk_gb300 as fm
+    torch.cuda.set_device(device)
+    M, e, s = w.B * w.n, w.e, w.s
+    d = e // 2
+    g = torch.Generator().manual_seed(21)
+    X = torch.randn(M, d, generator=g).to(torch.bfloat16).to(device)
+    Wt = (d ** -0.5 * torch.randn(2 * e + s, d, generator=g)).to(torch.bfloat16).to(device)
+    Y = torch.randn(M, e, generator=g).to(torch.bfloat16).to(device)
+    Wo_t = (e ** -0.5 * torch.randn(d, e, generator=g)).to(torch.bfloat16).to(device)
+    U = torch.empty(M, e, dtype=torch.bfloat16, device=device)
+    V, Z = torch.empty_like(U), torch.empty(M, s, dtype=torch.bfloat16, device=device)
+    Out = torch.empty(M, d, dtype=torch.bfloat16, device=device)
+    stream = torch.cuda.current_stream(device)
+    peaks, peak_kind = load_peaks()
+    bf16_peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+    cases = [("project", lambda: fm.flash_mca_gau_project(X, Wt, U, V, Z, stream),
+              2.0 * M * d * (2 * e + s), f"X[{M},{d}] x [W_u|W_v|W_z][{d},{2 * e + s}], SiLU"),
+             ("output", lambda: fm.flash_mca_gau_output(Y, Wo_t, Out, stream),
+              2.0 * M * e * d, f"Y[{M},{e}] x W_o[{e},{d}]")]
+    for name, fn, flops, what in cases:
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize(device)
+        sampler = ClockSampler(device.index or 0)
+        sampler.start()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        wall0 = time.time()
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize(device)
+        wall1 = time.time()
+        sampler.stop()
+        st, where = fm.flash_mca_device_status()
+        if st != fm.FMCA_OK:
+            raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
+        ms = a.elapsed_time(b) / args.steps
+        tf = flops / (ms / 1e3) / 1e12
+        print(json.dumps({
+            "metric": f"GAU {name} projection TFLOP/s at 1 GB300", "value": tf, "unit": "TFLOP/s",
+            "n_gpus": 1, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": f"gau_{name}_{w.name}", "gemm": what},
+            "roofline": {"bound": "tensor", "kernel": "tc_gemm", "achieved": tf,
+                         "peak": bf16_peak, "unit": "TFLOP/s", "frac": tf / bf16_peak,
+                         "traffic": None,
+                         "peak_source": f"{peak_kind} bf16_tflops (MEASURED_PEAKS.json)"},
+            "gpu_launches": args.steps, "clocks": sampler.summary(wall0, wall1)}), flush=True)
+
+
 # ---------------------------------------------------------------- our arm
 def run_ours(args, w, rank, world, device):
     import flash_mixed_chunk_gb300 as fm
@@ -635,6 +691,8 @@ def main():
                     help="time the autoregressive decode step instead of the forward pass "
                          "(its own JSON line)")
     ap.add_argument("--decode-batch", type=int, default=8)
+    ap.add_argument("--projections", action="store_true",
+                    help="time the GAU projection GEMMs (tensor cores) on the workload's tokens")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass on the workload (its own JSON line)")
     ap.add_argument("--lin-norm", default=None, choices=list(LIN_NORMS),
@@ -656,6 +714,10 @@ def main():
     if args.backward:
         if rank == 0 and args.impl == "ours":
             run_backward(args, w, torch.device("cuda", local))
+        return
+    if args.projections:
+        if rank == 0 and args.impl == "ours":
+            run_projections(args, w, torch.device("cuda", local))
         return
     if args.impl == "reference":
         if rank == 0:

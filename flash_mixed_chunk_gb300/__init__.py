@@ -30,7 +30,8 @@ __all__ = [
     "FmcaOptions",
     "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
     "flash_mca_decode_reset", "flash_mca_decode_step", "flash_mca_backward_workspace_bytes",
-    "flash_mca_backward", "backward",
+    "flash_mca_backward", "backward", "flash_mca_gau_project", "flash_mca_gau_output",
+    "gau_project", "gau_output",
 ]
 
 FMCA_OK, FMCA_ERR_INVALID_ARG, FMCA_ERR_SHAPE, FMCA_ERR_UNSUPPORTED = 0, 1, 2, 3
@@ -77,6 +78,8 @@ _SIGNATURES = [
     ("flash_mca_forward_ex", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions), _vp]),
     ("flash_mca_decode_state_bytes", _sz, [_int] * 4 + [_i32]),
     ("flash_mca_backward_workspace_bytes", _sz, [_int] * 6 + [_i32]),
+    ("flash_mca_gau_project", _i32, [_vp] * 5 + [_int] * 4 + [_vp]),
+    ("flash_mca_gau_output", _i32, [_vp] * 3 + [_int] * 3 + [_vp]),
     ("flash_mca_backward", _i32, [_vp] * 11 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
                                                           _vp, _sz, _vp]),
     ("flash_mca_decode_reset", _i32, [_vp, _sz] + [_int] * 4 + [_i32, _vp]),
@@ -383,6 +386,55 @@ def backward(Z, V, U, gamma, beta, dO, C: int, causal: bool, quad_scale: float |
     flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, C, causal, ws,
                        quad_scale, lin_norm, stream)
     return dZ, dV, dU, dgamma, dbeta
+
+
+def _bf16_cuda(name, t):
+    if not t.is_cuda or not t.is_contiguous() or t.dtype != torch.bfloat16:
+        raise ValueError(f"{name} must be a contiguous bfloat16 CUDA tensor")
+
+
+def flash_mca_gau_project(X, Wt, U, V, Z, stream=None) -> None:
+    """U, V, Z = SiLU(X W_u), SiLU(X W_v), SiLU(X W_z) with Wt = [W_u|W_v|W_z]^T
+    ([2e+s, d]); X [M, d], U and V [M, e], Z [M, s], bf16 CUDA tensors."""
+    for name, t in (("X", X), ("Wt", Wt), ("U", U), ("V", V), ("Z", Z)):
+        _bf16_cuda(name, t)
+    M, d = X.shape
+    e, s = U.shape[1], Z.shape[1]
+    if tuple(Wt.shape) != (2 * e + s, d) or tuple(V.shape) != (M, e) or U.shape[0] != M or \
+            Z.shape[0] != M:
+        raise ValueError("shapes: X [M, d], Wt [2e+s, d], U and V [M, e], Z [M, s]")
+    _check(lib.flash_mca_gau_project(X.data_ptr(), Wt.data_ptr(), U.data_ptr(), V.data_ptr(),
+                                     Z.data_ptr(), M, d, e, s, _stream_ptr(stream)),
+           "flash_mca_gau_project")
+
+
+def flash_mca_gau_output(Y, Wo_t, Out, stream=None) -> None:
+    """Out = Y W_o with Wo_t = W_o^T ([d, e]); Y [M, e], Out [M, d]."""
+    for name, t in (("Y", Y), ("Wo_t", Wo_t), ("Out", Out)):
+        _bf16_cuda(name, t)
+    M, e = Y.shape
+    d = Wo_t.shape[0]
+    if tuple(Wo_t.shape) != (d, e) or tuple(Out.shape) != (M, d):
+        raise ValueError("shapes: Y [M, e], Wo_t [d, e], Out [M, d]")
+    _check(lib.flash_mca_gau_output(Y.data_ptr(), Wo_t.data_ptr(), Out.data_ptr(), M, e, d,
+                                    _stream_ptr(stream)), "flash_mca_gau_output")
+
+
+def gau_project(X, Wt, e: int, s: int, stream=None):
+    """Allocating wrapper of flash_mca_gau_project: returns (U, V, Z)."""
+    M = X.shape[0]
+    U = torch.empty((M, e), dtype=torch.bfloat16, device=X.device)
+    V = torch.empty_like(U)
+    Z = torch.empty((M, s), dtype=torch.bfloat16, device=X.device)
+    flash_mca_gau_project(X, Wt, U, V, Z, stream)
+    return U, V, Z
+
+
+def gau_output(Y, Wo_t, stream=None):
+    """Allocating wrapper of flash_mca_gau_output."""
+    Out = torch.empty((Y.shape[0], Wo_t.shape[0]), dtype=torch.bfloat16, device=Y.device)
+    flash_mca_gau_output(Y, Wo_t, Out, stream)
+    return Out
 
 
 def flash_mca_device_status(stream=None) -> tuple[int, int]:

@@ -209,6 +209,59 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
              : FMCA_ERR_CUDA;
 }
 
+fmca_status flash_mca_gau_project(const void *X, const void *Wt, void *U, void *V, void *Z,
+                                  int M, int d, int e, int s, fmca_stream_t stream) {
+  if (!X || !Wt || !U || !V || !Z || M <= 0 || d <= 0 || e <= 0 || s <= 0)
+    return FMCA_ERR_INVALID_ARG;
+  if (d % 8 || e % 64 || s % 64) return FMCA_ERR_UNSUPPORTED;
+  if ((int64_t)M * (2 * (int64_t)e + s) >= ((int64_t)1 << 31) ||
+      (int64_t)M * d >= ((int64_t)1 << 31))
+    return FMCA_ERR_UNSUPPORTED;
+  const void *ptrs[] = {X, Wt, U, V, Z};
+  for (const void *p : ptrs)
+    if (!aligned16(p)) return FMCA_ERR_ALIGN;
+  {
+    struct Span { const void *p; size_t n; };
+    const Span ins[] = {{X, 2 * (size_t)M * d}, {Wt, 2 * (size_t)(2 * e + s) * d}};
+    const Span outs[] = {{U, 2 * (size_t)M * e}, {V, 2 * (size_t)M * e}, {Z, 2 * (size_t)M * s}};
+    auto overlap = [](const Span &a, const Span &b) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+      return a0 < b0 + b.n && b0 < a0 + a.n;
+    };
+    for (const Span &o : outs) {
+      for (const Span &i : ins)
+        if (overlap(o, i)) return FMCA_ERR_INVALID_ARG;
+      for (const Span &o2 : outs)
+        if (&o2 != &o && overlap(o, o2)) return FMCA_ERR_INVALID_ARG;
+    }
+  }
+  return launch_gemm(X, Wt, M, 2 * e + s, d, U, V, Z, e, 2 * e, 1,
+                     reinterpret_cast<cudaStream_t>(stream)) == 0
+             ? FMCA_OK
+             : FMCA_ERR_CUDA;
+}
+
+fmca_status flash_mca_gau_output(const void *Y, const void *Wo_t, void *Out, int M, int e, int d,
+                                 fmca_stream_t stream) {
+  if (!Y || !Wo_t || !Out || M <= 0 || d <= 0 || e <= 0) return FMCA_ERR_INVALID_ARG;
+  if (e % 8 || d % 64) return FMCA_ERR_UNSUPPORTED;
+  if ((int64_t)M * (e > d ? e : d) >= ((int64_t)1 << 31)) return FMCA_ERR_UNSUPPORTED;
+  if (!aligned16(Y) || !aligned16(Wo_t) || !aligned16(Out)) return FMCA_ERR_ALIGN;
+  {
+    const uintptr_t o0 = reinterpret_cast<uintptr_t>(Out), o1 = o0 + 2 * (size_t)M * d;
+    auto overlaps = [&](const void *p, size_t bytes) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(p), a1 = a0 + bytes;
+      return a0 < o1 && o0 < a1;
+    };
+    if (overlaps(Y, 2 * (size_t)M * e) || overlaps(Wo_t, 2 * (size_t)d * e))
+      return FMCA_ERR_INVALID_ARG;
+  }
+  return launch_gemm(Y, Wo_t, M, d, e, Out, Out, Out, d, d, 0,
+                     reinterpret_cast<cudaStream_t>(stream)) == 0
+             ? FMCA_OK
+             : FMCA_ERR_CUDA;
+}
+
 fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                                  const float *gamma, const float *beta, void *O, int B, int n,
                                  int s, int e, int C, int causal, fmca_dtype dtype,

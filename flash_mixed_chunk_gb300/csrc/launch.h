@@ -122,6 +122,11 @@ int launch_backward(const void *Z, const void *V, const void *U, const float *ga
                     int dtype_bf16, const Variant &var, void *workspace, cudaStream_t stream);
 constexpr int kBackwardLaunches = 12;  // kernels + memsets one backward call queues (at most)
 
+// D = act(A B^T) on the tensor cores: A [M][K], B [N][K] bf16; D's columns
+// [0, n0) go to D0 [M][n0], [n0, n1) to D1, [n1, N) to D2 (bf16, row-major).
+int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, void *D1,
+                void *D2, int n0, int n1, int silu, cudaStream_t stream);
+
 // Shapes the tensor-core path covers.
 bool tc_supported(int B, int n, int s, int e, int C);
 int tc_launch_count();

@@ -28,6 +28,7 @@
 #include "tc_prep.cuh"
 #include "tc_scan.cuh"
 #include "tc_attn.cuh"
+#include "tc_gemm.cuh"
 
 namespace fmca {
 namespace {
@@ -183,6 +184,33 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
       !record_event(events, 3, stream))
     return 1;
   return 0;
+}
+
+int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, void *D1,
+                void *D2, int n0, int n1, int silu, cudaStream_t stream) {
+  CUtensorMap mA, mB, m0, m1, m2;
+  if (!make_map_bf16(&mA, A, K, M, 64, 128) || !make_map_bf16(&mB, B, K, N, 64, GM_TILE_N) ||
+      !make_map_bf16(&m0, D0, n0, M, 64, 128))
+    return 2;
+  m1 = m0;
+  m2 = m0;
+  if (n1 > n0 && !make_map_bf16(&m1, D1, n1 - n0, M, 64, 128)) return 2;
+  if (N > n1 && !make_map_bf16(&m2, D2, N - n1, M, 64, 128)) return 2;
+  static bool attrs = false;
+  if (!attrs) {
+    if (cudaFuncSetAttribute(tc_gemm<GEMM_ACT_NONE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)GEMM_SMEM) != cudaSuccess ||
+        cudaFuncSetAttribute(tc_gemm<GEMM_ACT_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)GEMM_SMEM) != cudaSuccess)
+      return 1;
+    attrs = true;
+  }
+  const int units = ((M + 127) / 128) * ((N + GM_TILE_N - 1) / GM_TILE_N);
+  const int sms = num_sms();
+  auto *kern = silu ? tc_gemm<GEMM_ACT_SILU> : tc_gemm<GEMM_ACT_NONE>;
+  kern<<<units < sms ? units : sms, GEMM_THREADS, GEMM_SMEM, stream>>>(mA, mB, m0, m1, m2, M, N,
+                                                                      K, n0, n1);
+  return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 
 int read_and_clear_device_status(cudaStream_t stream, int32_t *where) {

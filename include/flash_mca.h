@@ -252,6 +252,28 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
                                int causal, fmca_dtype dtype, const fmca_options *opts,
                                void *workspace, size_t workspace_bytes, fmca_stream_t stream);
 
+/*
+ * The dense projections of a GAU layer around the attention core, on the
+ * tensor cores (bf16 in, fp32 accumulation, bf16 out):
+ *   flash_mca_gau_project  U = SiLU(X W_u), V = SiLU(X W_v), Z = SiLU(X W_z)
+ *                          ("Initial Power": U and V with the Swish activation;
+ *                          "Weak Attention": Z = phi(X W_z))
+ *   flash_mca_gau_output   Out = Y W_o ("Strong Combination", eq. mix: the
+ *                          layer output (U * A V) W_o, Y being the core's O)
+ * No biases (the equations have none).  Weights are passed transposed, one
+ * row per output feature:
+ *   Wt   [2e + s][d]  rows 0..e-1 = columns of W_u, e..2e-1 = W_v, 2e.. = W_z
+ *   Wo_t [d][e]       = W_o^T
+ * X [M][d], U and V [M][e], Z [M][s], Y [M][e], Out [M][d]: row-major bf16
+ * device arrays, 16-byte aligned, outputs not overlapping inputs.  Sizes:
+ * M >= 1; d % 8 == 0; e and s multiples of 64 (project); d a multiple of 64
+ * (output).  Queued on `stream`, nothing allocated.
+ */
+fmca_status flash_mca_gau_project(const void *X, const void *Wt, void *U, void *V, void *Z,
+                                  int M, int d, int e, int s, fmca_stream_t stream);
+fmca_status flash_mca_gau_output(const void *Y, const void *Wo_t, void *Out, int M, int e,
+                                 int d, fmca_stream_t stream);
+
 /* Which path FMCA_PATH_AUTO takes for these arguments (FMCA_PATH_SIMT or
  * FMCA_PATH_TCGEN05), or -1 for arguments that would be rejected. */
 int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype);

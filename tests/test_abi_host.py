@@ -265,3 +265,20 @@ def test_backward_workspace_and_validation():
     import ctypes
     o = fm.FmcaOptions(0.1, 9)
     assert call(opts=ctypes.byref(o)) == fm.FMCA_ERR_INVALID_ARG
+
+
+def test_gau_projection_validation():
+    f = fm.lib.flash_mca_gau_project
+    X, W, U, V, Z = P, P + 0x100000, P + 0x200000, P + 0x300000, P + 0x400000
+    assert f(0, W, U, V, Z, 128, 64, 64, 64, None) == fm.FMCA_ERR_INVALID_ARG
+    assert f(X, W, U, V, Z, 0, 64, 64, 64, None) == fm.FMCA_ERR_INVALID_ARG
+    assert f(X, W, U, V, Z, 128, 60, 64, 64, None) == fm.FMCA_ERR_UNSUPPORTED   # d % 8
+    assert f(X, W, U, V, Z, 128, 64, 96, 64, None) == fm.FMCA_ERR_UNSUPPORTED   # e % 64
+    assert f(X, W, U, V, Z, 128, 64, 64, 32, None) == fm.FMCA_ERR_UNSUPPORTED   # s % 64
+    assert f(X + 8, W, U, V, Z, 128, 64, 64, 64, None) == fm.FMCA_ERR_ALIGN
+    assert f(X, W, X, V, Z, 128, 64, 64, 64, None) == fm.FMCA_ERR_INVALID_ARG   # U overlaps X
+    assert f(X, W, U, U, Z, 128, 64, 64, 64, None) == fm.FMCA_ERR_INVALID_ARG   # V overlaps U
+    g = fm.lib.flash_mca_gau_output
+    assert g(X, W, U, 128, 64, 96, None) == fm.FMCA_ERR_UNSUPPORTED             # d % 64
+    assert g(X, W, X, 128, 64, 64, None) == fm.FMCA_ERR_INVALID_ARG             # Out overlaps Y
+    assert g(X, W, U + 4, 128, 64, 64, None) == fm.FMCA_ERR_ALIGN
