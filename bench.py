@@ -446,19 +446,31 @@ def run_backward(args, w, device):
     if st != fm.FMCA_OK:
         raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
     ms = a.elapsed_time(b) / args.steps
+    # the gradient's own products, twice the forward pass's (recompute not counted)
     flops = 2.0 * algorithmic_flops(w, ln)
     achieved = flops / (ms / 1e3) / 1e12
+    dcode = fm.FMCA_BF16 if w.dtype == "bf16" else fm.FMCA_F32
+    tc = fm.flash_mca_auto_path(w.B, w.n, w.s, w.e, w.C, w.causal, dcode) == fm.FMCA_PATH_TCGEN05
+    if tc:
+        peaks, peak_kind = load_peaks()
+        peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
+        roof = {"bound": "tensor", "kernel": "whole backward (tcgen05 products + elementwise)",
+                "peak_source": f"bf16_tflops ({peak_kind})"}
+        dtype = "bf16 (tensor cores, fp32 accumulate)"
+    else:
+        peak = FP32_ALU_TFLOPS
+        roof = {"bound": "alu", "kernel": "whole backward (SIMT fp32)",
+                "peak_source": "fp32 CUDA-core rate from unit counts and max clock"}
+        dtype = "f32 (CUDA cores; I/O " + w.dtype + ")"
+    roof.update({"achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                 "traffic": None, "algorithmic_flops_per_step": flops})
     line = {
         "metric": "mixed-chunk attn backward tokens/s at 1 GB300",
         "value": w.B * w.n / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "f32 (CUDA cores; I/O " + w.dtype + ")", "data": "synthetic",
+        "vs_baseline": None, "dtype": dtype, "data": "synthetic",
         "config": {**config_of(w, args), "pass": "backward"},
-        "roofline": {"bound": "alu", "kernel": "whole backward (SIMT fp32)",
-                     "achieved": achieved, "peak": FP32_ALU_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / FP32_ALU_TFLOPS, "traffic": None,
-                     "algorithmic_flops_per_step": flops,
-                     "peak_source": "fp32 CUDA-core rate from unit counts and max clock"},
+        "roofline": roof,
         "gpu_launches": None,
         "clocks": sampler.summary(wall0, wall1),
     }

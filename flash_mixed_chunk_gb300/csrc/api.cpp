@@ -160,10 +160,20 @@ fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
              : FMCA_ERR_CUDA;
 }
 
+// bf16 shapes of the tensor-core forward path run the tensor-core backward;
+// everything else the CUDA-core one.
+static bool tc_backward(int B, int n, int s, int e, int C, fmca_dtype dtype) {
+  return dtype == FMCA_BF16 && tc_supported(B, n, s, e, C);
+}
+static size_t backward_bytes(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype) {
+  return tc_backward(B, n, s, e, C, dtype) ? tc_backward_layout(B, n, s, e, C, causal).total
+                                           : backward_layout(B, n, s, e, C, causal).total;
+}
+
 size_t flash_mca_backward_workspace_bytes(int B, int n, int s, int e, int C, int causal,
                                           fmca_dtype dtype) {
   if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
-  return backward_layout(B, n, s, e, C, causal).total;
+  return backward_bytes(B, n, s, e, C, causal, dtype);
 }
 
 fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, const float *gamma,
@@ -183,7 +193,7 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
     if (!aligned16(p)) return FMCA_ERR_ALIGN;
   if (!workspace) return FMCA_ERR_WORKSPACE;
   if (!aligned256(workspace)) return FMCA_ERR_ALIGN;
-  if (workspace_bytes_ < backward_layout(B, n, s, e, C, causal).total) return FMCA_ERR_WORKSPACE;
+  if (workspace_bytes_ < backward_bytes(B, n, s, e, C, causal, dtype)) return FMCA_ERR_WORKSPACE;
   {  // outputs must not overlap the inputs or the workspace
     const size_t es = elem_size(dtype), zb = (size_t)B * n * s * es, vb = (size_t)B * n * e * es;
     const size_t gb = sizeof(float) * 4 * (size_t)s;
@@ -202,6 +212,12 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
         if (&o2 != &o && overlap(o, o2)) return FMCA_ERR_INVALID_ARG;
     }
   }
+  if (tc_backward(B, n, s, e, C, dtype))
+    return launch_tc_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C,
+                              causal ? 1 : 0, var, workspace,
+                              reinterpret_cast<cudaStream_t>(stream)) == 0
+               ? FMCA_OK
+               : FMCA_ERR_CUDA;
   return launch_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C,
                          causal ? 1 : 0, dtype == FMCA_BF16 ? 1 : 0, var, workspace,
                          reinterpret_cast<cudaStream_t>(stream)) == 0

@@ -240,9 +240,14 @@ fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
  *   dgamma, dbeta        device float32 [4][s] outputs (overwritten)
  *   workspace            at least flash_mca_backward_workspace_bytes(...) bytes,
  *                        256-byte aligned
- * fp32 arithmetic on the CUDA cores, fixed reduction order (deterministic).
- * Sizes as for flash_mca_forward (any supported shape, both dtypes).  The
- * outputs must not overlap the inputs or the workspace.
+ * bf16 inputs in the shapes of FMCA_PATH_TCGEN05 (s == 128, C % 128 == 0,
+ * e % 256 == 0) run on the tensor cores: the forward kernels recompute the
+ * ungated output and the relu^2 weights, and batched bf16 products with fp32
+ * accumulation form the gradients (intermediates rounded to bf16).  Every
+ * other shape, and float32, runs in fp32 on the CUDA cores.  Both use a fixed
+ * reduction order (deterministic).  Sizes as for flash_mca_forward (any
+ * supported shape, both dtypes); the workspace size depends on which path the
+ * shape takes.  The outputs must not overlap the inputs or the workspace.
  */
 size_t flash_mca_backward_workspace_bytes(int B, int n, int s, int e, int C, int causal,
                                           fmca_dtype dtype);
