@@ -58,7 +58,7 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events = nullptr, bool gate = true);
+                      cudaEvent_t const *events = nullptr);
 
 inline bool record_event(cudaEvent_t const *events, int i, cudaStream_t stream) {
   return events == nullptr || cudaEventRecord(events[i], stream) == cudaSuccess;
@@ -129,19 +129,18 @@ int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, voi
 
 // Workspace of the tensor-core backward (bf16 unless noted), each region
 // 256-byte aligned: the forward pass's own workspace (chunk states, scaled
-// prefix, relu^2 weights, lin_q rows), then Y [B*n][e], dY [B*n][e], T0, T1,
-// T3 [B*n][s], dw/dS [B*n][C], dS^T and W^T per chunk [B*n][C], dT0..dT3
-// [B*n][s], d(prefix) [B][G][s][e], dV partials [B*n][e] x 2, and fp32
-// per-block dgamma/dbeta partials.
+// prefix, relu^2 weights, lin_q rows), then dY [B*n][e], T0, T1, T3
+// [B*n][s], dw/dS [B*n][C], dS^T and W^T per chunk [B*n][C], dT0..dT3
+// [B*n][s], d(prefix) [B][G][s][e], and fp32 per-block dgamma/dbeta partials.
+constexpr int kTcbAffRows = 16;  // token rows per block of the dZ/dgamma/dbeta reduction
 struct TcBackwardLayout {
-  size_t fwd, Y, dY, T0, T1, T3, dw, dSt, Wt, dT0, dT1, dT2, dT3, dP, dVq, dVl, part, total;
+  size_t fwd, dY, T0, T1, T3, dw, dSt, Wt, dT0, dT1, dT2, dT3, dP, part, total;
 };
 inline TcBackwardLayout tc_backward_layout(int B, int n, int s, int e, int C, int causal) {
   const size_t rows = (size_t)B * n, G = (size_t)(n / C);
   TcBackwardLayout L;
   L.fwd = 0;
-  L.Y = align256(workspace_bytes(B, n, s, e, C, causal));
-  L.dY = L.Y + align256(2 * rows * e);
+  L.dY = align256(workspace_bytes(B, n, s, e, C, causal));
   L.T0 = L.dY + align256(2 * rows * e);
   L.T1 = L.T0 + align256(2 * rows * s);
   L.T3 = L.T1 + align256(2 * rows * s);
@@ -153,10 +152,8 @@ inline TcBackwardLayout tc_backward_layout(int B, int n, int s, int e, int C, in
   L.dT2 = L.dT1 + align256(2 * rows * s);
   L.dT3 = L.dT2 + align256(2 * rows * s);
   L.dP = L.dT3 + align256(2 * rows * s);
-  L.dVq = L.dP + align256(2 * (size_t)B * G * s * e);
-  L.dVl = L.dVq + align256(2 * rows * e);
-  L.part = L.dVl + align256(2 * rows * e);
-  L.total = L.part + align256(4 * 8 * (size_t)s * ((rows + 63) / 64));
+  L.part = L.dP + align256(2 * (size_t)B * G * s * e);
+  L.total = L.part + align256(4 * 8 * (size_t)s * ((rows + kTcbAffRows - 1) / kTcbAffRows));
   return L;
 }
 int launch_tc_backward(const void *Z, const void *V, const void *U, const float *gamma,

@@ -105,7 +105,7 @@ int tc_launch_count() { return 3; }
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events, bool gate) {
+                      cudaEvent_t const *events) {
   const int G = n / C;
   const int R = C / ROW_TILE;
   const int64_t se = (int64_t)s * e;
@@ -135,9 +135,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                              (int)PREP_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_chunk_prep<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PREP_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_attn<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)AT_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_attn<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)AT_SMEM) != cudaSuccess)
       return 1;
     attrs = true;
@@ -183,7 +181,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   cfg.gridDim = dim3(n_units < num_sms() ? n_units : num_sms());
   cfg.blockDim = dim3(AT_THREADS);
   cfg.dynamicSmemBytes = AT_SMEM;
-  if (cudaLaunchKernelEx(&cfg, gate ? tc_chunk_attn<true> : tc_chunk_attn<false>, mPw, mT2, mV,
+  if (cudaLaunchKernelEx(&cfg, tc_chunk_attn, mPw, mT2, mV,
                          mS, mU, mO, sched + 1, n, e, C, G,
                          causal, n_units, no_global ? 0 : S_DIM / KEY_STAGE) != cudaSuccess ||
       !record_event(events, 3, stream))
@@ -220,14 +218,24 @@ int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, voi
 
 namespace {
 
-// D_b = alpha A_b B_b on the tensor cores (see tc_bgemm.cuh); A and B are
-// row-major [rows][cols] bf16 arrays read K-major or MN-major.
+// A row-major bf16 operand [rows][cols] of tc_bgemm.
+struct BgOperand {
+  const void *p;
+  uint64_t cols, rows;
+};
+
+// D_b = alpha (A_b B_b [+ A2_b B2_b]) on the tensor cores (see tc_bgemm.cuh);
+// A and B are read K-major or MN-major, A2 and B2 (used when sh.K2 > 0) the
+// same way.
 template <bool A_MN, bool B_MN, int NT>
-int bgemm(const void *A, uint64_t a_cols, uint64_t a_rows, const void *Bm, uint64_t b_cols,
-          uint64_t b_rows, void *D, const BgShape &sh, cudaStream_t stream) {
-  CUtensorMap mA, mB, mD;
-  if (!make_map_bf16(&mA, A, a_cols, a_rows, 64, A_MN ? 64 : 128) ||
-      !make_map_bf16(&mB, Bm, b_cols, b_rows, 64, B_MN ? 64 : NT) ||
+int bgemm(const BgOperand &A, const BgOperand &Bm, void *D, const BgShape &sh,
+          cudaStream_t stream, const BgOperand *A2 = nullptr, const BgOperand *B2 = nullptr) {
+  CUtensorMap mA, mB, mD, mA2, mB2;
+  const BgOperand &a2 = A2 ? *A2 : A, &b2 = B2 ? *B2 : Bm;
+  if (!make_map_bf16(&mA, A.p, A.cols, A.rows, 64, A_MN ? 64 : 128) ||
+      !make_map_bf16(&mB, Bm.p, Bm.cols, Bm.rows, 64, B_MN ? 64 : NT) ||
+      !make_map_bf16(&mA2, a2.p, a2.cols, a2.rows, 64, A_MN ? 64 : 128) ||
+      !make_map_bf16(&mB2, b2.p, b2.cols, b2.rows, 64, B_MN ? 64 : NT) ||
       !make_map_bf16(&mD, D, (uint64_t)sh.N, (uint64_t)sh.batches * sh.M, 64, 128))
     return 2;
   static bool attr = false;
@@ -240,7 +248,7 @@ int bgemm(const void *A, uint64_t a_cols, uint64_t a_rows, const void *Bm, uint6
   const int units = sh.batches * (sh.M / 128) * (sh.N / NT);
   const int sms = num_sms();
   tc_bgemm<A_MN, B_MN, NT><<<units < sms ? units : sms, BGEMM_THREADS, BGEMM_SMEM, stream>>>(
-      mA, mB, mD, sh);
+      mA, mB, mD, mA2, mB2, sh);
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 
@@ -249,12 +257,13 @@ unsigned blocks_for(int64_t count) { return (unsigned)((count + 255) / 256); }
 }  // namespace
 
 // The backward pass on the tensor cores (bf16, shapes of the tensor-core
-// forward path).  Recompute with the forward kernels (Y ungated, plus the
-// relu^2 weights W, the lin_q rows T2 and the scaled prefix P~ they leave in
-// their workspace), then, per chunk:
-//   dw = dY V^T,  dS = dw 2a sqrt(W),  dT0 = dS T1,  dT1 = dS^T T0,
-//   dV = W^T dY (+ T3 dS_h),  dP~ = T2^T dY -> reverse scan -> dS_h,
-//   dT2 = dY P~^T,  dT3 = V dS_h^T,
+// forward path).  The forward kernels run once more with dO in place of U:
+// their gated output is dU = dO * (quad + glob), and they leave the relu^2
+// weights W, the lin_q rows T2 and the scaled prefix P~ in their workspace.
+// Then, per chunk:
+//   dY = dO * U,  dw = dY V^T,  dS = dw 2a sqrt(W),  dT0 = dS T1,
+//   dT1 = dS^T T0,  dP~ = T2^T dY -> reverse scan -> dS_h,  dT2 = dY P~^T,
+//   dT3 = V dS_h^T,  dV = W^T dY + T3 dS_h (one product of depth C + s),
 // and finally dZ, dgamma, dbeta from dT0..dT3.
 int launch_tc_backward(const void *Z, const void *V, const void *U, const float *gamma,
                        const float *beta, const void *dO, void *dZ, void *dV, void *dU,
@@ -265,66 +274,77 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
   char *ws = static_cast<char *>(workspace);
   typedef __nv_bfloat16 bf16;
   auto at = [&](size_t off) { return reinterpret_cast<bf16 *>(ws + off); };
-  bf16 *Y = at(L.Y), *dY = at(L.dY), *T0 = at(L.T0), *T1 = at(L.T1), *T3 = at(L.T3);
-  bf16 *dw = at(L.dw), *dSt = at(L.dSt), *Wt = at(L.Wt), *dP = at(L.dP), *dVq = at(L.dVq);
-  bf16 *dVl = at(L.dVl);
+  bf16 *dY = at(L.dY), *T0 = at(L.T0), *T1 = at(L.T1), *T3 = at(L.T3);
+  bf16 *dw = at(L.dw), *dSt = at(L.dSt), *Wt = at(L.Wt), *dP = at(L.dP);
   bf16 *dT0 = at(L.dT0), *dT1 = at(L.dT1), *dT2 = at(L.dT2), *dT3 = at(L.dT3);
   const bf16 *prefix = at(L.fwd + FL.prefix), *W = at(L.fwd + FL.scores);
   const bf16 *T2 = at(L.fwd + FL.lin_q);
   float *part = reinterpret_cast<float *>(ws + L.part);
   const int G = n / C, Gp = causal ? G : 1;
-  const int64_t rows = (int64_t)B * n;
+  const uint64_t rows = (uint64_t)B * n;
   const bool glob = var.lin_norm != kLinNormNone;
-  // the forward pass, ungated: Y = quad + glob, and its workspace
-  if (launch_tc_forward(Z, V, U, gamma, beta, Y, B, n, s, e, C, causal, var, ws + L.fwd, stream,
-                        nullptr, false) != 0)
+  // dU = dO * (quad + glob), and the forward workspace
+  if (launch_tc_forward(Z, V, dO, gamma, beta, dU, B, n, s, e, C, causal, var, ws + L.fwd,
+                        stream) != 0)
     return 1;
-  tcb_gate_grads<<<blocks_for(rows * e), 256, 0, stream>>>(
-      static_cast<const bf16 *>(dO), static_cast<const bf16 *>(U), Y, dY,
-      static_cast<bf16 *>(dU), rows * e);
-  tcb_affine_rows<<<blocks_for(rows * s), 256, 0, stream>>>(static_cast<const bf16 *>(Z), gamma,
-                                                            beta, T0, T1, T3, rows * s, s);
+  const int64_t ne8 = (int64_t)rows * e / 8, ns8 = (int64_t)rows * s / 8;
+  tcb_gate_dy<<<blocks_for(ne8), 256, 0, stream>>>(static_cast<const uint4 *>(dO),
+                                                   static_cast<const uint4 *>(U),
+                                                   reinterpret_cast<uint4 *>(dY), ne8);
+  tcb_affine_rows<<<blocks_for(ns8), 256, 0, stream>>>(
+      static_cast<const uint4 *>(Z), gamma, beta, reinterpret_cast<uint4 *>(T0),
+      reinterpret_cast<uint4 *>(T1), reinterpret_cast<uint4 *>(T3), ns8, s);
   if (cudaGetLastError() != cudaSuccess) return 1;
   const int BG = B * G;
+  const BgOperand oY{dY, (uint64_t)e, rows}, oV{V, (uint64_t)e, rows};
+  const BgOperand oT0{T0, (uint64_t)s, rows}, oT1{T1, (uint64_t)s, rows};
+  const BgOperand oT2{T2, (uint64_t)s, rows}, oT3{T3, (uint64_t)s, rows};
+  const BgOperand odS{dw, (uint64_t)C, rows}, odSt{dSt, (uint64_t)C, rows};
+  const BgOperand oWt{Wt, (uint64_t)C, rows};
+  const BgOperand oP{prefix, (uint64_t)e, (uint64_t)B * Gp * s};
+  const BgOperand odP{dP, (uint64_t)e, (uint64_t)BG * s};
   int rc = 0;
   // dw = dY V^T per chunk (C x C, K = e)
   const BgShape s_dw{C, C, e, BG, C, 1, C, 1, 1.f};
-  rc |= C % 256 == 0 ? bgemm<false, false, 256>(dY, e, rows, V, e, rows, dw, s_dw, stream)
-                     : bgemm<false, false, 128>(dY, e, rows, V, e, rows, dw, s_dw, stream);
+  rc |= C % 256 == 0 ? bgemm<false, false, 256>(oY, oV, dw, s_dw, stream)
+                     : bgemm<false, false, 128>(oY, oV, dw, s_dw, stream);
   tcb_score_grads<<<dim3(BG, C / 32, C / 32), dim3(32, 8), 0, stream>>>(dw, W, dSt, Wt, C,
                                                                         var.quad_a, causal);
   // dT0 = dS T1, dT1 = dS^T T0 (C x s, K = C)
   const BgShape s_t{C, s, C, BG, C, 1, C, 1, 1.f};
-  rc |= bgemm<false, true, 128>(dw, C, rows, T1, s, rows, dT0, s_t, stream);
-  rc |= bgemm<false, true, 128>(dSt, C, rows, T0, s, rows, dT1, s_t, stream);
-  // dV (intra-chunk part) = W^T dY (C x e, K = C)
-  const BgShape s_vq{C, e, C, BG, C, 1, C, 1, 1.f};
-  rc |= bgemm<false, true, 256>(Wt, C, rows, dY, e, rows, glob ? dVq : static_cast<bf16 *>(dV),
-                                s_vq, stream);
+  rc |= bgemm<false, true, 128>(odS, oT1, dT0, s_t, stream);
+  rc |= bgemm<false, true, 128>(odSt, oT0, dT1, s_t, stream);
+  // the chunk states' sources dS_h = d(state_h); the global term's pair of dV
+  const int h_rpb = causal ? s : G * s, h_div = causal ? 1 : G;
   if (glob) {
     // d(prefix) per chunk = T2^T dY (s x e, K = C), then the reverse scan
     const BgShape s_dp{s, e, C, BG, C, 1, C, 1, 1.f};
-    rc |= bgemm<true, true, 256>(T2, s, rows, dY, e, rows, dP, s_dp, stream);
-    tcb_reverse_scan<<<blocks_for((int64_t)B * s * e), 256, 0, stream>>>(
-        dP, B, G, (int64_t)s * e, n, C, causal, var.lin_norm);
+    rc |= bgemm<true, true, 256>(oT2, oY, dP, s_dp, stream);
+    const int64_t se8 = (int64_t)s * e / 8;
+    tcb_reverse_scan<<<blocks_for((int64_t)B * se8), 256, 0, stream>>>(
+        reinterpret_cast<uint4 *>(dP), B, G, se8, n, C, causal, var.lin_norm);
     // dT2 = dY P~^T (C x s, K = e); P~ per chunk, or one per sequence
     const BgShape s_t2{C, s, e, BG, C, 1, s, causal ? 1 : G, 1.f};
-    rc |= bgemm<false, false, 128>(dY, e, rows, prefix, e, (uint64_t)B * Gp * s, dT2, s_t2,
-                                   stream);
-    // dT3 = V dS_h^T (C x s, K = e); dV (global part) = T3 dS_h (C x e, K = s)
-    const int h_rpb = causal ? s : G * s, h_div = causal ? 1 : G;
+    rc |= bgemm<false, false, 128>(oY, oP, dT2, s_t2, stream);
+    // dT3 = V dS_h^T (C x s, K = e)
     const BgShape s_t3{C, s, e, BG, C, 1, h_rpb, h_div, 1.f};
-    rc |= bgemm<false, false, 128>(V, e, rows, dP, e, (uint64_t)BG * s, dT3, s_t3, stream);
-    const BgShape s_vl{C, e, s, BG, C, 1, h_rpb, h_div, 1.f};
-    rc |= bgemm<false, true, 256>(T3, s, rows, dP, e, (uint64_t)BG * s, dVl, s_vl, stream);
-    tcb_add<<<blocks_for(rows * e), 256, 0, stream>>>(dVq, dVl, static_cast<bf16 *>(dV), rows * e);
+    rc |= bgemm<false, false, 128>(oV, odP, dT3, s_t3, stream);
   }
+  // dV = W^T dY (C x e, K = C) [+ T3 dS_h (K = s)]
+  BgShape s_v{C, e, C, BG, C, 1, C, 1, 1.f};
+  if (glob) {
+    s_v.K2 = s;
+    s_v.a2_rpb = C;
+    s_v.b2_rpb = h_rpb;
+    s_v.b2_div = h_div;
+  }
+  rc |= bgemm<false, true, 256>(oWt, oY, dV, s_v, stream, &oT3, &odP);
   if (rc) return 1;
   const int nblk = (int)((rows + kTcbAffRows - 1) / kTcbAffRows);
   tcb_affine_reduce<<<nblk, s, 0, stream>>>(static_cast<const bf16 *>(Z), gamma, dT0, dT1, dT2,
-                                            dT3, static_cast<bf16 *>(dZ), part, rows, n, s,
-                                            var.lin_norm, glob ? 1 : 0);
-  tcb_gamma_beta<<<(8 * s + 255) / 256, 256, 0, stream>>>(part, nblk, s, dgamma, dbeta);
+                                            dT3, static_cast<bf16 *>(dZ), part, (int64_t)rows, n,
+                                            s, var.lin_norm, glob ? 1 : 0);
+  tcb_gamma_beta<<<(8 * s + 31) / 32, dim3(32, 32), 0, stream>>>(part, nblk, s, dgamma, dbeta);
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }
 

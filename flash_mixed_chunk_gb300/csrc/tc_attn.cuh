@@ -62,10 +62,6 @@ __device__ __forceinline__ AttnUnit decode_unit(int u, int n, int e, int C, int 
   return a;
 }
 
-// GATE = false: the kernel writes acc itself (Y = quad + glob, before the U
-// gate; the backward pass needs it); ring B then carries no U tiles and its
-// slots serve only as store staging.
-template <bool GATE>
 __global__ void __launch_bounds__(AT_THREADS, 1)
     tc_chunk_attn(const __grid_constant__ CUtensorMap mapPr,  // P [B*n][C], box {64,128}
                   const __grid_constant__ CUtensorMap mapT2,  // T2 [B*n][s], box {64,128}
@@ -213,13 +209,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             ok = false;
             break;
           }
-          if (GATE) {
-            mbar_arrive_expect_tx(&fullB[slot], AT_SLOT_B);
-            tma_load_2d_hint(ringB + slot * AT_SLOT_B, &mapU, &fullB[slot], a.e0 + 64 * q,
-                             a.row0, stream_policy);
-          } else {
-            mbar_arrive(&fullB[slot]);  // an empty staging slot
-          }
+          mbar_arrive_expect_tx(&fullB[slot], AT_SLOT_B);
+          tma_load_2d_hint(ringB + slot * AT_SLOT_B, &mapU, &fullB[slot], a.e0 + 64 * q, a.row0,
+                           stream_policy);
         }
       }
       for (int q = (ib > AT_RING_B ? ib - AT_RING_B : 0); q < ib; ++q)
@@ -324,22 +316,14 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
 #pragma unroll
             for (int j4 = 0; j4 < 4; ++j4) {
               uint4 *ptr = reinterpret_cast<uint4 *>(us + sw128_offset(row, c2 * 64 + 16 * j4));
+              const uint4 uv = *ptr;
+              const uint32_t w[4] = {uv.x, uv.y, uv.z, uv.w};
               uint32_t o[4];
-              if (GATE) {
-                const uint4 uv = *ptr;
-                const uint32_t w[4] = {uv.x, uv.y, uv.z, uv.w};
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int jj = 8 * j4 + 2 * i;
-                  o[i] = pack_bf16x2(bf16_lo(w[i]) * __uint_as_float(r[c2][jj]),
-                                     bf16_hi(w[i]) * __uint_as_float(r[c2][jj + 1]));
-                }
-              } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int jj = 8 * j4 + 2 * i;
-                  o[i] = pack_bf16x2(__uint_as_float(r[c2][jj]), __uint_as_float(r[c2][jj + 1]));
-                }
+              for (int i = 0; i < 4; ++i) {
+                const int jj = 8 * j4 + 2 * i;
+                o[i] = pack_bf16x2(bf16_lo(w[i]) * __uint_as_float(r[c2][jj]),
+                                   bf16_hi(w[i]) * __uint_as_float(r[c2][jj + 1]));
               }
               *ptr = make_uint4(o[0], o[1], o[2], o[3]);
             }

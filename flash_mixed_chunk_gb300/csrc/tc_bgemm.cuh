@@ -8,7 +8,9 @@
 // (div > 1 lets consecutive batches share an operand, e.g. every chunk of a
 // sequence reading one state matrix); D_b occupies rows b * M .. of D [rows][N].
 // M and K are multiples of 128 and 64, N a multiple of the N tile, so that no
-// tile reaches into another batch's rows.
+// tile reaches into another batch's rows.  A second operand pair (A2 [M][K2],
+// B2 [K2][N], same majorness) may extend the contraction:
+// D_b = alpha (A_b B_b + A2_b B2_b), one accumulator for both.
 //
 // Persistent kernel, one CTA per SM, tiles (batch, 128-row tile, NT-column
 // tile) dealt round-robin; K streamed in 64-deep stages through a four-slot
@@ -40,6 +42,8 @@ struct BgShape {
   int a_rpb, a_div;   // operand rows per batch step and batch divisor
   int b_rpb, b_div;
   float alpha;
+  int K2 = 0;         // depth of the second operand pair (0: none)
+  int a2_rpb = 0, a2_div = 1, b2_rpb = 0, b2_div = 1;
 };
 
 template <bool A_MN, bool B_MN, int NT>
@@ -47,6 +51,8 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1)
     tc_bgemm(const __grid_constant__ CUtensorMap mapA,  // K-major: box {64, 128}; MN: {64, 64}
              const __grid_constant__ CUtensorMap mapB,  // K-major: box {64, NT}; MN: {64, 64}
              const __grid_constant__ CUtensorMap mapD,  // D [batches*M][N], box {64, 128}
+             const __grid_constant__ CUtensorMap mapA2,  // as mapA, for k >= K
+             const __grid_constant__ CUtensorMap mapB2,  // as mapB, for k >= K
              const BgShape sh) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -61,7 +67,7 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1)
   const int n_mt = sh.M / 128, n_nt = sh.N / NT;
   const int per_batch = n_mt * n_nt;
   const int n_units = sh.batches * per_batch;
-  const int n_ks = sh.K / 64;
+  const int n_k1 = sh.K / 64, n_ks = n_k1 + sh.K2 / 64;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < BG_RING; ++i) {
@@ -93,6 +99,10 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&mapA);
       tma_prefetch_desc(&mapB);
+      if (sh.K2 > 0) {
+        tma_prefetch_desc(&mapA2);
+        tma_prefetch_desc(&mapB2);
+      }
       int it = 0;
       bool ok = true;
       constexpr uint32_t B_BYTES = NT * 64 * 2;
@@ -109,8 +119,13 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1)
         if (uu < 0) break;
         const int bt = uu / per_batch, w = uu % per_batch;
         const int mt = w / n_nt, nt = w % n_nt;
-        const int a_row0 = (bt / sh.a_div) * sh.a_rpb, b_row0 = (bt / sh.b_div) * sh.b_rpb;
+        const int a_row1 = (bt / sh.a_div) * sh.a_rpb, b_row1 = (bt / sh.b_div) * sh.b_rpb;
+        const int a_row2 = (bt / sh.a2_div) * sh.a2_rpb, b_row2 = (bt / sh.b2_div) * sh.b2_rpb;
         for (int ks = 0; ks < n_ks; ++ks, ++it) {
+          const bool second = ks >= n_k1;
+          const CUtensorMap *mA = second ? &mapA2 : &mapA, *mB = second ? &mapB2 : &mapB;
+          const int kr = (second ? ks - n_k1 : ks) * 64;
+          const int a_row0 = second ? a_row2 : a_row1, b_row0 = second ? b_row2 : b_row1;
           const int slot = it % BG_RING;
           if (it >= BG_RING && !mbar_wait(&empty[slot], ((it / BG_RING) - 1) & 1, kWaitLimitNs)) {
             record_timeout(701);
@@ -120,17 +135,17 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1)
           uint8_t *sz = smem + slot * BG_SLOT;
           mbar_arrive_expect_tx(&full[slot], BG_A_BYTES + B_BYTES);
           if (A_MN) {  // rows k, columns m: two 64-column boxes
-            tma_load_2d(sz, &mapA, &full[slot], mt * 128, a_row0 + ks * 64);
-            tma_load_2d(sz + 8192, &mapA, &full[slot], mt * 128 + 64, a_row0 + ks * 64);
+            tma_load_2d(sz, mA, &full[slot], mt * 128, a_row0 + kr);
+            tma_load_2d(sz + 8192, mA, &full[slot], mt * 128 + 64, a_row0 + kr);
           } else {     // rows m, columns k
-            tma_load_2d(sz, &mapA, &full[slot], ks * 64, a_row0 + mt * 128);
+            tma_load_2d(sz, mA, &full[slot], kr, a_row0 + mt * 128);
           }
           uint8_t *sb = sz + BG_A_BYTES;
           if (B_MN) {  // rows k, columns n: NT / 64 boxes of 64 columns
             for (int j = 0; j < NT / 64; ++j)
-              tma_load_2d(sb + j * 8192, &mapB, &full[slot], nt * NT + 64 * j, b_row0 + ks * 64);
+              tma_load_2d(sb + j * 8192, mB, &full[slot], nt * NT + 64 * j, b_row0 + kr);
           } else {     // rows n, columns k
-            tma_load_2d(sb, &mapB, &full[slot], ks * 64, b_row0 + nt * NT);
+            tma_load_2d(sb, mB, &full[slot], kr, b_row0 + nt * NT);
           }
         }
       }

@@ -1,13 +1,14 @@
 // tc_bwd.cuh -- the elementwise steps of the tensor-core backward pass
 // (the products run in tc_bgemm; see launch_tc_backward in tc.cu for the
-// order).  With Y = quad + glob recomputed by the forward kernels:
-//   dY = dO * U, dU = dO * Y;  T0, T1, T3 rows in bf16;
+// order).  The forward kernels, fed dO in place of U, give dU = dO * Y
+// directly; the rest:
+//   dY = dO * U;  T0, T1, T3 rows in bf16;
 //   dS_ij = dw_ij * 2 a relu(a S_ij), with relu(a S_ij) = sqrt(w_ij) taken
 //   from the stored weights w = relu(a S)^2 (0 where masked), plus the
 //   per-chunk transposes of dS and w;
 //   the reverse chunk scan of d(prefix): dS_h = sum_{g>h} f_g dP_g;
 //   dZ = sum_k dT_k * gamma_k with per-block dgamma/dbeta partials.
-// Included by tc.cu.
+// Row-wise kernels move 8 bf16 (16 bytes) per thread.  Included by tc.cu.
 #pragma once
 
 #include "tc_common.cuh"
@@ -18,30 +19,51 @@ namespace {
 __device__ __forceinline__ float bf(const __nv_bfloat16 &x) { return __bfloat162float(x); }
 __device__ __forceinline__ __nv_bfloat16 tob(float x) { return __float2bfloat16_rn(x); }
 
-// dY = dO * U and dU = dO * Y over [rows][e] (bf16)
-__global__ void tcb_gate_grads(const __nv_bfloat16 *__restrict__ dO,
-                               const __nv_bfloat16 *__restrict__ U,
-                               const __nv_bfloat16 *__restrict__ Y, __nv_bfloat16 *__restrict__ dY,
-                               __nv_bfloat16 *__restrict__ dU, int64_t count) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= count) return;
-  const float g = bf(dO[i]);
-  dY[i] = tob(g * bf(U[i]));
-  dU[i] = tob(g * bf(Y[i]));
+__device__ __forceinline__ void unpack8(const uint4 &v, float *f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = bf16_lo(w[i]);
+    f[2 * i + 1] = bf16_hi(w[i]);
+  }
+}
+__device__ __forceinline__ uint4 pack8(const float *f) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
 }
 
-// T0, T1, T3 = Z * gamma_k + beta_k over [rows][s] (bf16)
-__global__ void tcb_affine_rows(const __nv_bfloat16 *__restrict__ Z, const float *__restrict__ gamma,
-                                const float *__restrict__ beta, __nv_bfloat16 *__restrict__ T0,
-                                __nv_bfloat16 *__restrict__ T1, __nv_bfloat16 *__restrict__ T3,
-                                int64_t count, int s) {
+// dY = dO * U over [rows][e] (bf16), 8 elements per thread; count8 = count / 8
+__global__ void tcb_gate_dy(const uint4 *__restrict__ dO, const uint4 *__restrict__ U,
+                            uint4 *__restrict__ dY, int64_t count8) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= count) return;
-  const int a = (int)(i % s);
-  const float z = bf(Z[i]);
-  T0[i] = tob(z * gamma[a] + beta[a]);
-  T1[i] = tob(z * gamma[s + a] + beta[s + a]);
-  T3[i] = tob(z * gamma[3 * s + a] + beta[3 * s + a]);
+  if (i >= count8) return;
+  float g[8], u[8];
+  unpack8(__ldcs(dO + i), g);
+  unpack8(__ldcs(U + i), u);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) g[k] *= u[k];
+  dY[i] = pack8(g);
+}
+
+// T0, T1, T3 = Z * gamma_k + beta_k over [rows][s] (bf16), 8 columns per thread
+__global__ void tcb_affine_rows(const uint4 *__restrict__ Z, const float *__restrict__ gamma,
+                                const float *__restrict__ beta, uint4 *__restrict__ T0,
+                                uint4 *__restrict__ T1, uint4 *__restrict__ T3, int64_t count8,
+                                int s) {
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= count8) return;
+  const int a0 = (int)((i * 8) % s);
+  float z[8], t[8];
+  unpack8(Z[i], z);
+  uint4 *const out[3] = {T0, T1, T3};
+  const int ks[3] = {0, 1, 3};
+#pragma unroll
+  for (int m = 0; m < 3; ++m) {
+    const float *g = gamma + ks[m] * s + a0, *b = beta + ks[m] * s + a0;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t[k] = fmaf(z[k], g[k], b[k]);
+    out[m][i] = pack8(t);
+  }
 }
 
 // One 32 x 32 tile (query rows i, keys j) of chunk bg: dS = dw * 2 a sqrt(w)
@@ -74,45 +96,68 @@ __global__ void tcb_score_grads(__nv_bfloat16 *__restrict__ dw, const __nv_bfloa
 }
 
 // Reverse scan over chunks of d(prefix) [B][G][s][e] (bf16, in place, fp32
-// sums): causal dS_h = sum_{g>h} f_g dP_g; bidirectional slot (b, 0) gets
-// f * sum_g dP_g (every chunk of the sequence reads it).
-__global__ void tcb_reverse_scan(__nv_bfloat16 *__restrict__ dP, int B, int G, int64_t se, int n,
-                                 int C, int causal, int lin_norm) {
+// sums), 8 columns per thread: causal dS_h = sum_{g>h} f_g dP_g; bidirectional
+// slot (b, 0) gets f * sum_g dP_g (every chunk of the sequence reads it).
+// f_g is the divisor's inverse that the forward scan applied to chunk g's
+// prefix (1 with the per-position divisor, which the T2 rows carry).
+__global__ void tcb_reverse_scan(uint4 *__restrict__ dP, int B, int G, int64_t se8, int n, int C,
+                                 int causal, int lin_norm) {
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= (int64_t)B * se) return;
-  const int64_t b = t / se, x = t % se;
-  __nv_bfloat16 *p = dP + b * G * se + x;
+  if (t >= (int64_t)B * se8) return;
+  const int64_t b = t / se8, x = t % se8;
+  uint4 *p = dP + b * G * se8 + x;
   auto factor = [&](int g) -> float {
     if (lin_norm == kLinNormPosition) return 1.f;
     if (lin_norm == kLinNormSummed && causal) return g > 0 ? 1.f / ((float)g * (float)C) : 0.f;
     return 1.f / (float)n;
   };
+  float run[8], v[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) run[k] = 0.f;
+  constexpr int UN = 8;
   if (causal) {
-    float run = 0.f;
-    for (int g = G - 1; g >= 0; --g) {
-      const float v = bf(p[(int64_t)g * se]);
-      p[(int64_t)g * se] = tob(run);
-      run += factor(g) * v;
+    for (int g1 = G; g1 > 0; g1 -= UN) {  // chunks g1-1 down to g1-UN
+      uint4 in[UN];
+#pragma unroll
+      for (int u = 0; u < UN; ++u)
+        if (g1 - 1 - u >= 0) in[u] = p[(int64_t)(g1 - 1 - u) * se8];
+#pragma unroll
+      for (int u = 0; u < UN; ++u) {
+        const int g = g1 - 1 - u;
+        if (g >= 0) {
+          p[(int64_t)g * se8] = pack8(run);
+          unpack8(in[u], v);
+          const float f = factor(g);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) run[k] = fmaf(f, v[k], run[k]);
+        }
+      }
     }
   } else {
-    float tot = 0.f;
-    for (int g = 0; g < G; ++g) tot += bf(p[(int64_t)g * se]);
-    p[0] = tob(tot * factor(0));
+    for (int g0 = 0; g0 < G; g0 += UN) {
+      uint4 in[UN];
+#pragma unroll
+      for (int u = 0; u < UN; ++u)
+        if (g0 + u < G) in[u] = p[(int64_t)(g0 + u) * se8];
+#pragma unroll
+      for (int u = 0; u < UN; ++u)
+        if (g0 + u < G) {
+          unpack8(in[u], v);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) run[k] += v[k];
+        }
+    }
+    const float f = factor(0);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) run[k] *= f;
+    p[0] = pack8(run);
   }
 }
 
-// dV = dVq + dVl (bf16)
-__global__ void tcb_add(const __nv_bfloat16 *__restrict__ a, const __nv_bfloat16 *__restrict__ b,
-                        __nv_bfloat16 *__restrict__ out, int64_t count) {
-  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (i < count) out[i] = tob(bf(a[i]) + bf(b[i]));
-}
-
-// 64 token rows per block, one thread per column a (blockDim = s): dZ and
-// per-block partial sums of dgamma_k, dbeta_k; dT2 holds the gradient of the
-// lin_q rows as the kernels used them (times 1/(t+1) with the per-position
-// divisor), so its row factor is applied here.
-constexpr int kTcbAffRows = 64;
+// kTcbAffRows token rows per block, one thread per column a (blockDim = s):
+// dZ and per-block partial sums of dgamma_k, dbeta_k.  dT2 holds the gradient
+// of the lin_q rows as the kernels used them (times 1/(t+1) with the
+// per-position divisor), so that row factor is applied here.
 __global__ void tcb_affine_reduce(const __nv_bfloat16 *__restrict__ Z,
                                   const float *__restrict__ gamma,
                                   const __nv_bfloat16 *__restrict__ dT0,
@@ -126,7 +171,10 @@ __global__ void tcb_affine_reduce(const __nv_bfloat16 *__restrict__ Z,
   float g[4], pg[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int k = 0; k < 4; ++k) g[k] = gamma[k * s + a];
-  for (int64_t t = t0; t < t0 + kTcbAffRows && t < rows; ++t) {
+#pragma unroll 4
+  for (int r = 0; r < kTcbAffRows; ++r) {
+    const int64_t t = t0 + r;
+    if (t >= rows) break;
     const int64_t o = t * s + a;
     const float z = bf(Z[o]);
     float d[4];
@@ -152,16 +200,26 @@ __global__ void tcb_affine_reduce(const __nv_bfloat16 *__restrict__ Z,
   }
 }
 
+// Sum of the nblk partials of each of the 8 s outputs (dgamma, then dbeta),
+// in a fixed order: thread (x, y) of a (32, 32) block adds partials y, y+32,
+// ...; the 32 sums are then added in y order.  grid ceil(8 s / 32).
 __global__ void tcb_gamma_beta(const float *__restrict__ part, int nblk, int s,
                                float *__restrict__ dgamma, float *__restrict__ dbeta) {
-  const int x = blockIdx.x * blockDim.x + threadIdx.x;
-  if (x >= 8 * s) return;
-  float acc = 0.f;
-  for (int i = 0; i < nblk; ++i) acc += part[(int64_t)i * 8 * s + x];
-  if (x < 4 * s)
-    dgamma[x] = acc;
-  else
-    dbeta[x - 4 * s] = acc;
+  __shared__ float acc[32][33];
+  const int x = blockIdx.x * 32 + threadIdx.x, y = threadIdx.y;
+  float v = 0.f;
+  if (x < 8 * s)
+    for (int i = y; i < nblk; i += 32) v += part[(int64_t)i * 8 * s + x];
+  acc[y][threadIdx.x] = v;
+  __syncthreads();
+  if (y == 0 && x < 8 * s) {
+    float tot = 0.f;
+    for (int k = 0; k < 32; ++k) tot += acc[k][threadIdx.x];
+    if (x < 4 * s)
+      dgamma[x] = tot;
+    else
+      dbeta[x - 4 * s] = tot;
+  }
 }
 
 }  // namespace
