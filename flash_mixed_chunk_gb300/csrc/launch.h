@@ -130,11 +130,11 @@ int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, voi
 // Workspace of the tensor-core backward (bf16 unless noted), each region
 // 256-byte aligned: the forward pass's own workspace (chunk states, scaled
 // prefix, relu^2 weights, lin_q rows), then dY [B*n][e], T0, T1, T3
-// [B*n][s], dw/dS [B*n][C], dS^T and W^T per chunk [B*n][C], dT0..dT3
-// [B*n][s], d(prefix) [B][G][s][e], and fp32 per-block dgamma/dbeta partials.
+// [B*n][s], dS [B*n][C], dT0..dT3 [B*n][s], d(prefix) [B][G][s][e], and fp32
+// per-block dgamma/dbeta partials.
 constexpr int kTcbAffRows = 16;  // token rows per block of the dZ/dgamma/dbeta reduction
 struct TcBackwardLayout {
-  size_t fwd, dY, T0, T1, T3, dw, dSt, Wt, dT0, dT1, dT2, dT3, dP, part, total;
+  size_t fwd, dY, T0, T1, T3, dS, dT0, dT1, dT2, dT3, dP, part, total;
 };
 inline TcBackwardLayout tc_backward_layout(int B, int n, int s, int e, int C, int causal) {
   const size_t rows = (size_t)B * n, G = (size_t)(n / C);
@@ -144,10 +144,8 @@ inline TcBackwardLayout tc_backward_layout(int B, int n, int s, int e, int C, in
   L.T0 = L.dY + align256(2 * rows * e);
   L.T1 = L.T0 + align256(2 * rows * s);
   L.T3 = L.T1 + align256(2 * rows * s);
-  L.dw = L.T3 + align256(2 * rows * s);
-  L.dSt = L.dw + align256(2 * rows * C);
-  L.Wt = L.dSt + align256(2 * rows * C);
-  L.dT0 = L.Wt + align256(2 * rows * C);
+  L.dS = L.T3 + align256(2 * rows * s);
+  L.dT0 = L.dS + align256(2 * rows * C);
   L.dT1 = L.dT0 + align256(2 * rows * s);
   L.dT2 = L.dT1 + align256(2 * rows * s);
   L.dT3 = L.dT2 + align256(2 * rows * s);

@@ -280,6 +280,12 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t byte_in_
   return row * 128u + ((((byte_in_row >> 4) ^ (row & 7u)) << 4) | (byte_in_row & 15u));
 }
 
+// Same for a 64-byte-swizzled tile of 64-byte rows (32 bf16; 8-row groups
+// of 512 bytes; base 512-byte aligned).
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t byte_in_row) {
+  return row * 64u + ((((byte_in_row >> 4) ^ ((row >> 1) & 3u)) << 4) | (byte_in_row & 15u));
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);

@@ -3,9 +3,6 @@
 // order).  The forward kernels, fed dO in place of U, give dU = dO * Y
 // directly; the rest:
 //   dY = dO * U;  T0, T1, T3 rows in bf16;
-//   dS_ij = dw_ij * 2 a relu(a S_ij), with relu(a S_ij) = sqrt(w_ij) taken
-//   from the stored weights w = relu(a S)^2 (0 where masked), plus the
-//   per-chunk transposes of dS and w;
 //   the reverse chunk scan of d(prefix): dS_h = sum_{g>h} f_g dP_g;
 //   dZ = sum_k dT_k * gamma_k with per-block dgamma/dbeta partials.
 // Row-wise kernels move 8 bf16 (16 bytes) per thread.  Included by tc.cu.
@@ -63,35 +60,6 @@ __global__ void tcb_affine_rows(const uint4 *__restrict__ Z, const float *__rest
 #pragma unroll
     for (int k = 0; k < 8; ++k) t[k] = fmaf(z[k], g[k], b[k]);
     out[m][i] = pack8(t);
-  }
-}
-
-// One 32 x 32 tile (query rows i, keys j) of chunk bg: dS = dw * 2 a sqrt(w)
-// in place over dw, and the transposes dSt[j][i], Wt[j][i].  Causal: keys
-// j > i are masked (the forward pass never writes those weights: they are
-// not read, and the gradients there are 0).
-// grid (B*G, C/32, C/32); block (32, 8).
-__global__ void tcb_score_grads(__nv_bfloat16 *__restrict__ dw, const __nv_bfloat16 *__restrict__ W,
-                                __nv_bfloat16 *__restrict__ dSt, __nv_bfloat16 *__restrict__ Wt,
-                                int C, float quad_a, int causal) {
-  __shared__ float ts[32][33], tw[32][33];
-  const int64_t base = (int64_t)blockIdx.x * C * C;  // chunk bg: rows bg*C.. of [rows][C]
-  const int i0 = blockIdx.y * 32, j0 = blockIdx.z * 32;
-  const int tx = threadIdx.x, ty = threadIdx.y;
-  for (int r = ty; r < 32; r += 8) {
-    const int64_t o = base + (int64_t)(i0 + r) * C + j0 + tx;
-    const bool keep = !causal || j0 + tx <= i0 + r;
-    const float w = keep ? bf(W[o]) : 0.f;
-    const float d = keep ? bf(dw[o]) * 2.f * quad_a * sqrtf(w) : 0.f;
-    dw[o] = tob(d);
-    ts[r][tx] = d;
-    tw[r][tx] = w;
-  }
-  __syncthreads();
-  for (int r = ty; r < 32; r += 8) {
-    const int64_t o = base + (int64_t)(j0 + r) * C + i0 + tx;
-    dSt[o] = tob(ts[tx][r]);
-    Wt[o] = tob(tw[tx][r]);
   }
 }
 
