@@ -132,7 +132,7 @@ int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, voi
 // prefix, relu^2 weights, lin_q rows), then dY [B*n][e], T0, T1, T3
 // [B*n][s], dS [B*n][C], dT0..dT3 [B*n][s], d(prefix) [B][G][s][e], and fp32
 // per-block dgamma/dbeta partials.
-constexpr int kTcbAffRows = 16;  // token rows per block of the dZ/dgamma/dbeta reduction
+constexpr int kTcbAffRows = 64;  // token rows per block of the dZ/dgamma/dbeta reduction
 struct TcBackwardLayout {
   size_t fwd, dY, T0, T1, T3, dS, dT0, dT1, dT2, dT3, dP, part, total;
 };

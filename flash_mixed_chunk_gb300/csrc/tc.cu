@@ -326,7 +326,8 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
                                                    static_cast<const uint4 *>(U),
                                                    reinterpret_cast<uint4 *>(dY), ne8);
   tcb_affine_rows<<<blocks_for(ns8), 256, 0, stream>>>(
-      static_cast<const uint4 *>(Z), gamma, beta, reinterpret_cast<uint4 *>(T0),
+      static_cast<const uint4 *>(Z), reinterpret_cast<const float4 *>(gamma),
+      reinterpret_cast<const float4 *>(beta), reinterpret_cast<uint4 *>(T0),
       reinterpret_cast<uint4 *>(T1), reinterpret_cast<uint4 *>(T3), ns8, s);
   if (cudaGetLastError() != cudaSuccess) return 1;
   const BgOperand oY{dY, (uint64_t)e, rows}, oV{V, (uint64_t)e, rows};
@@ -396,9 +397,11 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
   }
   if (rc) return 1;
   const int nblk = (int)((rows + kTcbAffRows - 1) / kTcbAffRows);
-  tcb_affine_reduce<<<nblk, s, 0, stream>>>(static_cast<const bf16 *>(Z), gamma, dT0, dT1, dT2,
-                                            dT3, static_cast<bf16 *>(dZ), part, (int64_t)rows, n,
-                                            s, var.lin_norm, glob ? 1 : 0);
+  auto u2 = [](const void *p) { return static_cast<const uint2 *>(p); };
+  tcb_affine_reduce<<<nblk, dim3(s / 4, kTcbAffLanes), sizeof(float) * kTcbAffLanes * s,
+                      stream>>>(u2(Z), gamma, u2(dT0), u2(dT1), u2(dT2), u2(dT3),
+                                static_cast<uint2 *>(dZ), part, (int64_t)rows, n, s,
+                                var.lin_norm, glob ? 1 : 0);
   tcb_gamma_beta<<<(8 * s + 31) / 32, dim3(32, 32), 0, stream>>>(part, nblk, s, dgamma, dbeta);
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
 }

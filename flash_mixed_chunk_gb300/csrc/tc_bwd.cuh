@@ -42,21 +42,26 @@ __global__ void tcb_gate_dy(const uint4 *__restrict__ dO, const uint4 *__restric
   dY[i] = pack8(g);
 }
 
-// T0, T1, T3 = Z * gamma_k + beta_k over [rows][s] (bf16), 8 columns per thread
-__global__ void tcb_affine_rows(const uint4 *__restrict__ Z, const float *__restrict__ gamma,
-                                const float *__restrict__ beta, uint4 *__restrict__ T0,
+// T0, T1, T3 = Z * gamma_k + beta_k over [rows][s] (bf16), 8 columns per
+// thread; gamma, beta [4][s] read as float4 (s % 8 == 0).
+__global__ void tcb_affine_rows(const uint4 *__restrict__ Z, const float4 *__restrict__ gamma,
+                                const float4 *__restrict__ beta, uint4 *__restrict__ T0,
                                 uint4 *__restrict__ T1, uint4 *__restrict__ T3, int64_t count8,
                                 int s) {
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count8) return;
-  const int a0 = (int)((i * 8) % s);
+  const int a4 = (int)(i % (s / 8)) * 2;  // float4 index of the first column
   float z[8], t[8];
-  unpack8(Z[i], z);
+  unpack8(__ldcs(Z + i), z);
   uint4 *const out[3] = {T0, T1, T3};
   const int ks[3] = {0, 1, 3};
 #pragma unroll
   for (int m = 0; m < 3; ++m) {
-    const float *g = gamma + ks[m] * s + a0, *b = beta + ks[m] * s + a0;
+    const int o = ks[m] * (s / 4) + a4;
+    const float4 g0 = __ldg(gamma + o), g1 = __ldg(gamma + o + 1);
+    const float4 b0 = __ldg(beta + o), b1 = __ldg(beta + o + 1);
+    const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+    const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
 #pragma unroll
     for (int k = 0; k < 8; ++k) t[k] = fmaf(z[k], g[k], b[k]);
     out[m][i] = pack8(t);
@@ -122,49 +127,86 @@ __global__ void tcb_reverse_scan(uint4 *__restrict__ dP, int B, int G, int64_t s
   }
 }
 
-// kTcbAffRows token rows per block, one thread per column a (blockDim = s):
-// dZ and per-block partial sums of dgamma_k, dbeta_k.  dT2 holds the gradient
-// of the lin_q rows as the kernels used them (times 1/(t+1) with the
-// per-position divisor), so that row factor is applied here.
-__global__ void tcb_affine_reduce(const __nv_bfloat16 *__restrict__ Z,
-                                  const float *__restrict__ gamma,
-                                  const __nv_bfloat16 *__restrict__ dT0,
-                                  const __nv_bfloat16 *__restrict__ dT1,
-                                  const __nv_bfloat16 *__restrict__ dT2,
-                                  const __nv_bfloat16 *__restrict__ dT3,
-                                  __nv_bfloat16 *__restrict__ dZ, float *__restrict__ part,
-                                  int64_t rows, int n, int s, int lin_norm, int global) {
-  const int a = threadIdx.x;
+__device__ __forceinline__ void unpack4(const uint2 &v, float *f) {
+  f[0] = bf16_lo(v.x);
+  f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y);
+  f[3] = bf16_hi(v.y);
+}
+
+// dZ = sum_k dT_k gamma_k over kTcbAffRows token rows per block, and the
+// block's partial sums of dgamma_k = sum_t dT_k z and dbeta_k = sum_t dT_k.
+// Block (s / 4, kTcbAffLanes): thread (x, y) takes columns 4x .. 4x + 3 of
+// rows y, y + kTcbAffLanes, ...; the row lanes' sums are then added in lane
+// order through shared memory, one of the eight quantities at a time.  dT2
+// holds the gradient of the lin_q rows as the kernels used them (times
+// 1/(t+1) with the per-position divisor), so that row factor is applied here.
+constexpr int kTcbAffLanes = 8;
+__global__ void tcb_affine_reduce(const uint2 *__restrict__ Z, const float *__restrict__ gamma,
+                                  const uint2 *__restrict__ dT0, const uint2 *__restrict__ dT1,
+                                  const uint2 *__restrict__ dT2, const uint2 *__restrict__ dT3,
+                                  uint2 *__restrict__ dZ, float *__restrict__ part, int64_t rows,
+                                  int n, int s, int lin_norm, int global) {
+  extern __shared__ float red[];  // [kTcbAffLanes][s]
+  const int x = threadIdx.x, y = threadIdx.y, s4 = s / 4;
   const int64_t t0 = (int64_t)blockIdx.x * kTcbAffRows;
-  float g[4], pg[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
+  float g[4][4], pg[4][4], pb[4][4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) g[k] = gamma[k * s + a];
-#pragma unroll 4
-  for (int r = 0; r < kTcbAffRows; ++r) {
+  for (int k = 0; k < 4; ++k)
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      g[k][c] = gamma[k * s + 4 * x + c];
+      pg[k][c] = 0.f;
+      pb[k][c] = 0.f;
+    }
+#pragma unroll 2
+  for (int r = y; r < kTcbAffRows; r += kTcbAffLanes) {
     const int64_t t = t0 + r;
     if (t >= rows) break;
-    const int64_t o = t * s + a;
-    const float z = bf(Z[o]);
-    float d[4];
-    d[0] = bf(dT0[o]);
-    d[1] = bf(dT1[o]);
-    d[2] = global ? bf(dT2[o]) : 0.f;
-    d[3] = global ? bf(dT3[o]) : 0.f;
-    if (lin_norm == kLinNormPosition) d[2] *= 1.f / (float)(t % n + 1);
-    float dz = 0.f;
+    const int64_t o = t * s4 + x;
+    float z[4], d[4][4];
+    unpack4(__ldcs(Z + o), z);
+    unpack4(__ldcs(dT0 + o), d[0]);
+    unpack4(__ldcs(dT1 + o), d[1]);
+    if (global) {
+      unpack4(__ldcs(dT2 + o), d[2]);
+      unpack4(__ldcs(dT3 + o), d[3]);
+      if (lin_norm == kLinNormPosition) {
+        const float f = 1.f / (float)(t % n + 1);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      dz = fmaf(d[k], g[k], dz);
-      pg[k] = fmaf(d[k], z, pg[k]);
-      pb[k] += d[k];
+        for (int c = 0; c < 4; ++c) d[2][c] *= f;
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 4; ++c) d[2][c] = d[3][c] = 0.f;
     }
-    dZ[o] = tob(dz);
+    float dz[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      dz[c] = 0.f;
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        dz[c] = fmaf(d[k][c], g[k][c], dz[c]);
+        pg[k][c] = fmaf(d[k][c], z[c], pg[k][c]);
+        pb[k][c] += d[k][c];
+      }
+    }
+    dZ[o] = make_uint2(pack_bf16x2(dz[0], dz[1]), pack_bf16x2(dz[2], dz[3]));
   }
   float *pp = part + (int64_t)blockIdx.x * 8 * s;
+  const int tid = y * s4 + x, nthr = s4 * kTcbAffLanes;
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    pp[k * s + a] = pg[k];
-    pp[(4 + k) * s + a] = pb[k];
+  for (int q = 0; q < 8; ++q) {
+    const float *v = q < 4 ? pg[q] : pb[q - 4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) red[y * s + 4 * x + c] = v[c];
+    __syncthreads();
+    for (int a = tid; a < s; a += nthr) {
+      float tot = 0.f;
+      for (int l = 0; l < kTcbAffLanes; ++l) tot += red[l * s + a];
+      pp[q * s + a] = tot;
+    }
+    __syncthreads();
   }
 }
 
