@@ -64,7 +64,14 @@ def test_backward_fp32(B, n, C, s, e, causal, variant):
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("variant", [(None, 0), (None, 3)], ids=["default", "no-global"])
 def test_backward_bf16(causal, variant):
+    # a tensor-core shape: the bf16 tensor-core backward
     check(1, 512, 256, 128, 256, causal, torch.bfloat16, variant, seed=3)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_bf16_cuda_cores(causal):
+    # s = 64: not a tensor-core shape, so bf16 I/O through the CUDA-core backward
+    check(2, 256, 64, 64, 96, causal, torch.bfloat16, (None, 0), seed=4)
 
 
 def test_backward_is_deterministic():
