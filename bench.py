@@ -105,15 +105,18 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
+FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_scan.cuh", "tc_attn.cuh",
+                          "ptx.cuh")
+
+
 def kernel_source_sha() -> str:
-    """Hash of the tensor-core kernel sources (tc*.cu, tc*.cuh, ptx.cuh)."""
+    """Hash of the sources of the tensor-core forward kernels and their launch."""
     csrc = os.path.join(ROOT, "flash_mixed_chunk_gb300", "csrc")
     h = hashlib.sha256()
-    for f in sorted(os.listdir(csrc)):
-        if (f.startswith("tc") and f.endswith((".cu", ".cuh"))) or f == "ptx.cuh":
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    for f in FORWARD_KERNEL_SOURCES:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
