@@ -45,11 +45,22 @@ struct AttnUnit {
   int nkv;    // V / P stages (64 keys each)
 };
 
-__device__ __forceinline__ AttnUnit decode_unit(int u, int n, int e, int C, int G, int causal) {
+__device__ __forceinline__ AttnUnit decode_unit(int u, int n, int e, int C, int G, int causal,
+                                                int n_units) {
   const int R = C / ROW_TILE;
   const int n_et = e / E_TILE;
-  const int rt = u % R;  // row tiles of one chunk and e tile are adjacent (V reuse in L2)
-  const int t = u / R;
+  int rt, t;
+  if (causal && R >= 4) {
+    // long causal chunks: row tile rt reads 2 (rt + 1) key stages, so the
+    // units are numbered row tile major and (taken from the top) longest
+    // first, which keeps a long unit out of the tail
+    const int per_rt = n_units / R;
+    rt = u / per_rt;
+    t = u % per_rt;
+  } else {
+    rt = u % R;  // row tiles of one chunk and e tile are adjacent (V reuse in L2)
+    t = u / R;
+  }
   const int et = t % n_et;
   const int bg = t / n_et;
   const int b = bg / G, g = bg % G;
@@ -153,7 +164,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         mbar_arrive(&qm_full[qs]);
         mbar_arrive(&qb_full[qs]);
         if (uu < 0) break;
-        const AttnUnit a = decode_unit(uu, n, e, C, G, causal);
+        const AttnUnit a = decode_unit(uu, n, e, C, G, causal, n_units);
         const int items = a.nkv + lin_items;
         for (int k = 0; k < items; ++k, ++ia) {
           const int slot = ia % AT_RING_A;
@@ -200,7 +211,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         const int u = qb_unit[qs];
         mbar_arrive(&qb_empty[qs]);
         if (u < 0) break;
-        const AttnUnit a = decode_unit(u, n, e, C, G, causal);
+        const AttnUnit a = decode_unit(u, n, e, C, G, causal, n_units);
         for (int q = 0; q < E_TILE / 64; ++q, ++ib) {
           const int slot = ib % AT_RING_B;
           if (ib >= AT_RING_B &&
@@ -242,7 +253,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         }
         if (u < 0) break;
         tc_fence_after();
-        const AttnUnit a = decode_unit(u, n, e, C, G, causal);
+        const AttnUnit a = decode_unit(u, n, e, C, G, causal, n_units);
         const int items = a.nkv + lin_items;
         const uint32_t dcol = tbase + (uint32_t)buf * 256u;
         for (int k = 0; k < items; ++k, ++ia) {
@@ -299,7 +310,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const AttnUnit a = decode_unit(u, n, e, C, G, causal);
+      const AttnUnit a = decode_unit(u, n, e, C, G, causal, n_units);
       const uint32_t dcol = tbase + (uint32_t)buf * 256u + ((uint32_t)(quad * 32) << 16);
       bool ok = true;
       for (int q = 0; q < E_TILE / 64; ++q, ++ib) {
