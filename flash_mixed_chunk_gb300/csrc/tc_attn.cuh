@@ -127,9 +127,12 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
   const uint32_t tbase = tmem_base;
   uint8_t *ringA = smem;
   uint8_t *ringB = smem + AT_OFF_B;
-  // launched as a dependent of the scan: everything above overlapped its
-  // tail; nothing below reads the workspace before the scan has finished
-  griddep_wait();
+  // Launched as a dependent of the scan, which itself started only after the
+  // prep kernel had finished and flushed: the relu^2 weights and the lin_q
+  // rows are final already, so only the loads of the scan's prefix rows wait
+  // for the scan (griddepcontrol.wait in the ring A producer, before its first
+  // prefix load); the quad items and U tiles of the first units overlap the
+  // scan's tail.
 
   if (warp == 0) {
     // =========================== scheduler + ring A producer
@@ -139,7 +142,7 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapS);
       int ia = 0;
-      bool ok = true;
+      bool ok = true, scan_done = false;
       // the next unit is fetched one unit ahead, so the atomic's latency
       // overlaps the current unit's copies
       int u_next = (int)atomicAdd(sched, 1u);
@@ -182,6 +185,10 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
             for (int j = 0; j < 4; ++j)
               tma_load_2d(dst + AT_A_BYTES + j * 8192, &mapV, &fullA[slot], a.e0 + 64 * j, y);
           } else {  // T2 rows x s [64q, 64q+64) ; prefix rows [64q, +64) x e [e0, e0+256)
+            if (!scan_done) {
+              griddep_wait();
+              scan_done = true;
+            }
             const int q = k - a.nkv;
             tma_load_2d(dst, &mapT2, &fullA[slot], 64 * q, a.row0);
             const int y = a.prow + q * KEY_STAGE;
