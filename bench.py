@@ -307,13 +307,14 @@ def config_of(w, args=None):
 
 # ---------------------------------------------------------------- decode
 def decode_bytes_per_token(s, e, C, i):
-    """Bytes one decode step must move per sequence at chunk index i: the
-    carried fp32 state (s x e), the i cached Z and V rows of its chunk, the
-    token's z, v, u and its output o (bf16); plus, at the chunk's last token,
-    the fold (cache read once, state read and written)."""
-    b = 4 * s * e + 2 * i * (s + e) + 2 * (s + 3 * e)
+    """Bytes one bf16 decode step must move per sequence at chunk index i: the
+    bf16 copy of the carried state (s x e), the i cached Z and V rows of its
+    chunk, the token's z, v, u and its output o; plus, at the chunk's last
+    token, the fold (cache read once, fp32 state read and written, bf16 copy
+    written)."""
+    b = 2 * s * e + 2 * i * (s + e) + 2 * (s + 3 * e)
     if i == C - 1:
-        b += 2 * C * (s + e) + 8 * s * e
+        b += 2 * C * (s + e) + 10 * s * e
     return b
 
 

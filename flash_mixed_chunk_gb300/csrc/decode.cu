@@ -21,6 +21,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <type_traits>
+
 #include <cstdint>
 
 #include "launch.h"
@@ -63,7 +65,7 @@ template <typename T, int K>
 __global__ void __launch_bounds__(kDecThreads)
     decode_token(const T *__restrict__ z, const T *__restrict__ v, const T *__restrict__ u,
                  const float *__restrict__ gamma, const float *__restrict__ beta,
-                 T *__restrict__ o, const float *__restrict__ P, T *__restrict__ Zc,
+                 T *__restrict__ o, const T *__restrict__ P, T *__restrict__ Zc,
                  T *__restrict__ Vc, int s, int e, int C, int i, float quad_a, float lin_f,
                  float t2_w) {
   extern __shared__ float dsm[];
@@ -120,7 +122,7 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
   for (int k = 0; k < K; ++k) acc[k] = 0.f;
   const T *vcb = Vc + (int64_t)b * C * e;
-  const float *pb = P + (int64_t)b * s * e;
+  const T *pb = P + (int64_t)b * s * e;
   // intra-chunk keys: cached rows j < i, this token's row j = i
 #pragma unroll 8
   for (int j = warp; j < i; j += kDecWarps) {
@@ -145,7 +147,7 @@ __global__ void __launch_bounds__(kDecThreads)
 #pragma unroll
     for (int k = 0; k < K; ++k) {
       const int c = c0 + 32 * k;
-      if (c < e) acc[k] = fmaf(qa, pb[(int64_t)a * e + c], acc[k]);
+      if (c < e) acc[k] = fmaf(qa, dec_f(pb[(int64_t)a * e + c]), acc[k]);
     }
   }
 #pragma unroll
@@ -169,12 +171,14 @@ __global__ void __launch_bounds__(kDecThreads)
 }
 
 // P[b] += sum_{j < C} T3(Zc[b][j])^T Vc[b][j] : the finished chunk joins the
-// carried state.  grid (B, ceil(s / 32), ceil(e / 128)); smem T3 tile [C][32].
+// carried state (and, for bf16 I/O, its bf16 copy Pb the token kernel reads).
+// grid (B, ceil(s / 32), ceil(e / 128)); smem T3 tile [C][32].
 constexpr int kFoldThreads = 128;
 
 template <typename T>
 __global__ void __launch_bounds__(kFoldThreads)
-    decode_fold(float *__restrict__ P, const T *__restrict__ Zc, const T *__restrict__ Vc,
+    decode_fold(float *__restrict__ P, T *__restrict__ Pb, const T *__restrict__ Zc,
+                const T *__restrict__ Vc,
                 const float *__restrict__ gamma, const float *__restrict__ beta, int s, int e,
                 int C) {
   extern __shared__ float t3[];  // [C][32]
@@ -201,7 +205,12 @@ __global__ void __launch_bounds__(kFoldThreads)
   float *pb = P + (int64_t)b * s * e + c;
 #pragma unroll
   for (int a = 0; a < 32; ++a)
-    if (a0 + a < s) pb[(int64_t)(a0 + a) * e] += acc[a];
+    if (a0 + a < s) {
+      const float nv = pb[(int64_t)(a0 + a) * e] + acc[a];
+      pb[(int64_t)(a0 + a) * e] = nv;
+      if (std::is_same<T, __nv_bfloat16>::value)
+        Pb[(int64_t)b * s * e + c + (int64_t)(a0 + a) * e] = dec_t<T>(nv);
+    }
 }
 
 template <typename T>
@@ -211,6 +220,9 @@ int launch_decode_impl(const void *z, const void *v, const void *u, const float 
   const DecodeStateLayout L = decode_state_layout(B, s, e, C, sizeof(T));
   char *st = static_cast<char *>(state);
   float *P = reinterpret_cast<float *>(st + L.P);
+  // the rows the token kernel reads: P itself, or its bf16 copy
+  T *Pr = std::is_same<T, __nv_bfloat16>::value ? reinterpret_cast<T *>(st + L.Pb)
+                                                : reinterpret_cast<T *>(P);
   T *Zc = reinterpret_cast<T *>(st + L.Zc);
   T *Vc = reinterpret_cast<T *>(st + L.Vc);
   const int g = t / C, i = t % C;
@@ -232,7 +244,7 @@ int launch_decode_impl(const void *z, const void *v, const void *u, const float 
   auto *kern = K == 4 ? decode_token<T, 4> : (K == 2 ? decode_token<T, 2> : decode_token<T, 1>);
   kern<<<g1, kDecThreads, smem1, stream>>>(
       static_cast<const T *>(z), static_cast<const T *>(v), static_cast<const T *>(u), gamma,
-      beta, static_cast<T *>(o), P, Zc, Vc, s, e, C, i, var.quad_a, lin_f, t2_w);
+      beta, static_cast<T *>(o), Pr, Zc, Vc, s, e, C, i, var.quad_a, lin_f, t2_w);
   if (cudaGetLastError() != cudaSuccess) return 1;
   if (i == C - 1) {
     const size_t smem2 = sizeof(float) * (size_t)C * 32;
@@ -241,7 +253,7 @@ int launch_decode_impl(const void *z, const void *v, const void *u, const float 
                              (int)smem2) != cudaSuccess)
       return 1;
     dim3 g2(B, (s + 31) / 32, (e + kFoldThreads - 1) / kFoldThreads);
-    decode_fold<T><<<g2, kFoldThreads, smem2, stream>>>(P, Zc, Vc, gamma, beta, s, e, C);
+    decode_fold<T><<<g2, kFoldThreads, smem2, stream>>>(P, Pr, Zc, Vc, gamma, beta, s, e, C);
     if (cudaGetLastError() != cudaSuccess) return 1;
   }
   return 0;

@@ -67,15 +67,19 @@ inline bool record_event(cudaEvent_t const *events, int i, cudaStream_t stream) 
 // Decode state (caller-owned, flash_mca_decode_state_bytes), each region
 // 256-byte aligned:
 //   P   fp32 [B][s][e]   sum of T3^T V over the completed chunks
+//   Pb  bf16 [B][s][e]   P rounded to bf16 at each fold, read by the bf16
+//                        token kernel (bf16 I/O only; the forward pass also
+//                        reads its prefix in bf16)
 //   Zc  [B][C][s]        Z rows of the current chunk's tokens (I/O type)
 //   Vc  [B][C][e]        their V rows (I/O type)
 struct DecodeStateLayout {
-  size_t P, Zc, Vc, total;
+  size_t P, Pb, Zc, Vc, total;
 };
 inline DecodeStateLayout decode_state_layout(int B, int s, int e, int C, size_t elem) {
   DecodeStateLayout L;
   L.P = 0;
-  L.Zc = align256(sizeof(float) * (size_t)B * s * e);
+  L.Pb = align256(sizeof(float) * (size_t)B * s * e);
+  L.Zc = L.Pb + (elem == 2 ? align256(2 * (size_t)B * s * e) : 0);
   L.Vc = L.Zc + align256(elem * (size_t)B * C * s);
   L.total = L.Vc + align256(elem * (size_t)B * C * e);
   return L;

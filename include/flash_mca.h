@@ -205,7 +205,9 @@ fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
  * whose forward pass the decode must reproduce), g*C (FMCA_LIN_NORM_SUMMED) or
  * t+1 (FMCA_LIN_NORM_POSITION); quad_scale and lin_norm come from `opts`
  * (NULL: the defaults).  The caller-owned device `state` carries the fp32 sum
- * of T3^T V over completed chunks and the current chunk's Z and V rows:
+ * of T3^T V over completed chunks (with FMCA_BF16 also a bf16 copy of it,
+ * refreshed at each fold, which the per-token reads use) and the current
+ * chunk's Z and V rows:
  *
  *   flash_mca_decode_state_bytes  its size (0 for rejected sizes);
  *   flash_mca_decode_reset        clears it before position 0 (queued on

@@ -199,8 +199,9 @@ def test_decode_state_bytes_and_validation():
     nb = fm.flash_mca_decode_state_bytes(2, 32, 64, 16, fm.FMCA_F32)
     a = lambda x: (x + 255) // 256 * 256
     assert nb == a(4 * 2 * 32 * 64) + a(4 * 2 * 16 * 32) + a(4 * 2 * 16 * 64)
+    # bf16: the fp32 sum, its bf16 copy, and the bf16 chunk cache
     assert fm.flash_mca_decode_state_bytes(2, 32, 64, 16, fm.FMCA_BF16) == \
-        a(4 * 2 * 32 * 64) + a(2 * 2 * 16 * 32) + a(2 * 2 * 16 * 64)
+        a(4 * 2 * 32 * 64) + a(2 * 2 * 32 * 64) + a(2 * 2 * 16 * 32) + a(2 * 2 * 16 * 64)
     for bad in ((0, 32, 64, 16), (2, 300, 64, 16), (2, 32, 64, 2048), (2, 32, 0, 16)):
         assert fm.flash_mca_decode_state_bytes(*bad, fm.FMCA_F32) == 0
     step = fm.lib.flash_mca_decode_step
