@@ -12,8 +12,10 @@ Prints one JSON line (rank 0).  Our arm: `value` is tokens/s over K steps with
 inputs resident in HBM, timed with CUDA events on the launching stream between
 a barrier + synchronize on both sides (max over ranks); per-kernel durations
 come from events the library records between its kernels.  Inputs and outputs
-rotate over three buffer sets, each larger than L2 (129 MB), so no step reads
-what the previous step left in L2.  `e2e` is the same metric through the
+rotate over three buffer sets, each larger than L2 (129 MB) for the default
+workload, so no step reads what the previous step left in L2 (`config.l2`
+says how this holds for the workload run).  `--graph` replays one CUDA graph
+per step instead of calling the library each step.  `e2e` is the same metric through the
 host-buffer entry point (pinned host memory, copies in and out inside the
 timed region).  The reference arm (--impl reference) times the fp64 CPU
 oracle on the host cores on bounded samples of the same workload.
@@ -294,10 +296,28 @@ def variant_of(args, w):
     return qs, LIN_NORMS[args.lin_norm or w.lin_norm]
 
 
+L2_BYTES = 129 * 2 ** 20
+
+
+def l2_note(w) -> str:
+    """How the timed steps avoid L2 reuse between iterations, as it applies."""
+    es = 2 if w.dtype == "bf16" else 4
+    set_bytes = w.B * w.n * (w.s + 3 * w.e) * es
+    if set_bytes > L2_BYTES:
+        return "inputs larger than L2, 3 rotating buffer sets"
+    if 3 * set_bytes > L2_BYTES:
+        return (f"3 rotating buffer sets of {set_bytes / 2 ** 20:.1f} MB, together larger "
+                "than L2")
+    return (f"3 rotating buffer sets of {set_bytes / 2 ** 20:.2f} MB: L2-resident "
+            "(a launch-bound shape)")
+
+
 def config_of(w, args=None):
     return {"workload": w.name, "B": w.B, "n": w.n, "C": w.C, "G": w.G, "s": w.s, "e": w.e,
             "causal": w.causal, "io_dtype": w.dtype, "accumulate": "fp32",
-            "l2": "inputs larger than L2, 3 rotating buffer sets",
+            "l2": l2_note(w),
+            **({} if args is None or not getattr(args, "graph", False)
+               else {"launch": "CUDA graph replay, one graph per step"}),
             "parallelism": "replicas (one independent problem per GPU)",
             **({} if args is None or (args.quad_scale is None and
                                       (args.lin_norm or w.lin_norm) == "n") else
@@ -578,6 +598,23 @@ def run_ours(args, w, rank, world, device):
     if st != fm.FMCA_OK:
         raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
 
+    graphs = None
+    if args.graph:
+        # one CUDA graph per buffer set, each holding one whole forward step
+        # (its kernels and their programmatic dependencies); replayed in turn
+        graphs = []
+        for i in range(3):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cap = torch.cuda.current_stream(device)
+                si = sets[i]
+                fm.flash_mca_forward_ex(si["Z"], si["V"], si["U"], gd, bd, si["O"], w.C,
+                                        w.causal, ws, quad_scale, lin_norm, fm.FMCA_PATH_AUTO, cap)
+            graphs.append(g)
+        for i in range(args.warmup):
+            graphs[i % 3].replay()
+        torch.cuda.synchronize(device)
+
     # ---- timed region: exactly K steps of the forward pass, nothing between
     # its kernels (the library chains them with programmatic dependent launch)
     t_start = torch.cuda.Event(enable_timing=True)
@@ -586,8 +623,12 @@ def run_ours(args, w, rank, world, device):
     torch.cuda.synchronize(device)
     wall0 = time.time()
     t_start.record(stream)
-    for i in range(args.steps):
-        step(i)
+    if graphs is not None:
+        for i in range(args.steps):
+            graphs[i % 3].replay()
+    else:
+        for i in range(args.steps):
+            step(i)
     t_end.record(stream)
     torch.cuda.synchronize(device)
     wall1 = time.time()
@@ -709,6 +750,8 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=8)
     ap.add_argument("--projections", action="store_true",
                     help="time the GAU projection GEMMs (tensor cores) on the workload's tokens")
+    ap.add_argument("--graph", action="store_true",
+                    help="time the forward steps as CUDA graph replays (one graph per step)")
     ap.add_argument("--backward", action="store_true",
                     help="time the backward pass on the workload (its own JSON line)")
     ap.add_argument("--lin-norm", default=None, choices=list(LIN_NORMS),
