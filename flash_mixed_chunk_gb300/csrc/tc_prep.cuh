@@ -4,9 +4,10 @@
 //
 //   state units  (chunk h, 256-column slice of e):
 //                state_h = T3_h^T V_h, T3 = Z * gamma3 + beta3, bf16 [B*G*s][e]
-//   score units  (chunk, 128-row tile, 64-key stage):
+//   score units  (chunk, 128-row tile, block of up to four 64-key stages; one
+//                stage per unit when there are no state units):
 //                P = relu(T0 T1^T / C)^2, strict upper triangle masked in causal
-//                mode, bf16 [B*n][C]; the key-stage-0 unit of each row tile also
+//                mode, bf16 [B*n][C]; the first block of each row tile also
 //                writes T2 = Z * gamma2 + beta2, bf16 [B*n][s]
 //
 // One CTA per SM: the small, latency-bound score units first, dealt
@@ -16,10 +17,13 @@
 // four-slot ring:
 //   state item [Z: 64 keys x 128 s (16 KB) | V: 64 keys x 256 e (32 KB)]
 //   score item [Z: 128 query rows x 128 s (32 KB) | Z: 64 keys x 128 s (16 KB)]
+//              for the block's first stage, [- | Z: 64 keys x 128 s] for the
+//              others, whose products read the query rows from the first
+//              item's slot (released only after the block's last product)
 // Four transform warps form T3 (state) or T0, T1 and T2 (score) in place; the
 // MMA warp accumulates D = T3^T V (M = s, N = 256; both operands MN-major) or
-// S = T0 T1^T (M = 128 rows, N = 64 keys; both K-major) into one of two TMEM
-// accumulators; four epilogue warps round D (or relu(S/C)^2) to bf16 into a
+// S = T0 T1^T (M = 128 rows, N = 64 keys per stage; both K-major) into one of
+// two TMEM accumulators; four epilogue warps round D (or relu(S/C)^2) to bf16 into a
 // swizzled staging tile that a TMA store writes out.  Every barrier has one
 // consumer.  Included by tc.cu.
 #pragma once
@@ -48,15 +52,32 @@ struct PrepUnit {
   int kind;
   // state: hb = b*G + h, es = 256-column slice
   int hb, es;
-  // score: rows [row0, row0+128) of the chunk starting at crow; key stage ks
-  int crow, row0, rt, ks;
+  // score: rows [row0, row0+128) of the chunk starting at crow; key stages
+  // ks .. ks + nks - 1
+  int crow, row0, rt, ks, nks;
 };
 
+constexpr int PR_SCORE_BLOCK_MAX = 4;  // key stages per score unit: at most the ring's slots
+
+// Score units per chunk: row tile rt reads 2 (rt + 1) key stages (causal) or
+// C / 64 (bidirectional), in blocks of `sblk` stages.
+__host__ __device__ __forceinline__ int score_blocks(int rt, int C, int causal, int sblk) {
+  const int stages = causal ? 2 * (rt + 1) : C / KEY_STAGE;
+  return (stages + sblk - 1) / sblk;
+}
+__host__ __device__ __forceinline__ int score_units_per_chunk(int C, int causal, int sblk) {
+  int u = 0;
+  for (int rt = 0; rt < C / ROW_TILE; ++rt) u += score_blocks(rt, C, causal, sblk);
+  return u;
+}
+
+template <int SBLK>
 __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score, int n, int e,
                                                 int C, int G, int causal) {
+  constexpr int sblk = SBLK;
   PrepUnit p;
   p.kind = KIND_END;
-  p.hb = p.es = p.crow = p.row0 = p.rt = p.ks = 0;
+  p.hb = p.es = p.crow = p.row0 = p.rt = p.ks = p.nks = 0;
   if (u < 0 || u >= n_state + n_score) return p;
   if (u >= n_score) {
     u -= n_score;
@@ -68,33 +89,49 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
   }
   const int R = C / ROW_TILE;
   // causal: row tile rt covers keys [0, 128 (rt+1)); otherwise all C keys
-  const int per_chunk = causal ? R * (R + 1) : R * (C / KEY_STAGE);
-  const int bg = u / per_chunk;
-  const int w = u % per_chunk;
-  int rt, ks;
-  if (causal) {
-    // row tile rt has 2 (rt+1) key stages: its units are w in
-    // [rt (rt+1), (rt+1) (rt+2)) of the chunk
-    rt = (int)((sqrtf(4.0f * (float)w + 1.0f) - 1.0f) * 0.5f);
-    while (rt > 0 && rt * (rt + 1) > w) --rt;
-    while ((rt + 1) * (rt + 2) <= w) ++rt;
-    ks = w - rt * (rt + 1);
-  } else {
-    rt = w / (C / KEY_STAGE);
-    ks = w % (C / KEY_STAGE);
+  int bg, rt, ks, nks = 1;
+  if constexpr (SBLK == 1) {  // one unit per key stage, decoded in closed form
+    const int per_chunk = causal ? R * (R + 1) : R * (C / KEY_STAGE);
+    bg = u / per_chunk;
+    const int w = u % per_chunk;
+    if (causal) {
+      // row tile rt has 2 (rt+1) key stages: its units are w in
+      // [rt (rt+1), (rt+1) (rt+2)) of the chunk
+      rt = (int)((sqrtf(4.0f * (float)w + 1.0f) - 1.0f) * 0.5f);
+      while (rt > 0 && rt * (rt + 1) > w) --rt;
+      while ((rt + 1) * (rt + 2) <= w) ++rt;
+      ks = w - rt * (rt + 1);
+    } else {
+      rt = w / (C / KEY_STAGE);
+      ks = w % (C / KEY_STAGE);
+    }
+  } else {  // blocks of sblk stages (chunks of a few row tiles)
+    const int per_chunk = score_units_per_chunk(C, causal, sblk);
+    bg = u / per_chunk;
+    int w = u % per_chunk;
+    for (rt = 0; rt < R - 1; ++rt) {
+      const int nb = score_blocks(rt, C, causal, sblk);
+      if (w < nb) break;
+      w -= nb;
+    }
+    const int stages = causal ? 2 * (rt + 1) : C / KEY_STAGE;
+    ks = w * sblk;
+    nks = min(sblk, stages - ks);
   }
   p.kind = KIND_SCORE;
   p.crow = (bg / G) * n + (bg % G) * C;
   p.rt = rt;
   p.row0 = p.crow + rt * ROW_TILE;
   p.ks = ks;
+  p.nks = nks;
   return p;
 }
 
 // BY_POSITION: the lin_q rows carry the per-position divisor 1/(t+1) of the
 // global term (a separate instantiation, so that the default one carries no
-// code for it).
-template <bool BY_POSITION>
+// code for it).  SBLK: key stages per score unit (PR_SCORE_BLOCK_MAX beside
+// state units, 1 without them), a compile-time constant of each instantiation.
+template <bool BY_POSITION, int SBLK>
 __global__ void __launch_bounds__(PREP_THREADS, 1)
     tc_chunk_prep(const __grid_constant__ CUtensorMap mapZ64,   // Z [B*n][s], box {64, 64}
                   const __grid_constant__ CUtensorMap mapZ128,  // Z [B*n][s], box {64, 128}
@@ -110,7 +147,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
   __shared__ __align__(8) uint64_t full[PR_RING], tready[PR_RING], empty[PR_RING];
   __shared__ __align__(8) uint64_t q_full[PR_QUEUE], q_empty[PR_QUEUE];
   __shared__ __align__(8) uint64_t acc_full[2], acc_empty[2], mma_done;
-  __shared__ int q_unit[PR_QUEUE], acc_unit[2], slot_unit[PR_RING];
+  __shared__ int q_unit[PR_QUEUE], acc_unit[2], slot_unit[PR_RING], slot_item[PR_RING];
   __shared__ uint32_t tmem_base;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -179,10 +216,12 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         }
         q_unit[qs] = uu;
         mbar_arrive(&q_full[qs]);
-        const PrepUnit p = decode_prep(uu, n_state, n_score, n, e, C, G, causal);
-        // state: C/64 items; score: 1 item; end: one empty item that tells the
-        // transform warps the stream is over
-        const int items = p.kind == KIND_STATE ? C / KEY_STAGE : 1;
+        const PrepUnit p = decode_prep<SBLK>(uu, n_state, n_score, n, e, C, G, causal);
+        // state: C/64 items; score: one per key stage of the block; end: one
+        // empty item that tells the transform warps the stream is over
+        const int items = p.kind == KIND_STATE ? C / KEY_STAGE
+                          : p.kind == KIND_SCORE ? p.nks
+                                                 : 1;
         for (int k = 0; k < items; ++k, ++it) {
           const int slot = it % PR_RING;
           if (it >= PR_RING && !mbar_wait(&empty[slot], ((it / PR_RING) - 1) & 1, kWaitLimitNs)) {
@@ -191,13 +230,17 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             break;
           }
           slot_unit[slot] = uu;
+          slot_item[slot] = k;
           if (p.kind == KIND_END) {
             mbar_arrive(&full[slot]);
             ended = true;
             break;
           }
           uint8_t *sz = smem + slot * PR_SLOT;
-          mbar_arrive_expect_tx(&full[slot], PR_SLOT);
+          // a score block's later items carry only their keys
+          mbar_arrive_expect_tx(&full[slot], p.kind == KIND_SCORE && k > 0
+                                                 ? (uint32_t)(KEY_STAGE * S_DIM * 2)
+                                                 : PR_SLOT);
           if (p.kind == KIND_STATE) {
             const int y = (p.hb / G) * n + (p.hb % G) * C + k * KEY_STAGE;
             tma_load_2d(sz, &mapZ64, &full[slot], 0, y);
@@ -205,9 +248,11 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
             for (int j = 0; j < 4; ++j)
               tma_load_2d(sz + PR_ST_Z + j * 8192, &mapV, &full[slot], p.es * E_TILE + 64 * j, y);
           } else {
-            tma_load_2d(sz, &mapZ128, &full[slot], 0, p.row0);
-            tma_load_2d(sz + 16384, &mapZ128, &full[slot], 64, p.row0);
-            const int y = p.crow + p.ks * KEY_STAGE;
+            if (k == 0) {  // the query rows, for the whole block
+              tma_load_2d(sz, &mapZ128, &full[slot], 0, p.row0);
+              tma_load_2d(sz + 16384, &mapZ128, &full[slot], 64, p.row0);
+            }
+            const int y = p.crow + (p.ks + k) * KEY_STAGE;
             tma_load_2d(sz + PR_SC_K, &mapZ64, &full[slot], 0, y);
             tma_load_2d(sz + PR_SC_K + 8192, &mapZ64, &full[slot], 64, y);
           }
@@ -247,9 +292,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         }
         if (u < 0) break;
         tc_fence_after();
-        const PrepUnit p = decode_prep(u, n_state, n_score, n, e, C, G, causal);
+        const PrepUnit p = decode_prep<SBLK>(u, n_state, n_score, n, e, C, G, causal);
         const uint32_t dcol = tbase + (uint32_t)buf * 256u;
-        const int items = p.kind == KIND_STATE ? C / KEY_STAGE : 1;
+        const int items = p.kind == KIND_STATE ? C / KEY_STAGE : p.nks;
+        int slot0 = 0;  // a score block's first item: its slot holds the query rows
         for (int k = 0; k < items; ++k, ++it) {
           const int slot = it % PR_RING;
           if (!mbar_wait(&tready[slot], (it / PR_RING) & 1, kWaitLimitNs)) {
@@ -266,16 +312,22 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
               const uint64_t bd = smem_desc_sw128(sz + PR_ST_Z + kk * 2048, 8192, 1024);
               mma_bf16_ss(dcol, ad, bd, idesc_st, (k | kk) != 0);
             }
+            mma_commit(&empty[slot]);
           } else {
+            // S[:, 64k .. 64k+63] = T0 (first item's slot) T1_k (this item's slot)
+            if (k == 0) slot0 = slot;
+            const uint32_t sq = smem_u32(smem + slot0 * PR_SLOT);
 #pragma unroll
             for (int kk = 0; kk < S_DIM / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(sz + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t ad = smem_desc_sw128(sq + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
               const uint64_t bd =
                   smem_desc_sw128(sz + PR_SC_K + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-              mma_bf16_ss(dcol, ad, bd, idesc_sc, kk != 0);
+              mma_bf16_ss(dcol + (uint32_t)(KEY_STAGE * k), ad, bd, idesc_sc, kk != 0);
             }
+            if (k > 0) mma_commit(&empty[slot]);
+            // the query rows' slot goes back once the block's last product is done
+            if (k == items - 1) mma_commit(&empty[slot0]);
           }
-          mma_commit(&empty[slot]);
         }
         if (!ok) break;
         acc_unit[buf] = u;
@@ -314,7 +366,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
       const int slot = it % PR_RING;
       const bool got = mbar_wait(&full[slot], (it / PR_RING) & 1, kWaitLimitNs);
       const PrepUnit pu =
-          decode_prep(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
+          decode_prep<SBLK>(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
       uint8_t *sz = smem + slot * PR_SLOT;
       if (pu.kind == KIND_STATE) {
         // T3 in place over the Z part (atom a: 64 key rows)
@@ -325,22 +377,26 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         }
         fence_proxy_async_smem();
       } else if (pu.kind == KIND_SCORE) {
-        // query rows (atom a: 128 rows): T0 in place; T2 to global from the
-        // same Z values, once per row tile (by its key-stage-0 unit)
+        // query rows (atom a: 128 rows), in the block's first item only: T0 in
+        // place; T2 to global from the same Z values, once per row tile (by
+        // its first block)
         const int tpos0 = BY_POSITION ? pu.row0 % n : 0;  // position of the tile's first row
+        if (slot_item[slot] == 0) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const int r = rb + 8 * i;
-          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 16384 + r * 128 + p * 16);
-          const uint4 z = *ptr;
-          if (pu.ks == 0) {
-            uint4 *t2p = reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + cl);
-            if (BY_POSITION)  // row t of its sequence carries 1/(t+1)
-              *t2p = affine8_scaled(z, g2, b2, 1.0f / (float)(tpos0 + r + 1));
-            else
-              *t2p = affine8(z, g2, b2);
+          for (int i = 0; i < 16; ++i) {
+            const int r = rb + 8 * i;
+            uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 16384 + r * 128 + p * 16);
+            const uint4 z = *ptr;
+            if (pu.ks == 0) {
+              uint4 *t2p =
+                  reinterpret_cast<uint4 *>(t2out + (size_t)(pu.row0 + r) * S_DIM + cl);
+              if (BY_POSITION)  // row t of its sequence carries 1/(t+1)
+                *t2p = affine8_scaled(z, g2, b2, 1.0f / (float)(tpos0 + r + 1));
+              else
+                *t2p = affine8(z, g2, b2);
+            }
+            *ptr = affine8(z, g0, b0);
           }
-          *ptr = affine8(z, g0, b0);
         }
         // keys (atom a: 64 rows): T1 in place
 #pragma unroll
@@ -375,9 +431,9 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const PrepUnit p = decode_prep(u, n_state, n_score, n, e, C, G, causal);
+      const PrepUnit p = decode_prep<SBLK>(u, n_state, n_score, n, e, C, G, causal);
       const uint32_t dcol = tbase + (uint32_t)buf * 256u + ((uint32_t)(quad * 32) << 16);
-      const int nq = p.kind == KIND_STATE ? E_TILE / 64 : 1;
+      const int nq = p.kind == KIND_STATE ? E_TILE / 64 : p.nks;
       for (int q = 0; q < nq; ++q, ++nst) {
         uint8_t *sb = stage + (nst % PR_STAGE_BUFS) * PR_STAGE_BYTES;
         // the TMA store that last read this staging tile has finished reading it
@@ -391,7 +447,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
           // relu(S * quad_a)^2 (quad_a = 1/C by default); causal: key position >
           // query position -> 0
           const int qpos = p.rt * ROW_TILE + row;
-          const int kbase = p.ks * KEY_STAGE;
+          const int kbase = (p.ks + q) * KEY_STAGE;
 #pragma unroll
           for (int c2 = 0; c2 < 2; ++c2)
 #pragma unroll
@@ -420,7 +476,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
           if (p.kind == KIND_STATE)
             tma_store_2d(&mapSt, sb, p.es * E_TILE + 64 * q, p.hb * S_DIM);
           else
-            tma_store_2d(&mapPw, sb, p.ks * KEY_STAGE, p.row0);
+            tma_store_2d(&mapPw, sb, (p.ks + q) * KEY_STAGE, p.row0);
           bulk_commit_group();
           // every epilogue thread has read this unit's accumulator
           if (q == nq - 1) mbar_arrive(&acc_empty[buf]);
