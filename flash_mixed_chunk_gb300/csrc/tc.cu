@@ -137,7 +137,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
         cudaFuncSetAttribute(tc_chunk_prep<true, PR_SCORE_BLOCK_MAX>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PREP_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_prep<false, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(tc_chunk_prep<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)PREP_SMEM) != cudaSuccess ||
         cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)AT_SMEM) != cudaSuccess)
@@ -152,13 +152,13 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   const bool no_global = var.lin_norm == kLinNormNone;
   const int n_state = no_global ? 0 : B * G * (e / E_TILE);
   // score units of up to four key stages when state units stream beside them;
-  // single stages without (FLASH-Quad), where more, shorter units overlap better
-  const int sblk = no_global ? 1 : PR_SCORE_BLOCK_MAX;
+  // two without (FLASH-Quad), where more, shorter units overlap better
+  const int sblk = no_global ? 2 : PR_SCORE_BLOCK_MAX;
   const int n_score = B * G * score_units_per_chunk(C, causal, sblk);
   const int n_prep = n_state + n_score;
   // (without a global term the position divisor has no use, so the
-  // single-stage instantiation needs no BY_POSITION twin)
-  auto *prep = no_global ? tc_chunk_prep<false, 1>
+  // two-stage instantiation needs no BY_POSITION twin)
+  auto *prep = no_global ? tc_chunk_prep<false, 2>
                : var.lin_norm == kLinNormPosition ? tc_chunk_prep<true, PR_SCORE_BLOCK_MAX>
                                                   : tc_chunk_prep<false, PR_SCORE_BLOCK_MAX>;
   prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(

@@ -4,8 +4,8 @@
 //
 //   state units  (chunk h, 256-column slice of e):
 //                state_h = T3_h^T V_h, T3 = Z * gamma3 + beta3, bf16 [B*G*s][e]
-//   score units  (chunk, 128-row tile, block of up to four 64-key stages; one
-//                stage per unit when there are no state units):
+//   score units  (chunk, 128-row tile, block of up to four 64-key stages; two
+//                when there are no state units):
 //                P = relu(T0 T1^T / C)^2, strict upper triangle masked in causal
 //                mode, bf16 [B*n][C]; the first block of each row tile also
 //                writes T2 = Z * gamma2 + beta2, bf16 [B*n][s]
@@ -89,35 +89,19 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
   }
   const int R = C / ROW_TILE;
   // causal: row tile rt covers keys [0, 128 (rt+1)); otherwise all C keys
-  int bg, rt, ks, nks = 1;
-  if constexpr (SBLK == 1) {  // one unit per key stage, decoded in closed form
-    const int per_chunk = causal ? R * (R + 1) : R * (C / KEY_STAGE);
-    bg = u / per_chunk;
-    const int w = u % per_chunk;
-    if (causal) {
-      // row tile rt has 2 (rt+1) key stages: its units are w in
-      // [rt (rt+1), (rt+1) (rt+2)) of the chunk
-      rt = (int)((sqrtf(4.0f * (float)w + 1.0f) - 1.0f) * 0.5f);
-      while (rt > 0 && rt * (rt + 1) > w) --rt;
-      while ((rt + 1) * (rt + 2) <= w) ++rt;
-      ks = w - rt * (rt + 1);
-    } else {
-      rt = w / (C / KEY_STAGE);
-      ks = w % (C / KEY_STAGE);
-    }
-  } else {  // blocks of sblk stages (chunks of a few row tiles)
-    const int per_chunk = score_units_per_chunk(C, causal, sblk);
-    bg = u / per_chunk;
-    int w = u % per_chunk;
-    for (rt = 0; rt < R - 1; ++rt) {
-      const int nb = score_blocks(rt, C, causal, sblk);
-      if (w < nb) break;
-      w -= nb;
-    }
-    const int stages = causal ? 2 * (rt + 1) : C / KEY_STAGE;
-    ks = w * sblk;
-    nks = min(sblk, stages - ks);
+  // the row tile: a short walk over the chunk's row tiles (their block
+  // counts differ in causal mode)
+  const int per_chunk = score_units_per_chunk(C, causal, sblk);
+  const int bg = u / per_chunk;
+  int w = u % per_chunk, rt = 0;
+  for (; rt < R - 1; ++rt) {
+    const int nb = score_blocks(rt, C, causal, sblk);
+    if (w < nb) break;
+    w -= nb;
   }
+  const int stages = causal ? 2 * (rt + 1) : C / KEY_STAGE;
+  const int ks = w * sblk;
+  const int nks = min(sblk, stages - ks);
   p.kind = KIND_SCORE;
   p.crow = (bg / G) * n + (bg % G) * C;
   p.rt = rt;
@@ -130,7 +114,7 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
 // BY_POSITION: the lin_q rows carry the per-position divisor 1/(t+1) of the
 // global term (a separate instantiation, so that the default one carries no
 // code for it).  SBLK: key stages per score unit (PR_SCORE_BLOCK_MAX beside
-// state units, 1 without them), a compile-time constant of each instantiation.
+// state units, 2 without them), a compile-time constant of each instantiation.
 template <bool BY_POSITION, int SBLK>
 __global__ void __launch_bounds__(PREP_THREADS, 1)
     tc_chunk_prep(const __grid_constant__ CUtensorMap mapZ64,   // Z [B*n][s], box {64, 64}
