@@ -4,6 +4,8 @@
 
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include <cstddef>
 #include <cstdint>
 
@@ -59,6 +61,22 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
                       cudaEvent_t const *events = nullptr);
+
+// Runs a setup step (kernel attributes) once per device and process, safely
+// when several host threads make their first call at the same time; later
+// calls return the first run's result.
+struct OncePerDevice {
+  static constexpr int kMaxDevices = 64;
+  std::once_flag flags[kMaxDevices];
+  bool ok[kMaxDevices] = {};
+  template <typename F>
+  bool run(F &&setup) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    std::call_once(flags[dev], [&] { ok[dev] = setup(); });
+    return ok[dev];
+  }
+};
 
 inline bool record_event(cudaEvent_t const *events, int i, cudaStream_t stream) {
   return events == nullptr || cudaEventRecord(events[i], stream) == cudaSuccess;

@@ -129,21 +129,21 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
       !make_map_bf16(&mU, U, e, rows, 64, 128) || !make_map_bf16(&mO, O, e, rows, 64, 128))
     return 2;
 
-  static bool attrs = false;
-  if (!attrs) {
-    if (cudaFuncSetAttribute(tc_chunk_prep<false, PR_SCORE_BLOCK_MAX>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)PREP_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_prep<true, PR_SCORE_BLOCK_MAX>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)PREP_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_prep<false, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)PREP_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)AT_SMEM) != cudaSuccess)
-      return 1;
-    attrs = true;
-  }
+  static OncePerDevice attrs;
+  if (!attrs.run([] {
+        return cudaFuncSetAttribute(tc_chunk_prep<false, PR_SCORE_BLOCK_MAX>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PREP_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_prep<true, PR_SCORE_BLOCK_MAX>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PREP_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_prep<false, 2>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PREP_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)AT_SMEM) == cudaSuccess;
+      }))
+    return 1;
   if (!record_event(events, 0, stream)) return 1;
   // sched[0]: work counter of tc_chunk_prep; sched[1]: of tc_chunk_attn
   if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
@@ -210,15 +210,16 @@ int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, voi
   m2 = m0;
   if (n1 > n0 && !make_map_bf16(&m1, D1, n1 - n0, M, 64, 128)) return 2;
   if (N > n1 && !make_map_bf16(&m2, D2, N - n1, M, 64, 128)) return 2;
-  static bool attrs = false;
-  if (!attrs) {
-    if (cudaFuncSetAttribute(tc_gemm<GEMM_ACT_NONE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)GEMM_SMEM) != cudaSuccess ||
-        cudaFuncSetAttribute(tc_gemm<GEMM_ACT_SILU>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)GEMM_SMEM) != cudaSuccess)
-      return 1;
-    attrs = true;
-  }
+  static OncePerDevice attrs;
+  if (!attrs.run([] {
+        return cudaFuncSetAttribute(tc_gemm<GEMM_ACT_NONE>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)GEMM_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_gemm<GEMM_ACT_SILU>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)GEMM_SMEM) == cudaSuccess;
+      }))
+    return 1;
   const int units = ((M + 127) / 128) * ((N + GM_TILE_N - 1) / GM_TILE_N);
   const int sms = num_sms();
   auto *kern = silu ? tc_gemm<GEMM_ACT_SILU> : tc_gemm<GEMM_ACT_NONE>;

@@ -61,13 +61,12 @@ int launch_bgemm(const BgSpec *specs, int n, cudaStream_t stream) {
     if (!fill_problem(P.p[i], specs[i])) return 2;
     units += P.p[i].units;
   }
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(tc_bgemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)BGEMM_SMEM) != cudaSuccess)
-      return 1;
-    attr = true;
-  }
+  static OncePerDevice attr;
+  if (!attr.run([] {
+        return cudaFuncSetAttribute(tc_bgemm, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)BGEMM_SMEM) == cudaSuccess;
+      }))
+    return 1;
   const int sms = num_sms();
   tc_bgemm<<<units < sms ? units : sms, BGEMM_THREADS, BGEMM_SMEM, stream>>>(P);
   return cudaGetLastError() == cudaSuccess ? 0 : 1;
