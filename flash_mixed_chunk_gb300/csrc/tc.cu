@@ -131,13 +131,10 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
 
   static OncePerDevice attrs;
   if (!attrs.run([] {
-        return cudaFuncSetAttribute(tc_chunk_prep<false, PR_SCORE_BLOCK_MAX>,
+        return cudaFuncSetAttribute(tc_chunk_prep<false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)PREP_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(tc_chunk_prep<true, PR_SCORE_BLOCK_MAX>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)PREP_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(tc_chunk_prep<false, 2>,
+               cudaFuncSetAttribute(tc_chunk_prep<true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)PREP_SMEM) == cudaSuccess &&
                cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -151,16 +148,9 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   // scan has nothing to do and the attention units have no lin_q items
   const bool no_global = var.lin_norm == kLinNormNone;
   const int n_state = no_global ? 0 : B * G * (e / E_TILE);
-  // score units of up to four key stages when state units stream beside them;
-  // two without (FLASH-Quad), where more, shorter units overlap better
-  const int sblk = no_global ? 2 : PR_SCORE_BLOCK_MAX;
-  const int n_score = B * G * score_units_per_chunk(C, causal, sblk);
+  const int n_score = B * G * score_units_per_chunk(C, causal);
   const int n_prep = n_state + n_score;
-  // (without a global term the position divisor has no use, so the
-  // two-stage instantiation needs no BY_POSITION twin)
-  auto *prep = no_global ? tc_chunk_prep<false, 2>
-               : var.lin_norm == kLinNormPosition ? tc_chunk_prep<true, PR_SCORE_BLOCK_MAX>
-                                                  : tc_chunk_prep<false, PR_SCORE_BLOCK_MAX>;
+  auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
   prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
       mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n, e,
       C, G, causal, n_state, n_score, var.quad_a);

@@ -4,8 +4,7 @@
 //
 //   state units  (chunk h, 256-column slice of e):
 //                state_h = T3_h^T V_h, T3 = Z * gamma3 + beta3, bf16 [B*G*s][e]
-//   score units  (chunk, 128-row tile, block of up to four 64-key stages; two
-//                when there are no state units):
+//   score units  (chunk, 128-row tile, block of up to two 64-key stages):
 //                P = relu(T0 T1^T / C)^2, strict upper triangle masked in causal
 //                mode, bf16 [B*n][C]; the first block of each row tile also
 //                writes T2 = Z * gamma2 + beta2, bf16 [B*n][s]
@@ -57,24 +56,27 @@ struct PrepUnit {
   int crow, row0, rt, ks, nks;
 };
 
-constexpr int PR_SCORE_BLOCK_MAX = 4;  // key stages per score unit: at most the ring's slots
+// Key stages per score unit (at most the ring's slots: the first item's slot
+// is held until the block's last product).  Measured on long_causal, gau_base
+// and flash_quad: two beat one (the query rows loaded and transformed once per
+// stage) and four (fewer, longer chains to overlap).
+constexpr int PR_SCORE_BLOCK = 2;
+static_assert(PR_SCORE_BLOCK <= PR_RING, "a score block holds its first slot");
 
 // Score units per chunk: row tile rt reads 2 (rt + 1) key stages (causal) or
-// C / 64 (bidirectional), in blocks of `sblk` stages.
-__host__ __device__ __forceinline__ int score_blocks(int rt, int C, int causal, int sblk) {
+// C / 64 (bidirectional), in blocks of PR_SCORE_BLOCK stages.
+__host__ __device__ __forceinline__ int score_blocks(int rt, int C, int causal) {
   const int stages = causal ? 2 * (rt + 1) : C / KEY_STAGE;
-  return (stages + sblk - 1) / sblk;
+  return (stages + PR_SCORE_BLOCK - 1) / PR_SCORE_BLOCK;
 }
-__host__ __device__ __forceinline__ int score_units_per_chunk(int C, int causal, int sblk) {
+__host__ __device__ __forceinline__ int score_units_per_chunk(int C, int causal) {
   int u = 0;
-  for (int rt = 0; rt < C / ROW_TILE; ++rt) u += score_blocks(rt, C, causal, sblk);
+  for (int rt = 0; rt < C / ROW_TILE; ++rt) u += score_blocks(rt, C, causal);
   return u;
 }
 
-template <int SBLK>
 __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score, int n, int e,
                                                 int C, int G, int causal) {
-  constexpr int sblk = SBLK;
   PrepUnit p;
   p.kind = KIND_END;
   p.hb = p.es = p.crow = p.row0 = p.rt = p.ks = p.nks = 0;
@@ -91,17 +93,17 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
   // causal: row tile rt covers keys [0, 128 (rt+1)); otherwise all C keys
   // the row tile: a short walk over the chunk's row tiles (their block
   // counts differ in causal mode)
-  const int per_chunk = score_units_per_chunk(C, causal, sblk);
+  const int per_chunk = score_units_per_chunk(C, causal);
   const int bg = u / per_chunk;
   int w = u % per_chunk, rt = 0;
   for (; rt < R - 1; ++rt) {
-    const int nb = score_blocks(rt, C, causal, sblk);
+    const int nb = score_blocks(rt, C, causal);
     if (w < nb) break;
     w -= nb;
   }
   const int stages = causal ? 2 * (rt + 1) : C / KEY_STAGE;
-  const int ks = w * sblk;
-  const int nks = min(sblk, stages - ks);
+  const int ks = w * PR_SCORE_BLOCK;
+  const int nks = min(PR_SCORE_BLOCK, stages - ks);
   p.kind = KIND_SCORE;
   p.crow = (bg / G) * n + (bg % G) * C;
   p.rt = rt;
@@ -113,9 +115,8 @@ __device__ __forceinline__ PrepUnit decode_prep(int u, int n_state, int n_score,
 
 // BY_POSITION: the lin_q rows carry the per-position divisor 1/(t+1) of the
 // global term (a separate instantiation, so that the default one carries no
-// code for it).  SBLK: key stages per score unit (PR_SCORE_BLOCK_MAX beside
-// state units, 2 without them), a compile-time constant of each instantiation.
-template <bool BY_POSITION, int SBLK>
+// code for it).
+template <bool BY_POSITION>
 __global__ void __launch_bounds__(PREP_THREADS, 1)
     tc_chunk_prep(const __grid_constant__ CUtensorMap mapZ64,   // Z [B*n][s], box {64, 64}
                   const __grid_constant__ CUtensorMap mapZ128,  // Z [B*n][s], box {64, 128}
@@ -200,7 +201,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         }
         q_unit[qs] = uu;
         mbar_arrive(&q_full[qs]);
-        const PrepUnit p = decode_prep<SBLK>(uu, n_state, n_score, n, e, C, G, causal);
+        const PrepUnit p = decode_prep(uu, n_state, n_score, n, e, C, G, causal);
         // state: C/64 items; score: one per key stage of the block; end: one
         // empty item that tells the transform warps the stream is over
         const int items = p.kind == KIND_STATE ? C / KEY_STAGE
@@ -276,7 +277,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         }
         if (u < 0) break;
         tc_fence_after();
-        const PrepUnit p = decode_prep<SBLK>(u, n_state, n_score, n, e, C, G, causal);
+        const PrepUnit p = decode_prep(u, n_state, n_score, n, e, C, G, causal);
         const uint32_t dcol = tbase + (uint32_t)buf * 256u;
         const int items = p.kind == KIND_STATE ? C / KEY_STAGE : p.nks;
         int slot0 = 0;  // a score block's first item: its slot holds the query rows
@@ -350,7 +351,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
       const int slot = it % PR_RING;
       const bool got = mbar_wait(&full[slot], (it / PR_RING) & 1, kWaitLimitNs);
       const PrepUnit pu =
-          decode_prep<SBLK>(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
+          decode_prep(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
       uint8_t *sz = smem + slot * PR_SLOT;
       if (pu.kind == KIND_STATE) {
         // T3 in place over the Z part (atom a: 64 key rows)
@@ -415,7 +416,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
         break;
       }
       tc_fence_after();
-      const PrepUnit p = decode_prep<SBLK>(u, n_state, n_score, n, e, C, G, causal);
+      const PrepUnit p = decode_prep(u, n_state, n_score, n, e, C, G, causal);
       const uint32_t dcol = tbase + (uint32_t)buf * 256u + ((uint32_t)(quad * 32) << 16);
       const int nq = p.kind == KIND_STATE ? E_TILE / 64 : p.nks;
       for (int q = 0; q < nq; ++q, ++nst) {
