@@ -4,6 +4,8 @@
 // unit's device status with the forward kernels.
 #pragma once
 
+#include <utility>
+
 #include "tc_bgemm.cuh"
 #include "tc_bwd.cuh"
 
@@ -52,6 +54,27 @@ bool fill_problem(BgProblem &p, const BgSpec &s) {
   return true;
 }
 
+// Launches `kernel` as a programmatic dependent of the work before it on
+// `stream`: it may start launching (and run its prologue) while its
+// predecessor drains.  Every kernel of the backward pass waits
+// (griddepcontrol.wait) for its predecessor to complete before it reads, so
+// each one's completion implies all earlier ones'.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args &&...args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 // One tc_bgemm launch over n (1..3) independent products.
 int launch_bgemm(const BgSpec *specs, int n, cudaStream_t stream) {
   BgParams P;
@@ -68,8 +91,10 @@ int launch_bgemm(const BgSpec *specs, int n, cudaStream_t stream) {
       }))
     return 1;
   const int sms = num_sms();
-  tc_bgemm<<<units < sms ? units : sms, BGEMM_THREADS, BGEMM_SMEM, stream>>>(P);
-  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+  return launch_dependent(tc_bgemm, dim3(units < sms ? units : sms), dim3(BGEMM_THREADS),
+                          BGEMM_SMEM, stream, P) == cudaSuccess
+             ? 0
+             : 1;
 }
 
 unsigned blocks_for(int64_t count) { return (unsigned)((count + 255) / 256); }
@@ -112,14 +137,15 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
                         stream) != 0)
     return 1;
   const int64_t ne8 = (int64_t)rows * e / 8, ns8 = (int64_t)rows * s / 8;
-  tcb_gate_dy<<<blocks_for(ne8), 256, 0, stream>>>(static_cast<const uint4 *>(dO),
-                                                   static_cast<const uint4 *>(U),
-                                                   reinterpret_cast<uint4 *>(dY), ne8);
-  tcb_affine_rows<<<blocks_for(ns8), 256, 0, stream>>>(
-      static_cast<const uint4 *>(Z), reinterpret_cast<const float4 *>(gamma),
-      reinterpret_cast<const float4 *>(beta), reinterpret_cast<uint4 *>(T0),
-      reinterpret_cast<uint4 *>(T1), reinterpret_cast<uint4 *>(T3), ns8, s);
-  if (cudaGetLastError() != cudaSuccess) return 1;
+  if (launch_dependent(tcb_gate_dy, dim3(blocks_for(ne8)), dim3(256), 0, stream,
+                       static_cast<const uint4 *>(dO), static_cast<const uint4 *>(U),
+                       reinterpret_cast<uint4 *>(dY), ne8) != cudaSuccess ||
+      launch_dependent(tcb_affine_rows, dim3(blocks_for(ns8)), dim3(256), 0, stream,
+                       static_cast<const uint4 *>(Z), reinterpret_cast<const float4 *>(gamma),
+                       reinterpret_cast<const float4 *>(beta), reinterpret_cast<uint4 *>(T0),
+                       reinterpret_cast<uint4 *>(T1), reinterpret_cast<uint4 *>(T3), ns8,
+                       s) != cudaSuccess)
+    return 1;
   const BgOperand oY{dY, (uint64_t)e, rows}, oV{V, (uint64_t)e, rows};
   const BgOperand oT0{T0, (uint64_t)s, rows}, oT1{T1, (uint64_t)s, rows};
   const BgOperand oT2{T2, (uint64_t)s, rows}, oT3{T3, (uint64_t)s, rows};
@@ -163,8 +189,10 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
   }
   if (glob) {
     const int64_t se8 = (int64_t)s * e / 8;
-    tcb_reverse_scan<<<blocks_for((int64_t)B * se8), 256, 0, stream>>>(
-        reinterpret_cast<uint4 *>(dP), B, G, se8, n, C, causal, var.lin_norm);
+    if (launch_dependent(tcb_reverse_scan, dim3(blocks_for((int64_t)B * se8)), dim3(256), 0,
+                         stream, reinterpret_cast<uint4 *>(dP), B, G, se8, n, C, causal,
+                         var.lin_norm) != cudaSuccess)
+      return 1;
   }
   np = 0;
   {  // dT3 = V dS_h^T (C x s, K = e); dV = W^T dY [+ T3 dS_h] (C x e, K = C [+ s])
@@ -188,12 +216,14 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
   if (rc) return 1;
   const int nblk = (int)((rows + kTcbAffRows - 1) / kTcbAffRows);
   auto u2 = [](const void *p) { return static_cast<const uint2 *>(p); };
-  tcb_affine_reduce<<<nblk, dim3(s / 4, kTcbAffLanes), sizeof(float) * kTcbAffLanes * s,
-                      stream>>>(u2(Z), gamma, u2(dT0), u2(dT1), u2(dT2), u2(dT3),
-                                static_cast<uint2 *>(dZ), part, (int64_t)rows, n, s,
-                                var.lin_norm, glob ? 1 : 0);
-  tcb_gamma_beta<<<(8 * s + 31) / 32, dim3(32, 32), 0, stream>>>(part, nblk, s, dgamma, dbeta);
-  return cudaGetLastError() == cudaSuccess ? 0 : 1;
+  if (launch_dependent(tcb_affine_reduce, dim3(nblk), dim3(s / 4, kTcbAffLanes),
+                       sizeof(float) * kTcbAffLanes * s, stream, u2(Z), gamma, u2(dT0), u2(dT1),
+                       u2(dT2), u2(dT3), static_cast<uint2 *>(dZ), part, (int64_t)rows, n, s,
+                       var.lin_norm, glob ? 1 : 0) != cudaSuccess ||
+      launch_dependent(tcb_gamma_beta, dim3((8 * s + 31) / 32), dim3(32, 32), 0, stream, part,
+                       nblk, s, dgamma, dbeta) != cudaSuccess)
+    return 1;
+  return 0;
 }
 
 }  // namespace fmca

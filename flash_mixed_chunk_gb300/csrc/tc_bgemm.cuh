@@ -135,6 +135,9 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1) tc_bgemm(const __grid_consta
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = tmem_base;
+  // launched as a programmatic dependent: the set-up above overlapped the
+  // previous kernel's tail; nothing below runs before it has completed
+  griddep_wait();
 
   if (warp == 0) {
     // =========================== scheduler + TMA producer

@@ -32,6 +32,7 @@ __device__ __forceinline__ uint4 pack8(const float *f) {
 // dY = dO * U over [rows][e] (bf16), 8 elements per thread; count8 = count / 8
 __global__ void tcb_gate_dy(const uint4 *__restrict__ dO, const uint4 *__restrict__ U,
                             uint4 *__restrict__ dY, int64_t count8) {
+  griddep_wait();  // launched as a dependent of the previous step
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count8) return;
   float g[8], u[8];
@@ -48,6 +49,7 @@ __global__ void tcb_affine_rows(const uint4 *__restrict__ Z, const float4 *__res
                                 const float4 *__restrict__ beta, uint4 *__restrict__ T0,
                                 uint4 *__restrict__ T1, uint4 *__restrict__ T3, int64_t count8,
                                 int s) {
+  griddep_wait();  // launched as a dependent of the previous step
   const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= count8) return;
   const int a4 = (int)(i % (s / 8)) * 2;  // float4 index of the first column
@@ -75,6 +77,7 @@ __global__ void tcb_affine_rows(const uint4 *__restrict__ Z, const float4 *__res
 // prefix (1 with the per-position divisor, which the T2 rows carry).
 __global__ void tcb_reverse_scan(uint4 *__restrict__ dP, int B, int G, int64_t se8, int n, int C,
                                  int causal, int lin_norm) {
+  griddep_wait();  // launched as a dependent of the previous step
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * se8) return;
   const int64_t b = t / se8, x = t % se8;
@@ -147,6 +150,7 @@ __global__ void tcb_affine_reduce(const uint2 *__restrict__ Z, const float *__re
                                   const uint2 *__restrict__ dT2, const uint2 *__restrict__ dT3,
                                   uint2 *__restrict__ dZ, float *__restrict__ part, int64_t rows,
                                   int n, int s, int lin_norm, int global) {
+  griddep_wait();  // launched as a dependent of the previous step
   extern __shared__ float red[];  // [kTcbAffLanes][s]
   const int x = threadIdx.x, y = threadIdx.y, s4 = s / 4;
   const int64_t t0 = (int64_t)blockIdx.x * kTcbAffRows;
@@ -215,6 +219,7 @@ __global__ void tcb_affine_reduce(const uint2 *__restrict__ Z, const float *__re
 // ...; the 32 sums are then added in y order.  grid ceil(8 s / 32).
 __global__ void tcb_gamma_beta(const float *__restrict__ part, int nblk, int s,
                                float *__restrict__ dgamma, float *__restrict__ dbeta) {
+  griddep_wait();  // launched as a dependent of the previous step
   __shared__ float acc[32][33];
   const int x = blockIdx.x * 32 + threadIdx.x, y = threadIdx.y;
   float v = 0.f;
