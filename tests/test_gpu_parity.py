@@ -122,9 +122,10 @@ def test_causality_on_gpu():
     assert not torch.equal(pert[:, p:], base[:, p:])
 
 
-def test_host_buffer_entry_matches_device_entry():
+@pytest.mark.parametrize("B,causal", [(2, True), (5, False), (1, True)])
+def test_host_buffer_entry_matches_device_entry(B, causal):
     m = fm()
-    B, n, C, s, e, causal = 2, 512, 256, 128, 512, True
+    n, C, s, e = 512, 256, 128, 512
     Z, V, U, gamma, beta = mca_inputs.make_inputs(B, n, s, e, 3, torch.bfloat16)
     dev = run_gpu(Z, V, U, gamma, beta, C, causal).cpu()
     pins = [t.pin_memory() for t in (Z, V, U, gamma, beta)]
