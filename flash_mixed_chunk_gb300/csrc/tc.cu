@@ -167,10 +167,15 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   cfg.attrs = pdl;
   cfg.numAttrs = 1;
   const int64_t lanes = (int64_t)B * se / 8;
-  cfg.gridDim = dim3(no_global ? 1u : (unsigned)((lanes + 255) / 256));
+  // long chunk axes: the segmented scan (64 column groups x 4 segments a block)
+  const bool seg = !no_global && G >= kScanSegMinG;
+  cfg.gridDim = dim3(no_global ? 1u : (unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
   cfg.blockDim = dim3(256);
   cfg.dynamicSmemBytes = 0;
-  auto *scan = var.lin_norm == kLinNormSummed     ? tc_state_scan<kLinNormSummed>
+  auto *scan = seg ? (var.lin_norm == kLinNormSummed     ? tc_state_scan_seg<kLinNormSummed>
+                      : var.lin_norm == kLinNormPosition ? tc_state_scan_seg<kLinNormPosition>
+                                                         : tc_state_scan_seg<kLinNormN>)
+               : var.lin_norm == kLinNormSummed   ? tc_state_scan<kLinNormSummed>
                : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
                : no_global                        ? tc_state_scan<kLinNormNone>
                                                   : tc_state_scan<kLinNormN>;

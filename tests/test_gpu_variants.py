@@ -57,6 +57,18 @@ def test_tensor_core_path(B, n, C, s, e, causal, variant):
     check(B, n, C, s, e, causal, torch.bfloat16, variant, m.FMCA_PATH_TCGEN05, seed=7 + n)
 
 
+@pytest.mark.parametrize("variant", [(None, N)] + VARIANTS,
+                         ids=["default"] + [f"{q}-{l}" for q, l in VARIANTS])
+@pytest.mark.parametrize("B,n,C,s,e,causal", [
+    (1, 8192, 128, 128, 256, True),    # 64 chunks: the segmented chunk scan
+    (2, 8960, 128, 128, 256, True),    # 70 chunks: segments of 18, 18, 18, 16
+    (1, 8960, 128, 128, 256, False),
+])
+def test_tensor_core_path_long_chunk_axis(B, n, C, s, e, causal, variant):
+    m = fm()
+    check(B, n, C, s, e, causal, torch.bfloat16, variant, m.FMCA_PATH_TCGEN05, seed=5 + n)
+
+
 @pytest.mark.parametrize("variant", VARIANTS, ids=[f"{q}-{l}" for q, l in VARIANTS])
 @pytest.mark.parametrize("B,n,C,s,e,causal,dtype", [
     (1, 96, 32, 48, 80, True, torch.float32),     # ragged tiles
