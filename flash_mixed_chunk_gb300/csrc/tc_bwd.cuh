@@ -1,6 +1,6 @@
 // tc_bwd.cuh -- the elementwise steps of the tensor-core backward pass
-// (the products run in tc_bgemm; see launch_tc_backward in tc.cu for the
-// order).  The forward kernels, fed dO in place of U, give dU = dO * Y
+// (the products run in tc_bgemm; launch_tc_backward in tc_backward.cuh gives
+// the order).  The forward kernels, fed dO in place of U, give dU = dO * Y
 // directly; the rest:
 //   dY = dO * U;  T0, T1, T3 rows in bf16;
 //   the reverse chunk scan of d(prefix): dS_h = sum_{g>h} f_g dP_g;
