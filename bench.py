@@ -237,10 +237,21 @@ def oracle_sample_rate(w, inputs64, gamma, beta, budget_s: float):
         "element(s)", oracle.max_threads()
 
 
+def host_cores() -> int:
+    """Host cores this process may run on."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
 def run_reference(args, w):
-    """Reference arm: the fp64 CPU oracle as it stands, on host cores."""
+    """Reference arm: the fp64 CPU oracle as it stands, on host cores.  It
+    runs on rank 0 only, so it takes every core of the host, whatever thread
+    count a launcher set for the ranks (torchrun sets one)."""
     import oracle
     oracle.build()
+    threads = host_cores()
     seed = mca_inputs.WORKLOAD_ORDER.index(w.name) + 1
     Z, V, U, gamma, beta = mca_inputs.workload_inputs(w, seed)
     inputs64 = tuple(x.to(torch.float64).numpy() for x in (Z, V, U))
@@ -255,17 +266,16 @@ def run_reference(args, w):
     while True:
         rows = np.arange(m * w.C, dtype=np.int64)
         t = time.perf_counter()
-        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, **variant)
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, nthreads=threads, **variant)
         dt = time.perf_counter() - t
         if dt >= per_step or m >= w.G:
             break
         m = min(w.G, max(m + 1, int(m * per_step / max(dt, 1e-3))))
-    threads = oracle.max_threads()
     for _ in range(args.warmup):
-        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, **variant)
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, nthreads=threads, **variant)
     t = time.perf_counter()
     for _ in range(args.steps):
-        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, **variant)
+        oracle.rows(*inputs64, g64, b64, w.C, w.causal, rows, nthreads=threads, **variant)
     dt = time.perf_counter() - t
     value = args.steps * m * w.C / dt
     sample = (f"outputs of the first {m} chunk(s) of batch element 0 of {w.name} per step "
