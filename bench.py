@@ -458,10 +458,15 @@ def run_backward(args, w, device):
                                                            else fm.FMCA_F32),
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
+    if args.saved:
+        # the forward pass's intermediates, kept in the workspace for every step
+        O = torch.empty_like(U)
+        fm.flash_mca_forward_ex(Z, V, U, gamma, beta, O, w.C, w.causal, ws, qs, ln,
+                                fm.FMCA_PATH_AUTO, stream)
 
     def step():
         fm.flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dg, db, w.C, w.causal, ws, qs,
-                              ln, stream)
+                              ln, stream, saved=args.saved)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(device)
@@ -503,7 +508,8 @@ def run_backward(args, w, device):
         "value": w.B * w.n / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": dtype, "data": "synthetic",
-        "config": {**config_of(w, args), "pass": "backward"},
+        "config": {**config_of(w, args),
+                   "pass": "backward, forward intermediates kept" if args.saved else "backward"},
         "roofline": roof,
         "gpu_launches": None,
         "clocks": sampler.summary(wall0, wall1),
@@ -760,6 +766,8 @@ def main():
     ap.add_argument("--decode-batch", type=int, default=8)
     ap.add_argument("--projections", action="store_true",
                     help="time the GAU projection GEMMs (tensor cores) on the workload's tokens")
+    ap.add_argument("--saved", action="store_true",
+                    help="with --backward: flash_mca_backward_saved (forward intermediates kept)")
     ap.add_argument("--graph", action="store_true",
                     help="time the forward steps as CUDA graph replays (one graph per step)")
     ap.add_argument("--backward", action="store_true",

@@ -30,7 +30,8 @@ __all__ = [
     "FmcaOptions",
     "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
     "flash_mca_decode_reset", "flash_mca_decode_step", "flash_mca_backward_workspace_bytes",
-    "flash_mca_backward", "backward", "flash_mca_gau_project", "flash_mca_gau_output",
+    "flash_mca_backward", "flash_mca_backward_saved", "backward", "flash_mca_gau_project",
+    "flash_mca_gau_output",
     "gau_project", "gau_output",
 ]
 
@@ -82,6 +83,8 @@ _SIGNATURES = [
     ("flash_mca_gau_output", _i32, [_vp] * 3 + [_int] * 3 + [_vp]),
     ("flash_mca_backward", _i32, [_vp] * 11 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
                                                           _vp, _sz, _vp]),
+    ("flash_mca_backward_saved", _i32, [_vp] * 11 + [_int] * 6 +
+     [_i32, ctypes.POINTER(FmcaOptions), _vp, _sz, _vp]),
     ("flash_mca_decode_reset", _i32, [_vp, _sz] + [_int] * 4 + [_i32, _vp]),
     ("flash_mca_decode_step", _i32, [_vp] * 6 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
                                                              _vp, _sz, _vp]),
@@ -342,9 +345,11 @@ def flash_mca_backward_workspace_bytes(B: int, n: int, s: int, e: int, C: int, c
 
 def flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, C: int,
                        causal: bool, workspace, quad_scale: float | None = None,
-                       lin_norm: int = FMCA_LIN_NORM_N, stream=None) -> None:
+                       lin_norm: int = FMCA_LIN_NORM_N, stream=None, saved: bool = False) -> None:
     """Gradients of sum(O * dO) into dZ, dV, dU (I/O dtype) and dgamma, dbeta
-    (float32 [4, s]); all CUDA tensors the caller owns."""
+    (float32 [4, s]); all CUDA tensors the caller owns.  saved=True calls
+    flash_mca_backward_saved: `workspace` holds what flash_mca_forward left in
+    it for the same inputs and options."""
     B, n, s, e = _shapes(Z, V, U)
     for name, t in (("dO", dO), ("dZ", dZ), ("dV", dV), ("dU", dU), ("dgamma", dgamma),
                     ("dbeta", dbeta), ("workspace", workspace)):
@@ -362,13 +367,13 @@ def flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, C: i
     if quad_scale is not None:
         opts.quad_scale = float(quad_scale)
     opts.lin_norm = int(lin_norm)
-    st = lib.flash_mca_backward(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
-                                beta.data_ptr(), dO.data_ptr(), dZ.data_ptr(), dV.data_ptr(),
-                                dU.data_ptr(), dgamma.data_ptr(), dbeta.data_ptr(), B, n, s, e,
-                                int(C), int(bool(causal)), dt, ctypes.byref(opts),
-                                workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                _stream_ptr(stream))
-    _check(st, "flash_mca_backward")
+    fn = lib.flash_mca_backward_saved if saved else lib.flash_mca_backward
+    st = fn(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(), beta.data_ptr(),
+            dO.data_ptr(), dZ.data_ptr(), dV.data_ptr(), dU.data_ptr(), dgamma.data_ptr(),
+            dbeta.data_ptr(), B, n, s, e, int(C), int(bool(causal)), dt, ctypes.byref(opts),
+            workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_ptr(stream))
+    _check(st, "flash_mca_backward_saved" if saved else "flash_mca_backward")
 
 
 def backward(Z, V, U, gamma, beta, dO, C: int, causal: bool, quad_scale: float | None = None,

@@ -176,13 +176,15 @@ size_t flash_mca_backward_workspace_bytes(int B, int n, int s, int e, int C, int
   return backward_bytes(B, n, s, e, C, causal, dtype);
 }
 
-fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, const float *gamma,
-                               const float *beta, const void *dO, void *dZ, void *dV, void *dU,
-                               float *dgamma, float *dbeta, int B, int n, int s, int e, int C,
-                               int causal, fmca_dtype dtype, const fmca_options *opts,
-                               void *workspace, size_t workspace_bytes_, fmca_stream_t stream) {
+static fmca_status backward_impl(const void *Z, const void *V, const void *U, const float *gamma,
+                                 const float *beta, const void *dO, void *dZ, void *dV, void *dU,
+                                 float *dgamma, float *dbeta, int B, int n, int s, int e, int C,
+                                 int causal, fmca_dtype dtype, const fmca_options *opts,
+                                 void *workspace, size_t workspace_bytes_, fmca_stream_t stream,
+                                 bool saved) {
   fmca_status st = check_sizes(B, n, s, e, C, causal, dtype);
   if (st != FMCA_OK) return st;
+  if (saved && !tc_backward(B, n, s, e, C, dtype)) return FMCA_ERR_UNSUPPORTED;
   if (!Z || !V || !U || !gamma || !beta || !dO || !dZ || !dV || !dU || !dgamma || !dbeta)
     return FMCA_ERR_INVALID_ARG;
   Variant var;
@@ -215,7 +217,7 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
   if (tc_backward(B, n, s, e, C, dtype))
     return launch_tc_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C,
                               causal ? 1 : 0, var, workspace,
-                              reinterpret_cast<cudaStream_t>(stream)) == 0
+                              reinterpret_cast<cudaStream_t>(stream), saved) == 0
                ? FMCA_OK
                : FMCA_ERR_CUDA;
   return launch_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C,
@@ -223,6 +225,25 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
                          reinterpret_cast<cudaStream_t>(stream)) == 0
              ? FMCA_OK
              : FMCA_ERR_CUDA;
+}
+
+fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, const float *gamma,
+                               const float *beta, const void *dO, void *dZ, void *dV, void *dU,
+                               float *dgamma, float *dbeta, int B, int n, int s, int e, int C,
+                               int causal, fmca_dtype dtype, const fmca_options *opts,
+                               void *workspace, size_t workspace_bytes_, fmca_stream_t stream) {
+  return backward_impl(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C, causal,
+                       dtype, opts, workspace, workspace_bytes_, stream, false);
+}
+
+fmca_status flash_mca_backward_saved(const void *Z, const void *V, const void *U,
+                                     const float *gamma, const float *beta, const void *dO,
+                                     void *dZ, void *dV, void *dU, float *dgamma, float *dbeta,
+                                     int B, int n, int s, int e, int C, int causal,
+                                     fmca_dtype dtype, const fmca_options *opts, void *workspace,
+                                     size_t workspace_bytes_, fmca_stream_t stream) {
+  return backward_impl(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, B, n, s, e, C, causal,
+                       dtype, opts, workspace, workspace_bytes_, stream, true);
 }
 
 fmca_status flash_mca_gau_project(const void *X, const void *Wt, void *U, void *V, void *Z,

@@ -57,10 +57,12 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
                         int causal, int dtype_bf16, const Variant &var, void *workspace,
                         cudaStream_t stream, cudaEvent_t const *events = nullptr);
 
+// with_prep = false: only the output kernel runs, on the relu^2 weights, lin_q
+// rows and prefix an earlier call with the same inputs left in `workspace`.
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events = nullptr);
+                      cudaEvent_t const *events = nullptr, bool with_prep = true);
 
 // Runs a setup step (kernel attributes) once per device and process, safely
 // when several host threads make their first call at the same time; later
@@ -176,10 +178,13 @@ inline TcBackwardLayout tc_backward_layout(int B, int n, int s, int e, int C, in
   L.total = L.part + align256(4 * 8 * (size_t)s * ((rows + kTcbAffRows - 1) / kTcbAffRows));
   return L;
 }
+// saved: the workspace already holds the forward pass's intermediates (an
+// earlier flash_mca_forward with the same inputs, options and workspace).
 int launch_tc_backward(const void *Z, const void *V, const void *U, const float *gamma,
                        const float *beta, const void *dO, void *dZ, void *dV, void *dU,
                        float *dgamma, float *dbeta, int B, int n, int s, int e, int C, int causal,
-                       const Variant &var, void *workspace, cudaStream_t stream);
+                       const Variant &var, void *workspace, cudaStream_t stream,
+                       bool saved = false);
 
 // Shapes the tensor-core path covers.
 bool tc_supported(int B, int n, int s, int e, int C);

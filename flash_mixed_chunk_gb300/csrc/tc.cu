@@ -105,7 +105,7 @@ int tc_launch_count() { return 3; }
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events) {
+                      cudaEvent_t const *events, bool with_prep) {
   const int G = n / C;
   const int R = C / ROW_TILE;
   const int64_t se = (int64_t)s * e;
@@ -151,10 +151,12 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   const int n_score = B * G * score_units_per_chunk(C, causal);
   const int n_prep = n_state + n_score;
   auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
-  prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
-      mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n, e,
-      C, G, causal, n_state, n_score, var.quad_a);
-  if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
+  if (with_prep) {
+    prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
+        mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n,
+        e, C, G, causal, n_state, n_score, var.quad_a);
+    if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
+  }
   // The scan and the attention kernel are launched as programmatic dependents
   // of the kernel before them: each may start launching (and run its
   // prologue) while its predecessor drains, and waits (griddepcontrol.wait)
@@ -179,9 +181,9 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
                : no_global                        ? tc_state_scan<kLinNormNone>
                                                   : tc_state_scan<kLinNormN>;
-  if (cudaLaunchKernelEx(&cfg, scan, (const __nv_bfloat16 *)states, prefix, B, G, se,
-                         1.0f / (float)n, causal, C) != cudaSuccess ||
-      !record_event(events, 2, stream))
+  if (with_prep && (cudaLaunchKernelEx(&cfg, scan, (const __nv_bfloat16 *)states, prefix, B, G,
+                                       se, 1.0f / (float)n, causal, C) != cudaSuccess ||
+                    !record_event(events, 2, stream)))
     return 1;
   const int n_units = B * G * R * (e / E_TILE);
   cfg.gridDim = dim3(n_units < num_sms() ? n_units : num_sms());

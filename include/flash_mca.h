@@ -260,6 +260,25 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
                                void *workspace, size_t workspace_bytes, fmca_stream_t stream);
 
 /*
+ * flash_mca_backward for training loops that keep the forward pass's
+ * intermediates: the same gradients, but the relu^2 weights, lin_q rows and
+ * scaled prefix are not recomputed.  `workspace` must hold what an earlier
+ * flash_mca_forward (or _ex, FMCA_PATH_AUTO or FMCA_PATH_TCGEN05) left in it,
+ * called with the same Z, V, U, gamma, beta, sizes and options and with this
+ * workspace (sized by flash_mca_backward_workspace_bytes: the forward pass
+ * uses its first flash_mca_workspace_bytes), with nothing written to it
+ * since; the library cannot check this.  Only the output kernel of the
+ * forward pass runs again (fed dO, for dU).  Shapes of FMCA_PATH_TCGEN05 with
+ * FMCA_BF16 only; others return FMCA_ERR_UNSUPPORTED.
+ */
+fmca_status flash_mca_backward_saved(const void *Z, const void *V, const void *U,
+                                     const float *gamma, const float *beta, const void *dO,
+                                     void *dZ, void *dV, void *dU, float *dgamma, float *dbeta,
+                                     int B, int n, int s, int e, int C, int causal,
+                                     fmca_dtype dtype, const fmca_options *opts, void *workspace,
+                                     size_t workspace_bytes, fmca_stream_t stream);
+
+/*
  * The dense projections of a GAU layer around the attention core, on the
  * tensor cores (bf16 in, fp32 accumulation, bf16 out):
  *   flash_mca_gau_project  U = SiLU(X W_u), V = SiLU(X W_v), Z = SiLU(X W_z)

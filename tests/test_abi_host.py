@@ -283,3 +283,16 @@ def test_gau_projection_validation():
     assert g(X, W, U, 128, 64, 96, None) == fm.FMCA_ERR_UNSUPPORTED             # d % 64
     assert g(X, W, X, 128, 64, 64, None) == fm.FMCA_ERR_INVALID_ARG             # Out overlaps Y
     assert g(X, W, U + 4, 128, 64, 64, None) == fm.FMCA_ERR_ALIGN
+
+
+def test_backward_saved_validation():
+    # the saved mode exists for the tensor-core shapes only: fp32, or bf16 with
+    # s != 128, is refused before any pointer is looked at
+    f = fm.lib.flash_mca_backward_saved
+
+    def call(B, n, s, e, C, dt):
+        return f(P, P, P, P, P, P, P, P, P, P, P, B, n, s, e, C, 1, dt, None, P, 1 << 30, None)
+    assert call(2, 64, 16, 32, 16, fm.FMCA_F32) == fm.FMCA_ERR_UNSUPPORTED
+    assert call(1, 512, 64, 256, 256, fm.FMCA_BF16) == fm.FMCA_ERR_UNSUPPORTED
+    assert call(1, 512, 128, 200, 256, fm.FMCA_BF16) == fm.FMCA_ERR_UNSUPPORTED
+    assert call(2, 64, 16, 32, 60, fm.FMCA_F32) == fm.FMCA_ERR_SHAPE   # C does not divide n

@@ -14,6 +14,7 @@ import torch
 import mca_inputs
 
 from tests.test_gpu_backward import check, run_backward
+from tests.test_gpu_parity import fm
 
 pytestmark = pytest.mark.gpu
 
@@ -51,3 +52,34 @@ def test_tc_backward_is_deterministic():
     b = run_backward(Z, V, U, gamma, beta, dO, C, True, None, 0)
     for x, y in zip(a, b):
         assert np.array_equal(x, y)
+
+
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("variant", [(None, 0), (None, 2), (None, 3)], ids=["n", "position", "none"])
+def test_tc_backward_saved_matches_recompute(causal, variant):
+    # the forward pass's intermediates kept in the workspace: the same bits as
+    # the backward pass that recomputes them
+    m = fm()
+    dev = torch.device("cuda:0")
+    B, n, C, s, e = 2, 1024, 256, 128, 512
+    qs, ln = variant
+    Z, V, U, gamma, beta = (t.to(dev) for t in mca_inputs.make_inputs(B, n, s, e, 12, BF))
+    dO = torch.randn(B, n, e, generator=torch.Generator().manual_seed(13)).to(BF).to(dev)
+    nb = m.flash_mca_backward_workspace_bytes(B, n, s, e, C, causal, m.FMCA_BF16)
+    ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+    O = torch.empty_like(U)
+    m.flash_mca_forward_ex(Z, V, U, gamma, beta, O, C, causal, ws, qs, ln, m.FMCA_PATH_AUTO)
+
+    def grads(saved):
+        out = (torch.empty_like(Z), torch.empty_like(V), torch.empty_like(U),
+               torch.empty(4, s, device=dev), torch.empty(4, s, device=dev))
+        m.flash_mca_backward(Z, V, U, gamma, beta, dO, *out, C, causal, ws, qs, ln, saved=saved)
+        return out
+    kept = grads(True)          # right after the forward pass: its intermediates
+    torch.cuda.synchronize()
+    full = grads(False)         # recomputes them (into the same workspace)
+    torch.cuda.synchronize()
+    for a, b in zip(kept, full):
+        assert torch.equal(a, b)
+    st, where = m.flash_mca_device_status()
+    assert st == m.FMCA_OK, f"device status {st} at {where}"
