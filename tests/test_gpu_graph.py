@@ -51,3 +51,36 @@ def test_forward_graph_replay(B, n, C, s, e, causal, dtype):
     assert torch.equal(O_graph, O_eager)
     st, where = m.flash_mca_device_status()
     assert st == m.FMCA_OK, f"device status {st} at {where}"
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_backward_graph_replay(causal):
+    # the tensor-core backward (its launches chained by programmatic dependent
+    # launch) and the CUDA-core one, captured and replayed
+    m = fm()
+    dev = torch.device("cuda:0")
+    for (B, n, C, s, e, dtype) in ((2, 1024, 256, 128, 512, torch.bfloat16),
+                                   (1, 256, 64, 32, 64, torch.float32)):
+        Z, V, U, gamma, beta = (t.to(dev) for t in mca_inputs.make_inputs(B, n, s, e, 9, dtype))
+        dO = torch.randn(B, n, e, generator=torch.Generator().manual_seed(4)).to(dtype).to(dev)
+        code = m.FMCA_BF16 if dtype == torch.bfloat16 else m.FMCA_F32
+        ws = torch.empty(m.flash_mca_backward_workspace_bytes(B, n, s, e, C, causal, code),
+                         dtype=torch.uint8, device=dev)
+
+        def outs():
+            return (torch.empty_like(Z), torch.empty_like(V), torch.empty_like(U),
+                    torch.empty(4, s, device=dev), torch.empty(4, s, device=dev))
+        eager, graphed = outs(), outs()
+        m.flash_mca_backward(Z, V, U, gamma, beta, dO, *eager, C, causal, ws)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            m.flash_mca_backward(Z, V, U, gamma, beta, dO, *graphed, C, causal, ws,
+                                 stream=torch.cuda.current_stream(dev))
+        g.replay()
+        g.replay()
+        torch.cuda.synchronize()
+        for a, b in zip(graphed, eager):
+            assert torch.equal(a, b)
+        st, where = m.flash_mca_device_status()
+        assert st == m.FMCA_OK, f"device status {st} at {where}"
