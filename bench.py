@@ -511,7 +511,8 @@ def run_backward(args, w, device):
         "config": {**config_of(w, args),
                    "pass": "backward, forward intermediates kept" if args.saved else "backward"},
         "roofline": roof,
-        "gpu_launches": None,
+        "gpu_launches": args.steps * fm.flash_mca_backward_launch_count(
+            w.B, w.n, w.s, w.e, w.C, w.causal, dcode, qs, ln, saved=args.saved),
         "clocks": sampler.summary(wall0, wall1),
     }
     print(json.dumps(line), flush=True)

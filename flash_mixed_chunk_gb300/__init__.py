@@ -30,7 +30,8 @@ __all__ = [
     "FmcaOptions",
     "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
     "flash_mca_decode_reset", "flash_mca_decode_step", "flash_mca_backward_workspace_bytes",
-    "flash_mca_backward", "flash_mca_backward_saved", "backward", "flash_mca_gau_project",
+    "flash_mca_backward", "flash_mca_backward_saved", "flash_mca_backward_launch_count",
+    "backward", "flash_mca_gau_project",
     "flash_mca_gau_output",
     "gau_project", "gau_output",
 ]
@@ -85,6 +86,8 @@ _SIGNATURES = [
                                                           _vp, _sz, _vp]),
     ("flash_mca_backward_saved", _i32, [_vp] * 11 + [_int] * 6 +
      [_i32, ctypes.POINTER(FmcaOptions), _vp, _sz, _vp]),
+    ("flash_mca_backward_launch_count", _int,
+     [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions), _int]),
     ("flash_mca_decode_reset", _i32, [_vp, _sz] + [_int] * 4 + [_i32, _vp]),
     ("flash_mca_decode_step", _i32, [_vp] * 6 + [_int] * 6 + [_i32, ctypes.POINTER(FmcaOptions),
                                                              _vp, _sz, _vp]),
@@ -374,6 +377,18 @@ def flash_mca_backward(Z, V, U, gamma, beta, dO, dZ, dV, dU, dgamma, dbeta, C: i
             workspace.data_ptr(), workspace.numel() * workspace.element_size(),
             _stream_ptr(stream))
     _check(st, "flash_mca_backward_saved" if saved else "flash_mca_backward")
+
+
+def flash_mca_backward_launch_count(B: int, n: int, s: int, e: int, C: int, causal: bool,
+                                    dtype: int, quad_scale: float | None = None,
+                                    lin_norm: int = FMCA_LIN_NORM_N, saved: bool = False) -> int:
+    """Kernels one backward call launches (0 for rejected arguments)."""
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    opts.lin_norm = int(lin_norm)
+    return int(lib.flash_mca_backward_launch_count(B, n, s, e, C, int(bool(causal)), dtype,
+                                                   ctypes.byref(opts), int(bool(saved))))
 
 
 def backward(Z, V, U, gamma, beta, dO, C: int, causal: bool, quad_scale: float | None = None,

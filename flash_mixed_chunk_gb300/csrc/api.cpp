@@ -236,6 +236,23 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
                        dtype, opts, workspace, workspace_bytes_, stream, false);
 }
 
+int flash_mca_backward_launch_count(int B, int n, int s, int e, int C, int causal,
+                                    fmca_dtype dtype, const fmca_options *opts, int saved) {
+  if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
+  Variant var;
+  if (to_variant(opts, C, &var) != FMCA_OK) return 0;
+  const int glob = var.lin_norm != kLinNormNone ? 1 : 0;
+  if (tc_backward(B, n, s, e, C, dtype))
+    // forward kernels (or the output kernel alone), dY and the T rows, three
+    // product launches, the reverse scan, dZ with its partials and their sum
+    return (saved ? 1 : 3) + 2 + 3 + glob + 2;
+  if (saved) return 0;
+  // CUDA cores: the chunk states and prefix, dY, score gradients, dU, key
+  // gradients, the d(prefix) outer products, reverse scan and lin rows, dV,
+  // dZ with its partials and their sum
+  return glob ? 12 : 7;
+}
+
 fmca_status flash_mca_backward_saved(const void *Z, const void *V, const void *U,
                                      const float *gamma, const float *beta, const void *dO,
                                      void *dZ, void *dV, void *dU, float *dgamma, float *dbeta,

@@ -271,6 +271,11 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
  * forward pass runs again (fed dO, for dU).  Shapes of FMCA_PATH_TCGEN05 with
  * FMCA_BF16 only; others return FMCA_ERR_UNSUPPORTED.
  */
+/* Number of kernels one flash_mca_backward (saved = 0) or
+ * flash_mca_backward_saved (saved = 1) call launches for these arguments (0
+ * when they would be rejected). */
+int flash_mca_backward_launch_count(int B, int n, int s, int e, int C, int causal,
+                                    fmca_dtype dtype, const fmca_options *opts, int saved);
 fmca_status flash_mca_backward_saved(const void *Z, const void *V, const void *U,
                                      const float *gamma, const float *beta, const void *dO,
                                      void *dZ, void *dV, void *dU, float *dgamma, float *dbeta,

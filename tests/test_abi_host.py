@@ -296,3 +296,19 @@ def test_backward_saved_validation():
     assert call(1, 512, 64, 256, 256, fm.FMCA_BF16) == fm.FMCA_ERR_UNSUPPORTED
     assert call(1, 512, 128, 200, 256, fm.FMCA_BF16) == fm.FMCA_ERR_UNSUPPORTED
     assert call(2, 64, 16, 32, 60, fm.FMCA_F32) == fm.FMCA_ERR_SHAPE   # C does not divide n
+
+
+def test_backward_launch_count():
+    bf, f32 = fm.FMCA_BF16, fm.FMCA_F32
+    cnt = fm.flash_mca_backward_launch_count
+    # tensor cores: forward kernels (3, or 1 when the forward's intermediates
+    # are kept), 2 elementwise, 3 product launches, the reverse scan (global
+    # term only), 2 for dZ / dgamma / dbeta
+    assert cnt(2, 1024, 128, 512, 256, True, bf) == 11
+    assert cnt(2, 1024, 128, 512, 256, True, bf, saved=True) == 9
+    assert cnt(2, 1024, 128, 512, 256, True, bf, lin_norm=fm.FMCA_LIN_NORM_NONE) == 10
+    # CUDA cores
+    assert cnt(2, 1024, 128, 512, 256, True, f32) == 12
+    assert cnt(2, 1024, 128, 512, 256, True, f32, lin_norm=fm.FMCA_LIN_NORM_NONE) == 7
+    assert cnt(2, 1024, 128, 512, 256, True, f32, saved=True) == 0
+    assert cnt(2, 1024, 128, 512, 60, True, bf) == 0        # C does not divide n
