@@ -47,7 +47,7 @@ import mca_inputs  # noqa: E402
 
 METRIC = "mixed-chunk attn fwd tokens/s and TFLOP/s at 1 GB300; % of bf16 tensor peak"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DOMINANT_KERNEL = "tc_chunk_attn"
+DOMINANT_KERNEL = "tc_chunk_fused"
 
 
 # ---------------------------------------------------------------- ranks
@@ -107,7 +107,7 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_scan.cuh", "tc_attn.cuh",
+FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_scan.cuh", "tc_fused.cuh",
                           "ptx.cuh")
 
 
@@ -583,7 +583,9 @@ def run_ours(args, w, rank, world, device):
     Zc, Vc, Uc, gc, bc = mca_inputs.workload_inputs(w, seed)
     dt_code = fm.FMCA_BF16 if w.dtype == "bf16" else fm.FMCA_F32
     path = fm.flash_mca_auto_path(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code)
-    nl = fm.flash_mca_launch_count(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code)
+    quad_scale, lin_norm = variant_of(args, w)
+    nl = fm.flash_mca_launch_count(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code,
+                                   quad_scale=quad_scale, lin_norm=lin_norm)
     sets = []
     for _ in range(3):
         sets.append(dict(Z=Zc.to(device), V=Vc.to(device), U=Uc.to(device),
@@ -592,8 +594,6 @@ def run_ours(args, w, rank, world, device):
     ws = torch.empty(fm.flash_mca_workspace_bytes(w.B, w.n, w.s, w.e, w.C, w.causal, dt_code),
                      dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-
-    quad_scale, lin_norm = variant_of(args, w)
 
     def step(i, events=None):
         s = sets[i % 3]
@@ -699,9 +699,12 @@ def run_ours(args, w, rank, world, device):
     value = whole_job_rate(world, tokens, args.steps, ms / 1e3)
     flops = algorithmic_flops(w, lin_norm)
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
-    kernel_names = (["tc_chunk_prep", "tc_state_scan", "tc_chunk_attn"]
-                    if path == fm.FMCA_PATH_TCGEN05 else
-                    ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"])
+    if path != fm.FMCA_PATH_TCGEN05:
+        kernel_names = ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"]
+    elif lin_norm == fm.FMCA_LIN_NORM_NONE:  # the T0 / T1 rows, then the fused kernel
+        kernel_names = ["tc_affine_rows", "tc_chunk_fused"]
+    else:  # states and T rows, the scan, the fused kernel
+        kernel_names = ["tc_chunk_prep", "tc_state_scan", "tc_chunk_fused"]
     kernels = {name: {"ms": per_kernel_ms[i], "share": per_kernel_ms[i] / sum(per_kernel_ms)}
                for i, name in enumerate(kernel_names)}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])

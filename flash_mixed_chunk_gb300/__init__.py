@@ -22,7 +22,8 @@ __all__ = [
     "FMCA_PATH_AUTO", "FMCA_PATH_SIMT", "FMCA_PATH_TCGEN05", "FmcaError", "lib", "library_path",
     "flash_mca_workspace_bytes", "flash_mca_forward", "flash_mca_forward_path",
     "flash_mca_forward_timed",
-    "flash_mca_auto_path", "flash_mca_launch_count", "flash_mca_host_arena_bytes",
+    "flash_mca_auto_path", "flash_mca_launch_count", "flash_mca_launch_count_ex",
+    "flash_mca_host_arena_bytes",
     "flash_mca_forward_host", "flash_mca_forward_noalloc", "flash_mca_device_status",
     "flash_mca_selftest_timeout", "FMCA_NOALLOC_SCRATCH_BYTES",
     "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
@@ -93,6 +94,7 @@ _SIGNATURES = [
                                                              _vp, _sz, _vp]),
     ("flash_mca_auto_path", _int, [_int] * 6 + [_i32]),
     ("flash_mca_launch_count", _int, [_int] * 6 + [_i32, _i32]),
+    ("flash_mca_launch_count_ex", _int, [_int] * 6 + [_i32, _i32, ctypes.POINTER(FmcaOptions)]),
     ("flash_mca_host_arena_bytes", _sz, [_int] * 6 + [_i32]),
     ("flash_mca_forward_host", _i32, _fwd_args + [_vp]),
     ("flash_mca_forward_noalloc", _i32, _fwd_args[:13] + [_vp]),
@@ -157,8 +159,19 @@ def flash_mca_auto_path(B: int, n: int, s: int, e: int, C: int, causal: bool, dt
 
 
 def flash_mca_launch_count(B: int, n: int, s: int, e: int, C: int, causal: bool, dtype: int,
-                           path: int = FMCA_PATH_AUTO) -> int:
-    return int(lib.flash_mca_launch_count(B, n, s, e, C, int(bool(causal)), dtype, path))
+                           path: int = FMCA_PATH_AUTO, quad_scale: float | None = None,
+                           lin_norm: int | None = None) -> int:
+    """Kernels one forward call launches; with ``quad_scale`` or ``lin_norm``
+    given, the count of flash_mca_forward_ex with those options."""
+    if quad_scale is None and lin_norm is None:
+        return int(lib.flash_mca_launch_count(B, n, s, e, C, int(bool(causal)), dtype, path))
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    if lin_norm is not None:
+        opts.lin_norm = int(lin_norm)
+    return int(lib.flash_mca_launch_count_ex(B, n, s, e, C, int(bool(causal)), dtype, path,
+                                             ctypes.byref(opts)))
 
 
 def _shapes(Z: torch.Tensor, V: torch.Tensor, U: torch.Tensor):
@@ -178,7 +191,6 @@ def flash_mca_default_options(C: int) -> FmcaOptions:
 
 
 def _check_device_args(Z, V, U, gamma, beta, O, workspace):
-    B, n, s, e = _shapes(Z, V, U)
     B, n, s, e = _shapes(Z, V, U)
     for name, t in (("Z", Z), ("V", V), ("U", U), ("O", O), ("gamma", gamma), ("beta", beta),
                     ("workspace", workspace)):

@@ -80,15 +80,22 @@ int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtyp
   return want_tc(B, n, s, e, C, dtype) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
 }
 
-int flash_mca_launch_count(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype,
-                           fmca_path path) {
+int flash_mca_launch_count_ex(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                              fmca_path path, const fmca_options *opts) {
   if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
+  Variant var;
+  if (to_variant(opts, C, &var) != FMCA_OK) return 0;
   if (path == FMCA_PATH_AUTO)
     path = want_tc(B, n, s, e, C, dtype) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
   if (path == FMCA_PATH_TCGEN05)
-    return want_tc(B, n, s, e, C, dtype) ? tc_launch_count() : 0;
+    return want_tc(B, n, s, e, C, dtype) ? tc_launch_count(var) : 0;
   if (path == FMCA_PATH_SIMT) return kSimtLaunches;
   return 0;
+}
+
+int flash_mca_launch_count(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype,
+                           fmca_path path) {
+  return flash_mca_launch_count_ex(B, n, s, e, C, causal, dtype, path, nullptr);
 }
 
 fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
@@ -243,9 +250,10 @@ int flash_mca_backward_launch_count(int B, int n, int s, int e, int C, int causa
   if (to_variant(opts, C, &var) != FMCA_OK) return 0;
   const int glob = var.lin_norm != kLinNormNone ? 1 : 0;
   if (tc_backward(B, n, s, e, C, dtype))
-    // forward kernels (or the output kernel alone), dY and the T rows, three
-    // product launches, the reverse scan, dZ with its partials and their sum
-    return (saved ? 1 : 3) + 2 + 3 + glob + 2;
+    // forward kernels (with `saved`: the relu^2 weights and the output
+    // kernel), dY and the T rows, three product launches, the reverse scan,
+    // dZ with its partials and their sum
+    return (saved ? 2 : 3) + 2 + 3 + glob + 2;
   if (saved) return 0;
   // CUDA cores: the chunk states and prefix, dY, score gradients, dU, key
   // gradients, the d(prefix) outer products, reverse scan and lin rows, dV,
@@ -364,7 +372,7 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
   const bool tc_ok = want_tc(B, n, s, e, C, dtype);
   if (path == FMCA_PATH_TCGEN05 && !tc_ok) return FMCA_ERR_UNSUPPORTED;
   const bool use_tc = (path == FMCA_PATH_TCGEN05) || (path == FMCA_PATH_AUTO && tc_ok);
-  const int nlaunch = use_tc ? tc_launch_count() : kSimtLaunches;
+  const int nlaunch = use_tc ? tc_launch_count(var) : kSimtLaunches;
   if (events != nullptr) {
     if (n_events != nlaunch + 1) return FMCA_ERR_INVALID_ARG;
     for (int i = 0; i < n_events; ++i)

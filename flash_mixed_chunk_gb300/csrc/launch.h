@@ -13,31 +13,60 @@ namespace fmca {
 
 inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace layout (byte offsets, each region 256-byte aligned):
-//   states  per-chunk states, fp32 [B][G][s][e]
-//   prefix  state prefix sums / n, Gp = G (causal) or 1 (bidirectional) chunks
-//           of [s][e]; fp32 on the SIMT path, bf16 on the tensor-core path
-//   scores  intra-chunk relu^2 weights, bf16 [B*n][C] (tensor-core path)
-//   lin_q   T2 = Z*gamma2 + beta2, bf16 [B*n][s] (tensor-core path)
-//   sched   work counter of the persistent attention kernel (tensor-core path)
-struct WorkspaceLayout {
-  size_t states, prefix, scores, lin_q, sched, total;
+// Workspace of the CUDA-core (SIMT) forward path, fp32, each region 256-byte
+// aligned:
+//   states  per-chunk states [B][G][s][e]
+//   prefix  their prefix sums (causal: Gp = G chunks) or total (Gp = 1) / n
+struct SimtLayout {
+  size_t states, prefix, total;
 };
-inline WorkspaceLayout workspace_layout(int B, int n, int s, int e, int C, int causal) {
-  const size_t G = (size_t)(n / C);
-  const size_t se = (size_t)s * (size_t)e;
-  const size_t Gp = causal ? G : 1;
-  WorkspaceLayout L;
+inline SimtLayout simt_layout(int B, int n, int s, int e, int C, int causal) {
+  const size_t G = (size_t)(n / C), se = (size_t)s * (size_t)e, Gp = causal ? G : 1;
+  SimtLayout L;
   L.states = 0;
-  L.prefix = L.states + align256(sizeof(float) * (size_t)B * G * se);
-  L.scores = L.prefix + align256(sizeof(float) * (size_t)B * Gp * se);
-  L.lin_q = L.scores + align256(2 * (size_t)B * n * (size_t)C);
-  L.sched = L.lin_q + align256(2 * (size_t)B * n * (size_t)s);
-  L.total = L.sched + 256;
+  L.prefix = align256(sizeof(float) * (size_t)B * G * se);
+  L.total = L.prefix + align256(sizeof(float) * (size_t)B * Gp * se);
   return L;
 }
+
+// Workspace of the tensor-core forward path, each region 256-byte aligned:
+//   states  bf16 per-chunk states [B][G][s][e]
+//   prefix  bf16 prefix sums (causal: Gp = G chunks) or total (Gp = 1),
+//           scaled by the global term's divisor
+//   sched   work counters and per-chunk ready flags of the persistent kernels
+//   trows   bf16 rows T0, T1, T2 = Z * gamma_k + beta_k, [3][B*n][s] (the fused
+//           output kernel's operands; written by the state kernel)
+// and, only in the form the backward pass runs (materialised = true):
+//   scores  bf16 intra-chunk relu^2 weights [B*n][C]
+//   lin_q   bf16 T2 = Z * gamma2 + beta2 rows [B*n][s]
+// The forward pass keeps its relu^2 weights on chip and needs only the first
+// four regions; they sit at the same offsets in both forms.
+struct TcLayout {
+  size_t states, prefix, sched, trows, scores, lin_q, total;
+};
+inline size_t tc_sched_bytes() {
+  // the two work counters (of the state kernel and the chunk kernel)
+  return 256;
+}
+inline TcLayout tc_layout(int B, int n, int s, int e, int C, int causal, bool materialised) {
+  const size_t G = (size_t)(n / C), se = (size_t)s * (size_t)e, Gp = causal ? G : 1;
+  TcLayout L;
+  L.states = 0;
+  L.prefix = align256(2 * (size_t)B * G * se);
+  L.sched = L.prefix + align256(2 * (size_t)B * Gp * se);
+  L.trows = L.sched + tc_sched_bytes();
+  L.scores = L.trows + align256(3 * 2 * (size_t)B * n * (size_t)s);
+  L.lin_q = L.scores + (materialised ? align256(2 * (size_t)B * n * (size_t)C) : 0);
+  L.total = L.lin_q + (materialised ? align256(2 * (size_t)B * n * (size_t)s) : 0);
+  return L;
+}
+
+// flash_mca_workspace_bytes: enough for either forward path, so that a
+// workspace sized for a shape serves every path a call may pick.
 inline size_t workspace_bytes(int B, int n, int s, int e, int C, int causal) {
-  return workspace_layout(B, n, s, e, C, causal).total;
+  const size_t a = simt_layout(B, n, s, e, C, causal).total;
+  const size_t b = tc_layout(B, n, s, e, C, causal, false).total;
+  return a > b ? a : b;
 }
 
 // Scale and normalisation variants (flash_mca_forward_ex): intra-chunk weights
@@ -57,12 +86,25 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
                         int causal, int dtype_bf16, const Variant &var, void *workspace,
                         cudaStream_t stream, cudaEvent_t const *events = nullptr);
 
-// with_prep = false: only the output kernel runs, on the relu^2 weights, lin_q
-// rows and prefix an earlier call with the same inputs left in `workspace`.
+// The tensor-core forward pass (workspace: tc_layout(..., false)).
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events = nullptr, bool with_prep = true);
+                      cudaEvent_t const *events = nullptr);
+// Kernels one launch_tc_forward queues (the memset of its counters not
+// counted).
+int tc_launch_count(const Variant &var);
+
+// The forward pass as the backward pass needs it (workspace:
+// tc_layout(..., true)): besides O it leaves the relu^2 weights, the lin_q
+// rows and the scaled prefix in the workspace.  with_states = false: the
+// chunk states and prefix are taken as an earlier launch_tc_forward with the
+// same inputs left them in the workspace; only the relu^2 weights, lin_q rows
+// and the output are computed.
+int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
+                                   const float *gamma, const float *beta, void *O, int B, int n,
+                                   int s, int e, int C, int causal, const Variant &var,
+                                   void *workspace, cudaStream_t stream, bool with_states);
 
 // Runs a setup step (kernel attributes) once per device and process, safely
 // when several host threads make their first call at the same time; later
@@ -152,8 +194,8 @@ int launch_gemm(const void *A, const void *B, int M, int N, int K, void *D0, voi
                 void *D2, int n0, int n1, int silu, cudaStream_t stream);
 
 // Workspace of the tensor-core backward (bf16 unless noted), each region
-// 256-byte aligned: the forward pass's own workspace (chunk states, scaled
-// prefix, relu^2 weights, lin_q rows), then dY [B*n][e], T0, T1, T3
+// 256-byte aligned: the materialised forward workspace (chunk states, scaled
+// prefix, work counters, relu^2 weights, lin_q rows), then dY [B*n][e], T0, T1, T3
 // [B*n][s], dS [B*n][C], dT0..dT3 [B*n][s], d(prefix) [B][G][s][e], and fp32
 // per-block dgamma/dbeta partials.
 constexpr int kTcbAffRows = 64;  // token rows per block of the dZ/dgamma/dbeta reduction
@@ -164,7 +206,7 @@ inline TcBackwardLayout tc_backward_layout(int B, int n, int s, int e, int C, in
   const size_t rows = (size_t)B * n, G = (size_t)(n / C);
   TcBackwardLayout L;
   L.fwd = 0;
-  L.dY = align256(workspace_bytes(B, n, s, e, C, causal));
+  L.dY = align256(tc_layout(B, n, s, e, C, causal, true).total);
   L.T0 = L.dY + align256(2 * rows * e);
   L.T1 = L.T0 + align256(2 * rows * s);
   L.T3 = L.T1 + align256(2 * rows * s);
@@ -188,7 +230,6 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
 
 // Shapes the tensor-core path covers.
 bool tc_supported(int B, int n, int s, int e, int C);
-int tc_launch_count();
 constexpr int kSimtLaunches = 3;
 
 // Device-side status word (tensor-core kernels' bounded waits).

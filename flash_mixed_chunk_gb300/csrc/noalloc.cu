@@ -8,19 +8,23 @@
 // while another component holds an allocation lock, or a caller that must
 // never fail half-way because an allocation could not be satisfied.  Such a
 // caller can still pass its inputs and output, but cannot provide the
-// scratch (per-chunk states, their prefix sums, the relu^2 weights and lin_q
-// rows) that flash_mca_forward asks for.
+// scratch (per-chunk states, their prefix sums and the kernels' work
+// counters) that flash_mca_forward asks for.
 //
 // The scratch is one file-scope __device__ array of FMCA_NOALLOC_SCRATCH_BYTES.
-// Every GPU on which this entry point runs keeps that array until the process
-// exits (the array belongs to this file's module, which the CUDA runtime
-// loads the first time the module is used on a device).  All calls on a device
-// share it, so calls whose work overlaps on that GPU (for example on two
-// streams) race on it; calls queued on one stream are ordered and safe.  The
-// array keeps whatever the previous call left in it; the forward pass writes
-// every scratch byte it reads before reading it, and the one value that must
-// start at zero (the work counter of the attention kernel) is zeroed by the
-// scan kernel inside each call.
+// It belongs to this file's module (which holds no kernel): with the CUDA
+// runtime's default lazy module loading a GPU receives it the first time this
+// entry point looks its address up there, and with eager loading
+// (CUDA_MODULE_LOADING=EAGER) every GPU on which the process creates a
+// context does, whichever entry points run.  It stays until the process
+// exits (or the context is reset).  All calls on a device share it, so calls
+// whose work overlaps on that GPU (for example on two streams) race on it;
+// calls queued on one stream are ordered and safe.  The array keeps whatever
+// the previous call left in it: the forward pass writes every scratch byte it
+// reads before reading it, and the values that must start at zero (the work
+// counters of the persistent kernels) are cleared by the cudaMemsetAsync that
+// launch_tc_forward queues at the start of every call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -40,23 +44,59 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratch
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+struct CachedAddress {
+  void *ptr = nullptr;
+  unsigned long long ctx_id = 0;  // context the address belongs to (0: none)
+};
+CachedAddress g_scratch[kMaxDevices];
 
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current).  Returns nullptr on failure.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext *);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long *);
+
+// Unique ID of the calling thread's current context (0 when there is none or
+// the driver cannot say).  A device reset gives the device a new primary
+// context with a new ID, and the module -- with the array -- is loaded anew.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+  if (get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+// Device address of the scratch on the current device, looked up with that
+// device current the first time and again whenever the device's context has
+// changed since the last lookup.  Returns nullptr on failure.
 void *scratch_on_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   std::lock_guard<std::mutex> lock(g_mutex);
-  if (g_scratch_ptr[dev] == nullptr) {
-    void *ptr = nullptr;
-    if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
-      cudaGetLastError();  // do not leave the lookup failure as the sticky last error
-      return nullptr;
-    }
-    g_scratch_ptr[dev] = ptr;
+  CachedAddress &c = g_scratch[dev];
+  const unsigned long long id = current_context_id();
+  if (c.ptr != nullptr && id != 0 && id == c.ctx_id) return c.ptr;
+  void *ptr = nullptr;
+  if (cudaGetSymbolAddress(&ptr, g_noalloc_scratch) != cudaSuccess || ptr == nullptr) {
+    cudaGetLastError();  // do not leave the lookup failure as the sticky last error
+    return nullptr;
   }
-  return g_scratch_ptr[dev];
+  c.ptr = ptr;
+  c.ctx_id = current_context_id();  // the lookup made the context current if it was not
+  return ptr;
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -77,7 +117,7 @@ extern "C" fmca_status flash_mca_forward_noalloc(const void *Z, const void *V, c
       !aligned16(beta))
     return FMCA_ERR_ALIGN;
   // the problem's scratch must fit in the fixed array
-  if (fmca::workspace_bytes(B, n, s, e, C, causal ? 1 : 0) > kNoAllocScratchBytes)
+  if (fmca::tc_layout(B, n, s, e, C, causal ? 1 : 0, false).total > kNoAllocScratchBytes)
     return FMCA_ERR_WORKSPACE;
   void *scratch = scratch_on_current_device();
   if (scratch == nullptr) return FMCA_ERR_CUDA;

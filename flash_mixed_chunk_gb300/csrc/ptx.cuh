@@ -89,6 +89,28 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, u
       : "memory");
 }
 
+// 3-D tiled load: with a map that views a row-major [rows][cols] matrix as
+// (64 inner columns, rows, cols / 64 column blocks), one box {64, R, NB}
+// lands as NB consecutive [R][64] tiles, the same bytes as NB 2-D loads of
+// {64, R} boxes; z is the first column block.
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_3d_hint(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                                 int32_t x, int32_t y, int32_t z, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar)),
+      "l"(policy)
+      : "memory");
+}
+
 // Same with an L2 cache-policy hint (a policy made by createpolicy).
 __device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map,
                                                  uint64_t *bar, int32_t x, int32_t y,
@@ -116,6 +138,16 @@ __device__ __forceinline__ void tma_store_2d_hint(const CUtensorMap *map, const 
       "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group.L2::cache_hint"
       " [%0, {%1, %2}], [%3], %4;" ::"l"(reinterpret_cast<uint64_t>(map)),
       "r"(x), "r"(y), "r"(smem_u32(src)), "l"(policy)
+      : "memory");
+}
+// 3-D tiled store shared -> global, the inverse of tma_load_3d.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *map, const void *src,
+                                                  int32_t x, int32_t y, int32_t z,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group.L2::cache_hint"
+      " [%0, {%1, %2, %3}], [%4], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(smem_u32(src)), "l"(policy)
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit_group() {
@@ -151,6 +183,7 @@ __device__ __forceinline__ void griddep_launch_dependents() {
 __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
+
 
 // Drop a 128-byte line from L2 without writing it back (its contents become
 // undefined); for scratch that no one reads again.
@@ -218,6 +251,20 @@ __device__ __forceinline__ void mma_bf16_ss(uint32_t d_tmem, uint64_t a_desc, ui
       : "memory");
 }
 
+// D[tmem] (+)= A[tmem] * B[smem], kind::f16, with the A operand (M x 16 bf16
+// per instruction) read from tensor memory: row i in lane i, K elements in
+// consecutive 32-bit columns, two per column (the lower K index in the lower
+// 16 bits), so one K = 16 step spans 8 columns.
+__device__ __forceinline__ void mma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05.mma issued so far by this thread
 // has completed.
 __device__ __forceinline__ void mma_commit(uint64_t *bar) {
@@ -244,6 +291,25 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// The store counterpart of tmem_ld32: thread i of the warp writes lane
+// (base lane + i), columns [col, col + 32).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+      "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(
+          taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
 // Shared-memory matrix descriptor, 128-byte swizzle.
@@ -284,6 +350,29 @@ __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t byte_in_
 // of 512 bytes; base 512-byte aligned).
 __device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t byte_in_row) {
   return row * 64u + ((((byte_in_row >> 4) ^ ((row >> 1) & 3u)) << 4) | (byte_in_row & 15u));
+}
+
+// 32-byte global load through the non-coherent path, not kept in L1 and
+// first out of L2 (streamed data read once); p 32-byte aligned.
+struct u32x8 {
+  uint4 lo, hi;
+};
+__device__ __forceinline__ u32x8 ldg_stream(const void *p) {
+  u32x8 v;
+  asm volatile(
+      "ld.global.nc.L1::no_allocate.L2::evict_first.v8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+      : "=r"(v.lo.x), "=r"(v.lo.y), "=r"(v.lo.z), "=r"(v.lo.w), "=r"(v.hi.x), "=r"(v.hi.y),
+        "=r"(v.hi.z), "=r"(v.hi.w)
+      : "l"(p));
+  return v;
+}
+// 32-byte global store, first out of L2 (written once, read by nobody here).
+__device__ __forceinline__ void stg_stream(void *p, const u32x8 &v) {
+  asm volatile(
+      "st.global.L1::no_allocate.L2::evict_first.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p),
+      "r"(v.lo.x), "r"(v.lo.y), "r"(v.lo.z), "r"(v.lo.w), "r"(v.hi.x), "r"(v.hi.y), "r"(v.hi.z),
+      "r"(v.hi.w)
+      : "memory");
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

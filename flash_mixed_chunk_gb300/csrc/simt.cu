@@ -269,7 +269,7 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
                         const float *beta, void *O, int B, int n, int s, int e, int C,
                         int causal, int dtype_bf16, const Variant &var, void *workspace,
                         cudaStream_t stream, cudaEvent_t const *events) {
-  const WorkspaceLayout L = workspace_layout(B, n, s, e, C, causal);
+  const SimtLayout L = simt_layout(B, n, s, e, C, causal);
   float *states = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.states);
   float *prefix = reinterpret_cast<float *>(static_cast<char *>(workspace) + L.prefix);
   if (dtype_bf16)

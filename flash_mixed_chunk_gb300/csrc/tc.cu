@@ -1,18 +1,24 @@
 // tc.cu -- tensor-core path of the mixed-chunk attention forward core
 // (sm_103a: tcgen05 MMA into TMEM, TMA-staged 128-byte-swizzled bf16 tiles,
-// mbarrier pipelines) for bf16 I/O, s = 128, C in {128, 256}, e % 256 == 0.
+// mbarrier pipelines) for bf16 I/O, s = 128, C % 128 == 0, e % 256 == 0.
 //
-// Per call: one memset of the two work counters and three kernels
-// ("FLASH: Possibly the Most Interesting Efficient Transformer Design
-// Recently", sections "Weak Attention" and "Mixed Chunk"):
+// Per call ("FLASH: Possibly the Most Interesting Efficient Transformer
+// Design Recently", sections "Weak Attention" and "Mixed Chunk"): a memset of
+// the work counters and
 //
 //   tc_chunk_prep    state_g = T3_g^T V_g per chunk and 256-column slice of e
-//                    (bf16), P = relu(T0 T1^T / C)^2 (masked) and T2 rows
-//                    (bf16), as one persistent stream of work units
+//                    (bf16; state units only) and the rows T0, T1, T2
+//                    (without a global term: tc_affine_rows, T0 and T1 only)
 //   tc_state_scan    exclusive prefix over chunks (causal) or total
 //                    (bidirectional) of the states, times 1/n, to bf16
-//   tc_chunk_attn    O = U * (P V_g + T2 prefix_g) per (chunk, row tile,
-//                    e tile), both products accumulated in TMEM
+//   tc_chunk_fused   O = U * (relu(T0 T1^T / C)^2 V_g + T2 prefix_g) per
+//                    (chunk, row tile, e tile), the relu^2 weights kept on
+//                    chip (TMEM), both products accumulated in TMEM
+//
+// The backward pass runs the forward pass in its materialised form instead:
+// tc_chunk_prep also writes the relu^2 weights P and the T2 rows to the
+// workspace (score units), and tc_chunk_attn forms O = U * (P V_g + T2
+// prefix_g) from them, leaving P and T2 for the gradient products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -28,6 +34,7 @@
 #include "tc_prep.cuh"
 #include "tc_scan.cuh"
 #include "tc_attn.cuh"
+#include "tc_fused.cuh"
 #include "tc_gemm.cuh"
 
 namespace fmca {
@@ -80,6 +87,23 @@ bool make_map_bf16(CUtensorMap *m, const void *base, uint64_t cols, uint64_t row
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D bf16 map viewing a row-major [rows][cols] matrix (cols % 64 == 0) as
+// (64 inner columns, rows, cols / 64 column blocks), 128-byte swizzle: a box
+// {64, box_rows, box_blocks} lands as box_blocks consecutive [box_rows][64]
+// tiles (see tma_load_3d).
+bool make_map3_bf16(CUtensorMap *m, const void *base, uint64_t cols, uint64_t rows,
+                    uint32_t box_rows, uint32_t box_blocks) {
+  EncodeTiledFn enc = get_encode();
+  if (!enc || cols % 64) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, box_rows, box_blocks};
+  cuuint32_t es[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box,
+             es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Streaming multiprocessors of the current device (one persistent CTA each).
 int num_sms() {
   int dev = 0, sms = 0;
@@ -100,17 +124,160 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   return true;
 }
 
-int tc_launch_count() { return 3; }
+int tc_launch_count(const Variant &var) { return var.lin_norm == kLinNormNone ? 2 : 3; }
+
+namespace {
+
+// The scan kernel of a global-term divisor (segmented for long chunk axes).
+using ScanKernel = void (*)(const __nv_bfloat16 *, __nv_bfloat16 *, int, int, int64_t, float,
+                            int, int);
+ScanKernel pick_scan(const Variant &var, bool seg) {
+  if (var.lin_norm == kLinNormNone) return tc_state_scan<kLinNormNone>;
+  if (seg)
+    return var.lin_norm == kLinNormSummed     ? tc_state_scan_seg<kLinNormSummed>
+           : var.lin_norm == kLinNormPosition ? tc_state_scan_seg<kLinNormPosition>
+                                              : tc_state_scan_seg<kLinNormN>;
+  return var.lin_norm == kLinNormSummed     ? tc_state_scan<kLinNormSummed>
+         : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
+                                            : tc_state_scan<kLinNormN>;
+}
+
+// Units of the fused kernel: every (batch x chunk, row tile) split into e
+// groups of consecutive 128-column e tiles, as few groups as give about two
+// units per SM (a unit computes its relu^2 weights once for all its e tiles).
+FusedGrid fused_grid(int B, int n, int e, int C, int causal, int sms) {
+  FusedGrid g;
+  g.n = n;
+  g.C = C;
+  g.G = n / C;
+  g.causal = causal;
+  g.n_et = e / FU_ET;
+  const int row_tiles = B * g.G * (C / ROW_TILE);
+  int want = (2 * sms + row_tiles - 1) / row_tiles;
+  want = want < 1 ? 1 : (want > g.n_et ? g.n_et : want);
+  g.eg_tiles = (g.n_et + want - 1) / want;
+  g.n_eg = (g.n_et + g.eg_tiles - 1) / g.eg_tiles;
+  g.n_units = row_tiles * g.n_eg;
+  return g;
+}
+
+// Launch configuration of a programmatic dependent of the work before it on
+// the stream: it may start launching (and run its prologue) while its
+// predecessor drains, and waits (griddepcontrol.wait) before it reads what
+// the predecessor wrote.
+struct PdlConfig {
+  cudaLaunchAttribute attr[1];
+  cudaLaunchConfig_t cfg;
+  PdlConfig(cudaStream_t stream, bool dependent) {
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg = cudaLaunchConfig_t{};
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = dependent ? 1 : 0;
+  }
+};
+
+}  // namespace
 
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events, bool with_prep) {
+                      cudaEvent_t const *events) {
+  const int G = n / C;
+  const int64_t se = (int64_t)s * e;
+  const int Gp = causal ? G : 1;
+  const TcLayout L = tc_layout(B, n, s, e, C, causal, false);
+  char *ws = static_cast<char *>(workspace);
+  __nv_bfloat16 *states = reinterpret_cast<__nv_bfloat16 *>(ws + L.states);
+  __nv_bfloat16 *prefix = reinterpret_cast<__nv_bfloat16 *>(ws + L.prefix);
+  __nv_bfloat16 *trows = reinterpret_cast<__nv_bfloat16 *>(ws + L.trows);
+  unsigned int *sched = reinterpret_cast<unsigned int *>(ws + L.sched);
+  const uint64_t rows = (uint64_t)B * n;
+  const int64_t plane = (int64_t)rows * s;  // elements of one T-row plane
+
+  // state kernel: Z keys and V slices as one 3-D box each; fused kernel: 3-D
+  // boxes of 128 rows x two 64-column blocks (32 KB) for every operand
+  CUtensorMap mZ64, mZ128, mZ3, mV3p, mSt, mT0, mT1, mT2, mV, mS;
+  if (!make_map_bf16(&mZ64, Z, s, rows, 64, 64) || !make_map_bf16(&mZ128, Z, s, rows, 64, 128) ||
+      !make_map3_bf16(&mZ3, Z, s, rows, 64, 2) || !make_map3_bf16(&mV3p, V, e, rows, 64, 4) ||
+      !make_map_bf16(&mSt, states, e, (uint64_t)B * G * s, 64, 128) ||
+      !make_map3_bf16(&mT0, trows, s, rows, 128, 2) ||
+      !make_map3_bf16(&mT1, trows + plane, s, rows, 128, 2) ||
+      !make_map3_bf16(&mT2, trows + 2 * plane, s, rows, 128, 2) ||
+      !make_map3_bf16(&mV, V, e, rows, 128, 2) ||
+      !make_map3_bf16(&mS, prefix, e, (uint64_t)B * Gp * s, 128, 2))
+    return 2;
+
+  static OncePerDevice attrs;
+  if (!attrs.run([] {
+        return cudaFuncSetAttribute(tc_chunk_prep<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PREP_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_prep<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PREP_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)FUSED_SMEM) == cudaSuccess;
+      }))
+    return 1;
+  if (!record_event(events, 0, stream)) return 1;
+  // sched[0]: work counter of the state kernel; sched[1]: of the fused kernel
+  if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
+  const int sms = num_sms();
+  const bool no_global = var.lin_norm == kLinNormNone;
+  int ev = 1;
+  if (!no_global) {
+    // chunk states T3^T V and the rows T0, T1, T2 (the prep kernel with state
+    // units only)
+    const int n_state = B * G * (e / E_TILE);
+    auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
+    prep<<<n_state < sms ? n_state : sms, PREP_THREADS, PREP_SMEM, stream>>>(
+        mZ64, mZ128, mZ3, mV3p, mSt, mSt, gamma, beta, nullptr, trows, plane, sched, n, e, C, G,
+        causal, n_state, 0, var.quad_a);
+    if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
+    // the prefix (or total) of the states over chunks, a programmatic
+    // dependent of the state kernel
+    PdlConfig sc(stream, true);
+    const int64_t lanes = (int64_t)B * se / 8;
+    // long chunk axes: the segmented scan (64 column groups x 4 segments a block)
+    const bool seg = G >= kScanSegMinG;
+    sc.cfg.gridDim = dim3((unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
+    sc.cfg.blockDim = dim3(256);
+    sc.cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&sc.cfg, pick_scan(var, seg), (const __nv_bfloat16 *)states, prefix,
+                           B, G, se, 1.0f / (float)n, causal, C) != cudaSuccess ||
+        !record_event(events, ev++, stream))
+      return 1;
+  } else {
+    // without a global term there are no chunk states: the T0 and T1 rows only
+    const int64_t n_vec = plane / 8;
+    tc_affine_rows<<<(unsigned)((n_vec + 255) / 256), 256, 0, stream>>>(
+        static_cast<const __nv_bfloat16 *>(Z), gamma, beta, trows, plane, n_vec);
+    if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
+  }
+  const FusedGrid fg = fused_grid(B, n, e, C, causal, sms);
+  PdlConfig fc(stream, true);
+  fc.cfg.gridDim = dim3(fg.n_units < sms ? fg.n_units : sms);
+  fc.cfg.blockDim = dim3(FUSED_THREADS);
+  fc.cfg.dynamicSmemBytes = FUSED_SMEM;
+  if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_fused, mT0, mT1, mT2, mV, mS,
+                         static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
+                         sched + 1, fg, e, no_global ? 0 : 1, var.quad_a) != cudaSuccess ||
+      !record_event(events, ev++, stream))
+    return 1;
+  return 0;
+}
+
+int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
+                                   const float *gamma, const float *beta, void *O, int B, int n,
+                                   int s, int e, int C, int causal, const Variant &var,
+                                   void *workspace, cudaStream_t stream, bool with_states) {
   const int G = n / C;
   const int R = C / ROW_TILE;
   const int64_t se = (int64_t)s * e;
   const int Gp = causal ? G : 1;
-  const WorkspaceLayout L = workspace_layout(B, n, s, e, C, causal);
+  const TcLayout L = tc_layout(B, n, s, e, C, causal, true);
   char *ws = static_cast<char *>(workspace);
   __nv_bfloat16 *states = reinterpret_cast<__nv_bfloat16 *>(ws + L.states);
   __nv_bfloat16 *prefix = reinterpret_cast<__nv_bfloat16 *>(ws + L.prefix);
@@ -118,10 +285,10 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   void *t2 = ws + L.lin_q;
   unsigned int *sched = reinterpret_cast<unsigned int *>(ws + L.sched);
 
-  CUtensorMap mZ64, mZ128, mVs, mSt, mPw, mT2, mV, mS, mU, mO;
+  CUtensorMap mZ64, mZ128, mZ3, mV3p, mSt, mPw, mT2, mV, mS, mU, mO;
   const uint64_t rows = (uint64_t)B * n;
   if (!make_map_bf16(&mZ64, Z, s, rows, 64, 64) || !make_map_bf16(&mZ128, Z, s, rows, 64, 128) ||
-      !make_map_bf16(&mVs, V, e, rows, 64, 64) ||
+      !make_map3_bf16(&mZ3, Z, s, rows, 64, 2) || !make_map3_bf16(&mV3p, V, e, rows, 64, 4) ||
       !make_map_bf16(&mSt, states, e, (uint64_t)B * G * s, 64, 128) ||
       !make_map_bf16(&mPw, pw, C, rows, 64, 128) || !make_map_bf16(&mT2, t2, s, rows, 64, 128) ||
       !make_map_bf16(&mV, V, e, rows, 64, 64) ||
@@ -141,58 +308,43 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                                     (int)AT_SMEM) == cudaSuccess;
       }))
     return 1;
-  if (!record_event(events, 0, stream)) return 1;
   // sched[0]: work counter of tc_chunk_prep; sched[1]: of tc_chunk_attn
   if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
   // without a global term (FMCA_LIN_NORM_NONE) there are no chunk states, the
   // scan has nothing to do and the attention units have no lin_q items
   const bool no_global = var.lin_norm == kLinNormNone;
-  const int n_state = no_global ? 0 : B * G * (e / E_TILE);
+  const int n_state = (no_global || !with_states) ? 0 : B * G * (e / E_TILE);
   const int n_score = B * G * score_units_per_chunk(C, causal);
   const int n_prep = n_state + n_score;
+  const int sms = num_sms();
   auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
-  if (with_prep) {
-    prep<<<n_prep < num_sms() ? n_prep : num_sms(), PREP_THREADS, PREP_SMEM, stream>>>(
-        mZ64, mZ128, mVs, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2), sched, n,
-        e, C, G, causal, n_state, n_score, var.quad_a);
-    if (cudaGetLastError() != cudaSuccess || !record_event(events, 1, stream)) return 1;
+  prep<<<n_prep < sms ? n_prep : sms, PREP_THREADS, PREP_SMEM, stream>>>(
+      mZ64, mZ128, mZ3, mV3p, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2),
+      nullptr, 0, sched, n, e, C, G, causal, n_state, n_score, var.quad_a);
+  if (cudaGetLastError() != cudaSuccess) return 1;
+  // The scan and the attention kernel are programmatic dependents of the
+  // kernel before them.  The attention kernel reads the relu^2 weights and
+  // lin_q rows before its griddepcontrol.wait (which guards only the prefix):
+  // that is safe behind the scan (which waits for prep before it lets the
+  // attention kernel launch), so without the scan it is an ordinary launch.
+  if (with_states) {
+    PdlConfig sc(stream, true);
+    const int64_t lanes = (int64_t)B * se / 8;
+    const bool seg = !no_global && G >= kScanSegMinG;
+    sc.cfg.gridDim = dim3(no_global ? 1u : (unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
+    sc.cfg.blockDim = dim3(256);
+    sc.cfg.dynamicSmemBytes = 0;
+    if (cudaLaunchKernelEx(&sc.cfg, pick_scan(var, seg), (const __nv_bfloat16 *)states, prefix,
+                           B, G, se, 1.0f / (float)n, causal, C) != cudaSuccess)
+      return 1;
   }
-  // The scan and the attention kernel are launched as programmatic dependents
-  // of the kernel before them: each may start launching (and run its
-  // prologue) while its predecessor drains, and waits (griddepcontrol.wait)
-  // for it to complete before reading what it wrote.
-  cudaLaunchAttribute pdl[1];
-  pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  pdl[0].val.programmaticStreamSerializationAllowed = 1;
-  cudaLaunchConfig_t cfg = {};
-  cfg.stream = stream;
-  cfg.attrs = pdl;
-  cfg.numAttrs = 1;
-  const int64_t lanes = (int64_t)B * se / 8;
-  // long chunk axes: the segmented scan (64 column groups x 4 segments a block)
-  const bool seg = !no_global && G >= kScanSegMinG;
-  cfg.gridDim = dim3(no_global ? 1u : (unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
-  cfg.blockDim = dim3(256);
-  cfg.dynamicSmemBytes = 0;
-  auto *scan = seg ? (var.lin_norm == kLinNormSummed     ? tc_state_scan_seg<kLinNormSummed>
-                      : var.lin_norm == kLinNormPosition ? tc_state_scan_seg<kLinNormPosition>
-                                                         : tc_state_scan_seg<kLinNormN>)
-               : var.lin_norm == kLinNormSummed   ? tc_state_scan<kLinNormSummed>
-               : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
-               : no_global                        ? tc_state_scan<kLinNormNone>
-                                                  : tc_state_scan<kLinNormN>;
-  if (with_prep && (cudaLaunchKernelEx(&cfg, scan, (const __nv_bfloat16 *)states, prefix, B, G,
-                                       se, 1.0f / (float)n, causal, C) != cudaSuccess ||
-                    !record_event(events, 2, stream)))
-    return 1;
   const int n_units = B * G * R * (e / E_TILE);
-  cfg.gridDim = dim3(n_units < num_sms() ? n_units : num_sms());
-  cfg.blockDim = dim3(AT_THREADS);
-  cfg.dynamicSmemBytes = AT_SMEM;
-  if (cudaLaunchKernelEx(&cfg, tc_chunk_attn, mPw, mT2, mV,
-                         mS, mU, mO, sched + 1, n, e, C, G,
-                         causal, n_units, no_global ? 0 : S_DIM / KEY_STAGE) != cudaSuccess ||
-      !record_event(events, 3, stream))
+  PdlConfig ac(stream, with_states);
+  ac.cfg.gridDim = dim3(n_units < sms ? n_units : sms);
+  ac.cfg.blockDim = dim3(AT_THREADS);
+  ac.cfg.dynamicSmemBytes = AT_SMEM;
+  if (cudaLaunchKernelEx(&ac.cfg, tc_chunk_attn, mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C, G,
+                         causal, n_units, no_global ? 0 : S_DIM / KEY_STAGE) != cudaSuccess)
     return 1;
   return 0;
 }

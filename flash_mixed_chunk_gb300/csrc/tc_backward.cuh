@@ -119,7 +119,7 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
                        float *dgamma, float *dbeta, int B, int n, int s, int e, int C, int causal,
                        const Variant &var, void *workspace, cudaStream_t stream, bool saved) {
   const TcBackwardLayout L = tc_backward_layout(B, n, s, e, C, causal);
-  const WorkspaceLayout FL = workspace_layout(B, n, s, e, C, causal);
+  const TcLayout FL = tc_layout(B, n, s, e, C, causal, true);
   char *ws = static_cast<char *>(workspace);
   typedef __nv_bfloat16 bf16;
   auto at = [&](size_t off) { return reinterpret_cast<bf16 *>(ws + off); };
@@ -132,10 +132,10 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
   const int G = n / C, Gp = causal ? G : 1, BG = B * G;
   const uint64_t rows = (uint64_t)B * n;
   const bool glob = var.lin_norm != kLinNormNone;
-  // dU = dO * (quad + glob), and the forward workspace (kept from the forward
-  // pass when `saved`: then only the output kernel runs, fed dO)
-  if (launch_tc_forward(Z, V, dO, gamma, beta, dU, B, n, s, e, C, causal, var, ws + L.fwd,
-                        stream, nullptr, !saved) != 0)
+  // dU = dO * (quad + glob), and the forward workspace (with `saved`, the
+  // chunk states and prefix are the ones the forward pass left there)
+  if (launch_tc_forward_materialised(Z, V, dO, gamma, beta, dU, B, n, s, e, C, causal, var,
+                                     ws + L.fwd, stream, !saved) != 0)
     return 1;
   const int64_t ne8 = (int64_t)rows * e / 8, ns8 = (int64_t)rows * s / 8;
   if (launch_dependent(tcb_gate_dy, dim3(blocks_for(ne8)), dim3(256), 0, stream,

@@ -120,12 +120,14 @@ template <bool BY_POSITION>
 __global__ void __launch_bounds__(PREP_THREADS, 1)
     tc_chunk_prep(const __grid_constant__ CUtensorMap mapZ64,   // Z [B*n][s], box {64, 64}
                   const __grid_constant__ CUtensorMap mapZ128,  // Z [B*n][s], box {64, 128}
-                  const __grid_constant__ CUtensorMap mapV,     // V [B*n][e], box {64, 64}
+                  const __grid_constant__ CUtensorMap mapZ3,    // Z 3-D, box {64, 64, 2}
+                  const __grid_constant__ CUtensorMap mapV3,    // V 3-D, box {64, 64, 4}
                   const __grid_constant__ CUtensorMap mapSt,    // states [B*G*s][e], box {64, 128}
                   const __grid_constant__ CUtensorMap mapPw,    // P [B*n][C], box {64, 128}
                   const float *__restrict__ gamma, const float *__restrict__ beta,
-                  __nv_bfloat16 *__restrict__ t2out, unsigned int *__restrict__ sched, int n,
-                  int e, int C, int G, int causal, int n_state, int n_score, float quad_a) {
+                  __nv_bfloat16 *__restrict__ t2out, __nv_bfloat16 *__restrict__ trows,
+                  int64_t rows_plane, unsigned int *__restrict__ sched, int n, int e, int C,
+                  int G, int causal, int n_state, int n_score, float quad_a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -169,7 +171,8 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
     if (lane == 0) {
       tma_prefetch_desc(&mapZ64);
       tma_prefetch_desc(&mapZ128);
-      tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapZ3);
+      tma_prefetch_desc(&mapV3);
       int it = 0;
       bool ok = true, ended = false;
       // Score units are dealt round-robin (CTA c takes c, c + grid, ...): they
@@ -227,11 +230,10 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
                                                  ? (uint32_t)(KEY_STAGE * S_DIM * 2)
                                                  : PR_SLOT);
           if (p.kind == KIND_STATE) {
+            // Z keys [64 rows][2 x 64 s] and V [64 rows][4 x 64 e], one 3-D box each
             const int y = (p.hb / G) * n + (p.hb % G) * C + k * KEY_STAGE;
-            tma_load_2d(sz, &mapZ64, &full[slot], 0, y);
-            tma_load_2d(sz + 8192, &mapZ64, &full[slot], 64, y);
-            for (int j = 0; j < 4; ++j)
-              tma_load_2d(sz + PR_ST_Z + j * 8192, &mapV, &full[slot], p.es * E_TILE + 64 * j, y);
+            tma_load_3d(sz, &mapZ3, &full[slot], 0, y, 0);
+            tma_load_3d(sz + PR_ST_Z, &mapV3, &full[slot], 0, y, p.es * (E_TILE / 64));
           } else {
             if (k == 0) {  // the query rows, for the whole block
               tma_load_2d(sz, &mapZ128, &full[slot], 0, p.row0);
@@ -354,11 +356,27 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
           decode_prep(got ? slot_unit[slot] : -1, n_state, n_score, n, e, C, G, causal);
       uint8_t *sz = smem + slot * PR_SLOT;
       if (pu.kind == KIND_STATE) {
-        // T3 in place over the Z part (atom a: 64 key rows)
+        // T3 in place over the Z part (atom a: 64 key rows); the units of the
+        // first e slice also write the rows T0, T1, T2 of these keys for the
+        // fused output kernel (trows: [3][B*n][s], if given)
+        const bool rows_out = trows != nullptr && pu.es == 0;
+        const int row_base = (pu.hb / G) * n + (pu.hb % G) * C + slot_item[slot] * KEY_STAGE;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 8192 + (rb + 8 * i) * 128 + p * 16);
-          *ptr = affine8(*ptr, g3, b3);
+          const int r = rb + 8 * i;
+          uint4 *ptr = reinterpret_cast<uint4 *>(sz + a * 8192 + r * 128 + p * 16);
+          const uint4 z = *ptr;
+          if (rows_out) {
+            __nv_bfloat16 *dst = trows + (size_t)(row_base + r) * S_DIM + cl;
+            *reinterpret_cast<uint4 *>(dst) = affine8(z, g0, b0);
+            *reinterpret_cast<uint4 *>(dst + rows_plane) = affine8(z, g1, b1);
+            if (BY_POSITION)  // row t of its sequence carries 1/(t+1)
+              *reinterpret_cast<uint4 *>(dst + 2 * rows_plane) =
+                  affine8_scaled(z, g2, b2, 1.0f / (float)((row_base + r) % n + 1));
+            else
+              *reinterpret_cast<uint4 *>(dst + 2 * rows_plane) = affine8(z, g2, b2);
+          }
+          *ptr = affine8(z, g3, b3);
         }
         fence_proxy_async_smem();
       } else if (pu.kind == KIND_SCORE) {
@@ -400,7 +418,7 @@ __global__ void __launch_bounds__(PREP_THREADS, 1)
       if (mt == 0) mbar_arrive(&tready[slot]);
       __syncwarp();
     }
-  } else {
+  } else if (warp < 10) {
     // =========================== epilogue warps (128 threads)
     const int mt = threadIdx.x - 192;
     const int quad = warp & 3;

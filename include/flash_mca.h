@@ -85,8 +85,9 @@ typedef int32_t fmca_path;
 
 /*
  * Bytes of device workspace one flash_mca_forward call with these arguments
- * needs: the per-chunk linear-attention states and their prefix sums, and
- * (tensor-core path) the bf16 intra-chunk relu^2 weights and lin_q rows.
+ * needs, whichever path it takes: the per-chunk linear-attention states and
+ * their prefix sums (fp32 on the SIMT path; bf16 plus a few work counters and
+ * flags on the tensor-core path, whose relu^2 weights never leave the chip).
  * Returns 0 for arguments flash_mca_forward would reject.
  */
 size_t flash_mca_workspace_bytes(int B, int n, int s, int e, int C, int causal,
@@ -178,10 +179,11 @@ fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
  * first kernel and events[i] after kernel i (1-based), so `n_events` must be
  * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
  * stream it runs on.  `opts` as for flash_mca_forward_ex (NULL: defaults).
- * Kernel order: tensor-core path -- chunk preparation (states, relu^2
- * weights, lin_q rows; events[0] is recorded before the reset of its work
- * counters), state scan, chunk attention; SIMT path -- chunk states, state
- * scan, chunk output. */
+ * Kernel order: tensor-core path -- chunk states and the rows T0, T1, T2
+ * (events[0] is recorded before the reset of the work counters), state scan,
+ * fused chunk kernel (scores, relu^2 weights, both products and the gate);
+ * without a global term (FMCA_LIN_NORM_NONE) the rows T0, T1, then the fused
+ * kernel; SIMT path -- chunk states, state scan, chunk output. */
 fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     const float *gamma, const float *beta, void *O, int B,
                                     int n, int s, int e, int C, int causal,
@@ -261,15 +263,16 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
 
 /*
  * flash_mca_backward for training loops that keep the forward pass's
- * intermediates: the same gradients, but the relu^2 weights, lin_q rows and
- * scaled prefix are not recomputed.  `workspace` must hold what an earlier
+ * intermediates: the same gradients, but the chunk states and their scaled
+ * prefix are not recomputed.  `workspace` must hold what an earlier
  * flash_mca_forward (or _ex, FMCA_PATH_AUTO or FMCA_PATH_TCGEN05) left in it,
  * called with the same Z, V, U, gamma, beta, sizes and options and with this
  * workspace (sized by flash_mca_backward_workspace_bytes: the forward pass
  * uses its first flash_mca_workspace_bytes), with nothing written to it
- * since; the library cannot check this.  Only the output kernel of the
- * forward pass runs again (fed dO, for dU).  Shapes of FMCA_PATH_TCGEN05 with
- * FMCA_BF16 only; others return FMCA_ERR_UNSUPPORTED.
+ * since; the library cannot check this.  The relu^2 weights and lin_q rows
+ * (which the forward pass keeps on chip) and the output kernel (fed dO, for
+ * dU) run again.  Shapes of FMCA_PATH_TCGEN05 with FMCA_BF16 only; others
+ * return FMCA_ERR_UNSUPPORTED.
  */
 /* Number of kernels one flash_mca_backward (saved = 0) or
  * flash_mca_backward_saved (saved = 1) call launches for these arguments (0
@@ -310,9 +313,14 @@ fmca_status flash_mca_gau_output(const void *Y, const void *Wo_t, void *Out, int
 int flash_mca_auto_path(int B, int n, int s, int e, int C, int causal, fmca_dtype dtype);
 
 /* Number of kernel launches one flash_mca_forward call queues for these
- * arguments (0 when they would be rejected). */
+ * arguments (0 when they would be rejected); memsets are not counted. */
 int flash_mca_launch_count(int B, int n, int s, int e, int C, int causal,
                            fmca_dtype dtype, fmca_path path);
+/* The same for flash_mca_forward_ex with options `opts` (NULL: the defaults):
+ * without a global term (FMCA_LIN_NORM_NONE) the tensor-core path launches
+ * fewer kernels.  flash_mca_forward_timed takes this count + 1 events. */
+int flash_mca_launch_count_ex(int B, int n, int s, int e, int C, int causal,
+                              fmca_dtype dtype, fmca_path path, const fmca_options *opts);
 
 /*
  * End-to-end variant on HOST buffers: copies Z, V, U, gamma, beta from host
@@ -343,15 +351,20 @@ fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *h
  *
  * The scratch is one array of FMCA_NOALLOC_SCRATCH_BYTES compiled into the
  * library; a GPU keeps it until the process exits once this entry point has
- * run there.  Problems whose workspace (flash_mca_workspace_bytes) exceeds it
- * are rejected with FMCA_ERR_WORKSPACE; the long_causal-sized problems (B=2,
- * n=8192, e=1536) need more and must use flash_mca_forward.  Only the
- * tensor-core path is available (FMCA_BF16, s == 128, C in {128, 256},
- * e % 256 == 0); other shapes return FMCA_ERR_UNSUPPORTED.
+ * run there (with eager module loading, CUDA_MODULE_LOADING=EAGER, every GPU
+ * the process creates a context on holds it, whichever entry points run).
+ * Problems whose tensor-core scratch (the bf16 chunk states and their prefix
+ * sums, 2 B (G + Gp) s e bytes, the bf16 rows T0, T1, T2, 6 B n s bytes, and
+ * a few KB; Gp = G causal or 1) exceeds it are rejected with
+ * FMCA_ERR_WORKSPACE: B=2, n=8192, C=256, e=1536 fits (62.9 MB); B=1,
+ * n=32768, C=256, e=2048 (159 MB) must use flash_mca_forward.  Only the tensor-core path is available (FMCA_BF16,
+ * s == 128, C % 128 == 0, e % 256 == 0); other shapes return
+ * FMCA_ERR_UNSUPPORTED.
  *
  * The first call on a device looks up the array's device address on that
  * device (the current one); make that first call before any CUDA stream
- * capture begins.  All calls on a device share the array: calls whose work
+ * capture begins.  The address is looked up again when the device's primary
+ * context has changed since (after cudaDeviceReset).  All calls on a device share the array: calls whose work
  * overlaps on the GPU (different streams) race and give wrong results; calls
  * queued on one stream are ordered.  The call allocates nothing, queues its
  * kernels on `stream` and does not wait.  Arguments as for flash_mca_forward.

@@ -55,12 +55,17 @@ def test_status_strings():
                                               (1, 256, 32, 64, 64, 1),
                                               (3, 96, 48, 80, 32, 0)])
 def test_workspace_bytes_formula(B, n, s, e, C, causal):
+    """Enough for either path: fp32 states and prefix (SIMT) or bf16 states and
+    prefix with the work counters, per-chunk flags and the bf16 rows T0, T1, T2
+    (tensor cores); no [B*n][C] buffer of relu^2 weights on either."""
     a = lambda x: (x + 255) // 256 * 256
     G = n // C
-    want = (a(4 * B * G * s * e) + a(4 * B * (G if causal else 1) * s * e)
-            + a(2 * B * n * C) + a(2 * B * n * s) + 256)
+    Gp = G if causal else 1
+    simt = a(4 * B * G * s * e) + a(4 * B * Gp * s * e)
+    tc = (a(2 * B * G * s * e) + a(2 * B * Gp * s * e) + 256
+          + a(3 * 2 * B * n * s))  # + the bf16 rows T0, T1, T2
     for dt in (fm.FMCA_F32, fm.FMCA_BF16):
-        assert fm.flash_mca_workspace_bytes(B, n, s, e, C, causal, dt) == want
+        assert fm.flash_mca_workspace_bytes(B, n, s, e, C, causal, dt) == max(simt, tc)
 
 
 def test_workspace_bytes_zero_for_rejected_shapes():
@@ -86,7 +91,16 @@ def test_auto_path_choice():
 
 def test_launch_counts():
     bf = fm.FMCA_BF16
+    # states and T rows, the scan of the states, the fused chunk kernel
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 3
+    assert fm.flash_mca_launch_count(4, 4096, 128, 1536, 256, 0, bf) == 3
+    # without a global term: the T0 / T1 rows and the fused chunk kernel
+    assert fm.flash_mca_launch_count(8, 1024, 128, 1536, 1024, 1, bf,
+                                     lin_norm=fm.FMCA_LIN_NORM_NONE) == 2
+    assert fm.flash_mca_launch_count(8, 1024, 128, 1536, 1024, 1, bf, fm.FMCA_PATH_SIMT,
+                                     lin_norm=fm.FMCA_LIN_NORM_NONE) == 3
+    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf,
+                                     lin_norm=fm.FMCA_LIN_NORM_POSITION) == 3
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
     assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
     assert fm.flash_mca_launch_count(1, 500, 128, 256, 64, 1, bf) == 0
@@ -301,11 +315,12 @@ def test_backward_saved_validation():
 def test_backward_launch_count():
     bf, f32 = fm.FMCA_BF16, fm.FMCA_F32
     cnt = fm.flash_mca_backward_launch_count
-    # tensor cores: forward kernels (3, or 1 when the forward's intermediates
-    # are kept), 2 elementwise, 3 product launches, the reverse scan (global
-    # term only), 2 for dZ / dgamma / dbeta
+    # tensor cores: forward kernels (3; 2 when the forward's chunk states and
+    # prefix are kept: the relu^2 weights and the output kernel), 2
+    # elementwise, 3 product launches, the reverse scan (global term only), 2
+    # for dZ / dgamma / dbeta
     assert cnt(2, 1024, 128, 512, 256, True, bf) == 11
-    assert cnt(2, 1024, 128, 512, 256, True, bf, saved=True) == 9
+    assert cnt(2, 1024, 128, 512, 256, True, bf, saved=True) == 10
     assert cnt(2, 1024, 128, 512, 256, True, bf, lin_norm=fm.FMCA_LIN_NORM_NONE) == 10
     # CUDA cores
     assert cnt(2, 1024, 128, 512, 256, True, f32) == 12

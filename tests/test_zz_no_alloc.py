@@ -4,9 +4,11 @@ memory, or code that must not risk an out-of-memory failure), with its scratch
 in a fixed array inside the library.
 
 The GPU test calls the new entry point through the C ABI twice in a row, on
-different inputs, and compares each result with the regular entry point
-(flash_mca_forward with a caller workspace) under the bf16 parity bar used by
-every other test.  This file sorts last so that a run stopping at its first
+different inputs, then once more with another layout of the scratch (another
+batch size, e and mode, so the states and prefix sit at other offsets over
+what the earlier calls left), and compares each result with the regular entry
+point (flash_mca_forward with a caller workspace) under the bf16 parity bar
+used by every other test.  This file sorts last so that a run stopping at its first
 failure has already run every other test; it also passes on its own in a fresh
 process.
 """
@@ -30,10 +32,11 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
     """Host-side checks only: no GPU needed, nothing is queued."""
     m = fm()
     P = 0x7F0000000000
-    # long causal workload: its workspace exceeds the fixed scratch
-    B, n, C, s, e = 2, 8192, 256, 128, 1536
-    assert m.flash_mca_workspace_bytes(B, n, s, e, C, True, m.FMCA_BF16) > \
-        m.FMCA_NOALLOC_SCRATCH_BYTES
+    # the very long causal workload: its bf16 states and prefix (2 x 67 MB)
+    # exceed the fixed scratch
+    B, n, C, s, e = 1, 32768, 256, 128, 2048
+    G = n // C
+    assert 2 * 2 * B * G * s * e > m.FMCA_NOALLOC_SCRATCH_BYTES
     st = m.lib.flash_mca_forward_noalloc(P, P + (1 << 30), P + (2 << 30), P + (3 << 30),
                                          P + (3 << 30) + 4096, P + (4 << 30), B, n, s, e, C, 1,
                                          m.FMCA_BF16, None)
@@ -51,11 +54,14 @@ def test_noalloc_rejects_problems_larger_than_its_scratch():
 def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
     m = fm()
     dev = torch.device("cuda:0")
-    B, n, C, s, e, causal = 2, 1024, 256, 128, 512, True
-    assert m.flash_mca_workspace_bytes(B, n, s, e, C, causal, m.FMCA_BF16) <= \
-        m.FMCA_NOALLOC_SCRATCH_BYTES
+    C, s = 256, 128
     stream = torch.cuda.current_stream(dev)
-    for seed in (71, 72):  # two calls in a row on different inputs
+    # two calls in a row on different inputs, then a third whose states and
+    # prefix lie elsewhere in the scratch
+    for seed, B, n, e, causal in ((71, 2, 1024, 512, True), (72, 2, 1024, 512, True),
+                                  (73, 3, 2048, 768, False)):
+        assert m.flash_mca_workspace_bytes(B, n, s, e, C, causal, m.FMCA_BF16) <= \
+            m.FMCA_NOALLOC_SCRATCH_BYTES
         Z, V, U, gamma, beta = (t.to(dev) for t in
                                 mca_inputs.make_inputs(B, n, s, e, seed, torch.bfloat16))
         O_ref = torch.empty((B, n, e), dtype=torch.bfloat16, device=dev)
