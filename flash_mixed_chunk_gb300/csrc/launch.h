@@ -45,7 +45,7 @@ struct TcLayout {
   size_t states, prefix, sched, trows, scores, lin_q, total;
 };
 inline size_t tc_sched_bytes() {
-  // the two work counters (of the state kernel and the chunk kernel)
+  // the work counters
   return 256;
 }
 inline TcLayout tc_layout(int B, int n, int s, int e, int C, int causal, bool materialised) {

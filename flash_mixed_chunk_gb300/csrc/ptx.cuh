@@ -150,6 +150,20 @@ __device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap *map, const 
       "r"(x), "r"(y), "r"(z), "r"(smem_u32(src)), "l"(policy)
       : "memory");
 }
+// Untiled bulk copies (both addresses 16-byte aligned, size % 16 == 0).
+__device__ __forceinline__ void bulk_load(void *dst, const void *gsrc, uint32_t bytes,
+                                          uint64_t *bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(gsrc), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_store(void *gdst, const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(gdst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -184,6 +198,34 @@ __device__ __forceinline__ void griddep_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+
+// GPU-scope counters between CTAs (and grids): the writer makes its data
+// visible, then adds with release semantics; a reader polls with acquire
+// loads before it reads the data.
+__device__ __forceinline__ unsigned int ld_acquire_gpu(const unsigned int *p) {
+  unsigned int v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_release_add_gpu(unsigned int *p, unsigned int v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA, bulk copy) ones, in either direction.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// Bounded wait until *p >= want (acquire); false if the limit ran out.
+__device__ __forceinline__ bool wait_count_geq(const unsigned int *p, unsigned int want,
+                                               uint64_t limit_ns) {
+  if (ld_acquire_gpu(p) >= want) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (ld_acquire_gpu(p) < want) {
+    __nanosleep(128);
+    if (globaltimer_ns() - t0 > limit_ns) return false;
+  }
+  return true;
+}
 
 // Drop a 128-byte line from L2 without writing it back (its contents become
 // undefined); for scratch that no one reads again.

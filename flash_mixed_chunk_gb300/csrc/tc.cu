@@ -142,22 +142,17 @@ ScanKernel pick_scan(const Variant &var, bool seg) {
                                             : tc_state_scan<kLinNormN>;
 }
 
-// Units of the fused kernel: every (batch x chunk, row tile) split into e
-// groups of consecutive 128-column e tiles, as few groups as give about two
-// units per SM (a unit computes its relu^2 weights once for all its e tiles).
-FusedGrid fused_grid(int B, int n, int e, int C, int causal, int sms) {
+// Tiles of the fused kernel: (batch x chunk, row tile, e tile).
+FusedGrid fused_grid(int B, int n, int e, int C, int causal, bool lin) {
   FusedGrid g;
   g.n = n;
   g.C = C;
   g.G = n / C;
   g.causal = causal;
+  g.lin = lin ? 1 : 0;
+  g.R = C / ROW_TILE;
   g.n_et = e / FU_ET;
-  const int row_tiles = B * g.G * (C / ROW_TILE);
-  int want = (2 * sms + row_tiles - 1) / row_tiles;
-  want = want < 1 ? 1 : (want > g.n_et ? g.n_et : want);
-  g.eg_tiles = (g.n_et + want - 1) / want;
-  g.n_eg = (g.n_et + g.eg_tiles - 1) / g.eg_tiles;
-  g.n_units = row_tiles * g.n_eg;
+  g.n_tiles = B * g.G * g.R * g.n_et;
   return g;
 }
 
@@ -185,7 +180,6 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                       const Variant &var, void *workspace, cudaStream_t stream,
                       cudaEvent_t const *events) {
   const int G = n / C;
-  const int64_t se = (int64_t)s * e;
   const int Gp = causal ? G : 1;
   const TcLayout L = tc_layout(B, n, s, e, C, causal, false);
   char *ws = static_cast<char *>(workspace);
@@ -222,10 +216,12 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
       }))
     return 1;
   if (!record_event(events, 0, stream)) return 1;
-  // sched[0]: work counter of the state kernel; sched[1]: of the fused kernel
-  if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
   const int sms = num_sms();
   const bool no_global = var.lin_norm == kLinNormNone;
+  // sched[0]: work counter of the state kernel (the fused kernel's CTAs take
+  // fixed tile ranges)
+  if (!no_global && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
+    return 1;
   int ev = 1;
   if (!no_global) {
     // chunk states T3^T V and the rows T0, T1, T2 (the prep kernel with state
@@ -239,9 +235,11 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     // the prefix (or total) of the states over chunks, a programmatic
     // dependent of the state kernel
     PdlConfig sc(stream, true);
-    const int64_t lanes = (int64_t)B * se / 8;
-    // long chunk axes: the segmented scan (64 column groups x 4 segments a block)
+    // long chunk axes: the segmented scan (64 column groups of 8 x 4 segments
+    // a block); otherwise one thread per kScanCols columns
     const bool seg = G >= kScanSegMinG;
+    const int64_t se = (int64_t)s * e;
+    const int64_t lanes = (int64_t)B * se / (seg ? 8 : kScanCols);
     sc.cfg.gridDim = dim3((unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
     sc.cfg.blockDim = dim3(256);
     sc.cfg.dynamicSmemBytes = 0;
@@ -256,14 +254,14 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
         static_cast<const __nv_bfloat16 *>(Z), gamma, beta, trows, plane, n_vec);
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
   }
-  const FusedGrid fg = fused_grid(B, n, e, C, causal, sms);
+  const FusedGrid fg = fused_grid(B, n, e, C, causal, !no_global);
   PdlConfig fc(stream, true);
-  fc.cfg.gridDim = dim3(fg.n_units < sms ? fg.n_units : sms);
+  fc.cfg.gridDim = dim3(fg.n_tiles < sms ? fg.n_tiles : sms);
   fc.cfg.blockDim = dim3(FUSED_THREADS);
   fc.cfg.dynamicSmemBytes = FUSED_SMEM;
   if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_fused, mT0, mT1, mT2, mV, mS,
                          static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
-                         sched + 1, fg, e, no_global ? 0 : 1, var.quad_a) != cudaSuccess ||
+                         fg, e, var.quad_a) != cudaSuccess ||
       !record_event(events, ev++, stream))
     return 1;
   return 0;
@@ -329,8 +327,8 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
   // attention kernel launch), so without the scan it is an ordinary launch.
   if (with_states) {
     PdlConfig sc(stream, true);
-    const int64_t lanes = (int64_t)B * se / 8;
     const bool seg = !no_global && G >= kScanSegMinG;
+    const int64_t lanes = (int64_t)B * se / (seg ? 8 : kScanCols);
     sc.cfg.gridDim = dim3(no_global ? 1u : (unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
     sc.cfg.blockDim = dim3(256);
     sc.cfg.dynamicSmemBytes = 0;

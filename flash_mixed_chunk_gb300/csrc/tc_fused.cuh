@@ -7,8 +7,12 @@
 // affine maps of "Weak Attention") come as bf16 rows from the state kernel.
 // Included by tc.cu.
 //
-// Persistent kernel, one CTA per SM, units from a global counter taken last
-// chunk first.  A unit is (chunk, 128-row tile, group of 128-column e tiles):
+// Persistent kernel, one CTA per SM.  The (chunk, 128-row tile, 128-column
+// e tile) tiles, ordered chunk, row tile, e tile, are split into one
+// contiguous range per CTA of about equal cost (bytes streamed: V and, where
+// the weights are recomputed, T1 per key stage; U, O and the prefix), so
+// every CTA finishes at about the same time with one or two units.  A unit
+// is the run of one row tile's e tiles in a CTA's range:
 //   S_k = T0 T1_k^T        64 keys per stage k, M = 128, N = 64, K = s = 128,
 //                          into one of two TMEM S slots
 //   P_k = relu(S_k a)^2    masked (key > query -> 0) in registers by four
@@ -64,6 +68,7 @@ constexpr int FUSED_THREADS = 384;
 static_assert(FUSED_SMEM + 1024 <= 232448, "tc_chunk_fused exceeds 227 KB of shared memory");
 
 struct FusedUnit {
+  int g;      // chunk within its sequence
   int row0;   // first token row of the tile in [B*n]
   int crow;   // first token row of its chunk
   int prow;   // first prefix row of its chunk in [B*Gp*s]
@@ -73,36 +78,65 @@ struct FusedUnit {
   int nkv;    // 64-key stages of the row tile (even)
 };
 
-// The unit numbering: units are (batch x chunk, row tile, e group); an e
-// group is eg_tiles consecutive 128-column e tiles (the last may be shorter).
+// The tiles: t = (bg * R + rt) * n_et + et for sequence-chunk bg (of B * G),
+// row tile rt (of R = C / 128) and e tile et (of n_et = e / 128).
 struct FusedGrid {
-  int n, C, G, causal, n_units, n_eg, eg_tiles, n_et;
+  int n, C, G, causal, lin, R, n_et, n_tiles;
 };
 
-__device__ __forceinline__ FusedUnit decode_fused(int u, const FusedGrid &g) {
-  const int R = g.C / ROW_TILE;
-  int rt, t;
-  if (g.causal && R >= 4) {
-    // long causal chunks (FLASH-Quad): row tile rt reads 2 (rt + 1) key
-    // stages; units row tile major, taken from the top: longest first
-    const int per_rt = g.n_units / R;
-    rt = u / per_rt;
-    t = u % per_rt;
-  } else {
-    rt = u % R;  // the row tiles of one chunk and e group are adjacent (V reuse in L2)
-    t = u / R;
+// 64-key stages of row tile rt
+__device__ __forceinline__ int fused_nkv(int rt, const FusedGrid &g) {
+  return (g.causal ? (rt + 1) * ROW_TILE : g.C) / KEY_STAGE;
+}
+// the cost of one tile of row tile rt, in KB streamed: 16 per key stage of V,
+// 16 more of T1 where the relu^2 weights are recomputed per e tile (more than
+// FU_PSLOTS stages), 32 each of U and O, 32 of the prefix
+__device__ __forceinline__ int64_t fused_tile_cost(int rt, const FusedGrid &g) {
+  const int nkv = fused_nkv(rt, g);
+  return (int64_t)nkv * (nkv <= FU_PSLOTS ? 16 : 32) + 64 + (g.lin ? 32 : 0);
+}
+// the tile that holds cost position x (the tiles laid end to end in order)
+__device__ __forceinline__ int fused_tile_at(int64_t x, const FusedGrid &g) {
+  int64_t per_bg = 0;
+  for (int r = 0; r < g.R; ++r) per_bg += (int64_t)g.n_et * fused_tile_cost(r, g);
+  const int64_t bg = x / per_bg;
+  if (bg * g.R * g.n_et >= g.n_tiles) return g.n_tiles;
+  int64_t rem = x - bg * per_bg;
+  int rt = 0;
+  for (; rt < g.R - 1; ++rt) {
+    const int64_t w = (int64_t)g.n_et * fused_tile_cost(rt, g);
+    if (rem < w) break;
+    rem -= w;
   }
-  const int eg = t % g.n_eg;
-  const int bg = t / g.n_eg;
+  int et = (int)(rem / fused_tile_cost(rt, g));
+  if (et >= g.n_et) et = g.n_et - 1;
+  return (int)((bg * g.R + rt) * g.n_et + et);
+}
+// CTA c's tiles: [fused_range_start(c), fused_range_start(c + 1))
+__device__ __forceinline__ int fused_range_start(int c, int grid_size, const FusedGrid &g) {
+  if (c <= 0) return 0;
+  if (c >= grid_size) return g.n_tiles;
+  int64_t per_bg = 0;
+  for (int r = 0; r < g.R; ++r) per_bg += (int64_t)g.n_et * fused_tile_cost(r, g);
+  const int64_t total = per_bg * (g.n_tiles / (g.R * g.n_et));
+  return fused_tile_at(total * c / grid_size, g);
+}
+
+// The unit of net tiles from tile t (all of one row tile)
+__device__ __forceinline__ FusedUnit decode_fused(int t, int net, const FusedGrid &g) {
+  const int et = t % g.n_et;
+  const int rt = (t / g.n_et) % g.R;
+  const int bg = t / (g.n_et * g.R);
   const int b = bg / g.G, c = bg % g.G;
   FusedUnit f;
+  f.g = c;
   f.crow = b * g.n + c * g.C;
   f.row0 = f.crow + rt * ROW_TILE;
   f.prow = (g.causal ? bg : b) * S_DIM;
   f.rt = rt;
-  f.et0 = eg * g.eg_tiles;
-  f.net = min(g.eg_tiles, g.n_et - f.et0);
-  f.nkv = (g.causal ? (rt + 1) * ROW_TILE : g.C) / KEY_STAGE;
+  f.et0 = et;
+  f.net = net;
+  f.nkv = fused_nkv(rt, g);
   return f;
 }
 
@@ -121,8 +155,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                    const __grid_constant__ CUtensorMap mapS,   // prefix 3-D, box {64, 128, 2}
                    const __nv_bfloat16 *__restrict__ U,        // [B*n][e]
                    __nv_bfloat16 *__restrict__ O,              // [B*n][e]
-                   unsigned int *__restrict__ sched, FusedGrid grid, int e, int with_global,
-                   float quad_a) {
+                   FusedGrid grid, int e, float quad_a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -132,11 +165,11 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
   __shared__ __align__(8) uint64_t s_full[FU_SSLOTS], s_empty[FU_SSLOTS];
   __shared__ __align__(8) uint64_t p_full[FU_PSLOTS], p_empty[FU_PSLOTS];
   __shared__ __align__(8) uint64_t o_full[2], o_empty[2], mma_done;
-  __shared__ int uq_unit[FU_QUEUE];
+  __shared__ int uq_unit[FU_QUEUE], uq_net[FU_QUEUE];
   __shared__ uint32_t tmem_base;
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const bool lin = with_global != 0;
+  const bool lin = grid.lin != 0;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < FU_QUEUE; ++i) {
@@ -187,7 +220,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapS);
       int it = 0;
-      bool ok = true, rows_ready = false;
+      bool ok = true, rows_ready = false, prefix_ready = false;
       // one ring item: waits for its slot, then one 32 KB box
       auto issue = [&](const CUtensorMap *map, int y, int z) -> bool {
         const int slot = it % FU_RING;
@@ -200,28 +233,28 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         ++it;
         return true;
       };
-      // the next unit is fetched one unit ahead, so that the atomic's latency
-      // overlaps the current unit's copies
-      int u_next = (int)atomicAdd(sched, 1u);
+      // this CTA's tiles, one unit per row tile they touch
+      int t = fused_range_start((int)blockIdx.x, (int)gridDim.x, grid);
+      const int t_end = fused_range_start((int)blockIdx.x + 1, (int)gridDim.x, grid);
       for (int j = 0; ok; ++j) {
-        // last chunk first: the state kernel streamed V in chunk order, so the
-        // chunks it read last are the likeliest to still be in L2
-        const int u = u_next;
-        const int uu = u < grid.n_units ? grid.n_units - 1 - u : -1;
-        if (uu >= 0) u_next = (int)atomicAdd(sched, 1u);
+        const int uu = t < t_end ? t : -1;
+        const int et = t % grid.n_et;
+        const int net = uu >= 0 ? min(grid.n_et - et, t_end - t) : 0;
+        t += net;
         const int qs = j % FU_QUEUE;
         if (j >= FU_QUEUE && !mbar_wait(&uq_empty[qs], ((j / FU_QUEUE) - 1) & 1, kWaitLimitNs)) {
           record_timeout(600);
           break;
         }
         uq_unit[qs] = uu;
+        uq_net[qs] = net;
         mbar_arrive(&uq_full[qs]);
         if (uu < 0) break;
-        const FusedUnit f = decode_fused(uu, grid);
-        // the T rows and the prefix are written by the kernel before this one:
-        // wait for it once, before the first load of anything it wrote (V and
-        // U are inputs)
-        if (!rows_ready) {
+        const FusedUnit f = decode_fused(uu, net, grid);
+        // Without a global term the kernel before this one wrote the T rows.
+        // With one, the state kernel wrote them, and it had completed before
+        // the scan (which waits for it first) let this grid launch.
+        if (!lin && !rows_ready) {
           griddep_wait();
           rows_ready = true;
         }
@@ -255,6 +288,13 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             mbar_arrive_expect_tx(&b_full, FU_AB_BYTES);
             tma_load_3d(bbuf, &mapT2, &b_full, 0, f.row0, 0);
           }
+          // the prefix comes from the scan, the kernel before this one: wait
+          // for it once, before the first prefix load (the unit's rows,
+          // scores, weights and first products overlap the scan's tail)
+          if (!prefix_ready) {
+            griddep_wait();
+            prefix_ready = true;
+          }
           ok = issue(&mapS, f.prow, eb);  // prefix rows [0, s), e tile x
         }
       }
@@ -286,10 +326,10 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
           ok = false;
           break;
         }
-        const int u = uq_unit[qs];
+        const int u = uq_unit[qs], unet = uq_net[qs];
         mbar_arrive(&uq_empty[qs]);
         if (u < 0) break;
-        const FusedUnit f = decode_fused(u, grid);
+        const FusedUnit f = decode_fused(u, unet, grid);
         const bool res = p_resident(f);
         const int nkb = (f.nkv + FU_PSLOTS - 1) / FU_PSLOTS;
         if (!mbar_wait(&a_full, j & 1, kWaitLimitNs)) {
@@ -426,14 +466,14 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     for (int j = 0; ok; ++j) {
       const int qs = j % FU_QUEUE;
       const bool got = mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs);
-      const int u = got ? uq_unit[qs] : -1;
+      const int u = got ? uq_unit[qs] : -1, unet = got ? uq_net[qs] : 0;
       const bool more = named_bar_and(2, 128, u >= 0);
       if (mt == 0 && got) mbar_arrive(&uq_empty[qs]);
       if (!more) {
         if (!got && mt == 0) record_timeout(640);
         break;
       }
-      const FusedUnit f = decode_fused(u, grid);
+      const FusedUnit f = decode_fused(u, unet, grid);
       const bool res = p_resident(f);
       const int nkb = (f.nkv + FU_PSLOTS - 1) / FU_PSLOTS;
       const int qpos = f.rt * ROW_TILE + row;  // query position within the chunk
@@ -500,14 +540,14 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
     for (int j = 0; ok; ++j) {
       const int qs = j % FU_QUEUE;
       const bool got = mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs);
-      const int u = got ? uq_unit[qs] : -1;
+      const int u = got ? uq_unit[qs] : -1, unet = got ? uq_net[qs] : 0;
       const bool more = named_bar_and(3, 128, u >= 0);
       if (mt == 0 && got) mbar_arrive(&uq_empty[qs]);
       if (!more) {
         if (!got && mt == 0) record_timeout(650);
         break;
       }
-      const FusedUnit f = decode_fused(u, grid);
+      const FusedUnit f = decode_fused(u, unet, grid);
       const size_t roff = (size_t)(f.row0 + row) * (size_t)e;
       for (int x = 0; x < f.net && ok; ++x, ++oc) {
         const int ob = oc & 1;

@@ -14,9 +14,13 @@ namespace {
 // tc_state_scan: prefix (or total) over chunks of the bf16 states, in fp32,
 // scaled by the global-term divisor's inverse (1/n by default; 1/(g*C) for
 // causal chunk g with the tokens-summed divisor; 1 with the per-position
-// divisor, which the T2 rows carry instead) and rounded to bf16.  The thread count is a multiple of 32
-// for every shape this path takes (B * s * e / 8).
+// divisor, which the T2 rows carry instead) and rounded to bf16.  One thread
+// per 4 columns (8-byte accesses: more threads, so more loads in flight, for
+// the same bytes), the chunks of its column in rounds of kScanU loads; the
+// states are read once with evict-first loads.  The thread count is a
+// multiple of 32 for every shape this path takes (B * s * e / 4).
 // =====================================================================
+constexpr int kScanCols = 4;
 // LIN_NORM: the global-term divisor (kLinNorm*), one instantiation each, so
 // that the default one is the plain 1/n scan.
 template <int LIN_NORM>
@@ -28,61 +32,44 @@ __global__ void __launch_bounds__(256)
   griddep_wait();
   griddep_launch_dependents();
   if (LIN_NORM == kLinNormNone) return;  // no global term: nothing to sum
-  const int64_t per_b = se / 8;
+  const int64_t per_b = se / kScanCols;
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * per_b) return;
-  const int64_t b = t / per_b, x = (t % per_b) * 8;
+  const int64_t b = t / per_b, x = (t % per_b) * kScanCols;
   const __nv_bfloat16 *src = S + b * G * se + x;
   __nv_bfloat16 *dst = P + (causal ? b * G * se : b * se) + x;
-  float run[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) run[i] = 0.f;
+  float run[4] = {0.f, 0.f, 0.f, 0.f};
   const float keep = LIN_NORM == kLinNormPosition ? 1.0f : inv_n;  // all but summed+causal
-  constexpr int U = 8;
-  for (int g0 = 0; g0 < G; g0 += U) {
-    uint4 v[U];
+  constexpr int kScanU = 8;
+  for (int g0 = 0; g0 < G; g0 += kScanU) {
+    uint2 v[kScanU];
 #pragma unroll
-    for (int u = 0; u < U; ++u)
-      if (g0 + u < G) v[u] = __ldcs(reinterpret_cast<const uint4 *>(src + (int64_t)(g0 + u) * se));
+    for (int u = 0; u < kScanU; ++u)
+      if (g0 + u < G) v[u] = __ldcs(reinterpret_cast<const uint2 *>(src + (int64_t)(g0 + u) * se));
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
+    for (int u = 0; u < kScanU; ++u) {
       if (g0 + u < G) {
         if (causal) {
           const int g = g0 + u;
           const float f = LIN_NORM != kLinNormSummed ? keep
                           : (g > 0 ? 1.0f / ((float)g * (float)C) : 0.0f);
-          uint4 o;
+          uint2 o;
           o.x = pack_bf16x2(run[0] * f, run[1] * f);
           o.y = pack_bf16x2(run[2] * f, run[3] * f);
-          o.z = pack_bf16x2(run[4] * f, run[5] * f);
-          o.w = pack_bf16x2(run[6] * f, run[7] * f);
-          *reinterpret_cast<uint4 *>(dst + (int64_t)(g0 + u) * se) = o;
+          *reinterpret_cast<uint2 *>(dst + (int64_t)g * se) = o;
         }
-        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          run[2 * i] += bf16_lo(w[i]);
-          run[2 * i + 1] += bf16_hi(w[i]);
-        }
+        run[0] += bf16_lo(v[u].x);
+        run[1] += bf16_hi(v[u].x);
+        run[2] += bf16_lo(v[u].y);
+        run[3] += bf16_hi(v[u].y);
       }
-    }
-    // The states are dead once read: drop their lines from L2 so they are
-    // never written back (eight lanes share a 128-byte line; every lane's
-    // load has returned once the sums above used it).
-    __syncwarp();
-    if ((x & 63) == 0) {
-#pragma unroll
-      for (int u = 0; u < U; ++u)
-        if (g0 + u < G) discard_l2_line(src + (int64_t)(g0 + u) * se);
     }
   }
   if (!causal) {
-    uint4 o;
+    uint2 o;
     o.x = pack_bf16x2(run[0] * keep, run[1] * keep);
     o.y = pack_bf16x2(run[2] * keep, run[3] * keep);
-    o.z = pack_bf16x2(run[4] * keep, run[5] * keep);
-    o.w = pack_bf16x2(run[6] * keep, run[7] * keep);
-    *reinterpret_cast<uint4 *>(dst) = o;
+    *reinterpret_cast<uint2 *>(dst) = o;
   }
 }
 
