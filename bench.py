@@ -107,7 +107,7 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_scan.cuh", "tc_fused.cuh",
+FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_fused.cuh", "tc_walk.cuh",
                           "ptx.cuh")
 
 
@@ -703,8 +703,10 @@ def run_ours(args, w, rank, world, device):
         kernel_names = ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"]
     elif lin_norm == fm.FMCA_LIN_NORM_NONE:  # the T0 / T1 rows, then the fused kernel
         kernel_names = ["tc_affine_rows", "tc_chunk_fused"]
-    else:  # states and T rows, the scan, the fused kernel
-        kernel_names = ["tc_chunk_prep", "tc_state_scan", "tc_chunk_fused"]
+    elif nl == 2:  # one segment per sequence: the walkers, the fused kernel
+        kernel_names = ["tc_chunk_walk", "tc_chunk_fused"]
+    else:  # the segment walkers, the carries, the fused kernel
+        kernel_names = ["tc_chunk_walk", "tc_seg_carry", "tc_chunk_fused"]
     kernels = {name: {"ms": per_kernel_ms[i], "share": per_kernel_ms[i] / sum(per_kernel_ms)}
                for i, name in enumerate(kernel_names)}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])

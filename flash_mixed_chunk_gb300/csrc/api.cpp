@@ -88,7 +88,7 @@ int flash_mca_launch_count_ex(int B, int n, int s, int e, int C, int causal, fmc
   if (path == FMCA_PATH_AUTO)
     path = want_tc(B, n, s, e, C, dtype) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
   if (path == FMCA_PATH_TCGEN05)
-    return want_tc(B, n, s, e, C, dtype) ? tc_launch_count(var) : 0;
+    return want_tc(B, n, s, e, C, dtype) ? tc_launch_count(B, n, e, C, causal, var) : 0;
   if (path == FMCA_PATH_SIMT) return kSimtLaunches;
   return 0;
 }
@@ -250,10 +250,10 @@ int flash_mca_backward_launch_count(int B, int n, int s, int e, int C, int causa
   if (to_variant(opts, C, &var) != FMCA_OK) return 0;
   const int glob = var.lin_norm != kLinNormNone ? 1 : 0;
   if (tc_backward(B, n, s, e, C, dtype))
-    // forward kernels (with `saved`: the relu^2 weights and the output
-    // kernel), dY and the T rows, three product launches, the reverse scan,
-    // dZ with its partials and their sum
-    return (saved ? 2 : 3) + 2 + 3 + glob + 2;
+    // forward kernels (with `saved`: without the chunk walkers), dY and the
+    // T rows, three product launches, the reverse scan, dZ with its partials
+    // and their sum
+    return tc_materialised_launch_count(B, n, e, C, causal, var, !saved) + 2 + 3 + glob + 2;
   if (saved) return 0;
   // CUDA cores: the chunk states and prefix, dY, score gradients, dU, key
   // gradients, the d(prefix) outer products, reverse scan and lin rows, dV,
@@ -372,7 +372,7 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
   const bool tc_ok = want_tc(B, n, s, e, C, dtype);
   if (path == FMCA_PATH_TCGEN05 && !tc_ok) return FMCA_ERR_UNSUPPORTED;
   const bool use_tc = (path == FMCA_PATH_TCGEN05) || (path == FMCA_PATH_AUTO && tc_ok);
-  const int nlaunch = use_tc ? tc_launch_count(var) : kSimtLaunches;
+  const int nlaunch = use_tc ? tc_launch_count(B, n, e, C, causal, var) : kSimtLaunches;
   if (events != nullptr) {
     if (n_events != nlaunch + 1) return FMCA_ERR_INVALID_ARG;
     for (int i = 0; i < n_events; ++i)

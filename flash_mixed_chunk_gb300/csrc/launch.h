@@ -29,33 +29,50 @@ inline SimtLayout simt_layout(int B, int n, int s, int e, int C, int causal) {
   return L;
 }
 
+// Segments of the chunk axis for the chunk walkers: about kWalkUnits units
+// (sequence, 256 e columns, segment) in all, as few segments as give that,
+// every one non-empty; L chunks each.
+constexpr int kWalkUnits = 144;
+struct WalkSplit {
+  int S, L;
+};
+inline WalkSplit walk_split(int B, int n, int e, int C) {
+  const int G = n / C;
+  const int slices = B * (e / 256);
+  int S = slices > 0 ? kWalkUnits / slices : 1;
+  S = S < 1 ? 1 : (S > G ? G : S);
+  const int L = (G + S - 1) / S;
+  return WalkSplit{(G + L - 1) / L, L};
+}
+
 // Workspace of the tensor-core forward path, each region 256-byte aligned:
-//   states  bf16 per-chunk states [B][G][s][e]
-//   prefix  bf16 prefix sums (causal: Gp = G chunks) or total (Gp = 1),
-//           scaled by the global term's divisor
-//   sched   work counters and per-chunk ready flags of the persistent kernels
-//   trows   bf16 rows T0, T1, T2 = Z * gamma_k + beta_k, [3][B*n][s] (the fused
-//           output kernel's operands; written by the state kernel)
+//   local   bf16 sums of the states of a segment's chunks before each chunk
+//           [B][G][s][e] (causal only)
+//   seg     bf16 segment totals, then carries (the sum of the segments
+//           before; bidirectional: the total, in slot 0) [B][S][s][e]
+//   sched   the work counters
+//   trows   bf16 rows T0, T1, T2 [3][B*n][s] (T2 carrying the global term's
+//           divisor), the fused output kernel's operands
 // and, only in the form the backward pass runs (materialised = true):
+//   prefix  bf16 scaled prefix (causal: Gp = G chunks) or total (Gp = 1)
 //   scores  bf16 intra-chunk relu^2 weights [B*n][C]
 //   lin_q   bf16 T2 = Z * gamma2 + beta2 rows [B*n][s]
-// The forward pass keeps its relu^2 weights on chip and needs only the first
-// four regions; they sit at the same offsets in both forms.
+// The first four regions sit at the same offsets in both forms (the backward
+// pass that keeps the forward pass's intermediates reads local and seg).
 struct TcLayout {
-  size_t states, prefix, sched, trows, scores, lin_q, total;
+  size_t local, seg, sched, trows, prefix, scores, lin_q, total;
 };
-inline size_t tc_sched_bytes() {
-  // the work counters
-  return 256;
-}
+inline size_t tc_sched_bytes() { return 256; }
 inline TcLayout tc_layout(int B, int n, int s, int e, int C, int causal, bool materialised) {
   const size_t G = (size_t)(n / C), se = (size_t)s * (size_t)e, Gp = causal ? G : 1;
+  const WalkSplit ws = walk_split(B, n, e, C);
   TcLayout L;
-  L.states = 0;
-  L.prefix = align256(2 * (size_t)B * G * se);
-  L.sched = L.prefix + align256(2 * (size_t)B * Gp * se);
+  L.local = 0;
+  L.seg = causal ? align256(2 * (size_t)B * G * se) : 0;
+  L.sched = L.seg + align256(2 * (size_t)B * ws.S * se);
   L.trows = L.sched + tc_sched_bytes();
-  L.scores = L.trows + align256(3 * 2 * (size_t)B * n * (size_t)s);
+  L.prefix = L.trows + align256(3 * 2 * (size_t)B * n * (size_t)s);
+  L.scores = L.prefix + (materialised ? align256(2 * (size_t)B * Gp * se) : 0);
   L.lin_q = L.scores + (materialised ? align256(2 * (size_t)B * n * (size_t)C) : 0);
   L.total = L.lin_q + (materialised ? align256(2 * (size_t)B * n * (size_t)s) : 0);
   return L;
@@ -93,7 +110,11 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                       cudaEvent_t const *events = nullptr);
 // Kernels one launch_tc_forward queues (the memset of its counters not
 // counted).
-int tc_launch_count(const Variant &var);
+int tc_launch_count(int B, int n, int e, int C, int causal, const Variant &var);
+// kernels of launch_tc_forward_materialised (with_states: it forms the local
+// sums and carries itself, as the forward pass does)
+int tc_materialised_launch_count(int B, int n, int e, int C, int causal, const Variant &var,
+                                 bool with_states);
 
 // The forward pass as the backward pass needs it (workspace:
 // tc_layout(..., true)): besides O it leaves the relu^2 weights, the lin_q

@@ -6,14 +6,18 @@
 // Design Recently", sections "Weak Attention" and "Mixed Chunk"): a memset of
 // the work counters and
 //
-//   tc_chunk_prep    state_g = T3_g^T V_g per chunk and 256-column slice of e
-//                    (bf16; state units only) and the rows T0, T1, T2
-//                    (without a global term: tc_affine_rows, T0 and T1 only)
-//   tc_state_scan    exclusive prefix over chunks (causal) or total
-//                    (bidirectional) of the states, times 1/n, to bf16
+//   tc_chunk_walk    per (sequence, 128-column slice of e), the chunks in
+//                    order: state_g = T3_g^T V_g in TMEM, the running sum of
+//                    the states (fp32, TMEM), the exclusive prefix (causal) or
+//                    total (bidirectional) times 1/n to bf16, and the rows
+//                    T0, T1, T2; a few CTAs, with per-chunk completion
+//                    counters (without a global term: tc_affine_rows, T0 and
+//                    T1 only)
 //   tc_chunk_fused   O = U * (relu(T0 T1^T / C)^2 V_g + T2 prefix_g) per
 //                    (chunk, row tile, e tile), the relu^2 weights kept on
-//                    chip (TMEM), both products accumulated in TMEM
+//                    chip (TMEM), both products accumulated in TMEM; it runs
+//                    beside the walkers (a programmatic dependent that waits
+//                    on their counters, chunk by chunk)
 //
 // The backward pass runs the forward pass in its materialised form instead:
 // tc_chunk_prep also writes the relu^2 weights P and the T2 rows to the
@@ -32,7 +36,6 @@
 
 #include "tc_common.cuh"
 #include "tc_prep.cuh"
-#include "tc_scan.cuh"
 #include "tc_attn.cuh"
 #include "tc_fused.cuh"
 #include "tc_gemm.cuh"
@@ -124,23 +127,22 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   return true;
 }
 
-int tc_launch_count(const Variant &var) { return var.lin_norm == kLinNormNone ? 2 : 3; }
+int tc_launch_count(int B, int n, int e, int C, int causal, const Variant &var) {
+  if (var.lin_norm == kLinNormNone) return 2;  // T0 / T1 rows, fused kernel
+  const WalkSplit sp = walk_split(B, n, e, C);
+  return (sp.S > 1 || !causal) ? 3 : 2;  // walkers, [carries], fused kernel
+}
+
+int tc_materialised_launch_count(int B, int n, int e, int C, int causal, const Variant &var,
+                                 bool with_states) {
+  if (var.lin_norm == kLinNormNone) return 2;  // relu^2 weights, output kernel
+  const WalkSplit sp = walk_split(B, n, e, C);
+  // [walkers, [carries]], scaled prefix, relu^2 weights, output kernel
+  return (with_states ? 1 + ((sp.S > 1 || !causal) ? 1 : 0) : 0) + 3;
+}
 
 namespace {
 
-// The scan kernel of a global-term divisor (segmented for long chunk axes).
-using ScanKernel = void (*)(const __nv_bfloat16 *, __nv_bfloat16 *, int, int, int64_t, float,
-                            int, int);
-ScanKernel pick_scan(const Variant &var, bool seg) {
-  if (var.lin_norm == kLinNormNone) return tc_state_scan<kLinNormNone>;
-  if (seg)
-    return var.lin_norm == kLinNormSummed     ? tc_state_scan_seg<kLinNormSummed>
-           : var.lin_norm == kLinNormPosition ? tc_state_scan_seg<kLinNormPosition>
-                                              : tc_state_scan_seg<kLinNormN>;
-  return var.lin_norm == kLinNormSummed     ? tc_state_scan<kLinNormSummed>
-         : var.lin_norm == kLinNormPosition ? tc_state_scan<kLinNormPosition>
-                                            : tc_state_scan<kLinNormN>;
-}
 
 // Tiles of the fused kernel: (batch x chunk, row tile, e tile).
 FusedGrid fused_grid(int B, int n, int e, int C, int causal, bool lin) {
@@ -153,6 +155,9 @@ FusedGrid fused_grid(int B, int n, int e, int C, int causal, bool lin) {
   g.R = C / ROW_TILE;
   g.n_et = e / FU_ET;
   g.n_tiles = B * g.G * g.R * g.n_et;
+  g.S = 1;
+  g.L = g.G;
+  g.rows_early = 0;
   return g;
 }
 
@@ -180,37 +185,36 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                       const Variant &var, void *workspace, cudaStream_t stream,
                       cudaEvent_t const *events) {
   const int G = n / C;
-  const int Gp = causal ? G : 1;
+  const int64_t se = (int64_t)s * e;
   const TcLayout L = tc_layout(B, n, s, e, C, causal, false);
+  const WalkSplit sp = walk_split(B, n, e, C);
   char *ws = static_cast<char *>(workspace);
-  __nv_bfloat16 *states = reinterpret_cast<__nv_bfloat16 *>(ws + L.states);
-  __nv_bfloat16 *prefix = reinterpret_cast<__nv_bfloat16 *>(ws + L.prefix);
+  __nv_bfloat16 *local = reinterpret_cast<__nv_bfloat16 *>(ws + L.local);
+  __nv_bfloat16 *seg = reinterpret_cast<__nv_bfloat16 *>(ws + L.seg);
   __nv_bfloat16 *trows = reinterpret_cast<__nv_bfloat16 *>(ws + L.trows);
-  unsigned int *sched = reinterpret_cast<unsigned int *>(ws + L.sched);
   const uint64_t rows = (uint64_t)B * n;
   const int64_t plane = (int64_t)rows * s;  // elements of one T-row plane
 
-  // state kernel: Z keys and V slices as one 3-D box each; fused kernel: 3-D
-  // boxes of 128 rows x two 64-column blocks (32 KB) for every operand
-  CUtensorMap mZ64, mZ128, mZ3, mV3p, mSt, mT0, mT1, mT2, mV, mS;
-  if (!make_map_bf16(&mZ64, Z, s, rows, 64, 64) || !make_map_bf16(&mZ128, Z, s, rows, 64, 128) ||
-      !make_map3_bf16(&mZ3, Z, s, rows, 64, 2) || !make_map3_bf16(&mV3p, V, e, rows, 64, 4) ||
-      !make_map_bf16(&mSt, states, e, (uint64_t)B * G * s, 64, 128) ||
+  // walkers: Z keys and V slices as one 3-D box each (64 keys), sums out as
+  // [128 rows][64 cols] tiles; fused kernel: 3-D boxes of 128 rows x two
+  // 64-column blocks (32 KB) for every operand
+  CUtensorMap mZw, mVw, mL, mT, mT0, mT1, mT2, mV, mLoc, mCy;
+  const uint64_t lrows = causal ? (uint64_t)B * G * s : (uint64_t)s;  // (unused if bidirectional)
+  if (!make_map3_bf16(&mZw, Z, s, rows, 64, 2) || !make_map3_bf16(&mVw, V, e, rows, 64, 4) ||
+      !make_map_bf16(&mL, local, e, lrows, 64, 128) ||
+      !make_map_bf16(&mT, seg, e, (uint64_t)B * sp.S * s, 64, 128) ||
       !make_map3_bf16(&mT0, trows, s, rows, 128, 2) ||
       !make_map3_bf16(&mT1, trows + plane, s, rows, 128, 2) ||
       !make_map3_bf16(&mT2, trows + 2 * plane, s, rows, 128, 2) ||
       !make_map3_bf16(&mV, V, e, rows, 128, 2) ||
-      !make_map3_bf16(&mS, prefix, e, (uint64_t)B * Gp * s, 128, 2))
+      !make_map3_bf16(&mLoc, local, e, lrows, 128, 2) ||
+      !make_map3_bf16(&mCy, seg, e, (uint64_t)B * sp.S * s, 128, 2))
     return 2;
 
   static OncePerDevice attrs;
   if (!attrs.run([] {
-        return cudaFuncSetAttribute(tc_chunk_prep<false>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)PREP_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(tc_chunk_prep<true>,
-                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)PREP_SMEM) == cudaSuccess &&
+        return cudaFuncSetAttribute(tc_chunk_walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)WALK_SMEM) == cudaSuccess &&
                cudaFuncSetAttribute(tc_chunk_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)FUSED_SMEM) == cudaSuccess;
       }))
@@ -218,48 +222,42 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   if (!record_event(events, 0, stream)) return 1;
   const int sms = num_sms();
   const bool no_global = var.lin_norm == kLinNormNone;
-  // sched[0]: work counter of the state kernel (the fused kernel's CTAs take
-  // fixed tile ranges)
-  if (!no_global && cudaMemsetAsync(sched, 0, sizeof(unsigned int), stream) != cudaSuccess)
-    return 1;
+  FusedGrid fg = fused_grid(B, n, e, C, causal, !no_global);
+  fg.S = sp.S;
+  fg.L = sp.L;
+  fg.rows_early = 0;
   int ev = 1;
   if (!no_global) {
-    // chunk states T3^T V and the rows T0, T1, T2 (the prep kernel with state
-    // units only)
-    const int n_state = B * G * (e / E_TILE);
-    auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
-    prep<<<n_state < sms ? n_state : sms, PREP_THREADS, PREP_SMEM, stream>>>(
-        mZ64, mZ128, mZ3, mV3p, mSt, mSt, gamma, beta, nullptr, trows, plane, sched, n, e, C, G,
-        causal, n_state, 0, var.quad_a);
+    // the segment walkers: local sums, segment totals and the T rows
+    const int units = B * (e / WK_ET) * sp.S;
+    tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
+        mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S, sp.L);
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
-    // the prefix (or total) of the states over chunks, a programmatic
-    // dependent of the state kernel
-    PdlConfig sc(stream, true);
-    // long chunk axes: the segmented scan (64 column groups of 8 x 4 segments
-    // a block); otherwise one thread per kScanCols columns
-    const bool seg = G >= kScanSegMinG;
-    const int64_t se = (int64_t)s * e;
-    const int64_t lanes = (int64_t)B * se / (seg ? 8 : kScanCols);
-    sc.cfg.gridDim = dim3((unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
-    sc.cfg.blockDim = dim3(256);
-    sc.cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&sc.cfg, pick_scan(var, seg), (const __nv_bfloat16 *)states, prefix,
-                           B, G, se, 1.0f / (float)n, causal, C) != cudaSuccess ||
-        !record_event(events, ev++, stream))
-      return 1;
+    if (sp.S > 1 || !causal) {
+      // totals -> carries (bidirectional: the total), a programmatic
+      // dependent of the walkers
+      PdlConfig cc(stream, true);
+      const int64_t lanes = (int64_t)B * se / 8;
+      cc.cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
+      cc.cfg.blockDim = dim3(256);
+      cc.cfg.dynamicSmemBytes = 0;
+      if (cudaLaunchKernelEx(&cc.cfg, tc_seg_carry, seg, B, sp.S, se, causal) != cudaSuccess ||
+          !record_event(events, ev++, stream))
+        return 1;
+      fg.rows_early = 1;
+    }
   } else {
-    // without a global term there are no chunk states: the T0 and T1 rows only
+    // without a global term: the T0 and T1 rows only
     const int64_t n_vec = plane / 8;
     tc_affine_rows<<<(unsigned)((n_vec + 255) / 256), 256, 0, stream>>>(
         static_cast<const __nv_bfloat16 *>(Z), gamma, beta, trows, plane, n_vec);
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
   }
-  const FusedGrid fg = fused_grid(B, n, e, C, causal, !no_global);
   PdlConfig fc(stream, true);
   fc.cfg.gridDim = dim3(fg.n_tiles < sms ? fg.n_tiles : sms);
   fc.cfg.blockDim = dim3(FUSED_THREADS);
   fc.cfg.dynamicSmemBytes = FUSED_SMEM;
-  if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_fused, mT0, mT1, mT2, mV, mS,
+  if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_fused, mT0, mT1, mT2, mV, mLoc, mCy,
                          static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
                          fg, e, var.quad_a) != cudaSuccess ||
       !record_event(events, ev++, stream))
@@ -276,18 +274,24 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
   const int64_t se = (int64_t)s * e;
   const int Gp = causal ? G : 1;
   const TcLayout L = tc_layout(B, n, s, e, C, causal, true);
+  const WalkSplit sp = walk_split(B, n, e, C);
   char *ws = static_cast<char *>(workspace);
-  __nv_bfloat16 *states = reinterpret_cast<__nv_bfloat16 *>(ws + L.states);
+  __nv_bfloat16 *local = reinterpret_cast<__nv_bfloat16 *>(ws + L.local);
+  __nv_bfloat16 *seg = reinterpret_cast<__nv_bfloat16 *>(ws + L.seg);
+  __nv_bfloat16 *trows = reinterpret_cast<__nv_bfloat16 *>(ws + L.trows);
   __nv_bfloat16 *prefix = reinterpret_cast<__nv_bfloat16 *>(ws + L.prefix);
   void *pw = ws + L.scores;
   void *t2 = ws + L.lin_q;
   unsigned int *sched = reinterpret_cast<unsigned int *>(ws + L.sched);
-
-  CUtensorMap mZ64, mZ128, mZ3, mV3p, mSt, mPw, mT2, mV, mS, mU, mO;
   const uint64_t rows = (uint64_t)B * n;
+  const int64_t plane = (int64_t)rows * s;
+
+  CUtensorMap mZ64, mZ128, mZw, mVw, mL, mT, mPw, mT2, mV, mS, mU, mO;
+  const uint64_t lrows = causal ? (uint64_t)B * G * s : (uint64_t)s;
   if (!make_map_bf16(&mZ64, Z, s, rows, 64, 64) || !make_map_bf16(&mZ128, Z, s, rows, 64, 128) ||
-      !make_map3_bf16(&mZ3, Z, s, rows, 64, 2) || !make_map3_bf16(&mV3p, V, e, rows, 64, 4) ||
-      !make_map_bf16(&mSt, states, e, (uint64_t)B * G * s, 64, 128) ||
+      !make_map3_bf16(&mZw, Z, s, rows, 64, 2) || !make_map3_bf16(&mVw, V, e, rows, 64, 4) ||
+      !make_map_bf16(&mL, local, e, lrows, 64, 128) ||
+      !make_map_bf16(&mT, seg, e, (uint64_t)B * sp.S * s, 64, 128) ||
       !make_map_bf16(&mPw, pw, C, rows, 64, 128) || !make_map_bf16(&mT2, t2, s, rows, 64, 128) ||
       !make_map_bf16(&mV, V, e, rows, 64, 64) ||
       !make_map_bf16(&mS, prefix, e, (uint64_t)B * Gp * s, 64, 64) ||
@@ -302,42 +306,50 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
                cudaFuncSetAttribute(tc_chunk_prep<true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)PREP_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)WALK_SMEM) == cudaSuccess &&
                cudaFuncSetAttribute(tc_chunk_attn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)AT_SMEM) == cudaSuccess;
       }))
     return 1;
   // sched[0]: work counter of tc_chunk_prep; sched[1]: of tc_chunk_attn
   if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
-  // without a global term (FMCA_LIN_NORM_NONE) there are no chunk states, the
-  // scan has nothing to do and the attention units have no lin_q items
+  // without a global term (FMCA_LIN_NORM_NONE) there is no prefix and the
+  // attention units have no lin_q items
   const bool no_global = var.lin_norm == kLinNormNone;
-  const int n_state = (no_global || !with_states) ? 0 : B * G * (e / E_TILE);
-  const int n_score = B * G * score_units_per_chunk(C, causal);
-  const int n_prep = n_state + n_score;
   const int sms = num_sms();
-  auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
-  prep<<<n_prep < sms ? n_prep : sms, PREP_THREADS, PREP_SMEM, stream>>>(
-      mZ64, mZ128, mZ3, mV3p, mSt, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2),
-      nullptr, 0, sched, n, e, C, G, causal, n_state, n_score, var.quad_a);
-  if (cudaGetLastError() != cudaSuccess) return 1;
-  // The scan and the attention kernel are programmatic dependents of the
-  // kernel before them.  The attention kernel reads the relu^2 weights and
-  // lin_q rows before its griddepcontrol.wait (which guards only the prefix):
-  // that is safe behind the scan (which waits for prep before it lets the
-  // attention kernel launch), so without the scan it is an ordinary launch.
-  if (with_states) {
-    PdlConfig sc(stream, true);
-    const bool seg = !no_global && G >= kScanSegMinG;
-    const int64_t lanes = (int64_t)B * se / (seg ? 8 : kScanCols);
-    sc.cfg.gridDim = dim3(no_global ? 1u : (unsigned)(seg ? (lanes + 63) / 64 : (lanes + 255) / 256));
-    sc.cfg.blockDim = dim3(256);
-    sc.cfg.dynamicSmemBytes = 0;
-    if (cudaLaunchKernelEx(&sc.cfg, pick_scan(var, seg), (const __nv_bfloat16 *)states, prefix,
-                           B, G, se, 1.0f / (float)n, causal, C) != cudaSuccess)
-      return 1;
+  if (!no_global) {
+    if (with_states) {
+      // the local sums and carries exactly as the forward pass forms them
+      const int units = B * (e / WK_ET) * sp.S;
+      tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
+          mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S,
+          sp.L);
+      if (cudaGetLastError() != cudaSuccess) return 1;
+      if (sp.S > 1 || !causal) {
+        const int64_t lanes = (int64_t)B * se / 8;
+        tc_seg_carry<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(seg, B, sp.S, se,
+                                                                          causal);
+        if (cudaGetLastError() != cudaSuccess) return 1;
+      }
+    }
+    // the scaled prefix of the attention kernel (unscaled T2 rows)
+    const int64_t lanes = (int64_t)B * Gp * se / 8;
+    tc_prefix_fixup<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(
+        local, seg, prefix, B, G, sp.S, sp.L, se, causal, n, C, var.lin_norm);
+    if (cudaGetLastError() != cudaSuccess) return 1;
   }
+  // the relu^2 weights P and the T2 rows (score units only)
+  const int n_score = B * G * score_units_per_chunk(C, causal);
+  auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
+  prep<<<n_score < sms ? n_score : sms, PREP_THREADS, PREP_SMEM, stream>>>(
+      mZ64, mZ128, mZw, mVw, mL, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2),
+      nullptr, 0, sched, n, e, C, G, causal, 0, n_score, var.quad_a);
+  if (cudaGetLastError() != cudaSuccess) return 1;
+  // O = U * (P V_g + T2 prefix_g): an ordinary launch (it reads P and T2
+  // from the kernel before it as soon as it starts)
   const int n_units = B * G * R * (e / E_TILE);
-  PdlConfig ac(stream, with_states);
+  PdlConfig ac(stream, false);
   ac.cfg.gridDim = dim3(n_units < sms ? n_units : sms);
   ac.cfg.blockDim = dim3(AT_THREADS);
   ac.cfg.dynamicSmemBytes = AT_SMEM;

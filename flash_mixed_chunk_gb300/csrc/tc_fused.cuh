@@ -20,7 +20,11 @@
 //                          operand of the next product) in one of four P slots
 //   per e tile:
 //     O  = sum_k P_k V_k   M = 128, N = 128, K = 64 per stage, A from TMEM
-//     O += T2 prefix_g     K = s = 128
+//     O += T2 local_g      K = s = 128 (causal: the sum of the states of the
+//                          chunk's segment before it)
+//     O += T2 carry        K = s = 128 (causal: the sum of the segments
+//                          before the chunk's, past the first; bidirectional:
+//                          the total); T2 carries the global term's divisor
 //     out = U * O          four epilogue warps, in place in the U tile, one
 //                          TMA store
 // A row tile with at most four key stages (every chunk of 256) keeps its
@@ -38,7 +42,7 @@
 //   ring     5 x 32 KB items, the MMA warp's only input:
 //              keys   T1 rows of 128 keys   [2][128][64] (two stages)
 //              V      128 keys x 128 e      [2][128][64]
-//              prefix 128 s x 128 e         [2][128][64]
+//              local or carry 128 s x 128 e [2][128][64]
 // The epilogue warps read U and write O with 16-byte loads and stores, one
 // tile row per thread; a tile's U is loaded while its products run.
 // TMEM (512 columns): O [0, 256) as two 128-column buffers (the epilogue of
@@ -46,6 +50,7 @@
 #pragma once
 
 #include "tc_common.cuh"
+#include "tc_walk.cuh"
 
 namespace fmca {
 namespace {
@@ -71,7 +76,9 @@ struct FusedUnit {
   int g;      // chunk within its sequence
   int row0;   // first token row of the tile in [B*n]
   int crow;   // first token row of its chunk
-  int prow;   // first prefix row of its chunk in [B*Gp*s]
+  int lrow;   // first row of the chunk's local sums in [B*G*s]
+  int crow2;  // first row of its carry in [B*S*s] (its total when bidirectional)
+  bool carry; // a carry product (causal: past the first segment)
   int rt;     // row tile within the chunk
   int et0;    // first 128-column e tile
   int net;    // e tiles in the unit
@@ -82,6 +89,8 @@ struct FusedUnit {
 // row tile rt (of R = C / 128) and e tile et (of n_et = e / 128).
 struct FusedGrid {
   int n, C, G, causal, lin, R, n_et, n_tiles;
+  int S, L;        // segments of the chunk axis, chunks each
+  int rows_early;  // the T rows may be read before the grid-dependency wait
 };
 
 // 64-key stages of row tile rt
@@ -93,7 +102,8 @@ __device__ __forceinline__ int fused_nkv(int rt, const FusedGrid &g) {
 // FU_PSLOTS stages), 32 each of U and O, 32 of the prefix
 __device__ __forceinline__ int64_t fused_tile_cost(int rt, const FusedGrid &g) {
   const int nkv = fused_nkv(rt, g);
-  return (int64_t)nkv * (nkv <= FU_PSLOTS ? 16 : 32) + 64 + (g.lin ? 32 : 0);
+  return (int64_t)nkv * (nkv <= FU_PSLOTS ? 16 : 32) + 64 +
+         (g.lin ? (g.causal && g.S > 1 ? 64 : 32) : 0);
 }
 // the tile that holds cost position x (the tiles laid end to end in order)
 __device__ __forceinline__ int fused_tile_at(int64_t x, const FusedGrid &g) {
@@ -132,7 +142,9 @@ __device__ __forceinline__ FusedUnit decode_fused(int t, int net, const FusedGri
   f.g = c;
   f.crow = b * g.n + c * g.C;
   f.row0 = f.crow + rt * ROW_TILE;
-  f.prow = (g.causal ? bg : b) * S_DIM;
+  f.lrow = bg * S_DIM;
+  f.crow2 = (b * g.S + (g.causal ? c / g.L : 0)) * S_DIM;
+  f.carry = !g.causal || c / g.L > 0;
   f.rt = rt;
   f.et0 = et;
   f.net = net;
@@ -152,7 +164,8 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                    const __grid_constant__ CUtensorMap mapT1,  // T1 rows, 3-D box {64, 128, 2}
                    const __grid_constant__ CUtensorMap mapT2,  // T2 rows, 3-D box {64, 128, 2}
                    const __grid_constant__ CUtensorMap mapV,   // V 3-D, box {64, 128, 2}
-                   const __grid_constant__ CUtensorMap mapS,   // prefix 3-D, box {64, 128, 2}
+                   const __grid_constant__ CUtensorMap mapS,   // local sums 3-D, box {64, 128, 2}
+                   const __grid_constant__ CUtensorMap mapCy,  // carries 3-D, box {64, 128, 2}
                    const __nv_bfloat16 *__restrict__ U,        // [B*n][e]
                    __nv_bfloat16 *__restrict__ O,              // [B*n][e]
                    FusedGrid grid, int e, float quad_a) {
@@ -219,6 +232,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       tma_prefetch_desc(&mapT2);
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapS);
+      tma_prefetch_desc(&mapCy);
       int it = 0;
       bool ok = true, rows_ready = false, prefix_ready = false;
       // one ring item: waits for its slot, then one 32 KB box
@@ -251,10 +265,11 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         mbar_arrive(&uq_full[qs]);
         if (uu < 0) break;
         const FusedUnit f = decode_fused(uu, net, grid);
-        // Without a global term the kernel before this one wrote the T rows.
-        // With one, the state kernel wrote them, and it had completed before
-        // the scan (which waits for it first) let this grid launch.
-        if (!lin && !rows_ready) {
+        // The T rows: with the carry kernel between their writer and this
+        // grid, the writer had completed before it let this grid launch (it
+        // waits for it first); otherwise they come from the kernel just
+        // before: wait here.
+        if (!grid.rows_early && !rows_ready) {
           griddep_wait();
           rows_ready = true;
         }
@@ -288,14 +303,15 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
             mbar_arrive_expect_tx(&b_full, FU_AB_BYTES);
             tma_load_3d(bbuf, &mapT2, &b_full, 0, f.row0, 0);
           }
-          // the prefix comes from the scan, the kernel before this one: wait
-          // for it once, before the first prefix load (the unit's rows,
-          // scores, weights and first products overlap the scan's tail)
+          // the local sums and carries come from the kernels before: wait
+          // once, before the first such load (the unit's rows, scores,
+          // weights and first products overlap their tail)
           if (!prefix_ready) {
             griddep_wait();
             prefix_ready = true;
           }
-          ok = issue(&mapS, f.prow, eb);  // prefix rows [0, s), e tile x
+          if (grid.causal) ok = issue(&mapS, f.lrow, eb);  // local sums, e tile x
+          if (ok && f.carry) ok = issue(&mapCy, f.crow2, eb);
         }
       }
       // drain: the last load issued into every ring slot has landed
@@ -430,21 +446,26 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
               ok = false;
               break;
             }
-            if (!wait_item(it)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t pb = smem_u32(ring + (it % FU_RING) * FU_ITEM);
+            // O += T2 local_g (causal), then O += T2 carry (when present)
+            const int n_glob = (grid.causal ? 1 : 0) + (f.carry ? 1 : 0);
+            for (int gi = 0; gi < n_glob && ok; ++gi) {
+              if (!wait_item(it)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t pb = smem_u32(ring + (it % FU_RING) * FU_ITEM);
 #pragma unroll
-            for (int kk = 0; kk < S_DIM / 16; ++kk) {
-              const uint64_t ad =
-                  smem_desc_sw128(baddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(pb + kk * 2048, 16384, 1024);
-              mma_bf16_ss(ocol, ad, bd, idesc_o, 1u);
+              for (int kk = 0; kk < S_DIM / 16; ++kk) {
+                const uint64_t ad =
+                    smem_desc_sw128(baddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(pb + kk * 2048, 16384, 1024);
+                mma_bf16_ss(ocol, ad, bd, idesc_o, 1u);
+              }
+              mma_commit(&empty[it % FU_RING]);
+              ++it;
             }
-            mma_commit(&empty[it % FU_RING]);
-            ++it;
+            if (!ok) break;
             if (x == f.net - 1) mma_commit(&b_empty);  // B goes back after the unit
           }
           mma_commit(&o_full[ob]);

@@ -50,19 +50,31 @@ def test_status_strings():
     assert fm.flash_mca_version() == "0.1.0"
 
 
+def walk_segments(B, n, e, C):
+    """Segments of the chunk axis the tensor-core path's chunk walkers use:
+    about 144 (sequence, 256 e columns, segment) units, every segment
+    non-empty (whole 256-column slices only: the path takes e % 256 == 0)."""
+    G = n // C
+    slices = B * (e // 256)
+    S = max(1, min(G, 144 // slices)) if slices else 1
+    L = -(-G // S)
+    return -(-G // L)
+
+
 @pytest.mark.parametrize("B,n,s,e,C,causal", [(2, 8192, 128, 1536, 256, 1),
                                               (4, 4096, 128, 1536, 256, 0),
                                               (1, 256, 32, 64, 64, 1),
                                               (3, 96, 48, 80, 32, 0)])
 def test_workspace_bytes_formula(B, n, s, e, C, causal):
-    """Enough for either path: fp32 states and prefix (SIMT) or bf16 states and
-    prefix with the work counters, per-chunk flags and the bf16 rows T0, T1, T2
-    (tensor cores); no [B*n][C] buffer of relu^2 weights on either."""
+    """Enough for either path: fp32 states and prefix (SIMT) or, on the tensor
+    cores, the bf16 local sums of each chunk's segment (causal), the segment
+    totals/carries, the work counters and the bf16 rows T0, T1, T2; no
+    per-chunk states and no [B*n][C] buffer of relu^2 weights."""
     a = lambda x: (x + 255) // 256 * 256
     G = n // C
     Gp = G if causal else 1
     simt = a(4 * B * G * s * e) + a(4 * B * Gp * s * e)
-    tc = (a(2 * B * G * s * e) + a(2 * B * Gp * s * e) + 256
+    tc = (a(2 * B * G * s * e) * causal + a(2 * B * walk_segments(B, n, e, C) * s * e) + 256
           + a(3 * 2 * B * n * s))  # + the bf16 rows T0, T1, T2
     for dt in (fm.FMCA_F32, fm.FMCA_BF16):
         assert fm.flash_mca_workspace_bytes(B, n, s, e, C, causal, dt) == max(simt, tc)
@@ -91,9 +103,12 @@ def test_auto_path_choice():
 
 def test_launch_counts():
     bf = fm.FMCA_BF16
-    # states and T rows, the scan of the states, the fused chunk kernel
+    # the segment walkers (local sums, totals, T rows), the segment carries,
+    # the fused chunk kernel
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 3
     assert fm.flash_mca_launch_count(4, 4096, 128, 1536, 256, 0, bf) == 3
+    # one segment per sequence (B * e / 256 >= 144 units): no carries
+    assert fm.flash_mca_launch_count(16, 1024, 128, 2560, 256, 1, bf) == 2
     # without a global term: the T0 / T1 rows and the fused chunk kernel
     assert fm.flash_mca_launch_count(8, 1024, 128, 1536, 1024, 1, bf,
                                      lin_norm=fm.FMCA_LIN_NORM_NONE) == 2
@@ -315,13 +330,14 @@ def test_backward_saved_validation():
 def test_backward_launch_count():
     bf, f32 = fm.FMCA_BF16, fm.FMCA_F32
     cnt = fm.flash_mca_backward_launch_count
-    # tensor cores: forward kernels (3; 2 when the forward's chunk states and
-    # prefix are kept: the relu^2 weights and the output kernel), 2
-    # elementwise, 3 product launches, the reverse scan (global term only), 2
-    # for dZ / dgamma / dbeta
-    assert cnt(2, 1024, 128, 512, 256, True, bf) == 11
-    assert cnt(2, 1024, 128, 512, 256, True, bf, saved=True) == 10
-    assert cnt(2, 1024, 128, 512, 256, True, bf, lin_norm=fm.FMCA_LIN_NORM_NONE) == 10
+    # tensor cores: forward kernels (chunk walkers, segment carries, scaled
+    # prefix, relu^2 weights, output kernel: 5; 3 when the forward pass's local
+    # sums and carries are kept; 2 without a global term), 2 elementwise, 3
+    # product launches, the reverse scan (global term only), 2 for dZ /
+    # dgamma / dbeta
+    assert cnt(2, 1024, 128, 512, 256, True, bf) == 13
+    assert cnt(2, 1024, 128, 512, 256, True, bf, saved=True) == 11
+    assert cnt(2, 1024, 128, 512, 256, True, bf, lin_norm=fm.FMCA_LIN_NORM_NONE) == 9
     # CUDA cores
     assert cnt(2, 1024, 128, 512, 256, True, f32) == 12
     assert cnt(2, 1024, 128, 512, 256, True, f32, lin_norm=fm.FMCA_LIN_NORM_NONE) == 7
