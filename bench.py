@@ -47,8 +47,6 @@ import mca_inputs  # noqa: E402
 
 METRIC = "mixed-chunk attn fwd tokens/s and TFLOP/s at 1 GB300; % of bf16 tensor peak"
 PEAKS_FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-DOMINANT_KERNEL = "tc_chunk_fused"
-
 
 # ---------------------------------------------------------------- ranks
 def rank_seed(seed: int, rank: int) -> int:
@@ -107,7 +105,7 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_fused.cuh", "tc_walk.cuh",
+FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_fused.cuh", "tc_walk.cuh", "tc_pair.cuh",
                           "ptx.cuh")
 
 
@@ -703,10 +701,13 @@ def run_ours(args, w, rank, world, device):
         kernel_names = ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"]
     elif lin_norm == fm.FMCA_LIN_NORM_NONE:  # the T0 / T1 rows, then the fused kernel
         kernel_names = ["tc_affine_rows", "tc_chunk_fused"]
-    elif nl == 2:  # one segment per sequence: the walkers, the fused kernel
-        kernel_names = ["tc_chunk_walk", "tc_chunk_fused"]
-    else:  # the segment walkers, the carries, the fused kernel
-        kernel_names = ["tc_chunk_walk", "tc_seg_carry", "tc_chunk_fused"]
+    else:
+        # the segment walkers, the carries (with more than one segment or
+        # bidirectional), the output kernel (both row tiles of a causal chunk
+        # of 256 per unit, else one)
+        out_kernel = "tc_chunk_pair" if (w.causal and w.C == 256) else "tc_chunk_fused"
+        kernel_names = (["tc_chunk_walk", out_kernel] if nl == 2
+                        else ["tc_chunk_walk", "tc_seg_carry", out_kernel])
     kernels = {name: {"ms": per_kernel_ms[i], "share": per_kernel_ms[i] / sum(per_kernel_ms)}
                for i, name in enumerate(kernel_names)}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])

@@ -25,7 +25,7 @@ BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libflash_mca.so")
 
 SOURCES = ["api.cpp", "simt.cu", "tc.cu", "noalloc.cu", "decode.cu", "backward.cu"]
-HEADERS = ["launch.h", "ptx.cuh", "tc_common.cuh", "tc_prep.cuh", "tc_attn.cuh", "tc_fused.cuh", "tc_walk.cuh", "tc_gemm.cuh", "tc_bgemm.cuh", "tc_bwd.cuh", "tc_backward.cuh"]
+HEADERS = ["launch.h", "ptx.cuh", "tc_common.cuh", "tc_prep.cuh", "tc_attn.cuh", "tc_fused.cuh", "tc_walk.cuh", "tc_pair.cuh", "tc_gemm.cuh", "tc_bgemm.cuh", "tc_bwd.cuh", "tc_backward.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

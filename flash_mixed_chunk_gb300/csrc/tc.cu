@@ -38,6 +38,7 @@
 #include "tc_prep.cuh"
 #include "tc_attn.cuh"
 #include "tc_fused.cuh"
+#include "tc_pair.cuh"
 #include "tc_gemm.cuh"
 
 namespace fmca {
@@ -127,8 +128,15 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   return true;
 }
 
+// The row-pair output kernel (tc_chunk_pair): causal chunks of two 128-row
+// tiles with a global term.  It forms the segment carries itself.
+static bool use_pair_kernel(int C, int causal, bool lin) {
+  return lin && causal && C == 2 * ROW_TILE;
+}
+
 int tc_launch_count(int B, int n, int e, int C, int causal, const Variant &var) {
   if (var.lin_norm == kLinNormNone) return 2;  // T0 / T1 rows, fused kernel
+  if (use_pair_kernel(C, causal, true)) return 2;  // walkers, row-pair kernel
   const WalkSplit sp = walk_split(B, n, e, C);
   return (sp.S > 1 || !causal) ? 3 : 2;  // walkers, [carries], fused kernel
 }
@@ -198,7 +206,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   // walkers: Z keys and V slices as one 3-D box each (64 keys), sums out as
   // [128 rows][64 cols] tiles; fused kernel: 3-D boxes of 128 rows x two
   // 64-column blocks (32 KB) for every operand
-  CUtensorMap mZw, mVw, mL, mT, mT0, mT1, mT2, mV, mLoc, mCy;
+  CUtensorMap mZw, mVw, mL, mT, mT0, mT1, mT2, mV, mLoc, mCy, mU3;
   const uint64_t lrows = causal ? (uint64_t)B * G * s : (uint64_t)s;  // (unused if bidirectional)
   if (!make_map3_bf16(&mZw, Z, s, rows, 64, 2) || !make_map3_bf16(&mVw, V, e, rows, 64, 4) ||
       !make_map_bf16(&mL, local, e, lrows, 64, 128) ||
@@ -208,7 +216,8 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
       !make_map3_bf16(&mT2, trows + 2 * plane, s, rows, 128, 2) ||
       !make_map3_bf16(&mV, V, e, rows, 128, 2) ||
       !make_map3_bf16(&mLoc, local, e, lrows, 128, 2) ||
-      !make_map3_bf16(&mCy, seg, e, (uint64_t)B * sp.S * s, 128, 2))
+      !make_map3_bf16(&mCy, seg, e, (uint64_t)B * sp.S * s, 128, 2) ||
+      !make_map3_bf16(&mU3, U, e, rows, 128, 2))
     return 2;
 
   static OncePerDevice attrs;
@@ -216,12 +225,18 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
         return cudaFuncSetAttribute(tc_chunk_walk, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)WALK_SMEM) == cudaSuccess &&
                cudaFuncSetAttribute(tc_chunk_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)FUSED_SMEM) == cudaSuccess;
+                                    (int)FUSED_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PAIR_SMEM) == cudaSuccess;
       }))
     return 1;
   if (!record_event(events, 0, stream)) return 1;
   const int sms = num_sms();
   const bool no_global = var.lin_norm == kLinNormNone;
+  // the row-pair kernel forms the segment carries itself (counted in
+  // sched[2], which the walkers clear)
+  const bool pair = use_pair_kernel(C, causal, !no_global);
+  unsigned int *carried = reinterpret_cast<unsigned int *>(ws + L.sched) + 2;
   FusedGrid fg = fused_grid(B, n, e, C, causal, !no_global);
   fg.S = sp.S;
   fg.L = sp.L;
@@ -231,9 +246,10 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     // the segment walkers: local sums, segment totals and the T rows
     const int units = B * (e / WK_ET) * sp.S;
     tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
-        mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S, sp.L);
+        mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S, sp.L,
+        carried);
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
-    if (sp.S > 1 || !causal) {
+    if ((sp.S > 1 || !causal) && !pair) {
       // totals -> carries (bidirectional: the total), a programmatic
       // dependent of the walkers
       PdlConfig cc(stream, true);
@@ -254,10 +270,32 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
   }
   PdlConfig fc(stream, true);
+  if (pair) {
+    // both row tiles of a chunk per unit (the e tile's operands serve both)
+    PairGrid pg;
+    pg.n = n;
+    pg.G = G;
+    pg.n_et = e / FU_ET;
+    pg.n_tiles = B * G * pg.n_et;
+    pg.S = sp.S;
+    pg.L = sp.L;
+    pg.rows_early = 0;  // no kernel between: the T rows wait for the walkers too
+    pg.B = B;
+    pg.carries = sp.S > 1;
+    fc.cfg.gridDim = dim3(pg.n_tiles < sms ? pg.n_tiles : sms);
+    fc.cfg.blockDim = dim3(PAIR_THREADS);
+    fc.cfg.dynamicSmemBytes = PAIR_SMEM;
+    if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_pair, mT0, mT1, mT2, mV, mLoc, mCy, mU3,
+                           static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
+                           pg, e, var.quad_a, seg, carried) != cudaSuccess ||
+        !record_event(events, ev++, stream))
+      return 1;
+    return 0;
+  }
   fc.cfg.gridDim = dim3(fg.n_tiles < sms ? fg.n_tiles : sms);
   fc.cfg.blockDim = dim3(FUSED_THREADS);
   fc.cfg.dynamicSmemBytes = FUSED_SMEM;
-  if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_fused, mT0, mT1, mT2, mV, mLoc, mCy,
+  if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_fused, mT0, mT1, mT2, mV, mLoc, mCy, mU3,
                          static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
                          fg, e, var.quad_a) != cudaSuccess ||
       !record_event(events, ev++, stream))
@@ -324,7 +362,7 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
       const int units = B * (e / WK_ET) * sp.S;
       tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
           mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S,
-          sp.L);
+          sp.L, nullptr);
       if (cudaGetLastError() != cudaSuccess) return 1;
       if (sp.S > 1 || !causal) {
         const int64_t lanes = (int64_t)B * se / 8;

@@ -166,6 +166,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
                    const __grid_constant__ CUtensorMap mapV,   // V 3-D, box {64, 128, 2}
                    const __grid_constant__ CUtensorMap mapS,   // local sums 3-D, box {64, 128, 2}
                    const __grid_constant__ CUtensorMap mapCy,  // carries 3-D, box {64, 128, 2}
+                   const __grid_constant__ CUtensorMap mapU,   // U 3-D, box {64, 128, 2} (L2 prefetch)
                    const __nv_bfloat16 *__restrict__ U,        // [B*n][e]
                    __nv_bfloat16 *__restrict__ O,              // [B*n][e]
                    FusedGrid grid, int e, float quad_a) {
@@ -233,6 +234,7 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
       tma_prefetch_desc(&mapV);
       tma_prefetch_desc(&mapS);
       tma_prefetch_desc(&mapCy);
+      tma_prefetch_desc(&mapU);
       int it = 0;
       bool ok = true, rows_ready = false, prefix_ready = false;
       // one ring item: waits for its slot, then one 32 KB box
@@ -284,6 +286,8 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         const int nkb = (f.nkv + FU_PSLOTS - 1) / FU_PSLOTS;
         for (int x = 0; x < f.net && ok; ++x) {
           const int eb = (f.et0 + x) * (FU_ET / 64);  // first 64-column block of the tile
+          // the epilogue's U rows of this tile, into L2 ahead of its loads
+          tma_prefetch_l2_3d(&mapU, 0, f.row0, eb);
           for (int kb = 0; kb < nkb && ok; ++kb) {
             const int ni = block_stages(f, kb) / 2;   // items of 128 keys
             const int key0 = f.crow + kb * FU_PSLOTS * KEY_STAGE;

@@ -1,0 +1,655 @@
+// tc_pair.cuh -- the chunk-local kernel of the mixed-chunk attention core for
+// causal chunks of 256 tokens with a global term, both 128-row tiles of a
+// chunk in one unit:
+//     O = U * (relu(T0 T1^T * a)^2 V_g + T2 local_g + T2 carry)
+// ("FLASH: Possibly the Most Interesting Efficient Transformer Design
+// Recently", section "Mixed Chunk": V-hat^quad_g with the upper triangle
+// masked, plus V-hat^lin_g from the chunk walkers' local sums and carries,
+// gated by U_g).  Included by tc.cu.
+//
+// The chunk-local kernel streams V, the local sums and the carries once per
+// e tile; with one row tile per unit (tc_chunk_fused) both row tiles of a
+// chunk load them.  Here a unit is (chunk, run of 128-column e tiles) and
+// each e tile's operands serve both row tiles, about 40% fewer bytes through
+// an SM, which is what bounds the kernel (its loads take microseconds to
+// land, so the bytes each SM can have in flight set the rate).
+//   S   = T0_r T1_k^T    per row tile r and 64-key stage k (r = 0: k < 2;
+//                        r = 1: k < 4), M = 128, N = 64, K = s, through one
+//                        TMEM S slot, once per unit
+//   P   = relu(S a)^2    masked (key > query -> 0) by four relu^2 warps, bf16
+//                        in TMEM, resident for the unit (6 slots)
+//   per e tile, r = 1 then 0:
+//     O_r  = sum_k P_rk V_k + T2_r (local_g + carry)   (A of the first from
+//            TMEM; M = 128, N = 128); two merge warps add the carry tile into
+//            the local-sum tile in shared memory first (one product instead
+//            of two, and the carry's slot goes back at once)
+//     out  = U * O_r      eight warps (the epilogue warps columns 0-63, the
+//                         relu^2 warps, idle once a unit's weights are formed,
+//                         columns 64-127); O_1 drains while O_0 forms and the
+//                         reverse, so each accumulator buffers the other
+// Row tile 1 goes first: it alone reads the keys 128-255, whose V item then
+// goes back early for the next e tile's copies.
+// Shared memory: a ring of 5 items of 32 KB (3-D TMA boxes of 128 rows x two
+// 64-column blocks): T0 of each row tile, T1 of keys 0-127 and 128-255 (unit
+// start), then per e tile V of keys 0-127 and 128-255, the local sums and the
+// carry; and the T2 rows of both row tiles (64 KB) for the unit.
+// TMEM (512 columns): O_0 [0, 128), O_1 [128, 256), S [256, 320), P [320, 512).
+#pragma once
+
+#include "tc_common.cuh"
+#include "tc_fused.cuh"
+
+namespace fmca {
+namespace {
+
+constexpr int PA_RING = 5;
+constexpr uint32_t PA_ITEM = 32768;
+constexpr uint32_t PA_OFF_B = PA_RING * PA_ITEM;   // T2 rows of both row tiles
+constexpr uint32_t PAIR_SMEM = PA_OFF_B + 2 * PA_ITEM + 1024;
+constexpr int PA_PSLOTS = 6;                       // relu^2 weights: 2 + 4 stages
+constexpr uint32_t PA_COL_S = 256, PA_COL_P = 320;
+// warps: 0 producer, 1 MMA, 2-3 merge, 4-7 relu^2 then epilogue (columns
+// 64-127), 8-11 epilogue (columns 0-63)
+constexpr int PAIR_THREADS = 384;
+static_assert(PAIR_SMEM <= 232448, "tc_chunk_pair exceeds 227 KB of shared memory");
+
+// stages of row tile r and its first P slot
+__device__ __forceinline__ int pair_stages(int r) { return r == 0 ? 2 : 4; }
+__device__ __forceinline__ int pair_pslot(int r, int k) { return r == 0 ? k : 2 + k; }
+
+// Tiles t = bg * n_et + et; CTA c takes [c T / grid, (c + 1) T / grid) (equal
+// cost per tile); a unit is the run of one chunk's e tiles in that range.
+struct PairGrid {
+  int n, G, n_et, n_tiles;
+  int S, L;        // segments of the chunk axis, chunks each
+  int rows_early;  // the T rows may be read before the grid-dependency wait
+  int B;
+  int carries;     // form the segment carries here (S > 1) before the first carry load
+};
+
+struct PairUnit {
+  int crow;   // first token row of the chunk in [B*n]
+  int lrow;   // first row of its local sums in [B*G*s]
+  int crow2;  // first row of its carry in [B*S*s]
+  bool carry; // past the first segment
+  int et0, net;
+};
+
+__device__ __forceinline__ PairUnit decode_pair(int t, int net, const PairGrid &g) {
+  const int bg = t / g.n_et;
+  const int b = bg / g.G, c = bg % g.G;
+  PairUnit f;
+  f.crow = b * g.n + c * 256;
+  f.lrow = bg * S_DIM;
+  f.crow2 = (b * g.S + c / g.L) * S_DIM;
+  f.carry = c / g.L > 0;
+  f.et0 = t % g.n_et;
+  f.net = net;
+  return f;
+}
+
+// out = U * O for 64 columns of this thread's row: uv the U values (already
+// loaded), taddr the TMEM address of the accumulator's columns, roff the
+// element offset of the row's columns in O.
+__device__ __forceinline__ void pair_gate64(const u32x8 (&uv)[4], __nv_bfloat16 *__restrict__ O,
+                                            size_t roff, uint32_t taddr) {
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {  // 32 columns at a time
+    uint32_t o32[32];
+    tmem_ld32(taddr + 32 * q, o32);
+    tmem_ld_wait();
+#pragma unroll
+    for (int c2 = 0; c2 < 2; ++c2) {  // 16 columns per 32-byte access
+      const u32x8 &uu = uv[2 * q + c2];
+      const uint32_t wv[8] = {uu.lo.x, uu.lo.y, uu.lo.z, uu.lo.w, uu.hi.x, uu.hi.y, uu.hi.z, uu.hi.w};
+      uint32_t o[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int jj = 16 * c2 + 2 * i;
+        o[i] = pack_bf16x2(bf16_lo(wv[i]) * __uint_as_float(o32[jj]),
+                           bf16_hi(wv[i]) * __uint_as_float(o32[jj + 1]));
+      }
+      u32x8 ov;
+      ov.lo = make_uint4(o[0], o[1], o[2], o[3]);
+      ov.hi = make_uint4(o[4], o[5], o[6], o[7]);
+      stg_stream(O + roff + 32 * q + 16 * c2, ov);
+    }
+  }
+}
+
+__global__ void __launch_bounds__(PAIR_THREADS, 1)
+    tc_chunk_pair(const __grid_constant__ CUtensorMap mapT0,  // T0 rows, 3-D box {64, 128, 2}
+                  const __grid_constant__ CUtensorMap mapT1,  // T1 rows, 3-D box {64, 128, 2}
+                  const __grid_constant__ CUtensorMap mapT2,  // T2 rows, 3-D box {64, 128, 2}
+                  const __grid_constant__ CUtensorMap mapV,   // V 3-D, box {64, 128, 2}
+                  const __grid_constant__ CUtensorMap mapS,   // local sums 3-D, box {64, 128, 2}
+                  const __grid_constant__ CUtensorMap mapCy,  // carries 3-D, box {64, 128, 2}
+                  const __grid_constant__ CUtensorMap mapU,   // U 3-D, box {64, 128, 2} (L2 prefetch)
+                  const __nv_bfloat16 *__restrict__ U,        // [B*n][e]
+                  __nv_bfloat16 *__restrict__ O,              // [B*n][e]
+                  PairGrid grid, int e, float quad_a,
+                  __nv_bfloat16 *__restrict__ seg,  // segment totals -> carries, in place
+                  unsigned int *__restrict__ carried) {  // CTAs done with their carries
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  __shared__ __align__(8) uint64_t uq_full[FU_QUEUE], uq_empty[FU_QUEUE];
+  __shared__ __align__(8) uint64_t b_full, b_empty;
+  __shared__ __align__(8) uint64_t full[PA_RING], empty[PA_RING];
+  __shared__ __align__(8) uint64_t s_full, s_empty;
+  __shared__ __align__(8) uint64_t p_full[PA_PSLOTS], p_empty[PA_PSLOTS];
+  __shared__ __align__(8) uint64_t o_full[2], o_empty[2], mma_done;
+  // the MMA thread, the ring's only in-order consumer, hands an e tile's
+  // local-sum and carry items to the merge warps (mg_go) once they have
+  // landed; the merge warps hand the sum back (m_full)
+  __shared__ __align__(8) uint64_t mg_go, m_full;
+  __shared__ int uq_unit[FU_QUEUE], uq_net[FU_QUEUE];
+  __shared__ uint32_t tmem_base;
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < FU_QUEUE; ++i) {
+      mbar_init(&uq_full[i], 1);
+      mbar_init(&uq_empty[i], 4);  // MMA issuer, merge, relu^2 and epilogue warps
+    }
+    mbar_init(&b_full, 1);
+    mbar_init(&b_empty, 1);
+    for (int i = 0; i < PA_RING; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(&s_full, 1);
+    mbar_init(&s_empty, 1);
+    for (int i = 0; i < PA_PSLOTS; ++i) {
+      mbar_init(&p_full[i], 1);
+      mbar_init(&p_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&o_full[i], 1);   // tcgen05.commit
+      mbar_init(&o_empty[i], 2);  // both column halves drained
+    }
+    mbar_init(&mma_done, 1);
+    mbar_init(&mg_go, 1);
+    mbar_init(&m_full, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tbase = tmem_base;
+  uint8_t *ring = smem;
+  uint8_t *bbuf = smem + PA_OFF_B;
+
+  // The segment carries, formed while the unit's rows, scores and weights
+  // come in: warps 2-3 and 8-11 (idle until the first merge and output tile)
+  // turn this CTA's share of the column groups' totals into carries, then
+  // the CTA is counted; the producer loads no carry before every CTA is.
+  if (grid.carries && (warp == 2 || warp == 3 || warp >= 8)) {
+    const int ct = (warp < 8 ? warp - 2 : warp - 6) * 32 + lane;  // 0 .. 191
+    griddep_wait();  // the walkers' totals
+    const int64_t se = (int64_t)S_DIM * e;
+    const int64_t groups = (int64_t)grid.B * (se / 8);
+    for (int64_t t = (int64_t)blockIdx.x * 192 + ct; t < groups; t += (int64_t)gridDim.x * 192)
+      seg_carry_group(seg, grid.S, se, 1, t);
+    named_bar_sync(5, 192);
+    // every thread's carries are stored (the barrier orders them before the
+    // release)
+    if (ct == 0) red_release_add_gpu(carried, 1u);
+  }
+
+  if (warp == 0) {
+    // =========================== producer: unit queue, ring, T2 rows
+    if (lane == 0) {
+      tma_prefetch_desc(&mapT0);
+      tma_prefetch_desc(&mapT1);
+      tma_prefetch_desc(&mapT2);
+      tma_prefetch_desc(&mapV);
+      tma_prefetch_desc(&mapS);
+      tma_prefetch_desc(&mapCy);
+      tma_prefetch_desc(&mapU);
+      int it = 0;
+      bool ok = true, rows_ready = false, sums_ready = false;
+      // one ring item: waits for its slot, then one 32 KB box
+      auto issue = [&](const CUtensorMap *map, int y, int z) -> bool {
+        const int slot = it % PA_RING;
+        if (it >= PA_RING && !mbar_wait(&empty[slot], ((it / PA_RING) - 1) & 1, kWaitLimitNs)) {
+          record_timeout(802);
+          return false;
+        }
+        mbar_arrive_expect_tx(&full[slot], PA_ITEM);
+        tma_load_3d(ring + slot * PA_ITEM, map, &full[slot], 0, y, z);
+        ++it;
+        return true;
+      };
+      int t = (int)(((int64_t)blockIdx.x * grid.n_tiles) / gridDim.x);
+      const int t_end = (int)(((int64_t)(blockIdx.x + 1) * grid.n_tiles) / gridDim.x);
+      for (int j = 0; ok; ++j) {
+        const int uu = t < t_end ? t : -1;
+        const int net = uu >= 0 ? min(grid.n_et - t % grid.n_et, t_end - t) : 0;
+        t += net;
+        const int qs = j % FU_QUEUE;
+        if (j >= FU_QUEUE && !mbar_wait(&uq_empty[qs], ((j / FU_QUEUE) - 1) & 1, kWaitLimitNs)) {
+          record_timeout(800);
+          break;
+        }
+        uq_unit[qs] = uu;
+        uq_net[qs] = net;
+        mbar_arrive(&uq_full[qs]);
+        if (uu < 0) break;
+        const PairUnit f = decode_pair(uu, net, grid);
+        // the T rows: with the carry kernel between their writer and this
+        // grid, the writer had completed before this grid launched; otherwise
+        // wait for the kernel before
+        if (!grid.rows_early && !rows_ready) {
+          griddep_wait();
+          rows_ready = true;
+        }
+        // T0 of row tile 0, T1 of keys 0-127, T0 of row tile 1, T1 of keys
+        // 128-255, in the order the score products use them
+        ok = issue(&mapT0, f.crow, 0) && issue(&mapT1, f.crow, 0) &&
+             issue(&mapT0, f.crow + 128, 0) && issue(&mapT1, f.crow + 128, 0);
+        if (!ok) break;
+        // T2 of both row tiles: the previous unit's global products are done
+        if (j >= 1 && !mbar_wait(&b_empty, (j - 1) & 1, kWaitLimitNs)) {
+          record_timeout(804);
+          break;
+        }
+        mbar_arrive_expect_tx(&b_full, 2 * PA_ITEM);
+        tma_load_3d(bbuf, &mapT2, &b_full, 0, f.crow, 0);
+        tma_load_3d(bbuf + PA_ITEM, &mapT2, &b_full, 0, f.crow + 128, 0);
+        for (int x = 0; x < f.net && ok; ++x) {
+          const int eb = (f.et0 + x) * 2;  // first 64-column block of the e tile
+          ok = issue(&mapV, f.crow, eb) && issue(&mapV, f.crow + 128, eb);
+          // the epilogue's U rows of this e tile, into L2 ahead of its loads
+          // (their latency from DRAM otherwise sets the pace)
+          tma_prefetch_l2_3d(&mapU, 0, f.crow + 128, eb);
+          tma_prefetch_l2_3d(&mapU, 0, f.crow, eb);
+          // the local sums and carries come from the kernels before: wait
+          // once, before the first such load
+          if (ok && !sums_ready) {
+            griddep_wait();
+            // every CTA has formed its share of the carries
+            if (grid.carries) {
+              if (!wait_count_geq(carried, gridDim.x, kWaitLimitNs)) {
+                record_timeout(805);
+                ok = false;
+                break;
+              }
+              fence_proxy_async_global();  // read next through the async proxy
+            }
+            sums_ready = true;
+          }
+          if (ok) ok = issue(&mapS, f.lrow, eb);
+          if (ok && f.carry) ok = issue(&mapCy, f.crow2, eb);
+        }
+      }
+      // drain: the last load issued into every ring slot has landed
+      for (int q = (it > PA_RING ? it - PA_RING : 0); q < it; ++q)
+        if (!mbar_wait(&full[q % PA_RING], (q / PA_RING) & 1, kWaitLimitNs)) record_timeout(803);
+    }
+  } else if (warp == 1) {
+    // =========================== MMA issuer
+    if (lane == 0) {
+      // S = T0 T1^T: M = 128 rows, N = 64 keys, A and B K-major
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, KEY_STAGE, false, false);
+      // O += P V (A from TMEM) and O += T2 (local | carry) (A K-major); B MN-major
+      constexpr uint32_t idesc_o = idesc_bf16_f32(128, FU_ET, false, true);
+      const uint32_t baddr = smem_u32(bbuf);
+      int it = 0, sc = 0, tcnt = 0, mcnt = 0;
+      bool ok = true;
+      auto wait_item = [&](int item) -> bool {
+        if (!mbar_wait(&full[item % PA_RING], (item / PA_RING) & 1, kWaitLimitNs)) {
+          record_timeout(824);
+          return false;
+        }
+        return true;
+      };
+      auto slot_addr = [&](int item) -> uint32_t {
+        return smem_u32(ring + (item % PA_RING) * PA_ITEM);
+      };
+      for (int j = 0;; ++j) {
+        const int qs = j % FU_QUEUE;
+        if (!mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs)) {
+          record_timeout(820);
+          ok = false;
+          break;
+        }
+        const int u = uq_unit[qs], unet = uq_net[qs];
+        mbar_arrive(&uq_empty[qs]);
+        if (u < 0) break;
+        const PairUnit f = decode_pair(u, unet, grid);
+        // ---- scores, once per unit: row tile 0 (2 stages), row tile 1 (4)
+        const int i_a0 = it, i_k0 = it + 1, i_a1 = it + 2, i_k1 = it + 3;
+        it += 4;
+        for (int r = 0; r < 2 && ok; ++r) {
+          const int i_a = r ? i_a1 : i_a0;
+          if (!wait_item(i_a)) {
+            ok = false;
+            break;
+          }
+          const uint32_t aaddr = slot_addr(i_a);
+          for (int k = 0; k < pair_stages(r) && ok; ++k) {
+            const int i_k = k < 2 ? i_k0 : i_k1;
+            if (!wait_item(i_k)) {
+              ok = false;
+              break;
+            }
+            if (sc >= 1 && !mbar_wait(&s_empty, (sc - 1) & 1, kWaitLimitNs)) {
+              record_timeout(826);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t kaddr = slot_addr(i_k);
+            const uint32_t sd = tbase + PA_COL_S;
+#pragma unroll
+            for (int kk = 0; kk < S_DIM / 16; ++kk) {
+              const uint64_t ad =
+                  smem_desc_sw128(aaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(
+                  kaddr + (kk >> 2) * 16384 + (k & 1) * 8192 + (kk & 3) * 32, 16, 1024);
+              mma_bf16_ss(sd, ad, bd, idesc_s, kk != 0);
+            }
+            mma_commit(&s_full);
+            ++sc;
+            // the items go back after their last score product
+            if (r == 0 && k == 1) mma_commit(&empty[i_a0 % PA_RING]);
+            if (r == 1 && k == 1) mma_commit(&empty[i_k0 % PA_RING]);
+            if (r == 1 && k == 3) {
+              mma_commit(&empty[i_a1 % PA_RING]);
+              mma_commit(&empty[i_k1 % PA_RING]);
+            }
+          }
+        }
+        if (!ok) break;
+        // ---- e tiles: row tile 1 (stages 2, 3 then 0, 1), then row tile 0
+        // (stages 0, 1); O_r = sum_k P_rk V_k + T2_r (local + carry)
+        for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
+          const int iv0 = it, iv1 = it + 1, il = it + 2;
+          it += f.carry ? 4 : 3;
+          for (int rr = 0; rr < 2 && ok; ++rr) {
+            const int r = 1 - rr;
+            // the epilogue has drained O_r (the previous e tile's)
+            if (tcnt >= 1 && !mbar_wait(&o_empty[r], (tcnt - 1) & 1, kWaitLimitNs)) {
+              record_timeout(823);
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t ocol = tbase + (uint32_t)(r * FU_ET);
+            const int ns = pair_stages(r);
+            for (int q = 0; q < ns && ok; ++q) {
+              const int k = r == 1 ? (q + 2) % 4 : q;  // row tile 1: keys 128-255 first
+              const int iv = k < 2 ? iv0 : iv1, ps = pair_pslot(r, k);
+              if (!wait_item(iv)) {
+                ok = false;
+                break;
+              }
+              if (x == 0 && !mbar_wait(&p_full[ps], j & 1, kWaitLimitNs)) {
+                record_timeout(822);
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              const uint32_t vb = slot_addr(iv) + (k & 1) * 8192;
+              const uint32_t pa = tbase + PA_COL_P + (uint32_t)(32 * ps);
+#pragma unroll
+              for (int kk = 0; kk < KEY_STAGE / 16; ++kk)
+                mma_bf16_ts(ocol, pa + 8 * kk, smem_desc_sw128(vb + kk * 2048, 16384, 1024),
+                            idesc_o, (q == 0 && kk == 0) ? 0u : 1u);
+              // keys 128-255 are row tile 1's alone
+              if (r == 1 && k == 3) {
+                mma_commit(&empty[iv1 % PA_RING]);
+                // the local sums and the carry have landed: merge them while
+                // the keys 0-127 products run
+                if (f.carry) {
+                  if (!wait_item(il) || !wait_item(il + 1)) {
+                    ok = false;
+                    break;
+                  }
+                  mbar_arrive(&mg_go);
+                }
+              }
+            }
+            if (!ok) break;
+            if (r == 0) mma_commit(&empty[iv0 % PA_RING]);  // row tile 0 read keys 0-127 last
+            if (x == 0 && r == 1 && !mbar_wait(&b_full, j & 1, kWaitLimitNs)) {
+              record_timeout(827);
+              ok = false;
+              break;
+            }
+            // the local sums, with the carry added by the merge warps
+            if (r == 1) {
+              if (f.carry ? !mbar_wait(&m_full, mcnt & 1, kWaitLimitNs) : !wait_item(il)) {
+                record_timeout(828);
+                ok = false;
+                break;
+              }
+              if (f.carry) ++mcnt;
+            }
+            tc_fence_after();
+            const uint32_t pb = slot_addr(il);
+            const uint32_t ab = baddr + (uint32_t)r * PA_ITEM;
+#pragma unroll
+            for (int kk = 0; kk < S_DIM / 16; ++kk) {
+              const uint64_t ad = smem_desc_sw128(ab + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+              const uint64_t bd = smem_desc_sw128(pb + kk * 2048, 16384, 1024);
+              mma_bf16_ss(ocol, ad, bd, idesc_o, 1u);
+            }
+            if (r == 0) mma_commit(&empty[il % PA_RING]);
+            mma_commit(&o_full[r]);
+          }
+        }
+        if (!ok) break;
+        // the unit's relu^2 weights and T2 rows are done with
+        for (int ps = 0; ps < PA_PSLOTS; ++ps) mma_commit(&p_empty[ps]);
+        mma_commit(&b_empty);
+      }
+      // every MMA has finished before TMEM is released
+      mma_commit(&mma_done);
+      if (!mbar_wait(&mma_done, 0, kWaitLimitNs)) record_timeout(829);
+    }
+  } else if (warp == 2 || warp == 3) {
+    // =========================== merge warps (64 threads): local += carry
+    // in the local-sum item, in place (both items are the same 128-byte
+    // swizzled [2][128][64] layout, so the sum is element by element)
+    const int mt = threadIdx.x - 64;
+    int it = 0, mcnt = 0;
+    bool ok = true;
+    for (int j = 0; ok; ++j) {
+      const int qs = j % FU_QUEUE;
+      const bool got = mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs);
+      const int u = got ? uq_unit[qs] : -1, unet = got ? uq_net[qs] : 0;
+      const bool more = named_bar_and(4, 64, u >= 0);
+      if (mt == 0 && got) mbar_arrive(&uq_empty[qs]);
+      if (!more) {
+        if (!got && mt == 0) record_timeout(860);
+        break;
+      }
+      const PairUnit f = decode_pair(u, unet, grid);
+      it += 4;  // the unit's T0 and T1 items
+      for (int x = 0; x < f.net && ok; ++x) {
+        const int il = it + 2, icy = it + 3;
+        it += f.carry ? 4 : 3;
+        if (!f.carry) continue;
+        const bool w = mbar_wait(&mg_go, mcnt & 1, kWaitLimitNs);
+        ++mcnt;
+        if (w) {
+          uint4 *lp = reinterpret_cast<uint4 *>(ring + (il % PA_RING) * PA_ITEM);
+          const uint4 *cp = reinterpret_cast<const uint4 *>(ring + (icy % PA_RING) * PA_ITEM);
+#pragma unroll 4
+          for (int i = mt; i < (int)(PA_ITEM / 16); i += 64) {
+            const uint4 a = lp[i], c = cp[i];
+            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              o[q] = pack_bf16x2(bf16_lo(aw[q]) + bf16_lo(cw[q]), bf16_hi(aw[q]) + bf16_hi(cw[q]));
+            lp[i] = make_uint4(o[0], o[1], o[2], o[3]);
+          }
+          fence_proxy_async_smem();  // read next by the MMA
+        }
+        ok = named_bar_and(4, 64, w);
+        if (!ok) {
+          if (mt == 0) record_timeout(861);
+          break;
+        }
+        if (mt == 0) {
+          mbar_arrive(&m_full);
+          mbar_arrive(&empty[icy % PA_RING]);  // the carry item is no longer needed
+        }
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // =========================== relu^2 warps (128 threads): S -> P in TMEM
+    const int mt = threadIdx.x - 128;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // query row within its row tile (TMEM lane)
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    int sc = 0, tcnt = 0;
+    bool ok = true;
+    for (int j = 0; ok; ++j) {
+      const int qs = j % FU_QUEUE;
+      const bool got = mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs);
+      const int u = got ? uq_unit[qs] : -1, unet = got ? uq_net[qs] : 0;
+      const bool more = named_bar_and(2, 128, u >= 0);
+      if (mt == 0 && got) mbar_arrive(&uq_empty[qs]);
+      if (!more) {
+        if (!got && mt == 0) record_timeout(840);
+        break;
+      }
+      for (int r = 0; r < 2 && ok; ++r) {
+        const int qpos = r * ROW_TILE + row;  // query position within the chunk
+        for (int k = 0; k < pair_stages(r); ++k, ++sc) {
+          const int ps = pair_pslot(r, k);
+          bool w = mbar_wait(&s_full, sc & 1, kWaitLimitNs);
+          // the previous unit's last product that read this P slot has completed
+          if (w && j >= 1) w = mbar_wait(&p_empty[ps], (j - 1) & 1, kWaitLimitNs);
+          uint32_t sv[2][32];
+          if (w) {
+            tc_fence_after();
+            const uint32_t sa = tbase + lane_off + PA_COL_S;
+            tmem_ld32(sa, sv[0]);
+            tmem_ld32(sa + 32, sv[1]);
+            tmem_ld_wait();
+            tc_fence_before();
+          }
+          // every thread has read the S slot: the next score product may start
+          // while these weights are formed
+          if (!named_bar_and(2, 128, w)) {
+            if (mt == 0) record_timeout(842);
+            ok = false;
+            break;
+          }
+          if (mt == 0) mbar_arrive(&s_empty);
+          {
+            // relu(S a)^2 (a = 1/C by default); key position > query position
+            // -> 0; two keys a column, the lower key in the low half
+            const int kbase = k * KEY_STAGE;
+            uint32_t pk[32];
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2)
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const int key = kbase + c2 * 32 + 2 * i;
+                float x0 = fmaxf(__uint_as_float(sv[c2][2 * i]) * quad_a, 0.f);
+                float x1 = fmaxf(__uint_as_float(sv[c2][2 * i + 1]) * quad_a, 0.f);
+                x0 *= x0;
+                x1 *= x1;
+                if (key > qpos) x0 = 0.f;
+                if (key + 1 > qpos) x1 = 0.f;
+                pk[c2 * 16 + i] = pack_bf16x2(x0, x1);
+              }
+            tmem_st32(tbase + lane_off + PA_COL_P + (uint32_t)(32 * ps), pk);
+            tmem_st_wait();
+            tc_fence_before();
+          }
+          ok = named_bar_and(2, 128, w);
+          if (!ok) {
+            if (mt == 0) record_timeout(841);
+            break;
+          }
+          if (mt == 0) mbar_arrive(&p_full[ps]);
+        }
+      }
+      // then columns 64-127 of the unit's output tiles (the epilogue warps
+      // take 0-63)
+      const PairUnit f = decode_pair(u, unet, grid);
+      for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
+        for (int rr = 0; rr < 2 && ok; ++rr) {
+          const int r = 1 - rr;
+          const size_t roff =
+              (size_t)(f.crow + r * ROW_TILE + row) * (size_t)e + (f.et0 + x) * FU_ET + 64;
+          u32x8 uv[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) uv[c] = ldg_stream(U + roff + 16 * c);
+          const bool w = mbar_wait(&o_full[r], tcnt & 1, kWaitLimitNs);
+          if (w) {
+            tc_fence_after();
+            pair_gate64(uv, O, roff, tbase + lane_off + (uint32_t)(r * FU_ET + 64));
+            tc_fence_before();
+          }
+          ok = named_bar_and(2, 128, w);
+          if (!ok) {
+            if (mt == 0) record_timeout(852);
+            break;
+          }
+          if (mt == 0) mbar_arrive(&o_empty[r]);
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // =========================== epilogue warps (128 threads)
+    const int mt = threadIdx.x - 256;
+    const int quad = warp & 3;
+    const int row = quad * 32 + lane;  // tile row (TMEM lane)
+    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    int tcnt = 0;
+    bool ok = true;
+    for (int j = 0; ok; ++j) {
+      const int qs = j % FU_QUEUE;
+      const bool got = mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs);
+      const int u = got ? uq_unit[qs] : -1, unet = got ? uq_net[qs] : 0;
+      const bool more = named_bar_and(3, 128, u >= 0);
+      if (mt == 0 && got) mbar_arrive(&uq_empty[qs]);
+      if (!more) {
+        if (!got && mt == 0) record_timeout(850);
+        break;
+      }
+      const PairUnit f = decode_pair(u, unet, grid);
+      for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
+        for (int rr = 0; rr < 2 && ok; ++rr) {
+          const int r = 1 - rr;  // the order the accumulators are formed in
+          // columns 0-63 of the e tile (the relu^2 warps take 64-127)
+          const size_t roff = (size_t)(f.crow + r * ROW_TILE + row) * (size_t)e + (f.et0 + x) * FU_ET;
+          u32x8 uv[4];
+#pragma unroll
+          for (int c = 0; c < 4; ++c) uv[c] = ldg_stream(U + roff + 16 * c);
+          const bool w = mbar_wait(&o_full[r], tcnt & 1, kWaitLimitNs);
+          if (w) {
+            tc_fence_after();
+            pair_gate64(uv, O, roff, tbase + lane_off + (uint32_t)(r * FU_ET));
+            tc_fence_before();
+          }
+          ok = named_bar_and(3, 128, w);
+          if (!ok) {
+            if (mt == 0) record_timeout(851);
+            break;
+          }
+          if (mt == 0) mbar_arrive(&o_empty[r]);  // this half of O_r is drained
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) tmem_dealloc(tbase, 512);
+}
+
+}  // namespace
+}  // namespace fmca

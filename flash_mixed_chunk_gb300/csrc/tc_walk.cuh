@@ -70,7 +70,8 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
                   const __grid_constant__ CUtensorMap mapT,   // totals [B*S*s][e], box {64, 128}
                   const float *__restrict__ gamma, const float *__restrict__ beta,
                   __nv_bfloat16 *__restrict__ trows, int64_t rows_plane, int B, int n, int e,
-                  int C, int causal, int lin_norm, int S, int L) {
+                  int C, int causal, int lin_norm, int S, int L,
+                  unsigned int *__restrict__ zero_count) {  // cleared here if not null
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -110,6 +111,11 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
     tmem_alloc(&tmem_base, 512);
     tmem_relinquish();
   }
+  // the next kernel's CTAs may take the SMs this grid leaves free, and each
+  // SM as its walker ends; they read nothing of ours before their
+  // grid-dependency wait.  Its counter starts at zero.
+  if (threadIdx.x == 0 && blockIdx.x == 0 && zero_count != nullptr) *zero_count = 0u;
+  griddep_launch_dependents();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -349,17 +355,13 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
   if (warp == 1) tmem_dealloc(tbase, 512);
 }
 
-// tc_seg_carry: the walkers' segment totals [B][S][s][e] (bf16) into carries,
-// in place: causal, carry_sg = the sum of the totals before segment sg
-// (carry_0 = 0); bidirectional, the sum of all of them, in slot 0.  fp32
-// sums, one thread per 8 columns.  A programmatic dependent of the walkers.
-__global__ void __launch_bounds__(256)
-    tc_seg_carry(__nv_bfloat16 *__restrict__ T, int B, int S, int64_t se, int causal) {
-  griddep_wait();  // the walkers' totals
-  griddep_launch_dependents();
+// Segment totals -> carries for one group of 8 columns (t of B * s * e / 8),
+// in place in T [B][S][s][e] (bf16): causal, carry_sg = the sum of the
+// totals before segment sg (carry_0 = 0); bidirectional, the sum of all of
+// them, in slot 0.  fp32 sums.
+__device__ __forceinline__ void seg_carry_group(__nv_bfloat16 *__restrict__ T, int S, int64_t se,
+                                                int causal, int64_t t) {
   const int64_t per_b = se / 8;
-  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (t >= (int64_t)B * per_b) return;
   const int64_t b = t / per_b, x = (t % per_b) * 8;
   __nv_bfloat16 *p = T + b * S * se + x;
   float run[8];
@@ -392,6 +394,17 @@ __global__ void __launch_bounds__(256)
     }
   }
   if (!causal) put(p);
+}
+
+// tc_seg_carry: seg_carry_group over all column groups, one thread each; a
+// programmatic dependent of the walkers.
+__global__ void __launch_bounds__(256)
+    tc_seg_carry(__nv_bfloat16 *__restrict__ T, int B, int S, int64_t se, int causal) {
+  griddep_wait();  // the walkers' totals
+  griddep_launch_dependents();
+  const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= (int64_t)B * (se / 8)) return;
+  seg_carry_group(T, S, se, causal, t);
 }
 
 // tc_prefix_fixup (the form the backward pass runs): the scaled prefix

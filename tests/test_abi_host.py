@@ -103,9 +103,10 @@ def test_auto_path_choice():
 
 def test_launch_counts():
     bf = fm.FMCA_BF16
-    # the segment walkers (local sums, totals, T rows), the segment carries,
-    # the fused chunk kernel
-    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 3
+    # causal chunks of 256: the segment walkers (local sums, totals, T rows),
+    # then the row-pair kernel, which forms the segment carries itself
+    assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 2
+    # bidirectional: walkers, the segment carries, the fused chunk kernel
     assert fm.flash_mca_launch_count(4, 4096, 128, 1536, 256, 0, bf) == 3
     # one segment per sequence (B * e / 256 >= 144 units): no carries
     assert fm.flash_mca_launch_count(16, 1024, 128, 2560, 256, 1, bf) == 2
@@ -115,7 +116,7 @@ def test_launch_counts():
     assert fm.flash_mca_launch_count(8, 1024, 128, 1536, 1024, 1, bf, fm.FMCA_PATH_SIMT,
                                      lin_norm=fm.FMCA_LIN_NORM_NONE) == 3
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf,
-                                     lin_norm=fm.FMCA_LIN_NORM_POSITION) == 3
+                                     lin_norm=fm.FMCA_LIN_NORM_POSITION) == 2
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
     assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
     assert fm.flash_mca_launch_count(1, 500, 128, 256, 64, 1, bf) == 0
