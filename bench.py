@@ -95,6 +95,24 @@ def algorithmic_bytes(w) -> float:
     return float(w.B * w.n * (w.s + 3 * w.e) * es)
 
 
+def kernel_algorithmic_bytes(w, kernel: str) -> float:
+    """Compulsory HBM bytes of one launch of a forward kernel: what it must
+    read of Z, V, U and write of O (its intermediates excluded).  The walkers
+    read Z and V; the output kernels read V and U and write O; the T-row
+    kernel reads Z."""
+    es = 2 if w.dtype == "bf16" else 4
+    tokens = w.B * w.n
+    if kernel == "tc_chunk_walk":
+        return float(tokens * (w.s + w.e) * es)
+    if kernel in ("tc_chunk_pair", "tc_chunk_fused"):
+        return float(tokens * 3 * w.e * es)
+    if kernel == "tc_affine_rows":
+        return float(tokens * w.s * es)
+    if kernel == "tc_seg_carry":
+        return 0.0
+    return algorithmic_bytes(w)  # the CUDA-core kernels: the whole pass
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -167,6 +185,13 @@ class ClockSampler:
         for line in self.proc.stdout:
             self.samples.append((time.time(), line.strip()))
 
+    def wait_first(self, timeout_s: float = 5.0) -> bool:
+        """Wait (bounded) until nvidia-smi has printed its first sample."""
+        t_end = time.time() + timeout_s
+        while self.proc is not None and not self.samples and time.time() < t_end:
+            time.sleep(0.01)
+        return bool(self.samples)
+
     def stop(self):
         if self.proc is not None:
             self.proc.terminate()
@@ -177,9 +202,9 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self, t0: float, t1: float):
+    def summary(self, t0: float, t1: float, label: str = "timed"):
         rows = [s for t, s in self.samples if t0 <= t <= t1]
-        window = "timed"
+        window = label
         if not rows:  # timed region shorter than the sampling period
             near = sorted(self.samples, key=lambda ts: min(abs(ts[0] - t0), abs(ts[0] - t1)))
             rows = [s for _, s in near[:2]]
@@ -375,6 +400,7 @@ def run_decode(args, device):
     torch.cuda.synchronize(device)
     sampler = ClockSampler(device.index or 0)
     sampler.start()
+    sampler.wait_first()
     # the timed loop calls the C entry point directly (pointers prepared
     # above), so that it measures the library, not Python argument checks
     opts = fm.flash_mca_default_options(C)
@@ -470,6 +496,7 @@ def run_backward(args, w, device):
     torch.cuda.synchronize(device)
     sampler = ClockSampler(device.index or 0)
     sampler.start()
+    sampler.wait_first()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
     a.record(stream)
@@ -546,6 +573,7 @@ def run_projections(args, w, device):
         torch.cuda.synchronize(device)
         sampler = ClockSampler(device.index or 0)
         sampler.start()
+        sampler.wait_first()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         wall0 = time.time()
         a.record(stream)
@@ -606,6 +634,7 @@ def run_ours(args, w, rank, world, device):
 
     sampler = ClockSampler(torch.cuda.current_device() if device.index is None else device.index)
     sampler.start()
+    sampler.wait_first()  # so that the run's window holds samples however short it is
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(device)
@@ -648,7 +677,6 @@ def run_ours(args, w, rank, world, device):
     torch.cuda.synchronize(device)
     wall1 = time.time()
     barrier()
-    sampler.stop()
     st, where = fm.flash_mca_device_status()
     if st != fm.FMCA_OK:
         raise RuntimeError(f"device status {fm.flash_mca_status_string(st)} at {where}")
@@ -673,6 +701,7 @@ def run_ours(args, w, rank, world, device):
     ms_events = k_start.elapsed_time(k_end)
     per_kernel_ms = [statistics.fmean(ev[k].elapsed_time(ev[k + 1]) for ev in events)
                      for k in range(nl)]
+    step_us = sorted(1e3 * ev[0].elapsed_time(ev[nl]) for ev in events)
 
     # ---- end to end through the host-buffer entry point
     pin = [t.pin_memory() for t in (Zc, Vc, Uc, gc, bc)]
@@ -687,6 +716,8 @@ def run_ours(args, w, rank, world, device):
     for _ in range(k_e2e):
         fm.flash_mca_forward_host(*pin, Oh, w.C, w.causal, arena, stream)
     e2e_s = reduce_max(time.perf_counter() - t, device)
+    wall2 = time.time()
+    sampler.stop()
     h2d = sum(t.numel() * t.element_size() for t in pin)
     d2h = Oh.numel() * Oh.element_size()
 
@@ -712,10 +743,19 @@ def run_ours(args, w, rank, world, device):
                for i, name in enumerate(kernel_names)}
     dom = max(kernels, key=lambda k: kernels[k]["ms"])
     dom_ms = kernels[dom]["ms"]
-    achieved = algorithmic_bytes(w) / (dom_ms / 1e3) / 1e9
+    dom_bytes = kernel_algorithmic_bytes(w, dom)
+    achieved = dom_bytes / (dom_ms / 1e3) / 1e9
     hbm_peak = float(peaks.get("hbm_gbs", PEAKS_FALLBACK["hbm_gbs"]))
     bf16_peak = float(peaks.get("bf16_tflops", PEAKS_FALLBACK["bf16_tflops"]))
     traffic = profiled_traffic(dom, w.name)
+    # the whole step: the pass's compulsory bytes over the step time, and the
+    # profiled DRAM bytes of all its launches (null unless every kernel of the
+    # step was profiled on the current sources)
+    step_gbs = algorithmic_bytes(w) / (ms / args.steps / 1e3) / 1e9
+    per_kernel_traffic = [profiled_traffic(k, w.name) for k in kernel_names]
+    step_traffic = (sum(per_kernel_traffic)
+                    if per_kernel_traffic and all(t is not None for t in per_kernel_traffic)
+                    else None)
 
     # ---- CPU baseline: the oracle as it stands, bounded sample, host cores
     cpu = None
@@ -728,7 +768,10 @@ def run_ours(args, w, rank, world, device):
         cpu = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                "sample": f"{what} of {w.name} ({dt:.1f} s; fp64 oracle, OpenMP)"}
 
-    clocks = sampler.summary(wall0, wall1)
+    # clocks over the timed pass, the per-kernel event pass and the host-buffer
+    # pass (all of them keep the GPU busy); the sampler was started, and its
+    # first sample awaited, before the warm-up
+    clocks = sampler.summary(wall0, wall2, "timed+events+e2e")
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms / args.steps,
@@ -740,9 +783,14 @@ def run_ours(args, w, rank, world, device):
         "path": "tcgen05" if path == fm.FMCA_PATH_TCGEN05 else "simt",
         "kernels": kernels,
         "ms_per_step_with_kernel_events": ms_events / args.steps,
+        "step_us_spread": {"min": step_us[0], "median": statistics.median(step_us),
+                           "max": step_us[-1], "pass": "per-kernel event pass"},
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": hbm_peak,
                      "unit": "GB/s", "frac": achieved / hbm_peak, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": algorithmic_bytes(w),
+                     "algorithmic_bytes_per_launch": dom_bytes,
+                     "step_achieved": step_gbs, "step_frac": step_gbs / hbm_peak,
+                     "step_algorithmic_bytes": algorithmic_bytes(w),
+                     "step_traffic": step_traffic,
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s"},
         "cpu_baseline": cpu,

@@ -8,8 +8,8 @@
 // while another component holds an allocation lock, or a caller that must
 // never fail half-way because an allocation could not be satisfied.  Such a
 // caller can still pass its inputs and output, but cannot provide the
-// scratch (per-chunk states, their prefix sums and the kernels' work
-// counters) that flash_mca_forward asks for.
+// scratch (the chunks' local state sums, the segment totals and carries, the
+// T rows and a grid counter) that flash_mca_forward asks for.
 //
 // The scratch is one file-scope __device__ array of FMCA_NOALLOC_SCRATCH_BYTES.
 // It belongs to this file's module (which holds no kernel): with the CUDA
@@ -21,9 +21,10 @@
 // whose work overlaps on that GPU (for example on two streams) race on it;
 // calls queued on one stream are ordered and safe.  The array keeps whatever
 // the previous call left in it: the forward pass writes every scratch byte it
-// reads before reading it, and the values that must start at zero (the work
-// counters of the persistent kernels) are cleared by the cudaMemsetAsync that
-// launch_tc_forward queues at the start of every call.
+// reads before reading it, and the one value that must start at zero (the
+// counter of output CTAs that have formed their share of the segment
+// carries) is cleared by the first kernel of every call, the walkers, before
+// the output kernel passes its grid-dependency wait.
 #include <cuda.h>
 #include <cuda_runtime.h>
 

@@ -85,9 +85,12 @@ typedef int32_t fmca_path;
 
 /*
  * Bytes of device workspace one flash_mca_forward call with these arguments
- * needs, whichever path it takes: the per-chunk linear-attention states and
- * their prefix sums (fp32 on the SIMT path; bf16 plus a few work counters and
- * flags on the tensor-core path, whose relu^2 weights never leave the chip).
+ * needs, whichever path it takes.  SIMT path: the per-chunk linear-attention
+ * states and their prefix sums, fp32.  Tensor-core path (whose relu^2 weights
+ * never leave the chip): in causal mode the chunks' local state sums (bf16,
+ * the sum of the states before each chunk within its segment of the chunk
+ * axis), the segment totals that become carries (bf16), the rows T0, T1, T2
+ * (bf16) and 256 bytes of counters.
  * Returns 0 for arguments flash_mca_forward would reject.
  */
 size_t flash_mca_workspace_bytes(int B, int n, int s, int e, int C, int causal,
@@ -179,11 +182,14 @@ fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
  * first kernel and events[i] after kernel i (1-based), so `n_events` must be
  * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
  * stream it runs on.  `opts` as for flash_mca_forward_ex (NULL: defaults).
- * Kernel order: tensor-core path -- chunk states and the rows T0, T1, T2
- * (events[0] is recorded before the reset of the work counters), state scan,
- * fused chunk kernel (scores, relu^2 weights, both products and the gate);
- * without a global term (FMCA_LIN_NORM_NONE) the rows T0, T1, then the fused
- * kernel; SIMT path -- chunk states, state scan, chunk output. */
+ * Kernel order: tensor-core path -- the segment walkers (local state sums,
+ * segment totals and the rows T0, T1, T2); then, for causal chunks of 256,
+ * the row-pair output kernel, which forms the segment carries itself; for
+ * other chunk sizes or bidirectional attention the segment-carry kernel
+ * (only with more than one segment, or bidirectional) and the fused chunk
+ * kernel (scores, relu^2 weights, both products and the gate); without a
+ * global term (FMCA_LIN_NORM_NONE) the rows T0, T1, then the fused kernel;
+ * SIMT path -- chunk states, state scan, chunk output. */
 fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
                                     const float *gamma, const float *beta, void *O, int B,
                                     int n, int s, int e, int C, int causal,
@@ -353,11 +359,12 @@ fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *h
  * library; a GPU keeps it until the process exits once this entry point has
  * run there (with eager module loading, CUDA_MODULE_LOADING=EAGER, every GPU
  * the process creates a context on holds it, whichever entry points run).
- * Problems whose tensor-core scratch (the bf16 chunk states and their prefix
- * sums, 2 B (G + Gp) s e bytes, the bf16 rows T0, T1, T2, 6 B n s bytes, and
- * a few KB; Gp = G causal or 1) exceeds it are rejected with
- * FMCA_ERR_WORKSPACE: B=2, n=8192, C=256, e=1536 fits (62.9 MB); B=1,
- * n=32768, C=256, e=2048 (159 MB) must use flash_mca_forward.  Only the tensor-core path is available (FMCA_BF16,
+ * Problems whose tensor-core scratch (in causal mode the bf16 local state
+ * sums, 2 B G s e bytes; the bf16 segment totals, 2 B S s e bytes with S the
+ * segments of the chunk axis; the bf16 rows T0, T1, T2, 6 B n s bytes; 256
+ * bytes of counters) exceeds it are rejected with FMCA_ERR_WORKSPACE: B=2,
+ * n=8192, C=256, e=1536 fits (46.4 MB); B=1, n=32768, C=256, e=2048
+ * (100.7 MB) must use flash_mca_forward.  Only the tensor-core path is available (FMCA_BF16,
  * s == 128, C % 128 == 0, e % 256 == 0); other shapes return
  * FMCA_ERR_UNSUPPORTED.
  *

@@ -66,16 +66,14 @@ def test_no_global_term_simt(B, n, C, s, e, causal, dtype):
     assert rel_err(got, ref) <= TOL[dtype]
 
 
-def test_flash_quad_base_workload_sampled_rows():
+def test_flash_quad_base_workload_whole_output():
     """B = 8, n = 1024 (the pages' base-scale sequence length), s = 128,
-    e = 1536, causal, on sampled rows the oracle computes one by one."""
+    e = 1536, causal, compared over the whole output."""
     m = fm()
     w = mca_inputs.WORKLOADS["flash_quad_base"]
     Z, V, U, gamma, beta = mca_inputs.workload_inputs(w, mca_inputs.WORKLOAD_ORDER.index(w.name) + 1)
     got = run_ex(Z, V, U, gamma, beta, w.C, w.causal, None, NONE, m.FMCA_PATH_AUTO)
-    rng = np.random.default_rng(3)
-    rows = [0, 1, 127, 128, 511, 1023, w.n, 3 * w.n + 700, w.B * w.n - 1]
-    rows += list(rng.integers(0, w.B * w.n, 12))
-    ref = oracle.rows(Z, V, U, gamma, beta, w.C, w.causal, rows, lin_norm=NONE)
-    err = rel_err(got.reshape(w.B * w.n, w.e)[rows], ref)
+    ref = oracle.forward(Z, V, U, gamma, beta, w.C, w.causal, lin_norm=NONE)
+    err = rel_err(got, ref)
+    print(f"parity flash_quad_base: normwise error {err:.3e}")
     assert err <= TOL[torch.bfloat16], f"normwise error {err:.3e}"

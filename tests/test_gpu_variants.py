@@ -92,19 +92,15 @@ def test_paths_agree(ln):
 
 
 @pytest.mark.parametrize("ln", [SUMMED, POSITION])
-def test_long_causal_sampled_rows(ln):
+def test_long_causal_whole_output(ln):
     """The full long causal shape (B=2, n=8192, C=256, s=128, e=1536) with the
-    page's 1/(cs) scale, on rows the oracle computes one by one: the first
-    and last rows of chunks 0, 1, 2 and the last chunk, and random rows."""
+    page's 1/(cs) scale, compared over the whole output."""
     w = mca_inputs.WORKLOADS["long_causal"]
     m = fm()
     Z, V, U, gamma, beta = mca_inputs.workload_inputs(w, 77)
     qs = 1.0 / (w.C * w.s)
     got = run_ex(Z, V, U, gamma, beta, w.C, w.causal, qs, ln, m.FMCA_PATH_AUTO)
-    rng = np.random.default_rng(5)
-    rows = [0, w.C - 1, w.C, 2 * w.C - 1, 2 * w.C, w.n - w.C, w.n - 1]
-    rows += [w.n + r for r in (0, w.C, 3 * w.C + 17, w.n - 1)]
-    rows += list(rng.integers(0, w.B * w.n, 8))
-    ref = oracle.rows(Z, V, U, gamma, beta, w.C, w.causal, rows, quad_scale=qs, lin_norm=ln)
-    err = rel_err(got.reshape(w.B * w.n, w.e)[rows], ref)
+    ref = oracle.forward(Z, V, U, gamma, beta, w.C, w.causal, quad_scale=qs, lin_norm=ln)
+    err = rel_err(got, ref)
+    print(f"parity long_causal lin_norm={ln}: normwise error {err:.3e}")
     assert err <= TOL[torch.bfloat16], f"normwise error {err:.3e}"
