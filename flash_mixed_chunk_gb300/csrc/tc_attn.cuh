@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(AT_THREADS, 1)
       if (ib > 0) mbar_arrive(&emptyB[(ib - 1) % AT_RING_B]);  // nobody waits on it; keeps the count even
     }
   }
+  // the single-lane roles (TMA producer, MMA issuer) rejoin their warps
+  // before the block-wide barrier, which counts converged warps
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

@@ -357,6 +357,9 @@ __global__ void __launch_bounds__(BGEMM_THREADS, 1) tc_bgemm(const __grid_consta
     if (lane == 0) bulk_wait_group<0>();
     __syncwarp();
   }
+  // the single-lane roles (TMA producer, MMA issuer) rejoin their warps
+  // before the block-wide barrier, which counts converged warps
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

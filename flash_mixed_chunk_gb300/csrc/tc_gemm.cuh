@@ -255,6 +255,9 @@ __global__ void __launch_bounds__(GEMM_THREADS, 1)
     }
     if (mt_ == 0) bulk_wait_group<0>();
   }
+  // the single-lane roles (TMA producer, MMA issuer) rejoin their warps
+  // before the block-wide barrier, which counts converged warps
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

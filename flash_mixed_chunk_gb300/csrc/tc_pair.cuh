@@ -13,11 +13,14 @@
 // each e tile's operands serve both row tiles, about 40% fewer bytes through
 // an SM, which is what bounds the kernel (its loads take microseconds to
 // land, so the bytes each SM can have in flight set the rate).
-//   S   = T0_r T1_k^T    per row tile r and 64-key stage k (r = 0: k < 2;
-//                        r = 1: k < 4), M = 128, N = 64, K = s, through one
-//                        TMEM S slot, once per unit
-//   P   = relu(S a)^2    masked (key > query -> 0) by four relu^2 warps, bf16
-//                        in TMEM, resident for the unit (6 slots)
+//   S   = T0_r T1^T      once per unit in three stages of 128 keys (M = 128,
+//                        N = 128, K = s; an N = 64 product costs more than
+//                        half of an N = 128 one): row tile 1 with keys 0-127
+//                        and 128-255, then row tile 0 with keys 0-127, into
+//                        the drained accumulators' columns
+//   P   = relu(S a)^2    masked (key > query -> 0) by four relu^2 warps, 64
+//                        keys at a time, bf16 in TMEM, resident for the unit
+//                        (6 slots)
 //   per e tile, r = 1 then 0:
 //     O_r  = sum_k P_rk V_k + T2_r (local_g + carry)   (A of the first from
 //            TMEM; M = 128, N = 128); two merge warps add the carry tile into
@@ -33,7 +36,9 @@
 // 64-column blocks): T0 of each row tile, T1 of keys 0-127 and 128-255 (unit
 // start), then per e tile V of keys 0-127 and 128-255, the local sums and the
 // carry; and the T2 rows of both row tiles (64 KB) for the unit.
-// TMEM (512 columns): O_0 [0, 128), O_1 [128, 256), S [256, 320), P [320, 512).
+// TMEM (512 columns): O_0 [0, 128), O_1 [128, 256), P [320, 512); the score
+// stages use [0, 128), [128, 256), then [0, 128) again once the first is read,
+// all before the unit's first products there.
 #pragma once
 
 #include "tc_common.cuh"
@@ -47,7 +52,7 @@ constexpr uint32_t PA_ITEM = 32768;
 constexpr uint32_t PA_OFF_B = PA_RING * PA_ITEM;   // T2 rows of both row tiles
 constexpr uint32_t PAIR_SMEM = PA_OFF_B + 2 * PA_ITEM + 1024;
 constexpr int PA_PSLOTS = 6;                       // relu^2 weights: 2 + 4 stages
-constexpr uint32_t PA_COL_S = 256, PA_COL_P = 320;
+constexpr uint32_t PA_COL_P = 320;
 // warps: 0 producer, 1 MMA, 2-3 merge, 4-7 relu^2 then epilogue (columns
 // 64-127), 8-11 epilogue (columns 0-63)
 constexpr int PAIR_THREADS = 384;
@@ -56,6 +61,11 @@ static_assert(PAIR_SMEM <= 232448, "tc_chunk_pair exceeds 227 KB of shared memor
 // stages of row tile r and its first P slot
 __device__ __forceinline__ int pair_stages(int r) { return r == 0 ? 2 : 4; }
 __device__ __forceinline__ int pair_pslot(int r, int k) { return r == 0 ? k : 2 + k; }
+// Score stages: 0 row tile 1 keys 0-127, 1 row tile 1 keys 128-255, 2 row
+// tile 0 keys 0-127; their TMEM columns
+constexpr int PA_SSTAGES = 3;
+__device__ __forceinline__ int pair_srow(int st) { return st < 2 ? 1 : 0; }
+__device__ __forceinline__ uint32_t pair_scol(int st) { return st == 1 ? 128u : 0u; }
 
 // Tiles t = bg * n_et + et; CTA c takes [c T / grid, (c + 1) T / grid) (equal
 // cost per tile); a unit is the run of one chunk's e tiles in that range.
@@ -136,7 +146,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   __shared__ __align__(8) uint64_t uq_full[FU_QUEUE], uq_empty[FU_QUEUE];
   __shared__ __align__(8) uint64_t b_full, b_empty;
   __shared__ __align__(8) uint64_t full[PA_RING], empty[PA_RING];
-  __shared__ __align__(8) uint64_t s_full, s_empty;
+  __shared__ __align__(8) uint64_t s_full[PA_SSTAGES];  // stage st's scores are in TMEM
   __shared__ __align__(8) uint64_t p_full[PA_PSLOTS], p_empty[PA_PSLOTS];
   __shared__ __align__(8) uint64_t o_full[2], o_empty[2], mma_done;
   // the MMA thread, the ring's only in-order consumer, hands an e tile's
@@ -159,8 +169,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(&s_full, 1);
-    mbar_init(&s_empty, 1);
+    for (int i = 0; i < PA_SSTAGES; ++i) mbar_init(&s_full[i], 1);
     for (int i = 0; i < PA_PSLOTS; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_empty[i], 1);
@@ -214,15 +223,19 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       tma_prefetch_desc(&mapU);
       int it = 0;
       bool ok = true, rows_ready = false, sums_ready = false;
+      const uint64_t pol_first = policy_evict_first();
       // one ring item: waits for its slot, then one 32 KB box
-      auto issue = [&](const CUtensorMap *map, int y, int z) -> bool {
+      auto issue = [&](const CUtensorMap *map, int y, int z, bool last_use = false) -> bool {
         const int slot = it % PA_RING;
         if (it >= PA_RING && !mbar_wait(&empty[slot], ((it / PA_RING) - 1) & 1, kWaitLimitNs)) {
           record_timeout(802);
           return false;
         }
         mbar_arrive_expect_tx(&full[slot], PA_ITEM);
-        tma_load_3d(ring + slot * PA_ITEM, map, &full[slot], 0, y, z);
+        if (last_use)
+          tma_load_3d_hint(ring + slot * PA_ITEM, map, &full[slot], 0, y, z, pol_first);
+        else
+          tma_load_3d(ring + slot * PA_ITEM, map, &full[slot], 0, y, z);
         ++it;
         return true;
       };
@@ -249,10 +262,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           griddep_wait();
           rows_ready = true;
         }
-        // T0 of row tile 0, T1 of keys 0-127, T0 of row tile 1, T1 of keys
-        // 128-255, in the order the score products use them
-        ok = issue(&mapT0, f.crow, 0) && issue(&mapT1, f.crow, 0) &&
-             issue(&mapT0, f.crow + 128, 0) && issue(&mapT1, f.crow + 128, 0);
+        // T0 of row tile 1, T1 of keys 0-127, T1 of keys 128-255, T0 of row
+        // tile 0, in the order the score products use them
+        ok = issue(&mapT0, f.crow + 128, 0) && issue(&mapT1, f.crow, 0) &&
+             issue(&mapT1, f.crow + 128, 0) && issue(&mapT0, f.crow, 0);
         if (!ok) break;
         // T2 of both row tiles: the previous unit's global products are done
         if (j >= 1 && !mbar_wait(&b_empty, (j - 1) & 1, kWaitLimitNs)) {
@@ -264,7 +277,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         tma_load_3d(bbuf + PA_ITEM, &mapT2, &b_full, 0, f.crow + 128, 0);
         for (int x = 0; x < f.net && ok; ++x) {
           const int eb = (f.et0 + x) * 2;  // first 64-column block of the e tile
-          ok = issue(&mapV, f.crow, eb) && issue(&mapV, f.crow + 128, eb);
+          // V's last read: it may leave L2 first
+          ok = issue(&mapV, f.crow, eb, true) && issue(&mapV, f.crow + 128, eb, true);
           // the epilogue's U rows of this e tile, into L2 ahead of its loads
           // (their latency from DRAM otherwise sets the pace)
           tma_prefetch_l2_3d(&mapU, 0, f.crow + 128, eb);
@@ -295,12 +309,12 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   } else if (warp == 1) {
     // =========================== MMA issuer
     if (lane == 0) {
-      // S = T0 T1^T: M = 128 rows, N = 64 keys, A and B K-major
-      constexpr uint32_t idesc_s = idesc_bf16_f32(128, KEY_STAGE, false, false);
+      // S = T0 T1^T: M = 128 rows, N = 128 keys, A and B K-major
+      constexpr uint32_t idesc_s = idesc_bf16_f32(128, 128, false, false);
       // O += P V (A from TMEM) and O += T2 (local | carry) (A K-major); B MN-major
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, FU_ET, false, true);
       const uint32_t baddr = smem_u32(bbuf);
-      int it = 0, sc = 0, tcnt = 0, mcnt = 0;
+      int it = 0, tcnt = 0, mcnt = 0;
       bool ok = true;
       auto wait_item = [&](int item) -> bool {
         if (!mbar_wait(&full[item % PA_RING], (item / PA_RING) & 1, kWaitLimitNs)) {
@@ -323,47 +337,49 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         mbar_arrive(&uq_empty[qs]);
         if (u < 0) break;
         const PairUnit f = decode_pair(u, unet, grid);
-        // ---- scores, once per unit: row tile 0 (2 stages), row tile 1 (4)
-        const int i_a0 = it, i_k0 = it + 1, i_a1 = it + 2, i_k1 = it + 3;
+        // ---- scores, once per unit, into the accumulators' columns: the
+        // previous unit's last tile has been drained from both
+        const int i_a1 = it, i_k0 = it + 1, i_k1 = it + 2, i_a0 = it + 3;
         it += 4;
-        for (int r = 0; r < 2 && ok; ++r) {
-          const int i_a = r ? i_a1 : i_a0;
-          if (!wait_item(i_a)) {
+        if (tcnt >= 1) {
+          for (int r = 0; r < 2 && ok; ++r)
+            if (!mbar_wait(&o_empty[r], (tcnt - 1) & 1, kWaitLimitNs)) {
+              record_timeout(825);
+              ok = false;
+            }
+          if (!ok) break;
+        }
+        for (int st = 0; st < PA_SSTAGES && ok; ++st) {
+          const int i_a = st < 2 ? i_a1 : i_a0, i_k = st == 1 ? i_k1 : i_k0;
+          if (!wait_item(i_a) || !wait_item(i_k)) {
             ok = false;
             break;
           }
-          const uint32_t aaddr = slot_addr(i_a);
-          for (int k = 0; k < pair_stages(r) && ok; ++k) {
-            const int i_k = k < 2 ? i_k0 : i_k1;
-            if (!wait_item(i_k)) {
-              ok = false;
-              break;
-            }
-            if (sc >= 1 && !mbar_wait(&s_empty, (sc - 1) & 1, kWaitLimitNs)) {
-              record_timeout(826);
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            const uint32_t kaddr = slot_addr(i_k);
-            const uint32_t sd = tbase + PA_COL_S;
+          // stage 2 reuses stage 0's columns: the relu^2 warps have read them
+          if (st == 2 && (!mbar_wait(&p_full[2], j & 1, kWaitLimitNs) ||
+                          !mbar_wait(&p_full[3], j & 1, kWaitLimitNs))) {
+            record_timeout(826);
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aaddr = slot_addr(i_a), kaddr = slot_addr(i_k);
+          const uint32_t sd = tbase + pair_scol(st);
 #pragma unroll
-            for (int kk = 0; kk < S_DIM / 16; ++kk) {
-              const uint64_t ad =
-                  smem_desc_sw128(aaddr + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(
-                  kaddr + (kk >> 2) * 16384 + (k & 1) * 8192 + (kk & 3) * 32, 16, 1024);
-              mma_bf16_ss(sd, ad, bd, idesc_s, kk != 0);
-            }
-            mma_commit(&s_full);
-            ++sc;
-            // the items go back after their last score product
-            if (r == 0 && k == 1) mma_commit(&empty[i_a0 % PA_RING]);
-            if (r == 1 && k == 1) mma_commit(&empty[i_k0 % PA_RING]);
-            if (r == 1 && k == 3) {
-              mma_commit(&empty[i_a1 % PA_RING]);
-              mma_commit(&empty[i_k1 % PA_RING]);
-            }
+          for (int kk = 0; kk < S_DIM / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+            mma_bf16_ss(sd, smem_desc_sw128(aaddr + off, 16, 1024),
+                        smem_desc_sw128(kaddr + off, 16, 1024), idesc_s, kk != 0);
+          }
+          mma_commit(&s_full[st]);
+          // the items go back after their last score product
+          if (st == 1) {
+            mma_commit(&empty[i_k1 % PA_RING]);
+            mma_commit(&empty[i_a1 % PA_RING]);
+          }
+          if (st == 2) {
+            mma_commit(&empty[i_a0 % PA_RING]);
+            mma_commit(&empty[i_k0 % PA_RING]);
           }
         }
         if (!ok) break;
@@ -511,7 +527,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const int quad = warp & 3;
     const int row = quad * 32 + lane;  // query row within its row tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    int sc = 0, tcnt = 0;
+    int tcnt = 0;
     bool ok = true;
     for (int j = 0; ok; ++j) {
       const int qs = j % FU_QUEUE;
@@ -523,31 +539,24 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!got && mt == 0) record_timeout(840);
         break;
       }
-      for (int r = 0; r < 2 && ok; ++r) {
+      // the score stages in order, 64 keys at a time (one P slot each)
+      for (int st = 0; st < PA_SSTAGES && ok; ++st) {
+        const int r = pair_srow(st);
         const int qpos = r * ROW_TILE + row;  // query position within the chunk
-        for (int k = 0; k < pair_stages(r); ++k, ++sc) {
+        const bool got_s = mbar_wait(&s_full[st], j & 1, kWaitLimitNs);
+        for (int h = 0; h < 2; ++h) {
+          const int k = (st == 1 ? 2 : 0) + h;  // 64-key stage within the row tile
           const int ps = pair_pslot(r, k);
-          bool w = mbar_wait(&s_full, sc & 1, kWaitLimitNs);
+          bool w = got_s;
           // the previous unit's last product that read this P slot has completed
           if (w && j >= 1) w = mbar_wait(&p_empty[ps], (j - 1) & 1, kWaitLimitNs);
-          uint32_t sv[2][32];
           if (w) {
+            uint32_t sv[2][32];
             tc_fence_after();
-            const uint32_t sa = tbase + lane_off + PA_COL_S;
+            const uint32_t sa = tbase + lane_off + pair_scol(st) + (uint32_t)(64 * h);
             tmem_ld32(sa, sv[0]);
             tmem_ld32(sa + 32, sv[1]);
             tmem_ld_wait();
-            tc_fence_before();
-          }
-          // every thread has read the S slot: the next score product may start
-          // while these weights are formed
-          if (!named_bar_and(2, 128, w)) {
-            if (mt == 0) record_timeout(842);
-            ok = false;
-            break;
-          }
-          if (mt == 0) mbar_arrive(&s_empty);
-          {
             // relu(S a)^2 (a = 1/C by default); key position > query position
             // -> 0; two keys a column, the lower key in the low half
             const int kbase = k * KEY_STAGE;
@@ -646,6 +655,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       }
     }
   }
+  // the single-lane roles (TMA producer, MMA issuer) rejoin their warps
+  // before the block-wide barrier, which counts converged warps
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);

@@ -126,6 +126,9 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
     if (lane == 0) {
       const bool zp = warp == 0;
       tma_prefetch_desc(zp ? &mapZ3 : &mapV3);
+      // V stays in L2 for the output kernel's second read where it fits; Z
+      // is not read again (the T rows go out from here)
+      const uint64_t pol_v = policy_evict_last(), pol_z = policy_evict_first();
       int it = 0;
       bool ok = true;
       for (int u = (int)blockIdx.x; u < n_units && ok; u += W) {
@@ -144,9 +147,9 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
             mbar_arrive_expect_tx(&full[slot], zp ? WK_ITEM_V : WK_ITEM - WK_ITEM_V);
             const int y = b * n + g * C + k * WK_KEYS;
             if (zp)
-              tma_load_3d(sz, &mapZ3, &full[slot], 0, y, 0);
+              tma_load_3d_hint(sz, &mapZ3, &full[slot], 0, y, 0, pol_z);
             else
-              tma_load_3d(sz + WK_ITEM_V, &mapV3, &full[slot], 0, y, es * (WK_ET / 64));
+              tma_load_3d_hint(sz + WK_ITEM_V, &mapV3, &full[slot], 0, y, es * (WK_ET / 64), pol_v);
           }
       }
       // the last copy issued into each slot has landed
@@ -350,6 +353,9 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
     }
     if (mt == 0) bulk_wait_group<0>();
   }
+  // the single-lane roles (TMA producer, MMA issuer) rejoin their warps
+  // before the block-wide barrier, which counts converged warps
+  __syncwarp();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);
@@ -372,9 +378,9 @@ __device__ __forceinline__ void seg_carry_group(__nv_bfloat16 *__restrict__ T, i
         make_uint4(pack_bf16x2(run[0], run[1]), pack_bf16x2(run[2], run[3]),
                    pack_bf16x2(run[4], run[5]), pack_bf16x2(run[6], run[7]));
   };
-  // 8 segments' loads in flight before any of their carries is stored (the
-  // stores go to the same slots)
-  constexpr int kBatch = 8;
+  // 16 segments' loads in flight before any of their carries is stored (the
+  // stores go to the same slots): one round trip for up to 16 segments
+  constexpr int kBatch = 16;
   for (int s0 = 0; s0 < S; s0 += kBatch) {
     uint4 v[kBatch];
 #pragma unroll
