@@ -247,7 +247,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     const int units = B * (e / WK_ET) * sp.S;
     tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
         mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S, sp.L,
-        carried);
+        carried, pair ? 0 : 1);
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
     if ((sp.S > 1 || !causal) && !pair) {
       // totals -> carries (bidirectional: the total), a programmatic
@@ -362,7 +362,7 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
       const int units = B * (e / WK_ET) * sp.S;
       tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
           mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S,
-          sp.L, nullptr);
+          sp.L, nullptr, 1);
       if (cudaGetLastError() != cudaSuccess) return 1;
       if (sp.S > 1 || !causal) {
         const int64_t lanes = (int64_t)B * se / 8;

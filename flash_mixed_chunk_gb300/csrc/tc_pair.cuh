@@ -81,6 +81,7 @@ struct PairUnit {
   int crow;   // first token row of the chunk in [B*n]
   int lrow;   // first row of its local sums in [B*G*s]
   int crow2;  // first row of its carry in [B*S*s]
+  bool local; // not its segment's first chunk (whose local sums are zero and not stored)
   bool carry; // past the first segment
   int et0, net;
 };
@@ -92,6 +93,7 @@ __device__ __forceinline__ PairUnit decode_pair(int t, int net, const PairGrid &
   f.crow = b * g.n + c * 256;
   f.lrow = bg * S_DIM;
   f.crow2 = (b * g.S + c / g.L) * S_DIM;
+  f.local = c % g.L != 0;
   f.carry = c / g.L > 0;
   f.et0 = t % g.n_et;
   f.net = net;
@@ -285,7 +287,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           tma_prefetch_l2_3d(&mapU, 0, f.crow, eb);
           // the local sums and carries come from the kernels before: wait
           // once, before the first such load
-          if (ok && !sums_ready) {
+          if (ok && !sums_ready && (f.local || f.carry)) {
             griddep_wait();
             // every CTA has formed its share of the carries
             if (grid.carries) {
@@ -298,7 +300,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             }
             sums_ready = true;
           }
-          if (ok) ok = issue(&mapS, f.lrow, eb);
+          if (ok && f.local) ok = issue(&mapS, f.lrow, eb);
           if (ok && f.carry) ok = issue(&mapCy, f.crow2, eb);
         }
       }
@@ -386,8 +388,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         // ---- e tiles: row tile 1 (stages 2, 3 then 0, 1), then row tile 0
         // (stages 0, 1); O_r = sum_k P_rk V_k + T2_r (local + carry)
         for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
+          // il: the local sums, or the carry alone in a segment's first chunk
           const int iv0 = it, iv1 = it + 1, il = it + 2;
-          it += f.carry ? 4 : 3;
+          const int nglob = (int)f.local + (int)f.carry;
+          const bool merge = f.local && f.carry;
+          it += 2 + nglob;
           for (int rr = 0; rr < 2 && ok; ++rr) {
             const int r = 1 - rr;
             // the epilogue has drained O_r (the previous e tile's)
@@ -423,7 +428,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 mma_commit(&empty[iv1 % PA_RING]);
                 // the local sums and the carry have landed: merge them while
                 // the keys 0-127 products run
-                if (f.carry) {
+                if (merge) {
                   if (!wait_item(il) || !wait_item(il + 1)) {
                     ok = false;
                     break;
@@ -440,24 +445,27 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
               break;
             }
             // the local sums, with the carry added by the merge warps
-            if (r == 1) {
-              if (f.carry ? !mbar_wait(&m_full, mcnt & 1, kWaitLimitNs) : !wait_item(il)) {
+            if (r == 1 && nglob > 0) {
+              if (merge ? !mbar_wait(&m_full, mcnt & 1, kWaitLimitNs) : !wait_item(il)) {
                 record_timeout(828);
                 ok = false;
                 break;
               }
-              if (f.carry) ++mcnt;
+              if (merge) ++mcnt;
             }
             tc_fence_after();
-            const uint32_t pb = slot_addr(il);
-            const uint32_t ab = baddr + (uint32_t)r * PA_ITEM;
+            if (nglob > 0) {
+              const uint32_t pb = slot_addr(il);
+              const uint32_t ab = baddr + (uint32_t)r * PA_ITEM;
 #pragma unroll
-            for (int kk = 0; kk < S_DIM / 16; ++kk) {
-              const uint64_t ad = smem_desc_sw128(ab + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-              const uint64_t bd = smem_desc_sw128(pb + kk * 2048, 16384, 1024);
-              mma_bf16_ss(ocol, ad, bd, idesc_o, 1u);
+              for (int kk = 0; kk < S_DIM / 16; ++kk) {
+                const uint64_t ad =
+                    smem_desc_sw128(ab + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                const uint64_t bd = smem_desc_sw128(pb + kk * 2048, 16384, 1024);
+                mma_bf16_ss(ocol, ad, bd, idesc_o, 1u);
+              }
+              if (r == 0) mma_commit(&empty[il % PA_RING]);
             }
-            if (r == 0) mma_commit(&empty[il % PA_RING]);
             mma_commit(&o_full[r]);
           }
         }
@@ -491,8 +499,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       it += 4;  // the unit's T0 and T1 items
       for (int x = 0; x < f.net && ok; ++x) {
         const int il = it + 2, icy = it + 3;
-        it += f.carry ? 4 : 3;
-        if (!f.carry) continue;
+        it += 2 + (int)f.local + (int)f.carry;
+        if (!(f.local && f.carry)) continue;
         const bool w = mbar_wait(&mg_go, mcnt & 1, kWaitLimitNs);
         ++mcnt;
         if (w) {

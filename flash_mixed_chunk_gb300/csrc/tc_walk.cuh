@@ -71,7 +71,8 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
                   const float *__restrict__ gamma, const float *__restrict__ beta,
                   __nv_bfloat16 *__restrict__ trows, int64_t rows_plane, int B, int n, int e,
                   int C, int causal, int lin_norm, int S, int L,
-                  unsigned int *__restrict__ zero_count) {  // cleared here if not null
+                  unsigned int *__restrict__ zero_count,  // cleared here if not null
+                  int store_first_local) {  // 0: a segment's first chunk (zero sums) is not stored
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -338,12 +339,13 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
           for (int q = 0; q < WK_ET / 32; ++q) tmem_st32(rcol + 32 * q, z);
           tmem_st_wait();
         }
+        const bool out_local = causal && (g > g0 || store_first_local);
         if (g < g1 - 1) {
           // causal: local_g = R out; R += D_g
-          pass(causal != 0, false, true, &mapL, es * WK_ET, (b * G + g) * S_DIM);
+          pass(out_local, false, true, &mapL, es * WK_ET, (b * G + g) * S_DIM);
         } else {
           // the segment's last chunk: local_g (causal), then the total R + D_g
-          if (causal) pass(true, false, false, &mapL, es * WK_ET, (b * G + g) * S_DIM);
+          if (out_local) pass(true, false, false, &mapL, es * WK_ET, (b * G + g) * S_DIM);
           pass(false, true, false, &mapT, es * WK_ET, (b * S + sg) * S_DIM);
         }
         tc_fence_before();
@@ -439,7 +441,7 @@ __global__ void __launch_bounds__(256)
     v[2 * i] = sg > 0 || !causal ? bf16_lo(cw[i]) : 0.f;
     v[2 * i + 1] = sg > 0 || !causal ? bf16_hi(cw[i]) : 0.f;
   }
-  if (causal) {
+  if (causal && g % L != 0) {  // a segment's first chunk: zero local sums, maybe not stored
     const uint4 l = *reinterpret_cast<const uint4 *>(local + ((int64_t)b * G + g) * se + x);
     const uint32_t lw[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
