@@ -7,6 +7,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <mutex>
 
 #include "launch.h"
 
@@ -390,9 +391,54 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
   return rc == 0 ? FMCA_OK : FMCA_ERR_CUDA;
 }
 
+// Pieces of the host-buffer pipeline: with at least two sequences and 96 MB
+// of inputs and output, up to four pieces of whole sequences (their copies
+// overlap the passes); smaller problems keep one stream (their passes and
+// copies are too short for the overlap to pay for its extra launches).
+int host_pipeline_pieces(int B, size_t bytes) {
+  constexpr size_t kPipelineBytes = (size_t)96 << 20;
+  if (B < 2 || bytes < kPipelineBytes) return 1;
+  return B < 4 ? B : 4;
+}
+
+// The host-buffer pipeline's copy streams and events, one set per device,
+// created on first use; a call holds the set's mutex while it queues.
+constexpr int kMaxHostPieces = 4;
+struct HostStreams {
+  std::mutex mutex;
+  cudaStream_t in = nullptr, out = nullptr;
+  cudaEvent_t start = nullptr, out_done = nullptr;
+  cudaEvent_t in_done[kMaxHostPieces] = {}, pass_done[kMaxHostPieces] = {};
+  bool ready = false;
+};
+constexpr int kMaxHostDevices = 64;
+HostStreams g_host_streams[kMaxHostDevices];
+std::mutex g_host_streams_init;
+
+HostStreams *host_streams() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxHostDevices) return nullptr;
+  HostStreams &h = g_host_streams[dev];
+  std::lock_guard<std::mutex> lock(g_host_streams_init);
+  if (!h.ready) {
+    const unsigned ef = cudaEventDisableTiming;
+    bool ok = cudaStreamCreateWithFlags(&h.in, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaStreamCreateWithFlags(&h.out, cudaStreamNonBlocking) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.start, ef) == cudaSuccess &&
+              cudaEventCreateWithFlags(&h.out_done, ef) == cudaSuccess;
+    for (int k = 0; ok && k < kMaxHostPieces; ++k)
+      ok = cudaEventCreateWithFlags(&h.in_done[k], ef) == cudaSuccess &&
+           cudaEventCreateWithFlags(&h.pass_done[k], ef) == cudaSuccess;
+    if (!ok) return nullptr;
+    h.ready = true;
+  }
+  return &h;
+}
+
 }  // namespace
 
 extern "C" {
+
 
 fmca_status flash_mca_forward_path(const void *Z, const void *V, const void *U,
                                    const float *gamma, const float *beta, void *O, int B,
@@ -437,31 +483,77 @@ fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *h
   const size_t zb = (size_t)B * n * s * es, vb = (size_t)B * n * e * es;
   const size_t gbytes = sizeof(float) * 4 * (size_t)s;
   char *p = static_cast<char *>(device_arena);
-  void *dZ = p;
+  char *dZ = p;
   p += align256(zb);
-  void *dV = p;
+  char *dV = p;
   p += align256(vb);
-  void *dU = p;
+  char *dU = p;
   p += align256(vb);
   float *dg = reinterpret_cast<float *>(p);
   p += align256(gbytes);
   float *db = reinterpret_cast<float *>(p);
   p += align256(gbytes);
-  void *dO = p;
+  char *dO = p;
   p += align256(vb);
   void *ws = p;
   const size_t wsb = workspace_bytes(B, n, s, e, C, causal);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
-  if (cudaMemcpyAsync(dZ, hZ, zb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(dV, hV, vb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(dU, hU, vb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(dg, hgamma, gbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
-      cudaMemcpyAsync(db, hbeta, gbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+  const int pieces = host_pipeline_pieces(B, zb + 3 * vb);
+  if (pieces <= 1) {
+    // one stream: copies in, the pass, the copy out
+    if (cudaMemcpyAsync(dZ, hZ, zb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dV, hV, vb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dU, hU, vb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(dg, hgamma, gbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+        cudaMemcpyAsync(db, hbeta, gbytes, cudaMemcpyHostToDevice, cs) != cudaSuccess)
+      return FMCA_ERR_CUDA;
+    st = flash_mca_forward(dZ, dV, dU, dg, db, dO, B, n, s, e, C, causal, dtype, ws, wsb, stream);
+    if (st != FMCA_OK) return st;
+    if (cudaMemcpyAsync(hO, dO, vb, cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+      return FMCA_ERR_CUDA;
+    if (cudaStreamSynchronize(cs) != cudaSuccess) return FMCA_ERR_CUDA;
+    return FMCA_OK;
+  }
+  // Pieces of whole sequences: piece k's copies in (copy-in stream) overlap
+  // piece k-1's pass (the caller's stream) and its copy out (copy-out
+  // stream).  Each piece runs as a batch of its own through one workspace.
+  HostStreams *hs = host_streams();
+  if (hs == nullptr) return FMCA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(hs->mutex);
+  const size_t zrow = (size_t)n * s * es, vrow = (size_t)n * e * es;  // one sequence
+  if (cudaEventRecord(hs->start, cs) != cudaSuccess ||
+      cudaStreamWaitEvent(hs->in, hs->start, 0) != cudaSuccess ||
+      cudaMemcpyAsync(dg, hgamma, gbytes, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+      cudaMemcpyAsync(db, hbeta, gbytes, cudaMemcpyHostToDevice, hs->in) != cudaSuccess)
     return FMCA_ERR_CUDA;
-  st = flash_mca_forward(dZ, dV, dU, dg, db, dO, B, n, s, e, C, causal, dtype, ws, wsb, stream);
-  if (st != FMCA_OK) return st;
-  if (cudaMemcpyAsync(hO, dO, vb, cudaMemcpyDeviceToHost, cs) != cudaSuccess) return FMCA_ERR_CUDA;
-  if (cudaStreamSynchronize(cs) != cudaSuccess) return FMCA_ERR_CUDA;
+  for (int k = 0; k < pieces; ++k) {
+    const int b0 = (int)((int64_t)B * k / pieces), b1 = (int)((int64_t)B * (k + 1) / pieces);
+    const size_t bp = (size_t)(b1 - b0);
+    const char *hz = static_cast<const char *>(hZ) + b0 * zrow;
+    const char *hv = static_cast<const char *>(hV) + b0 * vrow;
+    const char *hu = static_cast<const char *>(hU) + b0 * vrow;
+    if (cudaMemcpyAsync(dZ + b0 * zrow, hz, bp * zrow, cudaMemcpyHostToDevice, hs->in) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(dV + b0 * vrow, hv, bp * vrow, cudaMemcpyHostToDevice, hs->in) !=
+            cudaSuccess ||
+        cudaMemcpyAsync(dU + b0 * vrow, hu, bp * vrow, cudaMemcpyHostToDevice, hs->in) !=
+            cudaSuccess ||
+        cudaEventRecord(hs->in_done[k], hs->in) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, hs->in_done[k], 0) != cudaSuccess)
+      return FMCA_ERR_CUDA;
+    st = flash_mca_forward(dZ + b0 * zrow, dV + b0 * vrow, dU + b0 * vrow, dg, db,
+                           dO + b0 * vrow, (int)bp, n, s, e, C, causal, dtype, ws, wsb, stream);
+    if (st != FMCA_OK) return st;
+    if (cudaEventRecord(hs->pass_done[k], cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hs->out, hs->pass_done[k], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<char *>(hO) + b0 * vrow, dO + b0 * vrow, bp * vrow,
+                        cudaMemcpyDeviceToHost, hs->out) != cudaSuccess)
+      return FMCA_ERR_CUDA;
+  }
+  if (cudaEventRecord(hs->out_done, hs->out) != cudaSuccess ||
+      cudaStreamWaitEvent(cs, hs->out_done, 0) != cudaSuccess ||
+      cudaStreamSynchronize(cs) != cudaSuccess)
+    return FMCA_ERR_CUDA;
   return FMCA_OK;
 }
 

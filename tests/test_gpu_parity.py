@@ -141,6 +141,27 @@ def test_host_buffer_entry_matches_device_entry(B, causal):
     assert torch.equal(Oh, dev)
 
 
+@pytest.mark.parametrize("B,n,causal", [(2, 8192, True), (5, 4096, False)])
+def test_host_buffer_pipeline_whole_output(B, n, causal):
+    """Problems of 96 MB and more go through the host-buffer entry point in
+    pieces of whole sequences (copies overlapping the passes): the whole
+    output against the oracle (each piece is a batch of its own, so the bits
+    may differ from one call on the whole batch; the bar is the same)."""
+    m = fm()
+    C, s, e = 256, 128, 1536
+    Z, V, U, gamma, beta = mca_inputs.make_inputs(B, n, s, e, 61 + B, torch.bfloat16)
+    pins = [t.pin_memory() for t in (Z, V, U, gamma, beta)]
+    Oh = torch.empty((B, n, e), dtype=torch.bfloat16).pin_memory()
+    arena = torch.empty(m.flash_mca_host_arena_bytes(B, n, s, e, C, causal, m.FMCA_BF16),
+                        dtype=torch.uint8, device="cuda:0")
+    m.flash_mca_forward_host(*pins, Oh, C, causal, arena)
+    assert m.flash_mca_device_status() == (m.FMCA_OK, 0)
+    ref = oracle.forward(Z, V, U, gamma, beta, C, causal)
+    err = rel_err(Oh.float().numpy(), ref)
+    report(f"host_pipeline_B{B}_n{n}_{'causal' if causal else 'bidir'}", err)
+    assert err <= TOL[torch.bfloat16], f"normwise error {err:.3e}"
+
+
 def test_timeout_path_records_status_and_context_survives():
     m = fm()
     assert m.flash_mca_device_status() == (m.FMCA_OK, 0)
