@@ -81,7 +81,15 @@ typedef int32_t fmca_path;
 
 /* Supported sizes: B, n, s, e >= 1; 1 <= C <= n with n % C == 0; s <= 256;
  * B * n * max(s, e) < 2^31.  The tensor-core path additionally needs the
- * conditions listed at FMCA_PATH_TCGEN05. */
+ * conditions listed at FMCA_PATH_TCGEN05.
+ *
+ * Tensor-core coverage of the bf16 shapes: the tcgen05 kernels take s = 128
+ * (the pages' attention width), C a multiple of 128 (128, 256, ..., up to
+ * C = n for the quadratic-only model) and e a multiple of 256.  Every other
+ * bf16 shape in the supported sizes (s = 16 ... 256 other than 128, C = 64
+ * or any C that is not a multiple of 128, e not a multiple of 256) runs the
+ * fp32 CUDA-core kernels: correct, to the fp32 bar, but several times
+ * slower.  FMCA_PATH_AUTO picks the tensor-core path whenever it applies. */
 
 /*
  * Bytes of device workspace one flash_mca_forward call with these arguments
@@ -333,7 +341,13 @@ int flash_mca_launch_count_ex(int B, int n, int s, int e, int C, int causal,
  * memory into `device_arena`, runs flash_mca_forward on `stream`, copies O
  * back to host memory and waits for the stream before returning, so hO is
  * ready on return.  Host buffers should be page-locked for the copies to run
- * at full speed (pageable memory works, more slowly).
+ * at full speed (pageable memory works, more slowly).  With at least two
+ * sequences and 96 MB of inputs and output, the call runs up to four pieces
+ * of whole sequences so that copies and passes overlap: the copies go on two
+ * streams of the library's own (created once per device), chained to
+ * `stream` by events, the passes on `stream`.  Each piece is a batch of its
+ * own, so the output bits can differ from one flash_mca_forward call on the
+ * whole batch (within the same error bounds).
  *   device_arena   caller-owned device buffer, 256-byte aligned, of at least
  *                  flash_mca_host_arena_bytes(...) bytes; it holds the device
  *                  copies of the inputs and output and the workspace.
