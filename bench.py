@@ -98,15 +98,16 @@ def algorithmic_bytes(w) -> float:
 def kernel_algorithmic_bytes(w, kernel: str) -> float:
     """Compulsory HBM bytes of one launch of a forward kernel: what it must
     read of Z, V, U and write of O (its intermediates excluded).  The walkers
-    read Z and V; the output kernels read V and U and write O; the T-row
-    kernel reads Z."""
+    read Z and V; the output kernels (row-pair, fused, and the one reading
+    stored relu^2 weights) read V and U and write O; the T-row kernel and the
+    relu^2-weight kernel read Z."""
     es = 2 if w.dtype == "bf16" else 4
     tokens = w.B * w.n
     if kernel == "tc_chunk_walk":
         return float(tokens * (w.s + w.e) * es)
-    if kernel in ("tc_chunk_pair", "tc_chunk_fused"):
+    if kernel in ("tc_chunk_pair", "tc_chunk_fused", "tc_chunk_attn"):
         return float(tokens * 3 * w.e * es)
-    if kernel == "tc_affine_rows":
+    if kernel in ("tc_affine_rows", "tc_chunk_prep"):
         return float(tokens * w.s * es)
     if kernel == "tc_seg_carry":
         return 0.0
@@ -123,8 +124,8 @@ def load_peaks():
         return dict(PEAKS_FALLBACK), "fallback"
 
 
-FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_fused.cuh", "tc_walk.cuh", "tc_pair.cuh",
-                          "ptx.cuh")
+FORWARD_KERNEL_SOURCES = ("tc.cu", "tc_common.cuh", "tc_prep.cuh", "tc_attn.cuh", "tc_fused.cuh",
+                          "tc_walk.cuh", "tc_pair.cuh", "ptx.cuh")
 
 
 def kernel_source_sha() -> str:
@@ -730,8 +731,11 @@ def run_ours(args, w, rank, world, device):
     tflops = world * flops * args.steps / (ms / 1e3) / 1e12
     if path != fm.FMCA_PATH_TCGEN05:
         kernel_names = ["simt_chunk_state", "simt_chunk_scan", "simt_chunk_output"]
-    elif lin_norm == fm.FMCA_LIN_NORM_NONE:  # the T0 / T1 rows, then the fused kernel
-        kernel_names = ["tc_affine_rows", "tc_chunk_fused"]
+    elif lin_norm == fm.FMCA_LIN_NORM_NONE:
+        # chunks of up to 256 tokens: the T0 / T1 rows, then the fused kernel;
+        # longer (the quadratic-only model): the relu^2 weights through HBM
+        kernel_names = (["tc_affine_rows", "tc_chunk_fused"] if w.C <= 256
+                        else ["tc_chunk_prep", "tc_chunk_attn"])
     else:
         # the segment walkers, the carries (with more than one segment or
         # bidirectional), the output kernel (both row tiles of a causal chunk

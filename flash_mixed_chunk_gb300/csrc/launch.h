@@ -82,7 +82,13 @@ inline TcLayout tc_layout(int B, int n, int s, int e, int C, int causal, bool ma
 // workspace sized for a shape serves every path a call may pick.
 inline size_t workspace_bytes(int B, int n, int s, int e, int C, int causal) {
   const size_t a = simt_layout(B, n, s, e, C, causal).total;
-  const size_t b = tc_layout(B, n, s, e, C, causal, false).total;
+  size_t b = tc_layout(B, n, s, e, C, causal, false).total;
+  // chunks longer than 256 tokens: the quadratic-only model keeps its relu^2
+  // weights in the workspace (tc_layout with the intermediates)
+  if (C > 256) {
+    const size_t bm = tc_layout(B, n, s, e, C, causal, true).total;
+    if (bm > b) b = bm;
+  }
   return a > b ? a : b;
 }
 
@@ -103,7 +109,9 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
                         int causal, int dtype_bf16, const Variant &var, void *workspace,
                         cudaStream_t stream, cudaEvent_t const *events = nullptr);
 
-// The tensor-core forward pass (workspace: tc_layout(..., false)).
+// The tensor-core forward pass (workspace: tc_layout(..., false); without a
+// global term and with C > 256 it runs the kernels of
+// launch_tc_forward_materialised and needs tc_layout(..., true)).
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
@@ -125,7 +133,8 @@ int tc_materialised_launch_count(int B, int n, int e, int C, int causal, const V
 int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
                                    const float *gamma, const float *beta, void *O, int B, int n,
                                    int s, int e, int C, int causal, const Variant &var,
-                                   void *workspace, cudaStream_t stream, bool with_states);
+                                   void *workspace, cudaStream_t stream, bool with_states,
+                                   cudaEvent_t const *events = nullptr);
 
 // Runs a setup step (kernel attributes) once per device and process, safely
 // when several host threads make their first call at the same time; later

@@ -192,6 +192,13 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
                       cudaEvent_t const *events) {
+  // Without a global term and with chunks longer than 256 tokens (the
+  // quadratic-only model), a row tile's relu^2 weights do not fit in TMEM
+  // beside its accumulators: the chunk kernel would form them again for every
+  // e tile.  Those go through HBM once instead (bf16 [B n][C]).
+  if (var.lin_norm == kLinNormNone && C > 2 * ROW_TILE)
+    return launch_tc_forward_materialised(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, var,
+                                          workspace, stream, false, events);
   const int G = n / C;
   const int64_t se = (int64_t)s * e;
   const TcLayout L = tc_layout(B, n, s, e, C, causal, false);
@@ -306,7 +313,8 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
 int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
                                    const float *gamma, const float *beta, void *O, int B, int n,
                                    int s, int e, int C, int causal, const Variant &var,
-                                   void *workspace, cudaStream_t stream, bool with_states) {
+                                   void *workspace, cudaStream_t stream, bool with_states,
+                                   cudaEvent_t const *events) {
   const int G = n / C;
   const int R = C / ROW_TILE;
   const int64_t se = (int64_t)s * e;
@@ -352,6 +360,8 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
     return 1;
   // sched[0]: work counter of tc_chunk_prep; sched[1]: of tc_chunk_attn
   if (cudaMemsetAsync(sched, 0, 2 * sizeof(unsigned int), stream) != cudaSuccess) return 1;
+  if (!record_event(events, 0, stream)) return 1;
+  int ev = 1;
   // without a global term (FMCA_LIN_NORM_NONE) there is no prefix and the
   // attention units have no lin_q items
   const bool no_global = var.lin_norm == kLinNormNone;
@@ -383,7 +393,7 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
   prep<<<n_score < sms ? n_score : sms, PREP_THREADS, PREP_SMEM, stream>>>(
       mZ64, mZ128, mZw, mVw, mL, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2),
       nullptr, 0, sched, n, e, C, G, causal, 0, n_score, var.quad_a);
-  if (cudaGetLastError() != cudaSuccess) return 1;
+  if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
   // O = U * (P V_g + T2 prefix_g): an ordinary launch (it reads P and T2
   // from the kernel before it as soon as it starts)
   const int n_units = B * G * R * (e / E_TILE);
@@ -392,7 +402,8 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
   ac.cfg.blockDim = dim3(AT_THREADS);
   ac.cfg.dynamicSmemBytes = AT_SMEM;
   if (cudaLaunchKernelEx(&ac.cfg, tc_chunk_attn, mPw, mT2, mV, mS, mU, mO, sched + 1, n, e, C, G,
-                         causal, n_units, no_global ? 0 : S_DIM / KEY_STAGE) != cudaSuccess)
+                         causal, n_units, no_global ? 0 : S_DIM / KEY_STAGE) != cudaSuccess ||
+      !record_event(events, ev++, stream))
     return 1;
   return 0;
 }
