@@ -366,38 +366,57 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
   // attention units have no lin_q items
   const bool no_global = var.lin_norm == kLinNormNone;
   const int sms = num_sms();
-  if (!no_global) {
-    if (with_states) {
-      // the local sums and carries exactly as the forward pass forms them
-      const int units = B * (e / WK_ET) * sp.S;
-      tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
-          mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S,
-          sp.L, nullptr, 1);
-      if (cudaGetLastError() != cudaSuccess) return 1;
-      if (sp.S > 1 || !causal) {
-        const int64_t lanes = (int64_t)B * se / 8;
-        tc_seg_carry<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(seg, B, sp.S, se,
-                                                                          causal);
-        if (cudaGetLastError() != cudaSuccess) return 1;
-      }
-    }
-    // the scaled prefix of the attention kernel (unscaled T2 rows)
-    const int64_t lanes = (int64_t)B * Gp * se / 8;
-    tc_prefix_fixup<<<(unsigned)((lanes + 255) / 256), 256, 0, stream>>>(
-        local, seg, prefix, B, G, sp.S, sp.L, se, causal, n, C, var.lin_norm);
-    if (cudaGetLastError() != cudaSuccess) return 1;
-  }
-  // the relu^2 weights P and the T2 rows (score units only)
+  // the relu^2 weights P and the T2 rows (score units only) first: they need
+  // nothing of the global term, and the kernels after it chain on it by
+  // programmatic dependent launch (each waits for the one before)
   const int n_score = B * G * score_units_per_chunk(C, causal);
   auto *prep = var.lin_norm == kLinNormPosition ? tc_chunk_prep<true> : tc_chunk_prep<false>;
   prep<<<n_score < sms ? n_score : sms, PREP_THREADS, PREP_SMEM, stream>>>(
       mZ64, mZ128, mZw, mVw, mL, mPw, gamma, beta, reinterpret_cast<__nv_bfloat16 *>(t2),
       nullptr, 0, sched, n, e, C, G, causal, 0, n_score, var.quad_a);
   if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
-  // O = U * (P V_g + T2 prefix_g): an ordinary launch (it reads P and T2
-  // from the kernel before it as soon as it starts)
+  if (!no_global) {
+    if (with_states) {
+      // the local sums and carries exactly as the forward pass forms them
+      // (the walkers end only after the weight kernel has)
+      const int units = B * (e / WK_ET) * sp.S;
+      PdlConfig wc(stream, true);
+      wc.cfg.gridDim = dim3(units < sms ? units : sms);
+      wc.cfg.blockDim = dim3(WK_THREADS);
+      wc.cfg.dynamicSmemBytes = WALK_SMEM;
+      if (cudaLaunchKernelEx(&wc.cfg, tc_chunk_walk, mZw, mVw, mL, mT, gamma, beta, trows, plane,
+                             B, n, e, C, causal, var.lin_norm, sp.S, sp.L,
+                             static_cast<unsigned int *>(nullptr), 1) != cudaSuccess ||
+          !record_event(events, ev++, stream))
+        return 1;
+      if (sp.S > 1 || !causal) {
+        const int64_t lanes = (int64_t)B * se / 8;
+        PdlConfig cc(stream, true);
+        cc.cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
+        cc.cfg.blockDim = dim3(256);
+        if (cudaLaunchKernelEx(&cc.cfg, tc_seg_carry, seg, B, sp.S, se, causal) != cudaSuccess ||
+            !record_event(events, ev++, stream))
+          return 1;
+      }
+    }
+    // the scaled prefix of the attention kernel (unscaled T2 rows)
+    const int64_t lanes = (int64_t)B * Gp * se / 8;
+    PdlConfig fc(stream, true);
+    fc.cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
+    fc.cfg.blockDim = dim3(256);
+    if (cudaLaunchKernelEx(&fc.cfg, tc_prefix_fixup, static_cast<const __nv_bfloat16 *>(local),
+                           static_cast<const __nv_bfloat16 *>(seg), prefix, B, G, sp.S, sp.L, se,
+                           causal, n, C, var.lin_norm) != cudaSuccess ||
+        !record_event(events, ev++, stream))
+      return 1;
+  }
+  // O = U * (P V_g + T2 prefix_g).  With a global term, a programmatic
+  // dependent of the prefix fix-up, whose grid ends after the weight kernel's
+  // (through the chain above): the weights and T2 rows are final when it
+  // starts, and only its prefix loads wait.  Without one, an ordinary launch
+  // after the weight kernel.
   const int n_units = B * G * R * (e / E_TILE);
-  PdlConfig ac(stream, false);
+  PdlConfig ac(stream, !no_global);
   ac.cfg.gridDim = dim3(n_units < sms ? n_units : sms);
   ac.cfg.blockDim = dim3(AT_THREADS);
   ac.cfg.dynamicSmemBytes = AT_SMEM;

@@ -361,6 +361,10 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
   tc_fence_before();
   __syncthreads();
   if (warp == 1) tmem_dealloc(tbase, 512);
+  // launched as a programmatic dependent of the relu^2-weight kernel (the
+  // stored-weights forward pass): this grid ends only after that one, so the
+  // kernels after it may take its outputs as final
+  griddep_wait();
 }
 
 // Segment totals -> carries for one group of 8 columns (t of B * s * e / 8),
@@ -426,6 +430,8 @@ __global__ void __launch_bounds__(256)
                     int causal, int n, int C, int lin_norm) {
   const int Gp = causal ? G : 1;
   const int64_t per = se / 8;
+  griddep_wait();  // the carries (or, with the states kept, the kernel before)
+  griddep_launch_dependents();
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * Gp * per) return;
   const int64_t bg = t / per, x = (t % per) * 8;
