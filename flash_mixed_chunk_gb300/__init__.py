@@ -29,7 +29,8 @@ __all__ = [
     "flash_mca_status_string", "flash_mca_version", "forward", "EXPORTED_SYMBOLS",
     "FMCA_LIN_NORM_N", "FMCA_LIN_NORM_SUMMED", "FMCA_LIN_NORM_POSITION", "FMCA_LIN_NORM_NONE",
     "FmcaOptions",
-    "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_decode_state_bytes",
+    "flash_mca_default_options", "flash_mca_forward_ex", "flash_mca_forward_seq", "FmcaSeq",
+    "flash_mca_decode_state_bytes",
     "flash_mca_decode_reset", "flash_mca_decode_step", "flash_mca_backward_workspace_bytes",
     "flash_mca_backward", "flash_mca_backward_saved", "flash_mca_backward_launch_count",
     "backward", "flash_mca_gau_project",
@@ -70,6 +71,14 @@ class FmcaOptions(ctypes.Structure):
     _fields_ = [("quad_scale", ctypes.c_float), ("lin_norm", _i32)]
 
 
+class FmcaSeq(ctypes.Structure):
+    """``fmca_seq`` of the header: one piece of longer causal sequences
+    (carried-in state, state out, the piece's first token, the divisor's
+    length)."""
+    _fields_ = [("state_in", _vp), ("state_out", _vp), ("token_offset", ctypes.c_int64),
+                ("n_norm", ctypes.c_int64)]
+
+
 # (name, restype, argtypes) for every symbol the header declares
 _SIGNATURES = [
     ("flash_mca_workspace_bytes", _sz, [_int] * 6 + [_i32]),
@@ -79,6 +88,8 @@ _SIGNATURES = [
     ("flash_mca_forward_timed", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions),
                                                    ctypes.POINTER(_vp), _int, _vp]),
     ("flash_mca_forward_ex", _i32, _fwd_args + [_i32, ctypes.POINTER(FmcaOptions), _vp]),
+    ("flash_mca_forward_seq", _i32, _fwd_args + [ctypes.POINTER(FmcaOptions),
+                                                 ctypes.POINTER(FmcaSeq), _vp]),
     ("flash_mca_decode_state_bytes", _sz, [_int] * 4 + [_i32]),
     ("flash_mca_backward_workspace_bytes", _sz, [_int] * 6 + [_i32]),
     ("flash_mca_gau_project", _i32, [_vp] * 5 + [_int] * 4 + [_vp]),
@@ -237,6 +248,35 @@ def flash_mca_forward_ex(Z, V, U, gamma, beta, O, C: int, causal: bool, workspac
                                   int(bool(causal)), dt, workspace.data_ptr(), ws_bytes, path,
                                   ctypes.byref(opts), _stream_ptr(stream))
     _check(st, "flash_mca_forward_ex")
+
+
+def flash_mca_forward_seq(Z, V, U, gamma, beta, O, C: int, workspace, state_in=None,
+                          state_out=None, token_offset: int = 0, n_norm: int = 0,
+                          quad_scale: float | None = None, lin_norm: int = FMCA_LIN_NORM_N,
+                          stream=None) -> None:
+    """``flash_mca_forward_seq``: the causal forward pass on one piece of
+    longer sequences.  ``state_in`` / ``state_out``: fp32 CUDA tensors
+    [B][s][e] (or None), the sum of T3^T V over the chunks before the piece and
+    after it; ``token_offset``: the piece's first token (a multiple of C);
+    ``n_norm``: the divisor's length (0: the piece's n)."""
+    B, n, s, e, dt, ws_bytes = _check_device_args(Z, V, U, gamma, beta, O, workspace)
+    for name, t in (("state_in", state_in), ("state_out", state_out)):
+        if t is not None and (t.dtype != torch.float32 or tuple(t.shape) != (B, s, e)
+                              or not t.is_contiguous() or t.device != Z.device):
+            raise ValueError(f"{name} must be a contiguous float32 [B, s, e] tensor on "
+                             f"{Z.device}")
+    opts = flash_mca_default_options(C)
+    if quad_scale is not None:
+        opts.quad_scale = float(quad_scale)
+    opts.lin_norm = int(lin_norm)
+    seq = FmcaSeq(state_in.data_ptr() if state_in is not None else None,
+                  state_out.data_ptr() if state_out is not None else None,
+                  int(token_offset), int(n_norm))
+    st = lib.flash_mca_forward_seq(Z.data_ptr(), V.data_ptr(), U.data_ptr(), gamma.data_ptr(),
+                                   beta.data_ptr(), O.data_ptr(), B, n, s, e, int(C), 1, dt,
+                                   workspace.data_ptr(), ws_bytes, ctypes.byref(opts),
+                                   ctypes.byref(seq), _stream_ptr(stream))
+    _check(st, "flash_mca_forward_seq")
 
 
 def flash_mca_forward_timed(Z, V, U, gamma, beta, O, C: int, causal: bool, workspace,

@@ -57,7 +57,7 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
                          const float *beta, void *O, int B, int n, int s, int e, int C,
                          int causal, fmca_dtype dtype, void *workspace, size_t workspace_bytes_,
                          fmca_path path, const fmca_options *opts, void *const *events,
-                         int n_events, fmca_stream_t stream);
+                         int n_events, fmca_stream_t stream, const fmca_seq *seq = nullptr);
 
 }  // namespace
 
@@ -334,6 +334,16 @@ fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                       workspace_bytes_, path, opts, nullptr, 0, stream);
 }
 
+fmca_status flash_mca_forward_seq(const void *Z, const void *V, const void *U,
+                                  const float *gamma, const float *beta, void *O, int B, int n,
+                                  int s, int e, int C, int causal, fmca_dtype dtype,
+                                  void *workspace, size_t workspace_bytes_,
+                                  const fmca_options *opts, const fmca_seq *seq,
+                                  fmca_stream_t stream) {
+  return forward_impl(Z, V, U, gamma, beta, O, B, n, s, e, C, causal, dtype, workspace,
+                      workspace_bytes_, FMCA_PATH_AUTO, opts, nullptr, 0, stream, seq);
+}
+
 }  // extern "C"
 
 namespace {
@@ -342,7 +352,7 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
                          const float *beta, void *O, int B, int n, int s, int e, int C,
                          int causal, fmca_dtype dtype, void *workspace, size_t workspace_bytes_,
                          fmca_path path, const fmca_options *opts, void *const *events,
-                         int n_events, fmca_stream_t stream) {
+                         int n_events, fmca_stream_t stream, const fmca_seq *seq) {
   fmca_status st = check_sizes(B, n, s, e, C, causal, dtype);
   if (st != FMCA_OK) return st;
   Variant var;
@@ -372,6 +382,32 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
   }
   const bool tc_ok = want_tc(B, n, s, e, C, dtype);
   if (path == FMCA_PATH_TCGEN05 && !tc_ok) return FMCA_ERR_UNSUPPORTED;
+  // a piece of longer sequences: causal, the tensor-core path, a global term
+  SeqCarry carry;
+  if (seq != nullptr) {
+    if (!causal || !tc_ok || var.lin_norm == kLinNormNone) return FMCA_ERR_UNSUPPORTED;
+    if (seq->token_offset < 0 || seq->token_offset % C != 0 || seq->n_norm < 0 ||
+        seq->token_offset + (int64_t)n >= ((int64_t)1 << 31) || seq->n_norm >= ((int64_t)1 << 31))
+      return FMCA_ERR_INVALID_ARG;
+    if (!aligned16(seq->state_in) || !aligned16(seq->state_out)) return FMCA_ERR_ALIGN;
+    if (seq->state_out != nullptr) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(seq->state_out);
+      const uintptr_t a1 = a0 + sizeof(float) * (size_t)B * s * e;
+      auto hits = [&](const void *p, size_t bytes) {
+        const uintptr_t b0 = reinterpret_cast<uintptr_t>(p), b1 = b0 + bytes;
+        return b0 < a1 && a0 < b1;
+      };
+      const size_t es = elem_size(dtype);
+      if (hits(Z, (size_t)B * n * s * es) || hits(V, (size_t)B * n * e * es) ||
+          hits(U, (size_t)B * n * e * es) || hits(O, (size_t)B * n * e * es) ||
+          hits(workspace, workspace_bytes_))
+        return FMCA_ERR_INVALID_ARG;
+    }
+    carry.state_in = seq->state_in;
+    carry.state_out = seq->state_out;
+    carry.tok0 = (int)seq->token_offset;
+    carry.n_norm = (int)seq->n_norm;
+  }
   const bool use_tc = (path == FMCA_PATH_TCGEN05) || (path == FMCA_PATH_AUTO && tc_ok);
   const int nlaunch = use_tc ? tc_launch_count(B, n, e, C, causal, var) : kSimtLaunches;
   if (events != nullptr) {
@@ -384,7 +420,7 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
   int rc;
   if (use_tc)
     rc = launch_tc_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0, var,
-                           workspace, cs, ev);
+                           workspace, cs, ev, seq != nullptr ? &carry : nullptr);
   else
     rc = launch_simt_forward(Z, V, U, gamma, beta, O, B, n, s, e, C, causal ? 1 : 0,
                              dtype == FMCA_BF16 ? 1 : 0, var, workspace, cs, ev);

@@ -112,10 +112,21 @@ int launch_simt_forward(const void *Z, const void *V, const void *U, const float
 // The tensor-core forward pass (workspace: tc_layout(..., false); without a
 // global term and with C > 256 it runs the kernels of
 // launch_tc_forward_materialised and needs tc_layout(..., true)).
+// A call on one piece of longer causal sequences (flash_mca_forward_seq):
+// state_in (fp32 [B][s][e], or null) is the sum of the states T3^T V of the
+// sequences' chunks before the piece, state_out (or null) receives that sum
+// with the piece's chunks added; tok0 is the piece's first token in its
+// sequence (a multiple of C) and n_norm the length the divisor 1/n uses.
+struct SeqCarry {
+  const float *state_in = nullptr;
+  float *state_out = nullptr;
+  int tok0 = 0;
+  int n_norm = 0;
+};
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events = nullptr);
+                      cudaEvent_t const *events = nullptr, const SeqCarry *carry = nullptr);
 // Kernels one launch_tc_forward queues (the memset of its counters not
 // counted).
 int tc_launch_count(int B, int n, int e, int C, int causal, const Variant &var);

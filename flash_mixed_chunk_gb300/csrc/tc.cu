@@ -3,26 +3,29 @@
 // mbarrier pipelines) for bf16 I/O, s = 128, C % 128 == 0, e % 256 == 0.
 //
 // Per call ("FLASH: Possibly the Most Interesting Efficient Transformer
-// Design Recently", sections "Weak Attention" and "Mixed Chunk"): a memset of
-// the work counters and
+// Design Recently", sections "Weak Attention" and "Mixed Chunk"):
 //
-//   tc_chunk_walk    per (sequence, 128-column slice of e), the chunks in
-//                    order: state_g = T3_g^T V_g in TMEM, the running sum of
-//                    the states (fp32, TMEM), the exclusive prefix (causal) or
-//                    total (bidirectional) times 1/n to bf16, and the rows
-//                    T0, T1, T2; a few CTAs, with per-chunk completion
-//                    counters (without a global term: tc_affine_rows, T0 and
-//                    T1 only)
-//   tc_chunk_fused   O = U * (relu(T0 T1^T / C)^2 V_g + T2 prefix_g) per
-//                    (chunk, row tile, e tile), the relu^2 weights kept on
-//                    chip (TMEM), both products accumulated in TMEM; it runs
-//                    beside the walkers (a programmatic dependent that waits
-//                    on their counters, chunk by chunk)
+//   tc_chunk_walk    segment walkers: per (segment of the chunk axis,
+//                    sequence, 256-column slice of e), the segment's chunks
+//                    in order: state_g = T3_g^T V_g in TMEM, the running sum
+//                    (fp32, TMEM) out as each chunk's local sum and the
+//                    segment's total (bf16), and the rows T0, T1, T2 (T2
+//                    carrying the global term's divisor)
+//   tc_chunk_pair    causal chunks of 256: the segment carries from the
+//                    totals, then per (chunk, run of e tiles) the relu^2
+//                    weights in TMEM and O = U * (P V_g + T2 (local + carry))
+//                    for both row tiles; a programmatic dependent of the
+//                    walkers
+//   tc_seg_carry +   other chunk lengths and bidirectional attention: the
+//   tc_chunk_fused   carries (or the total) in a launch of their own, then
+//                    the same per (chunk, row tile, e tiles)
 //
-// The backward pass runs the forward pass in its materialised form instead:
-// tc_chunk_prep also writes the relu^2 weights P and the T2 rows to the
-// workspace (score units), and tc_chunk_attn forms O = U * (P V_g + T2
-// prefix_g) from them, leaving P and T2 for the gradient products.
+// Without a global term: tc_affine_rows (T0, T1) and the fused kernel, or,
+// for chunks over 256 tokens, the stored-weights form below.  The backward
+// pass runs that stored-weights form (launch_tc_forward_materialised):
+// tc_chunk_prep writes the relu^2 weights P and the T2 rows to the workspace
+// and tc_chunk_attn forms O = U * (P V_g + T2 prefix_g) from them, leaving P
+// and T2 for the gradient products.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -166,6 +169,7 @@ FusedGrid fused_grid(int B, int n, int e, int C, int causal, bool lin) {
   g.S = 1;
   g.L = g.G;
   g.rows_early = 0;
+  g.carry_all = 0;
   return g;
 }
 
@@ -191,7 +195,7 @@ struct PdlConfig {
 int launch_tc_forward(const void *Z, const void *V, const void *U, const float *gamma,
                       const float *beta, void *O, int B, int n, int s, int e, int C, int causal,
                       const Variant &var, void *workspace, cudaStream_t stream,
-                      cudaEvent_t const *events) {
+                      cudaEvent_t const *events, const SeqCarry *carry) {
   // Without a global term and with chunks longer than 256 tokens (the
   // quadratic-only model), a row tile's relu^2 weights do not fit in TMEM
   // beside its accumulators: the chunk kernel would form them again for every
@@ -243,20 +247,24 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   // the row-pair kernel forms the segment carries itself (counted in
   // sched[2], which the walkers clear)
   const bool pair = use_pair_kernel(C, causal, !no_global);
+  const SeqCarry sq = carry != nullptr ? *carry : SeqCarry{};
+  const bool with_state = causal && (sq.state_in != nullptr || sq.state_out != nullptr);
+  const int n_norm = sq.n_norm > 0 ? sq.n_norm : n;
   unsigned int *carried = reinterpret_cast<unsigned int *>(ws + L.sched) + 2;
   FusedGrid fg = fused_grid(B, n, e, C, causal, !no_global);
   fg.S = sp.S;
   fg.L = sp.L;
   fg.rows_early = 0;
+  fg.carry_all = causal && sq.state_in != nullptr ? 1 : 0;
   int ev = 1;
   if (!no_global) {
     // the segment walkers: local sums, segment totals and the T rows
     const int units = B * (e / WK_ET) * sp.S;
     tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
         mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S, sp.L,
-        carried, pair ? 0 : 1);
+        carried, pair ? 0 : 1, sq.tok0, n_norm);
     if (cudaGetLastError() != cudaSuccess || !record_event(events, ev++, stream)) return 1;
-    if ((sp.S > 1 || !causal) && !pair) {
+    if ((sp.S > 1 || !causal || with_state) && !pair) {
       // totals -> carries (bidirectional: the total), a programmatic
       // dependent of the walkers
       PdlConfig cc(stream, true);
@@ -264,7 +272,8 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
       cc.cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
       cc.cfg.blockDim = dim3(256);
       cc.cfg.dynamicSmemBytes = 0;
-      if (cudaLaunchKernelEx(&cc.cfg, tc_seg_carry, seg, B, sp.S, se, causal) != cudaSuccess ||
+      if (cudaLaunchKernelEx(&cc.cfg, tc_seg_carry, seg, B, sp.S, se, causal, sq.state_in,
+                             sq.state_out) != cudaSuccess ||
           !record_event(events, ev++, stream))
         return 1;
       fg.rows_early = 1;
@@ -288,13 +297,15 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     pg.L = sp.L;
     pg.rows_early = 0;  // no kernel between: the T rows wait for the walkers too
     pg.B = B;
-    pg.carries = sp.S > 1;
+    pg.carries = sp.S > 1 || with_state;
+    pg.carry_all = sq.state_in != nullptr ? 1 : 0;
     fc.cfg.gridDim = dim3(pg.n_tiles < sms ? pg.n_tiles : sms);
     fc.cfg.blockDim = dim3(PAIR_THREADS);
     fc.cfg.dynamicSmemBytes = PAIR_SMEM;
     if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_pair, mT0, mT1, mT2, mV, mLoc, mCy, mU3,
                            static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
-                           pg, e, var.quad_a, seg, carried) != cudaSuccess ||
+                           pg, e, var.quad_a, seg, carried, sq.state_in, sq.state_out) !=
+                               cudaSuccess ||
         !record_event(events, ev++, stream))
       return 1;
     return 0;
@@ -386,7 +397,7 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
       wc.cfg.dynamicSmemBytes = WALK_SMEM;
       if (cudaLaunchKernelEx(&wc.cfg, tc_chunk_walk, mZw, mVw, mL, mT, gamma, beta, trows, plane,
                              B, n, e, C, causal, var.lin_norm, sp.S, sp.L,
-                             static_cast<unsigned int *>(nullptr), 1) != cudaSuccess ||
+                             static_cast<unsigned int *>(nullptr), 1, 0, n) != cudaSuccess ||
           !record_event(events, ev++, stream))
         return 1;
       if (sp.S > 1 || !causal) {
@@ -394,7 +405,9 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
         PdlConfig cc(stream, true);
         cc.cfg.gridDim = dim3((unsigned)((lanes + 255) / 256));
         cc.cfg.blockDim = dim3(256);
-        if (cudaLaunchKernelEx(&cc.cfg, tc_seg_carry, seg, B, sp.S, se, causal) != cudaSuccess ||
+        if (cudaLaunchKernelEx(&cc.cfg, tc_seg_carry, seg, B, sp.S, se, causal,
+                               static_cast<const float *>(nullptr),
+                               static_cast<float *>(nullptr)) != cudaSuccess ||
             !record_event(events, ev++, stream))
           return 1;
       }

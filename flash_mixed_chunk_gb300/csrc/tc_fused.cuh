@@ -91,6 +91,7 @@ struct FusedGrid {
   int n, C, G, causal, lin, R, n_et, n_tiles;
   int S, L;        // segments of the chunk axis, chunks each
   int rows_early;  // the T rows may be read before the grid-dependency wait
+  int carry_all;   // a carried-in state: every causal chunk has a carry
 };
 
 // 64-key stages of row tile rt
@@ -144,7 +145,7 @@ __device__ __forceinline__ FusedUnit decode_fused(int t, int net, const FusedGri
   f.row0 = f.crow + rt * ROW_TILE;
   f.lrow = bg * S_DIM;
   f.crow2 = (b * g.S + (g.causal ? c / g.L : 0)) * S_DIM;
-  f.carry = !g.causal || c / g.L > 0;
+  f.carry = !g.causal || g.carry_all || c / g.L > 0;
   f.rt = rt;
   f.et0 = et;
   f.net = net;

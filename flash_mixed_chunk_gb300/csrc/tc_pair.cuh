@@ -74,7 +74,8 @@ struct PairGrid {
   int S, L;        // segments of the chunk axis, chunks each
   int rows_early;  // the T rows may be read before the grid-dependency wait
   int B;
-  int carries;     // form the segment carries here (S > 1) before the first carry load
+  int carries;     // form the segment carries here before the first carry load
+  int carry_all;   // a carried-in state: every chunk has a carry
 };
 
 struct PairUnit {
@@ -94,7 +95,7 @@ __device__ __forceinline__ PairUnit decode_pair(int t, int net, const PairGrid &
   f.lrow = bg * S_DIM;
   f.crow2 = (b * g.S + c / g.L) * S_DIM;
   f.local = c % g.L != 0;
-  f.carry = c / g.L > 0;
+  f.carry = g.carry_all || c / g.L > 0;
   f.et0 = t % g.n_et;
   f.net = net;
   return f;
@@ -141,7 +142,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                   __nv_bfloat16 *__restrict__ O,              // [B*n][e]
                   PairGrid grid, int e, float quad_a,
                   __nv_bfloat16 *__restrict__ seg,  // segment totals -> carries, in place
-                  unsigned int *__restrict__ carried) {  // CTAs done with their carries
+                  unsigned int *__restrict__ carried,  // CTAs done with their carries
+                  const float *__restrict__ state_in,  // carried-in state, or null
+                  float *__restrict__ state_out) {     // the state after this call, or null
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -206,7 +209,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const int64_t se = (int64_t)S_DIM * e;
     const int64_t groups = (int64_t)grid.B * (se / 8);
     for (int64_t t = (int64_t)blockIdx.x * 192 + ct; t < groups; t += (int64_t)gridDim.x * 192)
-      seg_carry_group(seg, grid.S, se, 1, t);
+      seg_carry_group(seg, grid.S, se, 1, t, state_in, state_out);
     named_bar_sync(5, 192);
     // every thread's carries are stored (the barrier orders them before the
     // release)

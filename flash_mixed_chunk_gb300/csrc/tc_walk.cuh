@@ -72,7 +72,8 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
                   __nv_bfloat16 *__restrict__ trows, int64_t rows_plane, int B, int n, int e,
                   int C, int causal, int lin_norm, int S, int L,
                   unsigned int *__restrict__ zero_count,  // cleared here if not null
-                  int store_first_local) {  // 0: a segment's first chunk (zero sums) is not stored
+                  int store_first_local,  // 0: a segment's first chunk (zero sums) is not stored
+                  int tok0, int n_norm) {  // the call's first token in its sequence; divisor length
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -242,7 +243,8 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
                 *reinterpret_cast<uint4 *>(dst + rows_plane) = affine8(z, g1v, b1v);
                 const int t = g * C + k * WK_KEYS + r;  // position in the sequence
                 *reinterpret_cast<uint4 *>(dst + 2 * rows_plane) =
-                    affine8_scaled(z, g2v, b2v, t2_weight(lin_norm, causal, t, g, n, C));
+                    affine8_scaled(z, g2v, b2v,
+                                   t2_weight(lin_norm, causal, tok0 + t, tok0 / C + g, n_norm, C));
               }
               *ptr = affine8(z, g3v, b3v);
             }
@@ -371,14 +373,27 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
 // in place in T [B][S][s][e] (bf16): causal, carry_sg = the sum of the
 // totals before segment sg (carry_0 = 0); bidirectional, the sum of all of
 // them, in slot 0.  fp32 sums.
+// With a carried-in state (causal: the sum of the states of the sequence's
+// chunks before this call, fp32 [B][s][e]) the running sum starts from it, so
+// every carry includes it; with state_out the sum of the state and all the
+// totals (the state after this call) is written there, fp32.
 __device__ __forceinline__ void seg_carry_group(__nv_bfloat16 *__restrict__ T, int S, int64_t se,
-                                                int causal, int64_t t) {
+                                                int causal, int64_t t,
+                                                const float *__restrict__ state_in,
+                                                float *__restrict__ state_out) {
   const int64_t per_b = se / 8;
   const int64_t b = t / per_b, x = (t % per_b) * 8;
   __nv_bfloat16 *p = T + b * S * se + x;
   float run[8];
+  if (state_in != nullptr) {
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(state_in + b * se + x));
+    const float4 c = __ldcg(reinterpret_cast<const float4 *>(state_in + b * se + x + 4));
+    run[0] = a.x, run[1] = a.y, run[2] = a.z, run[3] = a.w;
+    run[4] = c.x, run[5] = c.y, run[6] = c.z, run[7] = c.w;
+  } else {
 #pragma unroll
-  for (int i = 0; i < 8; ++i) run[i] = 0.f;
+    for (int i = 0; i < 8; ++i) run[i] = 0.f;
+  }
   auto put = [&](__nv_bfloat16 *dst) {
     *reinterpret_cast<uint4 *>(dst) =
         make_uint4(pack_bf16x2(run[0], run[1]), pack_bf16x2(run[2], run[3]),
@@ -406,17 +421,23 @@ __device__ __forceinline__ void seg_carry_group(__nv_bfloat16 *__restrict__ T, i
     }
   }
   if (!causal) put(p);
+  if (state_out != nullptr) {
+    float4 *q = reinterpret_cast<float4 *>(state_out + b * se + x);
+    q[0] = make_float4(run[0], run[1], run[2], run[3]);
+    q[1] = make_float4(run[4], run[5], run[6], run[7]);
+  }
 }
 
 // tc_seg_carry: seg_carry_group over all column groups, one thread each; a
 // programmatic dependent of the walkers.
 __global__ void __launch_bounds__(256)
-    tc_seg_carry(__nv_bfloat16 *__restrict__ T, int B, int S, int64_t se, int causal) {
+    tc_seg_carry(__nv_bfloat16 *__restrict__ T, int B, int S, int64_t se, int causal,
+                 const float *__restrict__ state_in, float *__restrict__ state_out) {
   griddep_wait();  // the walkers' totals
   griddep_launch_dependents();
   const int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
   if (t >= (int64_t)B * (se / 8)) return;
-  seg_carry_group(T, S, se, causal, t);
+  seg_carry_group(T, S, se, causal, t, state_in, state_out);
 }
 
 // tc_prefix_fixup (the form the backward pass runs): the scaled prefix

@@ -185,6 +185,47 @@ fmca_status flash_mca_forward_ex(const void *Z, const void *V, const void *U,
                                  void *workspace, size_t workspace_bytes, fmca_path path,
                                  const fmca_options *opts, fmca_stream_t stream);
 
+/*
+ * One piece of longer causal sequences: the pages' cumsum form of the global
+ * term ("Mixed Chunk") carried across calls, so that a long sequence can be
+ * split over calls (chunked prefill) or over ranks (each rank one piece).
+ *   state_in     NULL, or fp32 device [B][s][e], 16-byte aligned: the sum of
+ *                T3_h^T V_h over the sequences' chunks before this piece
+ *                (unscaled); every chunk of the piece adds it to its sum.
+ *   state_out    NULL, or fp32 device [B][s][e], 16-byte aligned: receives
+ *                state_in (or 0) plus the sum over the piece's chunks, the
+ *                state_in of the next piece.  It may be state_in itself and
+ *                must not overlap the other buffers.
+ *   token_offset the piece's first token in its sequences (a multiple of C,
+ *                >= 0): positions and chunk indices of the divisors
+ *                (FMCA_LIN_NORM_SUMMED, FMCA_LIN_NORM_POSITION) count from
+ *                the sequence start.
+ *   n_norm       the length the default divisor 1/n uses (the whole
+ *                sequence's length); 0 means the piece's n.
+ */
+typedef struct fmca_seq {
+  const float *state_in;
+  float *state_out;
+  int64_t token_offset;
+  int64_t n_norm;
+} fmca_seq;
+
+/* flash_mca_forward_ex (path FMCA_PATH_AUTO) on one piece of longer
+ * sequences.  Only causal attention on the tensor-core path, with a global
+ * term: other arguments return FMCA_ERR_UNSUPPORTED (bidirectional attention
+ * needs every piece's total before any output; gather the totals first).
+ * seq == NULL is flash_mca_forward_ex.  Splitting a sequence at a chunk
+ * boundary and running the pieces in order with state_out of one as state_in
+ * of the next gives the output of one call on the whole sequence (within the
+ * same error bounds: the sums are rounded at other points).  The workspace is
+ * the one flash_mca_workspace_bytes gives for the piece. */
+fmca_status flash_mca_forward_seq(const void *Z, const void *V, const void *U,
+                                  const float *gamma, const float *beta, void *O, int B, int n,
+                                  int s, int e, int C, int causal, fmca_dtype dtype,
+                                  void *workspace, size_t workspace_bytes,
+                                  const fmca_options *opts, const fmca_seq *seq,
+                                  fmca_stream_t stream);
+
 /* flash_mca_forward_ex that also records caller-created CUDA events
  * (cudaEvent_t handles) on `stream` around its kernels: events[0] before the
  * first kernel and events[i] after kernel i (1-based), so `n_events` must be

@@ -69,3 +69,31 @@ def test_single_process_helpers_are_identity():
     bench.barrier()  # no process group: a no-op
     assert bench.whole_job_rate(1, 100, 10, 2.0) == 500.0
     assert bench.rank_seed(4, 0) == 4
+
+
+def _scan_worker(rank: int, world: int, port: int, out_dir: str):
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        from flash_mixed_chunk_gb300.seqsplit import exclusive_state_scan
+        g = torch.Generator().manual_seed(100 + rank)
+        local = torch.randn(2, 3, 4, generator=g, dtype=torch.float32)
+        state_in = exclusive_state_scan(local)
+        torch.save({"local": local, "state_in": state_in}, os.path.join(out_dir, f"s{rank}.pt"))
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.timeout(180)
+@pytest.mark.parametrize("world", [2, 3])
+def test_exclusive_state_scan_over_ranks(tmp_path, world):
+    """The carried-in state of a sequence split over ranks: rank r receives the
+    sum of the per-rank state sums of ranks 0 .. r-1 (zeros on rank 0)."""
+    mp.start_processes(_scan_worker, args=(world, _free_port(), str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    got = [torch.load(tmp_path / f"s{k}.pt") for k in range(world)]
+    run = torch.zeros(2, 3, 4)
+    for k in range(world):
+        assert torch.equal(got[k]["state_in"], run)
+        run = run + got[k]["local"]
