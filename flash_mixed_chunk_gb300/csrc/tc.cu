@@ -237,7 +237,11 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                                     (int)WALK_SMEM) == cudaSuccess &&
                cudaFuncSetAttribute(tc_chunk_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)FUSED_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(tc_chunk_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+               cudaFuncSetAttribute(tc_chunk_pair<false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PAIR_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_pair<true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)PAIR_SMEM) == cudaSuccess;
       }))
     return 1;
@@ -302,7 +306,8 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     fc.cfg.gridDim = dim3(pg.n_tiles < sms ? pg.n_tiles : sms);
     fc.cfg.blockDim = dim3(PAIR_THREADS);
     fc.cfg.dynamicSmemBytes = PAIR_SMEM;
-    if (cudaLaunchKernelEx(&fc.cfg, tc_chunk_pair, mT0, mT1, mT2, mV, mLoc, mCy, mU3,
+    auto *pair_kernel = with_state ? tc_chunk_pair<true> : tc_chunk_pair<false>;
+    if (cudaLaunchKernelEx(&fc.cfg, pair_kernel, mT0, mT1, mT2, mV, mLoc, mCy, mU3,
                            static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
                            pg, e, var.quad_a, seg, carried, sq.state_in, sq.state_out) !=
                                cudaSuccess ||

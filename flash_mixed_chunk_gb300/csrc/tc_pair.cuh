@@ -87,6 +87,7 @@ struct PairUnit {
   int et0, net;
 };
 
+template <bool kState>
 __device__ __forceinline__ PairUnit decode_pair(int t, int net, const PairGrid &g) {
   const int bg = t / g.n_et;
   const int b = bg / g.G, c = bg % g.G;
@@ -95,7 +96,7 @@ __device__ __forceinline__ PairUnit decode_pair(int t, int net, const PairGrid &
   f.lrow = bg * S_DIM;
   f.crow2 = (b * g.S + c / g.L) * S_DIM;
   f.local = c % g.L != 0;
-  f.carry = g.carry_all || c / g.L > 0;
+  f.carry = (kState && g.carry_all) || c / g.L > 0;
   f.et0 = t % g.n_et;
   f.net = net;
   return f;
@@ -130,6 +131,9 @@ __device__ __forceinline__ void pair_gate64(const u32x8 (&uv)[4], __nv_bfloat16 
   }
 }
 
+// kState: a carried-in state or a state out (flash_mca_forward_seq); the
+// plain forward pass compiles without that code.
+template <bool kState>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     tc_chunk_pair(const __grid_constant__ CUtensorMap mapT0,  // T0 rows, 3-D box {64, 128, 2}
                   const __grid_constant__ CUtensorMap mapT1,  // T1 rows, 3-D box {64, 128, 2}
@@ -209,7 +213,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const int64_t se = (int64_t)S_DIM * e;
     const int64_t groups = (int64_t)grid.B * (se / 8);
     for (int64_t t = (int64_t)blockIdx.x * 192 + ct; t < groups; t += (int64_t)gridDim.x * 192)
-      seg_carry_group(seg, grid.S, se, 1, t, state_in, state_out);
+      seg_carry_group(seg, grid.S, se, 1, t, kState ? state_in : nullptr,
+                      kState ? state_out : nullptr);
     named_bar_sync(5, 192);
     // every thread's carries are stored (the barrier orders them before the
     // release)
@@ -259,7 +264,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         uq_net[qs] = net;
         mbar_arrive(&uq_full[qs]);
         if (uu < 0) break;
-        const PairUnit f = decode_pair(uu, net, grid);
+        const PairUnit f = decode_pair<kState>(uu, net, grid);
         // the T rows: with the carry kernel between their writer and this
         // grid, the writer had completed before this grid launched; otherwise
         // wait for the kernel before
@@ -341,7 +346,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         const int u = uq_unit[qs], unet = uq_net[qs];
         mbar_arrive(&uq_empty[qs]);
         if (u < 0) break;
-        const PairUnit f = decode_pair(u, unet, grid);
+        const PairUnit f = decode_pair<kState>(u, unet, grid);
         // ---- scores, once per unit, into the accumulators' columns: the
         // previous unit's last tile has been drained from both
         const int i_a1 = it, i_k0 = it + 1, i_k1 = it + 2, i_a0 = it + 3;
@@ -498,7 +503,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!got && mt == 0) record_timeout(860);
         break;
       }
-      const PairUnit f = decode_pair(u, unet, grid);
+      const PairUnit f = decode_pair<kState>(u, unet, grid);
       it += 4;  // the unit's T0 and T1 items
       for (int x = 0; x < f.net && ok; ++x) {
         const int il = it + 2, icy = it + 3;
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       }
       // then columns 64-127 of the unit's output tiles (the epilogue warps
       // take 0-63)
-      const PairUnit f = decode_pair(u, unet, grid);
+      const PairUnit f = decode_pair<kState>(u, unet, grid);
       for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
         for (int rr = 0; rr < 2 && ok; ++rr) {
           const int r = 1 - rr;
@@ -641,7 +646,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!got && mt == 0) record_timeout(850);
         break;
       }
-      const PairUnit f = decode_pair(u, unet, grid);
+      const PairUnit f = decode_pair<kState>(u, unet, grid);
       for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
         for (int rr = 0; rr < 2 && ok; ++rr) {
           const int r = 1 - rr;  // the order the accumulators are formed in

@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
     load8(beta + 2 * S_DIM + cl, b2v);
     load8(gamma + 3 * S_DIM + cl, g3v);
     load8(beta + 3 * S_DIM + cl, b3v);
+    const int g_off = tok0 / C;  // the call's first chunk in its sequence
     int it = 0;
     bool ok = true;
     for (int u = (int)blockIdx.x; u < n_units && ok; u += W) {
@@ -244,7 +245,7 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
                 const int t = g * C + k * WK_KEYS + r;  // position in the sequence
                 *reinterpret_cast<uint4 *>(dst + 2 * rows_plane) =
                     affine8_scaled(z, g2v, b2v,
-                                   t2_weight(lin_norm, causal, tok0 + t, tok0 / C + g, n_norm, C));
+                                   t2_weight(lin_norm, causal, tok0 + t, g_off + g, n_norm, C));
               }
               *ptr = affine8(z, g3v, b3v);
             }
