@@ -7,6 +7,13 @@
 // masked, plus V-hat^lin_g from the chunk walkers' local sums and carries,
 // gated by U_g).  Included by tc.cu.
 //
+// At its start every CTA turns its share of the walkers' segment totals into
+// carries (warps 2-3 and 8-11, idle until the first merge and output tile)
+// and counts itself on a grid counter; the producer loads no carry before
+// every CTA is counted.  A segment's first chunk has no local-sum item (its
+// local sum is zero and the walkers do not store it), a sequence's first
+// chunk no global product at all.
+//
 // The chunk-local kernel streams V, the local sums and the carries once per
 // e tile; with one row tile per unit (tc_chunk_fused) both row tiles of a
 // chunk load them.  Here a unit is (chunk, run of 128-column e tiles) and

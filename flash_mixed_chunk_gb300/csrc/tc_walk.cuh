@@ -10,12 +10,16 @@
 // order:
 //   D_g = T3_g^T V_g[:, slice]      M = 128 (s), N = 256, K = C keys, both
 //                                   operands MN-major, into TMEM
-//   causal: local_g = R, stored as bf16, then R += D_g (R = the fp32 sum of
-//           the segment's states before g, in TMEM)
+//   causal: local_g = R, stored as bf16 (not for the segment's first chunk,
+//           where it is zero, when the output kernel is the row-pair one),
+//           then R += D_g (R = the fp32 sum of the segment's states before
+//           g, in TMEM)
 //   after the segment's last chunk: its total R, stored as bf16
 // The chunk states are never rounded; the sums are fp32 sums of the fp32
-// products.  tc_seg_carry then turns the segment totals into carries (the sum
-// of the segments before each; the total of all when bidirectional), so that
+// products.  seg_carry_group (run by the row-pair kernel's idle warps, or as
+// the launch tc_seg_carry) then turns the segment totals into carries (the
+// sum of the segments before each, from a carried-in state when the call is
+// one piece of longer sequences; the total of all when bidirectional), so that
 //   prefix_g = carry_sg(g) + local_g     (causal)
 //   total    = carry_0                   (bidirectional)
 // which the output kernel forms as two products of the same T2 rows.  The
