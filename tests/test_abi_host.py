@@ -344,3 +344,32 @@ def test_backward_launch_count():
     assert cnt(2, 1024, 128, 512, 256, True, f32, lin_norm=fm.FMCA_LIN_NORM_NONE) == 7
     assert cnt(2, 1024, 128, 512, 256, True, f32, saved=True) == 0
     assert cnt(2, 1024, 128, 512, 60, True, bf) == 0        # C does not divide n
+
+
+def test_forward_seq_rejects_before_queueing():
+    """flash_mca_forward_seq checks its arguments on the host before anything is
+    queued: bidirectional attention and the no-global-term variant are not
+    covered, the piece must start on a chunk boundary, state pointers must be
+    16-byte aligned and state_out must not overlap the other buffers.  The
+    pointers here are never dereferenced."""
+    import ctypes
+    B, n, s, e, C = 1, 512, 128, 256, 256
+    P = 0x7F0000000000
+    z, v, u, g, b, o = P, P + (1 << 24), P + (2 << 24), P + (3 << 24), P + (3 << 24) + 4096, P + (4 << 24)
+    ws = P + (8 << 24)
+    nb = fm.flash_mca_workspace_bytes(B, n, s, e, C, 1, fm.FMCA_BF16)
+    opts = fm.flash_mca_default_options(C)
+    state = P + (16 << 24)
+
+    def call(causal, offset, lin_norm=fm.FMCA_LIN_NORM_N, s_in=state, s_out=state, dt=fm.FMCA_BF16):
+        opts.lin_norm = lin_norm
+        seq = fm.FmcaSeq(s_in, s_out, offset, 0)
+        return fm.lib.flash_mca_forward_seq(z, v, u, g, b, o, B, n, s, e, C, causal, dt, ws, nb,
+                                            ctypes.byref(opts), ctypes.byref(seq), None)
+    assert call(0, 0) == fm.FMCA_ERR_UNSUPPORTED                      # bidirectional
+    assert call(1, 0, lin_norm=fm.FMCA_LIN_NORM_NONE) == fm.FMCA_ERR_UNSUPPORTED
+    assert call(1, 0, dt=fm.FMCA_F32) != fm.FMCA_OK                   # not the tensor-core path
+    assert call(1, 128) == fm.FMCA_ERR_INVALID_ARG                    # off a chunk boundary
+    assert call(1, -256) == fm.FMCA_ERR_INVALID_ARG
+    assert call(1, 0, s_in=state + 4) == fm.FMCA_ERR_ALIGN
+    assert call(1, 0, s_out=o) == fm.FMCA_ERR_INVALID_ARG             # state_out overlaps O
