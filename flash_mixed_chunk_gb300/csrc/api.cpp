@@ -430,10 +430,12 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
 // Pieces of the host-buffer pipeline: with at least two sequences and 96 MB
 // of inputs and output, up to four pieces of whole sequences (their copies
 // overlap the passes); smaller problems keep one stream (their passes and
-// copies are too short for the overlap to pay for its extra launches).
+// copies are too short for the overlap to pay for its extra launches).  Fewer
+// than four causal sequences of 96 MB or more on the tensor cores run pieces
+// of every sequence's tokens instead (flash_mca_forward_host).
+constexpr size_t kHostPipelineBytes = (size_t)96 << 20;
 int host_pipeline_pieces(int B, size_t bytes) {
-  constexpr size_t kPipelineBytes = (size_t)96 << 20;
-  if (B < 2 || bytes < kPipelineBytes) return 1;
+  if (B < 2 || bytes < kHostPipelineBytes) return 1;
   return B < 4 ? B : 4;
 }
 
@@ -500,7 +502,8 @@ size_t flash_mca_host_arena_bytes(int B, int n, int s, int e, int C, int causal,
   if (check_sizes(B, n, s, e, C, causal, dtype) != FMCA_OK) return 0;
   const size_t es = elem_size(dtype);
   return align256((size_t)B * n * s * es) + 3 * align256((size_t)B * n * e * es) +
-         2 * align256(sizeof(float) * 4 * (size_t)s) + workspace_bytes(B, n, s, e, C, causal);
+         2 * align256(sizeof(float) * 4 * (size_t)s) + workspace_bytes(B, n, s, e, C, causal) +
+         align256(sizeof(float) * (size_t)B * s * e);  // the carried state of token pieces
 }
 
 fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *hU,
@@ -533,8 +536,67 @@ fmca_status flash_mca_forward_host(const void *hZ, const void *hV, const void *h
   p += align256(vb);
   void *ws = p;
   const size_t wsb = workspace_bytes(B, n, s, e, C, causal);
+  p += align256(wsb);
+  float *dstate = reinterpret_cast<float *>(p);
   cudaStream_t cs = reinterpret_cast<cudaStream_t>(stream);
   const int pieces = host_pipeline_pieces(B, zb + 3 * vb);
+  // Fewer than four sequences, causal, on the tensor cores: pieces of every
+  // sequence's tokens instead (a quarter or a half of each), run in order
+  // with the chunk-state sum carried from piece to piece (flash_mca_forward_seq),
+  // so that the last piece's pass and copy out are short.
+  int parts = 1;
+  if (zb + 3 * vb >= kHostPipelineBytes && B < 4 && causal && want_tc(B, n, s, e, C, dtype))
+    for (int p2 : {4, 2})
+      if (n % p2 == 0 && (n / p2) % C == 0) {
+        parts = p2;
+        break;
+      }
+  if (parts > 1) {
+    HostStreams *hs = host_streams();
+    if (hs == nullptr) return FMCA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(hs->mutex);
+    const int np = n / parts;
+    const size_t zr = (size_t)np * s * es, vr = (size_t)np * e * es;  // one sequence's part
+    const size_t zpiece = (size_t)B * zr, vpiece = (size_t)B * vr;     // a piece, all sequences
+    if (cudaEventRecord(hs->start, cs) != cudaSuccess ||
+        cudaStreamWaitEvent(hs->in, hs->start, 0) != cudaSuccess ||
+        cudaMemcpyAsync(dg, hgamma, gbytes, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+        cudaMemcpyAsync(db, hbeta, gbytes, cudaMemcpyHostToDevice, hs->in) != cudaSuccess)
+      return FMCA_ERR_CUDA;
+    for (int k = 0; k < parts; ++k) {
+      // piece k: tokens [k np, (k + 1) np) of every sequence, gathered into a
+      // contiguous [B][np][.] block of the arena (one strided copy each)
+      char *pz = dZ + k * zpiece, *pv = dV + k * vpiece, *pu = dU + k * vpiece;
+      char *po = dO + k * vpiece;
+      if (cudaMemcpy2DAsync(pz, zr, static_cast<const char *>(hZ) + k * zr, (size_t)n * s * es,
+                            zr, B, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+          cudaMemcpy2DAsync(pv, vr, static_cast<const char *>(hV) + k * vr, (size_t)n * e * es,
+                            vr, B, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+          cudaMemcpy2DAsync(pu, vr, static_cast<const char *>(hU) + k * vr, (size_t)n * e * es,
+                            vr, B, cudaMemcpyHostToDevice, hs->in) != cudaSuccess ||
+          cudaEventRecord(hs->in_done[k], hs->in) != cudaSuccess ||
+          cudaStreamWaitEvent(cs, hs->in_done[k], 0) != cudaSuccess)
+        return FMCA_ERR_CUDA;
+      fmca_seq seq;
+      seq.state_in = k > 0 ? dstate : nullptr;
+      seq.state_out = dstate;
+      seq.token_offset = (int64_t)k * np;
+      seq.n_norm = n;
+      st = flash_mca_forward_seq(pz, pv, pu, dg, db, po, B, np, s, e, C, causal, dtype, ws, wsb,
+                                 nullptr, &seq, stream);
+      if (st != FMCA_OK) return st;
+      if (cudaEventRecord(hs->pass_done[k], cs) != cudaSuccess ||
+          cudaStreamWaitEvent(hs->out, hs->pass_done[k], 0) != cudaSuccess ||
+          cudaMemcpy2DAsync(static_cast<char *>(hO) + k * vr, (size_t)n * e * es, po, vr, vr, B,
+                            cudaMemcpyDeviceToHost, hs->out) != cudaSuccess)
+        return FMCA_ERR_CUDA;
+    }
+    if (cudaEventRecord(hs->out_done, hs->out) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, hs->out_done, 0) != cudaSuccess ||
+        cudaStreamSynchronize(cs) != cudaSuccess)
+      return FMCA_ERR_CUDA;
+    return FMCA_OK;
+  }
   if (pieces <= 1) {
     // one stream: copies in, the pass, the copy out
     if (cudaMemcpyAsync(dZ, hZ, zb, cudaMemcpyHostToDevice, cs) != cudaSuccess ||

@@ -383,15 +383,19 @@ int flash_mca_launch_count_ex(int B, int n, int s, int e, int C, int causal,
  * back to host memory and waits for the stream before returning, so hO is
  * ready on return.  Host buffers should be page-locked for the copies to run
  * at full speed (pageable memory works, more slowly).  With at least two
- * sequences and 96 MB of inputs and output, the call runs up to four pieces
- * of whole sequences so that copies and passes overlap: the copies go on two
+ * sequences and 96 MB of inputs and output, the call runs pieces so that
+ * copies and passes overlap: up to four pieces of whole sequences, or, with
+ * fewer than four causal sequences on the tensor-core path, four (or two)
+ * pieces of every sequence's tokens run in order with the chunk-state sum
+ * carried between them (flash_mca_forward_seq).  The copies go on two
  * streams of the library's own (created once per device), chained to
  * `stream` by events, the passes on `stream`.  Each piece is a batch of its
  * own, so the output bits can differ from one flash_mca_forward call on the
  * whole batch (within the same error bounds).
  *   device_arena   caller-owned device buffer, 256-byte aligned, of at least
  *                  flash_mca_host_arena_bytes(...) bytes; it holds the device
- *                  copies of the inputs and output and the workspace.
+ *                  copies of the inputs and output, the workspace and the
+ *                  carried state of token pieces (fp32 [B][s][e]).
  */
 size_t flash_mca_host_arena_bytes(int B, int n, int s, int e, int C, int causal,
                                   fmca_dtype dtype);

@@ -141,12 +141,15 @@ def test_host_buffer_entry_matches_device_entry(B, causal):
     assert torch.equal(Oh, dev)
 
 
-@pytest.mark.parametrize("B,n,causal", [(2, 8192, True), (5, 4096, False)])
+@pytest.mark.parametrize("B,n,causal", [(2, 8192, True), (5, 4096, False), (1, 32768, True)])
 def test_host_buffer_pipeline_whole_output(B, n, causal):
     """Problems of 96 MB and more go through the host-buffer entry point in
-    pieces of whole sequences (copies overlapping the passes): the whole
-    output against the oracle (each piece is a batch of its own, so the bits
-    may differ from one call on the whole batch; the bar is the same)."""
+    pieces (copies overlapping the passes): of whole sequences (B = 5,
+    bidirectional), or, for fewer than four causal sequences, of every
+    sequence's tokens with the chunk-state sum carried between them (B = 2
+    and B = 1).  The whole output against the oracle (each piece is a batch
+    of its own, so the bits may differ from one call on the whole batch; the
+    bar is the same)."""
     m = fm()
     C, s, e = 256, 128, 1536
     Z, V, U, gamma, beta = mca_inputs.make_inputs(B, n, s, e, 61 + B, torch.bfloat16)
