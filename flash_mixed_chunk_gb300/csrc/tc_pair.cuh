@@ -41,7 +41,7 @@
 // goes back early for the next e tile's copies.
 // Shared memory: a ring of 5 items of 32 KB (3-D TMA boxes of 128 rows x two
 // 64-column blocks): T0 of each row tile, T1 of keys 0-127 and 128-255 (unit
-// start), then per e tile V of keys 0-127 and 128-255, the local sums and the
+// start), then per e tile V of keys 128-255 and 0-127, the local sums and the
 // carry; and the T2 rows of both row tiles (64 KB) for the unit.
 // TMEM (512 columns): O_0 [0, 128), O_1 [128, 256), P [320, 512); the score
 // stages use [0, 128), [128, 256), then [0, 128) again once the first is read,
@@ -294,8 +294,9 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         tma_load_3d(bbuf + PA_ITEM, &mapT2, &b_full, 0, f.crow + 128, 0);
         for (int x = 0; x < f.net && ok; ++x) {
           const int eb = (f.et0 + x) * 2;  // first 64-column block of the e tile
-          // V's last read: it may leave L2 first
-          ok = issue(&mapV, f.crow, eb, true) && issue(&mapV, f.crow + 128, eb, true);
+          // V's last read: it may leave L2 first.  Keys 128-255 first: row
+          // tile 1's first products read them
+          ok = issue(&mapV, f.crow + 128, eb, true) && issue(&mapV, f.crow, eb, true);
           // the epilogue's U rows of this e tile, into L2 ahead of its loads
           // (their latency from DRAM otherwise sets the pace)
           tma_prefetch_l2_3d(&mapU, 0, f.crow + 128, eb);
@@ -404,7 +405,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         // (stages 0, 1); O_r = sum_k P_rk V_k + T2_r (local + carry)
         for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
           // il: the local sums, or the carry alone in a segment's first chunk
-          const int iv0 = it, iv1 = it + 1, il = it + 2;
+          const int iv1 = it, iv0 = it + 1, il = it + 2;
           const int nglob = (int)f.local + (int)f.carry;
           const bool merge = f.local && f.carry;
           it += 2 + nglob;
