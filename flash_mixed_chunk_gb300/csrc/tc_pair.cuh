@@ -417,18 +417,22 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
               ok = false;
               break;
             }
-            tc_fence_after();
             const uint32_t ocol = tbase + (uint32_t)(r * FU_ET);
             const int ns = pair_stages(r);
+            // the unit's first tile: every relu^2 weight of the row tile is
+            // formed, so its score stage, whose columns O_r reuses, has been
+            // read in full before the first product overwrites them
+            for (int k = 0; x == 0 && k < ns && ok; ++k)
+              if (!mbar_wait(&p_full[pair_pslot(r, k)], j & 1, kWaitLimitNs)) {
+                record_timeout(822);
+                ok = false;
+              }
+            if (!ok) break;
+            tc_fence_after();
             for (int q = 0; q < ns && ok; ++q) {
               const int k = r == 1 ? (q + 2) % 4 : q;  // row tile 1: keys 128-255 first
               const int iv = k < 2 ? iv0 : iv1, ps = pair_pslot(r, k);
               if (!wait_item(iv)) {
-                ok = false;
-                break;
-              }
-              if (x == 0 && !mbar_wait(&p_full[ps], j & 1, kWaitLimitNs)) {
-                record_timeout(822);
                 ok = false;
                 break;
               }
