@@ -738,9 +738,9 @@ def run_ours(args, w, rank, world, device):
                         else ["tc_chunk_prep", "tc_chunk_attn"])
     else:
         # the segment walkers, the carries (with more than one segment or
-        # bidirectional), the output kernel (both row tiles of a causal chunk
-        # of 256 per unit, else one)
-        out_kernel = "tc_chunk_pair" if (w.causal and w.C == 256) else "tc_chunk_fused"
+        # bidirectional), the output kernel (both row tiles of a chunk of 256
+        # per unit, else one)
+        out_kernel = "tc_chunk_pair" if w.C == 256 else "tc_chunk_fused"
         kernel_names = (["tc_chunk_walk", out_kernel] if nl == 2
                         else ["tc_chunk_walk", "tc_seg_carry", out_kernel])
     kernels = {name: {"ms": per_kernel_ms[i], "share": per_kernel_ms[i] / sum(per_kernel_ms)}

@@ -11,14 +11,14 @@
 //                    (fp32, TMEM) out as each chunk's local sum and the
 //                    segment's total (bf16), and the rows T0, T1, T2 (T2
 //                    carrying the global term's divisor)
-//   tc_chunk_pair    causal chunks of 256: the segment carries from the
-//                    totals, then per (chunk, run of e tiles) the relu^2
-//                    weights in TMEM and O = U * (P V_g + T2 (local + carry))
-//                    for both row tiles; a programmatic dependent of the
-//                    walkers
-//   tc_seg_carry +   other chunk lengths and bidirectional attention: the
-//   tc_chunk_fused   carries (or the total) in a launch of their own, then
-//                    the same per (chunk, row tile, e tiles)
+//   tc_chunk_pair    chunks of 256: the segment carries (bidirectional: the
+//                    total) from the walkers' totals, then per (chunk, run
+//                    of e tiles) the relu^2 weights in TMEM and O = U * (P V_g
+//                    + T2 (local + carry)) (bidirectional: + T2 total) for
+//                    both row tiles; a programmatic dependent of the walkers
+//   tc_seg_carry +   chunks of 128 or over 256 tokens: the carries (or the
+//   tc_chunk_fused   total) in a launch of their own, then the same per
+//                    (chunk, row tile, e tiles)
 //
 // Without a global term: tc_affine_rows (T0, T1) and the fused kernel, or,
 // for chunks over 256 tokens, the stored-weights form below.  The backward
@@ -131,10 +131,12 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   return true;
 }
 
-// The row-pair output kernel (tc_chunk_pair): causal chunks of two 128-row
-// tiles with a global term.  It forms the segment carries itself.
+// The row-pair output kernel (tc_chunk_pair): chunks of two 128-row tiles
+// with a global term, causal or bidirectional.  It forms the segment carries
+// (or the total) itself.
 static bool use_pair_kernel(int C, int causal, bool lin) {
-  return lin && causal && C == 2 * ROW_TILE;
+  (void)causal;
+  return lin && C == 2 * ROW_TILE;
 }
 
 int tc_launch_count(int B, int n, int e, int C, int causal, const Variant &var) {
@@ -237,10 +239,13 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
                                     (int)WALK_SMEM) == cudaSuccess &&
                cudaFuncSetAttribute(tc_chunk_fused, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)FUSED_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(tc_chunk_pair<false>,
+               cudaFuncSetAttribute(tc_chunk_pair<false, true>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)PAIR_SMEM) == cudaSuccess &&
-               cudaFuncSetAttribute(tc_chunk_pair<true>,
+               cudaFuncSetAttribute(tc_chunk_pair<true, true>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)PAIR_SMEM) == cudaSuccess &&
+               cudaFuncSetAttribute(tc_chunk_pair<false, false>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)PAIR_SMEM) == cudaSuccess;
       }))
@@ -306,7 +311,9 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     fc.cfg.gridDim = dim3(pg.n_tiles < sms ? pg.n_tiles : sms);
     fc.cfg.blockDim = dim3(PAIR_THREADS);
     fc.cfg.dynamicSmemBytes = PAIR_SMEM;
-    auto *pair_kernel = with_state ? tc_chunk_pair<true> : tc_chunk_pair<false>;
+    auto *pair_kernel = !causal      ? tc_chunk_pair<false, false>
+                        : with_state ? tc_chunk_pair<true, true>
+                                     : tc_chunk_pair<false, true>;
     if (cudaLaunchKernelEx(&fc.cfg, pair_kernel, mT0, mT1, mT2, mV, mLoc, mCy, mU3,
                            static_cast<const __nv_bfloat16 *>(U), static_cast<__nv_bfloat16 *>(O),
                            pg, e, var.quad_a, seg, carried, sq.state_in, sq.state_out) !=

@@ -1,18 +1,22 @@
 // tc_pair.cuh -- the chunk-local kernel of the mixed-chunk attention core for
-// causal chunks of 256 tokens with a global term, both 128-row tiles of a
-// chunk in one unit:
-//     O = U * (relu(T0 T1^T * a)^2 V_g + T2 local_g + T2 carry)
+// chunks of 256 tokens with a global term, both 128-row tiles of a chunk in
+// one unit:
+//     causal:         O = U * (relu(T0 T1^T * a)^2 V_g + T2 local_g + T2 carry)
+//     bidirectional:  O = U * (relu(T0 T1^T * a)^2 V_g + T2 total)
 // ("FLASH: Possibly the Most Interesting Efficient Transformer Design
-// Recently", section "Mixed Chunk": V-hat^quad_g with the upper triangle
-// masked, plus V-hat^lin_g from the chunk walkers' local sums and carries,
-// gated by U_g).  Included by tc.cu.
+// Recently", section "Mixed Chunk": V-hat^quad_g, with the upper triangle
+// masked when causal, plus V-hat^lin_g from the chunk walkers' local sums and
+// carries, or the sum of all chunks' states when bidirectional, gated by
+// U_g).  Included by tc.cu.
 //
 // At its start every CTA turns its share of the walkers' segment totals into
-// carries (warps 2-3 and 8-11, idle until the first merge and output tile)
-// and counts itself on a grid counter; the producer loads no carry before
-// every CTA is counted.  A segment's first chunk has no local-sum item (its
+// carries (bidirectional: the total of each sequence, in its first segment's
+// slot; warps 2-3 and 8-11, idle until the first merge and output tile) and
+// counts itself on a grid counter; the producer loads no carry before every
+// CTA is counted.  Causal: a segment's first chunk has no local-sum item (its
 // local sum is zero and the walkers do not store it), a sequence's first
-// chunk no global product at all.
+// chunk no global product at all.  Bidirectional: every chunk's one global
+// item is its sequence's total.
 //
 // The chunk-local kernel streams V, the local sums and the carries once per
 // e tile; with one row tile per unit (tc_chunk_fused) both row tiles of a
@@ -20,14 +24,15 @@
 // each e tile's operands serve both row tiles, about 40% fewer bytes through
 // an SM, which is what bounds the kernel (its loads take microseconds to
 // land, so the bytes each SM can have in flight set the rate).
-//   S   = T0_r T1^T      once per unit in three stages of 128 keys (M = 128,
-//                        N = 128, K = s; an N = 64 product costs more than
-//                        half of an N = 128 one): row tile 1 with keys 0-127
-//                        and 128-255, then row tile 0 with keys 0-127, into
-//                        the drained accumulators' columns
-//   P   = relu(S a)^2    masked (key > query -> 0) by four relu^2 warps, 64
+//   S   = T0_r T1^T      once per unit in stages of 128 keys (M = 128, N =
+//                        128, K = s; an N = 64 product costs more than half
+//                        of an N = 128 one): row tile 1 with keys 0-127 and
+//                        128-255, then row tile 0 with keys 0-127 (and,
+//                        bidirectional, 128-255), into the drained
+//                        accumulators' columns
+//   P   = relu(S a)^2    (causal: key > query -> 0) by four relu^2 warps, 64
 //                        keys at a time, bf16 in TMEM, resident for the unit
-//                        (6 slots)
+//                        (causal 2 + 4 slots, bidirectional 4 + 4)
 //   per e tile, r = 1 then 0:
 //     O_r  = sum_k P_rk V_k + T2_r (local_g + carry)   (A of the first from
 //            TMEM; M = 128, N = 128); two merge warps add the carry tile into
@@ -37,15 +42,18 @@
 //                         relu^2 warps, idle once a unit's weights are formed,
 //                         columns 64-127); O_1 drains while O_0 forms and the
 //                         reverse, so each accumulator buffers the other
-// Row tile 1 goes first: it alone reads the keys 128-255, whose V item then
-// goes back early for the next e tile's copies.
+// Row tile 1 goes first.  Causal, it alone reads the keys 128-255, whose V
+// item then goes back early for the next e tile's copies; bidirectional,
+// both row tiles read the keys 128-255 first and row tile 0 frees them.
 // Shared memory: a ring of 5 items of 32 KB (3-D TMA boxes of 128 rows x two
 // 64-column blocks): T0 of each row tile, T1 of keys 0-127 and 128-255 (unit
 // start), then per e tile V of keys 128-255 and 0-127, the local sums and the
-// carry; and the T2 rows of both row tiles (64 KB) for the unit.
-// TMEM (512 columns): O_0 [0, 128), O_1 [128, 256), P [320, 512); the score
-// stages use [0, 128), [128, 256), then [0, 128) again once the first is read,
-// all before the unit's first products there.
+// carry (bidirectional: the total); and the T2 rows of both row tiles (64
+// KB) for the unit.
+// TMEM (512 columns): O_0 [0, 128), O_1 [128, 256), P [320, 512) (causal) or
+// [256, 512) (bidirectional); the score stages use [0, 128), [128, 256), then
+// the same columns again once the stage before is read, all before the
+// unit's first products there.
 #pragma once
 
 #include "tc_common.cuh"
@@ -58,21 +66,34 @@ constexpr int PA_RING = 5;
 constexpr uint32_t PA_ITEM = 32768;
 constexpr uint32_t PA_OFF_B = PA_RING * PA_ITEM;   // T2 rows of both row tiles
 constexpr uint32_t PAIR_SMEM = PA_OFF_B + 2 * PA_ITEM + 1024;
-constexpr int PA_PSLOTS = 6;                       // relu^2 weights: 2 + 4 stages
-constexpr uint32_t PA_COL_P = 320;
+// relu^2 weight slots (32 TMEM columns, 64 keys each) and their first
+// column: causal, row tile 0 reads keys 0-127 only (2 + 4 slots in [320,
+// 512)); bidirectional, both row tiles read all 256 keys (4 + 4 in [256, 512))
+template <bool kCausal>
+__host__ __device__ constexpr int pair_pslots() { return kCausal ? 6 : 8; }
+template <bool kCausal>
+__host__ __device__ constexpr uint32_t pair_col_p() { return kCausal ? 320u : 256u; }
 // warps: 0 producer, 1 MMA, 2-3 merge, 4-7 relu^2 then epilogue (columns
 // 64-127), 8-11 epilogue (columns 0-63)
 constexpr int PAIR_THREADS = 384;
 static_assert(PAIR_SMEM <= 232448, "tc_chunk_pair exceeds 227 KB of shared memory");
 
-// stages of row tile r and its first P slot
-__device__ __forceinline__ int pair_stages(int r) { return r == 0 ? 2 : 4; }
-__device__ __forceinline__ int pair_pslot(int r, int k) { return r == 0 ? k : 2 + k; }
-// Score stages: 0 row tile 1 keys 0-127, 1 row tile 1 keys 128-255, 2 row
-// tile 0 keys 0-127; their TMEM columns
-constexpr int PA_SSTAGES = 3;
+// 64-key stages of row tile r, and the P slot of its stage k
+template <bool kCausal>
+__device__ __forceinline__ int pair_stages(int r) {
+  return kCausal && r == 0 ? 2 : 4;
+}
+template <bool kCausal>
+__device__ __forceinline__ int pair_pslot(int r, int k) {
+  return kCausal ? (r == 0 ? k : 2 + k) : (r == 1 ? k : 4 + k);
+}
+// Score stages (128 keys each): 0 row tile 1 keys 0-127, 1 row tile 1 keys
+// 128-255, 2 row tile 0 keys 0-127, and bidirectional 3 row tile 0 keys
+// 128-255; stage st is in TMEM columns [128 (st & 1), + 128)
+template <bool kCausal>
+__host__ __device__ constexpr int pair_sstages() { return kCausal ? 3 : 4; }
 __device__ __forceinline__ int pair_srow(int st) { return st < 2 ? 1 : 0; }
-__device__ __forceinline__ uint32_t pair_scol(int st) { return st == 1 ? 128u : 0u; }
+__device__ __forceinline__ uint32_t pair_scol(int st) { return (uint32_t)(st & 1) * 128u; }
 
 // Tiles t = bg * n_et + et; CTA c takes [c T / grid, (c + 1) T / grid) (equal
 // cost per tile); a unit is the run of one chunk's e tiles in that range.
@@ -94,16 +115,23 @@ struct PairUnit {
   int et0, net;
 };
 
-template <bool kState>
+template <bool kState, bool kCausal>
 __device__ __forceinline__ PairUnit decode_pair(int t, int net, const PairGrid &g) {
   const int bg = t / g.n_et;
   const int b = bg / g.G, c = bg % g.G;
   PairUnit f;
   f.crow = b * g.n + c * 256;
   f.lrow = bg * S_DIM;
-  f.crow2 = (b * g.S + c / g.L) * S_DIM;
-  f.local = c % g.L != 0;
-  f.carry = (kState && g.carry_all) || c / g.L > 0;
+  if (kCausal) {
+    f.crow2 = (b * g.S + c / g.L) * S_DIM;
+    f.local = c % g.L != 0;
+    f.carry = (kState && g.carry_all) || c / g.L > 0;
+  } else {
+    // every chunk: the sequence's total, in its first segment's slot
+    f.crow2 = b * g.S * S_DIM;
+    f.local = false;
+    f.carry = true;
+  }
   f.et0 = t % g.n_et;
   f.net = net;
   return f;
@@ -139,8 +167,10 @@ __device__ __forceinline__ void pair_gate64(const u32x8 (&uv)[4], __nv_bfloat16 
 }
 
 // kState: a carried-in state or a state out (flash_mca_forward_seq); the
-// plain forward pass compiles without that code.
-template <bool kState>
+// plain forward pass compiles without that code.  kCausal: causal chunks
+// (masked scores, prefix sums); otherwise bidirectional (every key, the
+// sequence's total).
+template <bool kState, bool kCausal>
 __global__ void __launch_bounds__(PAIR_THREADS, 1)
     tc_chunk_pair(const __grid_constant__ CUtensorMap mapT0,  // T0 rows, 3-D box {64, 128, 2}
                   const __grid_constant__ CUtensorMap mapT1,  // T1 rows, 3-D box {64, 128, 2}
@@ -162,8 +192,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   __shared__ __align__(8) uint64_t uq_full[FU_QUEUE], uq_empty[FU_QUEUE];
   __shared__ __align__(8) uint64_t b_full, b_empty;
   __shared__ __align__(8) uint64_t full[PA_RING], empty[PA_RING];
-  __shared__ __align__(8) uint64_t s_full[PA_SSTAGES];  // stage st's scores are in TMEM
-  __shared__ __align__(8) uint64_t p_full[PA_PSLOTS], p_empty[PA_PSLOTS];
+  constexpr int kSS = pair_sstages<kCausal>(), kPS = pair_pslots<kCausal>();
+  constexpr uint32_t kColP = pair_col_p<kCausal>();
+  __shared__ __align__(8) uint64_t s_full[kSS];  // stage st's scores are in TMEM
+  __shared__ __align__(8) uint64_t p_full[kPS], p_empty[kPS];
   __shared__ __align__(8) uint64_t o_full[2], o_empty[2], mma_done;
   // the MMA thread, the ring's only in-order consumer, hands an e tile's
   // local-sum and carry items to the merge warps (mg_go) once they have
@@ -185,8 +217,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    for (int i = 0; i < PA_SSTAGES; ++i) mbar_init(&s_full[i], 1);
-    for (int i = 0; i < PA_PSLOTS; ++i) {
+    for (int i = 0; i < kSS; ++i) mbar_init(&s_full[i], 1);
+    for (int i = 0; i < kPS; ++i) {
       mbar_init(&p_full[i], 1);
       mbar_init(&p_empty[i], 1);
     }
@@ -220,7 +252,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const int64_t se = (int64_t)S_DIM * e;
     const int64_t groups = (int64_t)grid.B * (se / 8);
     for (int64_t t = (int64_t)blockIdx.x * 192 + ct; t < groups; t += (int64_t)gridDim.x * 192)
-      seg_carry_group(seg, grid.S, se, 1, t, kState ? state_in : nullptr,
+      seg_carry_group(seg, grid.S, se, kCausal ? 1 : 0, t, kState ? state_in : nullptr,
                       kState ? state_out : nullptr);
     named_bar_sync(5, 192);
     // every thread's carries are stored (the barrier orders them before the
@@ -271,7 +303,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         uq_net[qs] = net;
         mbar_arrive(&uq_full[qs]);
         if (uu < 0) break;
-        const PairUnit f = decode_pair<kState>(uu, net, grid);
+        const PairUnit f = decode_pair<kState, kCausal>(uu, net, grid);
         // the T rows: with the carry kernel between their writer and this
         // grid, the writer had completed before this grid launched; otherwise
         // wait for the kernel before
@@ -354,7 +386,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         const int u = uq_unit[qs], unet = uq_net[qs];
         mbar_arrive(&uq_empty[qs]);
         if (u < 0) break;
-        const PairUnit f = decode_pair<kState>(u, unet, grid);
+        const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
         // ---- scores, once per unit, into the accumulators' columns: the
         // previous unit's last tile has been drained from both
         const int i_a1 = it, i_k0 = it + 1, i_k1 = it + 2, i_a0 = it + 3;
@@ -367,15 +399,17 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             }
           if (!ok) break;
         }
-        for (int st = 0; st < PA_SSTAGES && ok; ++st) {
-          const int i_a = st < 2 ? i_a1 : i_a0, i_k = st == 1 ? i_k1 : i_k0;
+        for (int st = 0; st < kSS && ok; ++st) {
+          const int i_a = st < 2 ? i_a1 : i_a0, i_k = (st & 1) ? i_k1 : i_k0;
           if (!wait_item(i_a) || !wait_item(i_k)) {
             ok = false;
             break;
           }
-          // stage 2 reuses stage 0's columns: the relu^2 warps have read them
-          if (st == 2 && (!mbar_wait(&p_full[2], j & 1, kWaitLimitNs) ||
-                          !mbar_wait(&p_full[3], j & 1, kWaitLimitNs))) {
+          // stages 2 and 3 reuse the columns of stages 0 and 1 (row tile 1's):
+          // the relu^2 warps have read them
+          if (st >= 2 &&
+              (!mbar_wait(&p_full[pair_pslot<kCausal>(1, (st & 1) * 2)], j & 1, kWaitLimitNs) ||
+               !mbar_wait(&p_full[pair_pslot<kCausal>(1, (st & 1) * 2 + 1)], j & 1, kWaitLimitNs))) {
             record_timeout(826);
             ok = false;
             break;
@@ -390,14 +424,19 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                         smem_desc_sw128(kaddr + off, 16, 1024), idesc_s, kk != 0);
           }
           mma_commit(&s_full[st]);
-          // the items go back after their last score product
+          // the items go back after their last score product (bidirectional:
+          // row tile 0 reads the keys 128-255 too)
           if (st == 1) {
-            mma_commit(&empty[i_k1 % PA_RING]);
+            if (kCausal) mma_commit(&empty[i_k1 % PA_RING]);
             mma_commit(&empty[i_a1 % PA_RING]);
           }
           if (st == 2) {
-            mma_commit(&empty[i_a0 % PA_RING]);
+            if (kCausal) mma_commit(&empty[i_a0 % PA_RING]);
             mma_commit(&empty[i_k0 % PA_RING]);
+          }
+          if (st == 3) {
+            mma_commit(&empty[i_a0 % PA_RING]);
+            mma_commit(&empty[i_k1 % PA_RING]);
           }
         }
         if (!ok) break;
@@ -418,34 +457,39 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
               break;
             }
             const uint32_t ocol = tbase + (uint32_t)(r * FU_ET);
-            const int ns = pair_stages(r);
-            // the unit's first tile: every relu^2 weight of the row tile is
-            // formed, so its score stage, whose columns O_r reuses, has been
-            // read in full before the first product overwrites them
-            for (int k = 0; x == 0 && k < ns && ok; ++k)
-              if (!mbar_wait(&p_full[pair_pslot(r, k)], j & 1, kWaitLimitNs)) {
+            const int ns = pair_stages<kCausal>(r);
+            // the unit's first tile: every score stage in the columns O_r
+            // reuses has been read in full before the first product
+            // overwrites them (causal: the row tile's own weights are formed;
+            // bidirectional, where both row tiles' stages share the columns:
+            // all weights, before the first product)
+            for (int k = 0; x == 0 && (kCausal || r == 1) && k < (kCausal ? ns : kPS) && ok; ++k)
+              if (!mbar_wait(&p_full[kCausal ? pair_pslot<kCausal>(r, k) : k], j & 1,
+                             kWaitLimitNs)) {
                 record_timeout(822);
                 ok = false;
               }
             if (!ok) break;
             tc_fence_after();
             for (int q = 0; q < ns && ok; ++q) {
-              const int k = r == 1 ? (q + 2) % 4 : q;  // row tile 1: keys 128-255 first
-              const int iv = k < 2 ? iv0 : iv1, ps = pair_pslot(r, k);
+              // keys 128-255 first (causal row tile 0 reads keys 0-127 only)
+              const int k = (r == 1 || !kCausal) ? (q + 2) % 4 : q;
+              const int iv = k < 2 ? iv0 : iv1, ps = pair_pslot<kCausal>(r, k);
               if (!wait_item(iv)) {
                 ok = false;
                 break;
               }
               tc_fence_after();
               const uint32_t vb = slot_addr(iv) + (k & 1) * 8192;
-              const uint32_t pa = tbase + PA_COL_P + (uint32_t)(32 * ps);
+              const uint32_t pa = tbase + kColP + (uint32_t)(32 * ps);
 #pragma unroll
               for (int kk = 0; kk < KEY_STAGE / 16; ++kk)
                 mma_bf16_ts(ocol, pa + 8 * kk, smem_desc_sw128(vb + kk * 2048, 16384, 1024),
                             idesc_o, (q == 0 && kk == 0) ? 0u : 1u);
-              // keys 128-255 are row tile 1's alone
+              // keys 128-255 are read last by row tile 1 (causal) or row tile
+              // 0 (bidirectional)
+              if (k == 3 && r == (kCausal ? 1 : 0)) mma_commit(&empty[iv1 % PA_RING]);
               if (r == 1 && k == 3) {
-                mma_commit(&empty[iv1 % PA_RING]);
                 // the local sums and the carry have landed: merge them while
                 // the keys 0-127 products run
                 if (merge) {
@@ -491,7 +535,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         }
         if (!ok) break;
         // the unit's relu^2 weights and T2 rows are done with
-        for (int ps = 0; ps < PA_PSLOTS; ++ps) mma_commit(&p_empty[ps]);
+        for (int ps = 0; ps < kPS; ++ps) mma_commit(&p_empty[ps]);
         mma_commit(&b_empty);
       }
       // every MMA has finished before TMEM is released
@@ -515,7 +559,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!got && mt == 0) record_timeout(860);
         break;
       }
-      const PairUnit f = decode_pair<kState>(u, unet, grid);
+      const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
       it += 4;  // the unit's T0 and T1 items
       for (int x = 0; x < f.net && ok; ++x) {
         const int il = it + 2, icy = it + 3;
@@ -568,13 +612,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         break;
       }
       // the score stages in order, 64 keys at a time (one P slot each)
-      for (int st = 0; st < PA_SSTAGES && ok; ++st) {
+      for (int st = 0; st < kSS && ok; ++st) {
         const int r = pair_srow(st);
         const int qpos = r * ROW_TILE + row;  // query position within the chunk
         const bool got_s = mbar_wait(&s_full[st], j & 1, kWaitLimitNs);
         for (int h = 0; h < 2; ++h) {
-          const int k = (st == 1 ? 2 : 0) + h;  // 64-key stage within the row tile
-          const int ps = pair_pslot(r, k);
+          const int k = (st & 1) * 2 + h;  // 64-key stage within the row tile
+          const int ps = pair_pslot<kCausal>(r, k);
           bool w = got_s;
           // the previous unit's last product that read this P slot has completed
           if (w && j >= 1) w = mbar_wait(&p_empty[ps], (j - 1) & 1, kWaitLimitNs);
@@ -585,8 +629,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
             tmem_ld32(sa, sv[0]);
             tmem_ld32(sa + 32, sv[1]);
             tmem_ld_wait();
-            // relu(S a)^2 (a = 1/C by default); key position > query position
-            // -> 0; two keys a column, the lower key in the low half
+            // relu(S a)^2 (a = 1/C by default); causal, key position > query
+            // position -> 0; two keys a column, the lower key in the low half
             const int kbase = k * KEY_STAGE;
             uint32_t pk[32];
 #pragma unroll
@@ -598,11 +642,11 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 float x1 = fmaxf(__uint_as_float(sv[c2][2 * i + 1]) * quad_a, 0.f);
                 x0 *= x0;
                 x1 *= x1;
-                if (key > qpos) x0 = 0.f;
-                if (key + 1 > qpos) x1 = 0.f;
+                if (kCausal && key > qpos) x0 = 0.f;
+                if (kCausal && key + 1 > qpos) x1 = 0.f;
                 pk[c2 * 16 + i] = pack_bf16x2(x0, x1);
               }
-            tmem_st32(tbase + lane_off + PA_COL_P + (uint32_t)(32 * ps), pk);
+            tmem_st32(tbase + lane_off + kColP + (uint32_t)(32 * ps), pk);
             tmem_st_wait();
             tc_fence_before();
           }
@@ -616,7 +660,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       }
       // then columns 64-127 of the unit's output tiles (the epilogue warps
       // take 0-63)
-      const PairUnit f = decode_pair<kState>(u, unet, grid);
+      const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
       for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
         for (int rr = 0; rr < 2 && ok; ++rr) {
           const int r = 1 - rr;
@@ -658,7 +702,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!got && mt == 0) record_timeout(850);
         break;
       }
-      const PairUnit f = decode_pair<kState>(u, unet, grid);
+      const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
       for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
         for (int rr = 0; rr < 2 && ok; ++rr) {
           const int r = 1 - rr;  // the order the accumulators are formed in

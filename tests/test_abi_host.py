@@ -103,11 +103,13 @@ def test_auto_path_choice():
 
 def test_launch_counts():
     bf = fm.FMCA_BF16
-    # causal chunks of 256: the segment walkers (local sums, totals, T rows),
-    # then the row-pair kernel, which forms the segment carries itself
+    # chunks of 256: the segment walkers (local sums, totals, T rows), then
+    # the row-pair kernel, which forms the segment carries (or, bidirectional,
+    # the total) itself
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf) == 2
-    # bidirectional: walkers, the segment carries, the fused chunk kernel
-    assert fm.flash_mca_launch_count(4, 4096, 128, 1536, 256, 0, bf) == 3
+    assert fm.flash_mca_launch_count(4, 4096, 128, 1536, 256, 0, bf) == 2
+    # chunks of 128, bidirectional: walkers, the total, the fused chunk kernel
+    assert fm.flash_mca_launch_count(4, 4096, 128, 1536, 128, 0, bf) == 3
     # one segment per sequence (B * e / 256 >= 144 units): no carries
     assert fm.flash_mca_launch_count(16, 1024, 128, 2560, 256, 1, bf) == 2
     # without a global term: the T0 / T1 rows and the fused chunk kernel

@@ -207,6 +207,7 @@ def test_full_size_workload_whole_output(name):
     # 160 walker units (one segment per sequence and e slice): more than the
     # SMs, so walkers take a second unit; 1280 row-pair tiles
     (16, 1024, 256, 2560, True),
+    (16, 1024, 256, 2560, False),
 ])
 def test_more_units_than_sms_whole_output(B, n, C, e, causal):
     """Shapes that are not benchmark workloads, with more work units than SMs."""
