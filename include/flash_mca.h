@@ -232,11 +232,11 @@ fmca_status flash_mca_forward_seq(const void *Z, const void *V, const void *U,
  * flash_mca_launch_count(...) + 1.  Lets a caller time each kernel on the
  * stream it runs on.  `opts` as for flash_mca_forward_ex (NULL: defaults).
  * Kernel order: tensor-core path -- the segment walkers (local state sums,
- * segment totals and the rows T0, T1, T2); then, for causal chunks of 256,
- * the row-pair output kernel, which forms the segment carries itself; for
- * other chunk sizes or bidirectional attention the segment-carry kernel
- * (only with more than one segment, or bidirectional) and the fused chunk
- * kernel (scores, relu^2 weights, both products and the gate); without a
+ * segment totals and the rows T0, T1, T2); then, for chunks of 256, the
+ * row-pair output kernel, which forms the segment carries (bidirectional: the
+ * total) itself; for other chunk sizes the segment-carry kernel (only with
+ * more than one segment, or bidirectional) and the fused chunk kernel
+ * (scores, relu^2 weights, both products and the gate); without a
  * global term (FMCA_LIN_NORM_NONE) the rows T0, T1, then the fused kernel;
  * SIMT path -- chunk states, state scan, chunk output. */
 fmca_status flash_mca_forward_timed(const void *Z, const void *V, const void *U,
