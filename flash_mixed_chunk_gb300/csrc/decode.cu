@@ -170,6 +170,168 @@ __global__ void __launch_bounds__(kDecThreads)
     for (int a = tid; a < s; a += kDecThreads) Zc[((int64_t)b * C + i) * s + a] = zt[a];
 }
 
+// Eight consecutive elements, loaded raw (one 16-byte load for bf16, two for
+// fp32) so that a batch of rows is in flight before any is used, then
+// widened to floats.
+template <typename T>
+struct Raw8;
+template <>
+struct Raw8<__nv_bfloat16> {
+  uint4 r;
+  __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+    r = __ldg(reinterpret_cast<const uint4 *>(p));
+  }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      f[2 * k] = __uint_as_float(w[k] << 16);
+      f[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+    }
+  }
+};
+template <>
+struct Raw8<float> {
+  float4 a, b;
+  __device__ __forceinline__ void load(const float *p) {
+    a = __ldg(reinterpret_cast<const float4 *>(p));
+    b = __ldg(reinterpret_cast<const float4 *>(p + 4));
+  }
+  __device__ __forceinline__ void get(float (&f)[8]) const {
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
+  }
+};
+
+// The same step with 16-byte loads, for s and e multiples of 8: grid (B,
+// ceil(e / W)); a block is one sequence and W columns (W = 256, 128 or 64).
+// W / 8 lanes cover a row, eight columns each, so a warp takes 256 / W rows
+// at a time and the block's 8 * 256 / W row slots split the rows (cached
+// keys, then state rows); each thread forms the relu^2 weight of its own
+// keys (one key a thread for chunks of up to 256).  dynamic smem: q0[s]
+// q2[s] g1[s] b1[s] w[C] part[2048] floats.
+template <typename T, int W>
+__global__ void __launch_bounds__(kDecThreads)
+    decode_token_v8(const T *__restrict__ z, const T *__restrict__ v, const T *__restrict__ u,
+                    const float *__restrict__ gamma, const float *__restrict__ beta,
+                    T *__restrict__ o, const T *__restrict__ P, T *__restrict__ Zc,
+                    T *__restrict__ Vc, int s, int e, int C, int i, float quad_a, float lin_f,
+                    float t2_w) {
+  extern __shared__ float dsm[];
+  float *q0 = dsm;
+  float *q2 = q0 + s;
+  float *g1 = q2 + s;
+  float *b1 = g1 + s;
+  float *w = b1 + s;
+  constexpr int kL = W / 8;                // lanes a row
+  constexpr int kSlots = kDecWarps * (32 / kL);  // rows in flight a block
+  float *part = w + C;  // [kSlots][W]
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int slot = warp * (32 / kL) + lane / kL;
+  const int c = blockIdx.y * W + 8 * (lane % kL);  // this lane's first column
+  const T *zt = z + (int64_t)b * s;
+  const T *vt = v + (int64_t)b * e;
+  for (int a = tid; a < s; a += kDecThreads) {
+    const float zz = dec_f(zt[a]);
+    q0[a] = zz * gamma[a] + beta[a];
+    q2[a] = (zz * gamma[2 * s + a] + beta[2 * s + a]) * t2_w * lin_f;
+    g1[a] = gamma[s + a];
+    b1[a] = beta[s + a];
+  }
+  __syncthreads();
+  // relu^2 weights of the chunk's keys j <= i, a key a thread (its row's
+  // 16-byte pieces eight at a time in flight)
+  constexpr int kR = 8;
+  for (int j = tid; j <= i; j += kDecThreads) {
+    const T *zj = j < i ? Zc + ((int64_t)b * C + j) * s : zt;
+    float dot = 0.f;
+    for (int a0 = 0; a0 < s; a0 += 8 * kR) {
+      Raw8<T> raw[kR];
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        if (a0 + 8 * q < s) raw[q].load(zj + a0 + 8 * q);
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        if (a0 + 8 * q < s) {
+          float f[8];
+          raw[q].get(f);
+          const int a = a0 + 8 * q;
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dot = fmaf(q0[a + k], fmaf(f[k], g1[a + k], b1[a + k]), dot);
+        }
+    }
+    const float r = fmaxf(dot * quad_a, 0.f);
+    w[j] = r * r;
+  }
+  __syncthreads();
+  float acc[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) acc[k] = 0.f;
+  if (c < e) {
+    const T *vcb = Vc + (int64_t)b * C * e + c;
+    const T *pb = P + (int64_t)b * s * e + c;
+    // intra-chunk keys: cached rows j < i (eight of this warp's rows in
+    // flight), this token's row j = i
+    for (int j0 = slot; j0 < i; j0 += kR * kSlots) {
+      Raw8<T> raw[kR];
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        if (j0 + q * kSlots < i) raw[q].load(vcb + (int64_t)(j0 + q * kSlots) * e);
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        if (j0 + q * kSlots < i) {
+          float f[8];
+          raw[q].get(f);
+          const float wj = w[j0 + q * kSlots];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[k] = fmaf(wj, f[k], acc[k]);
+        }
+    }
+    if (slot == i % kSlots) {
+      Raw8<T> raw;
+      raw.load(vt + c);
+      float f[8];
+      raw.get(f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] = fmaf(w[i], f[k], acc[k]);
+    }
+    // global term: rows of the carried state
+    for (int a0 = slot; a0 < s; a0 += kR * kSlots) {
+      Raw8<T> raw[kR];
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        if (a0 + q * kSlots < s) raw[q].load(pb + (int64_t)(a0 + q * kSlots) * e);
+#pragma unroll
+      for (int q = 0; q < kR; ++q)
+        if (a0 + q * kSlots < s) {
+          float f[8];
+          raw[q].get(f);
+          const float qa = q2[a0 + q * kSlots];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) acc[k] = fmaf(qa, f[k], acc[k]);
+        }
+    }
+  }
+  float4 *pp = reinterpret_cast<float4 *>(part + slot * W + 8 * (lane % kL));
+  pp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+  pp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+  __syncthreads();
+  // thread tid < W: column blockIdx.y * W + tid, summed over the row slots
+  const int cc = blockIdx.y * W + tid;
+  if (tid < W && cc < e) {
+    float out = 0.f;
+#pragma unroll
+    for (int r = 0; r < kSlots; ++r) out += part[r * W + tid];
+    o[(int64_t)b * e + cc] = dec_t<T>(dec_f(u[(int64_t)b * e + cc]) * out);
+    // append this token to the chunk cache (slot i; this launch reads only
+    // slots j < i)
+    Vc[((int64_t)b * C + i) * e + cc] = vt[cc];
+  }
+  if (blockIdx.y == 0)
+    for (int a = tid; a < s; a += kDecThreads) Zc[((int64_t)b * C + i) * s + a] = zt[a];
+}
+
 // P[b] += sum_{j < C} T3(Zc[b][j])^T Vc[b][j] : the finished chunk joins the
 // carried state (and, for bf16 I/O, its bf16 copy Pb the token kernel reads).
 // grid (B, ceil(s / 32), ceil(e / 128)); smem T3 tile [C][32].
@@ -235,16 +397,31 @@ int launch_decode_impl(const void *z, const void *v, const void *u, const float 
     t2_w = 1.0f / (float)(t + 1);
   }
   if (var.lin_norm == kLinNormNone) lin_f = 0.0f;
-  // block width: 32 columns while that leaves fewer than about three blocks
-  // per SM, wider (fewer repeats of the key weights) beyond
-  const int64_t blocks32 = (int64_t)B * ((e + 31) / 32);
-  const int K = blocks32 >= 12 * 152 ? 4 : (blocks32 >= 6 * 152 ? 2 : 1);
-  dim3 g1(B, (e + 32 * K - 1) / (32 * K));
-  const size_t smem1 = sizeof(float) * (2 * (size_t)s + (size_t)C + kDecWarps * 32 * K);
-  auto *kern = K == 4 ? decode_token<T, 4> : (K == 2 ? decode_token<T, 2> : decode_token<T, 1>);
-  kern<<<g1, kDecThreads, smem1, stream>>>(
-      static_cast<const T *>(z), static_cast<const T *>(v), static_cast<const T *>(u), gamma,
-      beta, static_cast<T *>(o), Pr, Zc, Vc, s, e, C, i, var.quad_a, lin_f, t2_w);
+  // 16-byte rows for s and e multiples of 8: the widest block (256, 128 or
+  // 64 columns) that still gives at least one block per SM, else 64 columns
+  auto blocks = [&](int w) { return (int64_t)B * ((e + w - 1) / w); };
+  const int W = blocks(256) >= 152 ? 256 : (blocks(128) >= 152 ? 128 : 64);
+  if (s % 8 == 0 && e % 8 == 0) {
+    dim3 g1(B, (e + W - 1) / W);
+    const size_t smem1 = sizeof(float) * (4 * (size_t)s + (size_t)C + 2048);
+    auto *kern = W == 256 ? decode_token_v8<T, 256>
+                          : (W == 128 ? decode_token_v8<T, 128> : decode_token_v8<T, 64>);
+    kern<<<g1, kDecThreads, smem1, stream>>>(
+        static_cast<const T *>(z), static_cast<const T *>(v), static_cast<const T *>(u), gamma,
+        beta, static_cast<T *>(o), Pr, Zc, Vc, s, e, C, i, var.quad_a, lin_f, t2_w);
+  } else {
+    // other widths, a column a lane: 32 columns while that leaves fewer than
+    // about three blocks per SM, wider (fewer repeats of the key weights)
+    // beyond
+    const int64_t blocks32 = (int64_t)B * ((e + 31) / 32);
+    const int K = blocks32 >= 12 * 152 ? 4 : (blocks32 >= 6 * 152 ? 2 : 1);
+    dim3 g1(B, (e + 32 * K - 1) / (32 * K));
+    const size_t smem1 = sizeof(float) * (2 * (size_t)s + (size_t)C + kDecWarps * 32 * K);
+    auto *kern = K == 4 ? decode_token<T, 4> : (K == 2 ? decode_token<T, 2> : decode_token<T, 1>);
+    kern<<<g1, kDecThreads, smem1, stream>>>(
+        static_cast<const T *>(z), static_cast<const T *>(v), static_cast<const T *>(u), gamma,
+        beta, static_cast<T *>(o), Pr, Zc, Vc, s, e, C, i, var.quad_a, lin_f, t2_w);
+  }
   if (cudaGetLastError() != cudaSuccess) return 1;
   if (i == C - 1) {
     const size_t smem2 = sizeof(float) * (size_t)C * 32;

@@ -51,11 +51,18 @@ VARIANTS = [(None, 0), (None, 1), (None, 2), ("cs", 0), ("cs", 1)]
 
 @pytest.mark.parametrize("variant", VARIANTS, ids=[f"{q}-{l}" for q, l in VARIANTS])
 @pytest.mark.parametrize("B,n,C,s,e,dtype", [
-    (2, 192, 64, 32, 80, torch.float32),      # e not a multiple of the 128-column block
+    # s or e not a multiple of 8: a column a lane
     (1, 100, 25, 20, 130, torch.float32),     # ragged everything
-    (2, 512, 128, 128, 256, torch.bfloat16),
-    (140, 64, 32, 16, 200, torch.float32),    # wide blocks (two 32-column groups per lane)
-    (280, 64, 32, 16, 200, torch.float32),    # wider blocks (four groups), ragged e
+    (140, 64, 32, 16, 204, torch.float32),    # wide blocks (two 32-column groups per lane)
+    (280, 64, 32, 16, 204, torch.float32),    # wider blocks (four groups), ragged e
+    # s and e multiples of 8: 16-byte rows, a key weight a thread, blocks of
+    # 256, 128 or 64 columns
+    (2, 192, 64, 32, 80, torch.float32),      # 64 columns, few blocks; ragged e
+    (2, 512, 128, 128, 256, torch.bfloat16),  # 64 columns, few blocks
+    (280, 64, 32, 16, 200, torch.float32),    # 256 columns; ragged e: 25 of 32 lanes
+    (160, 128, 64, 32, 512, torch.bfloat16),  # 256 columns, two blocks, two chunks
+    (40, 64, 32, 16, 512, torch.bfloat16),    # 128 columns, two rows a warp
+    (20, 96, 32, 16, 456, torch.float32),     # 64 columns, four rows a warp; ragged e
 ])
 def test_decode_equals_the_causal_forward(B, n, C, s, e, dtype, variant):
     qs, ln = variant
