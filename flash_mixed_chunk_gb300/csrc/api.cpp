@@ -31,8 +31,11 @@ fmca_status check_sizes(int B, int n, int s, int e, int C, int causal, fmca_dtyp
   return FMCA_OK;
 }
 
-bool want_tc(int B, int n, int s, int e, int C, fmca_dtype dtype) {
-  return dtype == FMCA_BF16 && tc_supported(B, n, s, e, C);
+// the forward pass on the tensor cores (lin_norm: the call's global-term
+// divisor, which selects the stored-weights form for chunks over 256 tokens
+// without a global term)
+bool want_tc(int B, int n, int s, int e, int C, fmca_dtype dtype, int lin_norm = kLinNormN) {
+  return dtype == FMCA_BF16 && tc_forward_supported(B, n, s, e, C, lin_norm);
 }
 
 size_t elem_size(fmca_dtype dtype) { return dtype == FMCA_BF16 ? 2 : 4; }
@@ -87,9 +90,10 @@ int flash_mca_launch_count_ex(int B, int n, int s, int e, int C, int causal, fmc
   Variant var;
   if (to_variant(opts, C, &var) != FMCA_OK) return 0;
   if (path == FMCA_PATH_AUTO)
-    path = want_tc(B, n, s, e, C, dtype) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
+    path = want_tc(B, n, s, e, C, dtype, var.lin_norm) ? FMCA_PATH_TCGEN05 : FMCA_PATH_SIMT;
   if (path == FMCA_PATH_TCGEN05)
-    return want_tc(B, n, s, e, C, dtype) ? tc_launch_count(B, n, e, C, causal, var) : 0;
+    return want_tc(B, n, s, e, C, dtype, var.lin_norm) ? tc_launch_count(B, n, e, C, causal, var)
+                                                       : 0;
   if (path == FMCA_PATH_SIMT) return kSimtLaunches;
   return 0;
 }
@@ -380,7 +384,7 @@ fmca_status forward_impl(const void *Z, const void *V, const void *U, const floa
         overlaps(U, (size_t)B * n * e * es) || overlaps(workspace, workspace_bytes_))
       return FMCA_ERR_INVALID_ARG;
   }
-  const bool tc_ok = want_tc(B, n, s, e, C, dtype);
+  const bool tc_ok = want_tc(B, n, s, e, C, dtype, var.lin_norm);
   if (path == FMCA_PATH_TCGEN05 && !tc_ok) return FMCA_ERR_UNSUPPORTED;
   // a piece of longer sequences: causal, the tensor-core path, a global term
   SeqCarry carry;

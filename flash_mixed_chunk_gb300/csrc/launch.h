@@ -38,7 +38,7 @@ struct WalkSplit {
 };
 inline WalkSplit walk_split(int B, int n, int e, int C) {
   const int G = n / C;
-  const int slices = B * (e / 256);
+  const int slices = B * ((e + 255) / 256);
   int S = slices > 0 ? kWalkUnits / slices : 1;
   S = S < 1 ? 1 : (S > G ? G : S);
   const int L = (G + S - 1) / S;
@@ -270,7 +270,8 @@ int launch_tc_backward(const void *Z, const void *V, const void *U, const float 
                        bool saved = false);
 
 // Shapes the tensor-core path covers.
-bool tc_supported(int B, int n, int s, int e, int C);
+bool tc_supported(int B, int n, int s, int e, int C);  // every tensor-core kernel (e % 256)
+bool tc_forward_supported(int B, int n, int s, int e, int C, int lin_norm);  // the forward pass
 constexpr int kSimtLaunches = 3;
 
 // Device-side status word (tensor-core kernels' bounded waits).

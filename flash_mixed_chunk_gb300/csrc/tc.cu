@@ -1,6 +1,7 @@
 // tc.cu -- tensor-core path of the mixed-chunk attention forward core
 // (sm_103a: tcgen05 MMA into TMEM, TMA-staged 128-byte-swizzled bf16 tiles,
-// mbarrier pipelines) for bf16 I/O, s = 128, C % 128 == 0, e % 256 == 0.
+// mbarrier pipelines) for bf16 I/O, s = 128, C % 128 == 0, e % 128 == 0 (the
+// stored-weights form and the backward pass: e % 256 == 0).
 //
 // Per call ("FLASH: Possibly the Most Interesting Efficient Transformer
 // Design Recently", sections "Weak Attention" and "Mixed Chunk"):
@@ -127,6 +128,17 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   if (C % ROW_TILE) return false;  // whole 128-row tiles (C = n: FLASH-Quad)
   if (e % E_TILE) return false;
   if (n % C) return false;
+  (void)B;
+  return true;
+}
+
+// The forward pass's own forms take e in 128-column tiles (the output
+// kernels' e tiles; the walkers' last slice is half wide), except the
+// stored-weights form (no global term, chunks over 256 tokens), whose output
+// kernel takes 256-column tiles.
+bool tc_forward_supported(int B, int n, int s, int e, int C, int lin_norm) {
+  if (s != S_DIM || C % ROW_TILE || n % C || e % FU_ET) return false;
+  if (lin_norm == kLinNormNone && C > 2 * ROW_TILE && e % E_TILE) return false;
   (void)B;
   return true;
 }
@@ -268,7 +280,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
   int ev = 1;
   if (!no_global) {
     // the segment walkers: local sums, segment totals and the T rows
-    const int units = B * (e / WK_ET) * sp.S;
+    const int units = B * ((e + WK_ET - 1) / WK_ET) * sp.S;
     tc_chunk_walk<<<units < sms ? units : sms, WK_THREADS, WALK_SMEM, stream>>>(
         mZw, mVw, mL, mT, gamma, beta, trows, plane, B, n, e, C, causal, var.lin_norm, sp.S, sp.L,
         carried, pair ? 0 : 1, sq.tok0, n_norm);
@@ -402,7 +414,7 @@ int launch_tc_forward_materialised(const void *Z, const void *V, const void *U,
     if (with_states) {
       // the local sums and carries exactly as the forward pass forms them
       // (the walkers end only after the weight kernel has)
-      const int units = B * (e / WK_ET) * sp.S;
+      const int units = B * ((e + WK_ET - 1) / WK_ET) * sp.S;
       PdlConfig wc(stream, true);
       wc.cfg.gridDim = dim3(units < sms ? units : sms);
       wc.cfg.blockDim = dim3(WK_THREADS);

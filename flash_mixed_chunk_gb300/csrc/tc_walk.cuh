@@ -25,7 +25,7 @@
 // which the output kernel forms as two products of the same T2 rows.  The
 // global term's divisor is carried by the T2 rows (1/n; 1/(t+1) per
 // position; 1/(g C) for causal chunk g with the tokens-summed divisor), which
-// the walker of e slice g % (e / 256) writes with T0 and T1.
+// the walker of e slice g % ceil(e / 256) writes with T0 and T1.
 //
 // The kernel is bound by the bytes each SM can have in flight (its loads take
 // microseconds to land), so a unit takes 256 e columns: each Z chunk it loads
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = n / C;
-  const int n_es = e / WK_ET;
+  const int n_es = (e + WK_ET - 1) / WK_ET;  // the last slice may be 128 columns
   const int n_slices = B * n_es;
   const int n_units = n_slices * S;
   const int W = (int)gridDim.x;
@@ -319,8 +319,11 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
           if (mt == 0) {
-            tma_store_2d(map, stage, col0 + 128 * h, prow);
-            tma_store_2d(map, stage + WK_STAGE_TILE, col0 + 128 * h + 64, prow);
+            // a 128-column last slice: its upper half is past e (zeros)
+            if (col0 + 128 * h < e) {
+              tma_store_2d(map, stage, col0 + 128 * h, prow);
+              tma_store_2d(map, stage + WK_STAGE_TILE, col0 + 128 * h + 64, prow);
+            }
             bulk_commit_group();
           }
         }

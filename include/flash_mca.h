@@ -77,7 +77,9 @@ typedef int32_t fmca_path;
                                else the SIMT path */
 #define FMCA_PATH_SIMT 1    /* CUDA-core fp32 kernels, any supported shape */
 #define FMCA_PATH_TCGEN05 2 /* tcgen05/TMEM + TMA kernels; FMCA_BF16 only,
-                               s == 128, C % 128 == 0, e % 256 == 0 */
+                               s == 128, C % 128 == 0, e % 128 == 0
+                               (e % 256 == 0 without a global term for
+                               C > 256, and for the backward pass) */
 
 /* Supported sizes: B, n, s, e >= 1; 1 <= C <= n with n % C == 0; s <= 256;
  * B * n * max(s, e) < 2^31.  The tensor-core path additionally needs the
@@ -85,11 +87,15 @@ typedef int32_t fmca_path;
  *
  * Tensor-core coverage of the bf16 shapes: the tcgen05 kernels take s = 128
  * (the pages' attention width), C a multiple of 128 (128, 256, ..., up to
- * C = n for the quadratic-only model) and e a multiple of 256.  Every other
- * bf16 shape in the supported sizes (s = 16 ... 256 other than 128, C = 64
- * or any C that is not a multiple of 128, e not a multiple of 256) runs the
- * fp32 CUDA-core kernels: correct, to the fp32 bar, but several times
- * slower.  FMCA_PATH_AUTO picks the tensor-core path whenever it applies. */
+ * C = n for the quadratic-only model) and e a multiple of 128.  Two forms
+ * need e a multiple of 256: the quadratic-only model with chunks over 256
+ * tokens (FMCA_LIN_NORM_NONE, C > 256), whose relu^2 weights go through the
+ * workspace, and the backward pass.  Every other bf16 shape in the
+ * supported sizes (s = 16 ... 256 other than 128, C = 64 or any C that is
+ * not a multiple of 128, e not a multiple of 128) runs the fp32 CUDA-core
+ * kernels: correct, to the fp32 bar, but several times slower.
+ * FMCA_PATH_AUTO picks the tensor-core path whenever it applies
+ * (flash_mca_auto_path answers for the default options). */
 
 /*
  * Bytes of device workspace one flash_mca_forward call with these arguments
@@ -299,8 +305,8 @@ fmca_status flash_mca_decode_step(const void *z, const void *v, const void *u,
  *   dgamma, dbeta        device float32 [4][s] outputs (overwritten)
  *   workspace            at least flash_mca_backward_workspace_bytes(...) bytes,
  *                        256-byte aligned
- * bf16 inputs in the shapes of FMCA_PATH_TCGEN05 (s == 128, C % 128 == 0,
- * e % 256 == 0) run on the tensor cores: the forward kernels recompute the
+ * bf16 inputs with s == 128, C % 128 == 0 and e % 256 == 0 run on the
+ * tensor cores: the forward kernels recompute the
  * ungated output and the relu^2 weights, and batched bf16 products with fp32
  * accumulation form the gradients (intermediates rounded to bf16).  Every
  * other shape, and float32, runs in fp32 on the CUDA cores.  Both use a fixed
@@ -326,8 +332,8 @@ fmca_status flash_mca_backward(const void *Z, const void *V, const void *U, cons
  * uses its first flash_mca_workspace_bytes), with nothing written to it
  * since; the library cannot check this.  The relu^2 weights and lin_q rows
  * (which the forward pass keeps on chip) and the output kernel (fed dO, for
- * dU) run again.  Shapes of FMCA_PATH_TCGEN05 with FMCA_BF16 only; others
- * return FMCA_ERR_UNSUPPORTED.
+ * dU) run again.  FMCA_BF16 with s == 128, C % 128 == 0 and e % 256 == 0
+ * only; others return FMCA_ERR_UNSUPPORTED.
  */
 /* Number of kernels one flash_mca_backward (saved = 0) or
  * flash_mca_backward_saved (saved = 1) call launches for these arguments (0

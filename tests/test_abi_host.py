@@ -53,9 +53,9 @@ def test_status_strings():
 def walk_segments(B, n, e, C):
     """Segments of the chunk axis the tensor-core path's chunk walkers use:
     about 144 (sequence, 256 e columns, segment) units, every segment
-    non-empty (whole 256-column slices only: the path takes e % 256 == 0)."""
+    non-empty (the last slice of e may be narrower)."""
     G = n // C
-    slices = B * (e // 256)
+    slices = B * (-(-e // 256))
     S = max(1, min(G, 144 // slices)) if slices else 1
     L = -(-G // S)
     return -(-G // L)
@@ -96,7 +96,9 @@ def test_auto_path_choice():
     assert fm.flash_mca_auto_path(2, 8192, 128, 1536, 256, 1, f32) == fm.FMCA_PATH_SIMT
     assert fm.flash_mca_auto_path(1, 256, 32, 64, 64, 1, f32) == fm.FMCA_PATH_SIMT
     assert fm.flash_mca_auto_path(1, 512, 64, 256, 256, 1, bf) == fm.FMCA_PATH_SIMT   # s != 128
-    assert fm.flash_mca_auto_path(1, 512, 128, 320, 256, 1, bf) == fm.FMCA_PATH_SIMT  # e % 256
+    assert fm.flash_mca_auto_path(1, 512, 128, 320, 256, 1, bf) == fm.FMCA_PATH_SIMT  # e % 128
+    # e a multiple of 128 but not of 256: the forward pass's own forms take it
+    assert fm.flash_mca_auto_path(1, 512, 128, 640, 256, 1, bf) == fm.FMCA_PATH_TCGEN05
     assert fm.flash_mca_auto_path(1, 512, 128, 256, 64, 1, bf) == fm.FMCA_PATH_SIMT   # C = 64
     assert fm.flash_mca_auto_path(1, 500, 128, 256, 64, 1, bf) == -1
 
@@ -121,6 +123,15 @@ def test_launch_counts():
                                      lin_norm=fm.FMCA_LIN_NORM_POSITION) == 2
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
     assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
+    # e % 256 == 128: every form but the stored-weights one (no global term,
+    # chunks over 256 tokens), which goes to the CUDA cores
+    assert fm.flash_mca_launch_count(2, 2048, 128, 640, 256, 1, bf) == 2
+    assert fm.flash_mca_launch_count(2, 2048, 128, 640, 512, 1, bf, fm.FMCA_PATH_TCGEN05,
+                                     lin_norm=fm.FMCA_LIN_NORM_NONE) == 0
+    assert fm.flash_mca_launch_count(2, 2048, 128, 640, 512, 1, bf,
+                                     lin_norm=fm.FMCA_LIN_NORM_NONE) == 3
+    assert fm.flash_mca_launch_count(2, 2048, 128, 768, 512, 1, bf,
+                                     lin_norm=fm.FMCA_LIN_NORM_NONE) == 2
     assert fm.flash_mca_launch_count(1, 500, 128, 256, 64, 1, bf) == 0
 
 

@@ -208,6 +208,10 @@ def test_full_size_workload_whole_output(name):
     # SMs, so walkers take a second unit; 1280 row-pair tiles
     (16, 1024, 256, 2560, True),
     (16, 1024, 256, 2560, False),
+    # e % 256 == 128: the walkers' last e slice is 128 columns wide
+    (4, 2048, 256, 640, True),
+    (4, 2048, 256, 640, False),
+    (4, 2048, 128, 384, True),
 ])
 def test_more_units_than_sms_whole_output(B, n, C, e, causal):
     """Shapes that are not benchmark workloads, with more work units than SMs."""
