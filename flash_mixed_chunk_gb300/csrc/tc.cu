@@ -1,6 +1,6 @@
 // tc.cu -- tensor-core path of the mixed-chunk attention forward core
 // (sm_103a: tcgen05 MMA into TMEM, TMA-staged 128-byte-swizzled bf16 tiles,
-// mbarrier pipelines) for bf16 I/O, s = 128, C % 128 == 0, e % 128 == 0 (the
+// mbarrier pipelines) for bf16 I/O, s = 128, C % 128 == 0, e % 64 == 0 (the
 // stored-weights form and the backward pass: e % 256 == 0).
 //
 // Per call ("FLASH: Possibly the Most Interesting Efficient Transformer
@@ -132,12 +132,13 @@ bool tc_supported(int B, int n, int s, int e, int C) {
   return true;
 }
 
-// The forward pass's own forms take e in 128-column tiles (the output
-// kernels' e tiles; the walkers' last slice is half wide), except the
+// The forward pass's own forms take e in 64-column steps (the output
+// kernels' e tiles are 128 columns, the last may be 64; the walkers' last
+// slice may be 64 or 128 of its 256), except the
 // stored-weights form (no global term, chunks over 256 tokens), whose output
 // kernel takes 256-column tiles.
 bool tc_forward_supported(int B, int n, int s, int e, int C, int lin_norm) {
-  if (s != S_DIM || C % ROW_TILE || n % C || e % FU_ET) return false;
+  if (s != S_DIM || C % ROW_TILE || n % C || e % (FU_ET / 2)) return false;
   if (lin_norm == kLinNormNone && C > 2 * ROW_TILE && e % E_TILE) return false;
   (void)B;
   return true;
@@ -178,7 +179,7 @@ FusedGrid fused_grid(int B, int n, int e, int C, int causal, bool lin) {
   g.causal = causal;
   g.lin = lin ? 1 : 0;
   g.R = C / ROW_TILE;
-  g.n_et = e / FU_ET;
+  g.n_et = (e + FU_ET - 1) / FU_ET;  // the last e tile may be 64 columns
   g.n_tiles = B * g.G * g.R * g.n_et;
   g.S = 1;
   g.L = g.G;
@@ -312,7 +313,7 @@ int launch_tc_forward(const void *Z, const void *V, const void *U, const float *
     PairGrid pg;
     pg.n = n;
     pg.G = G;
-    pg.n_et = e / FU_ET;
+    pg.n_et = (e + FU_ET - 1) / FU_ET;
     pg.n_tiles = B * G * pg.n_et;
     pg.S = sp.S;
     pg.L = sp.L;

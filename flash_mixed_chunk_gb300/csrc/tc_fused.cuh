@@ -86,7 +86,8 @@ struct FusedUnit {
 };
 
 // The tiles: t = (bg * R + rt) * n_et + et for sequence-chunk bg (of B * G),
-// row tile rt (of R = C / 128) and e tile et (of n_et = e / 128).
+// row tile rt (of R = C / 128) and e tile et (of n_et = ceil(e / 128); the
+// last may be 64 columns).
 struct FusedGrid {
   int n, C, G, causal, lin, R, n_et, n_tiles;
   int S, L;        // segments of the chunk axis, chunks each
@@ -582,13 +583,15 @@ __global__ void __launch_bounds__(FUSED_THREADS, 1)
         u32x8 uv[FU_ET / 16];
         const __nv_bfloat16 *usrc = U + roff + e0;
 #pragma unroll
-        for (int c = 0; c < FU_ET / 16; ++c) uv[c] = ldg_stream(usrc + 16 * c);
+        for (int c = 0; c < FU_ET / 16; ++c)
+          if (e0 + 16 * c < e) uv[c] = ldg_stream(usrc + 16 * c);  // a 64-column last tile
         const bool w = mbar_wait(&o_full[ob], (oc >> 1) & 1, kWaitLimitNs);
         if (w) {
           tc_fence_after();
           __nv_bfloat16 *odst = O + roff + e0;
 #pragma unroll
           for (int q = 0; q < FU_ET / 32; ++q) {  // 32 columns at a time
+            if (e0 + 32 * q >= e) break;
             uint32_t r[32];
             tmem_ld32(tbase + lane_off + (uint32_t)(ob * FU_ET + 32 * q), r);
             tmem_ld_wait();

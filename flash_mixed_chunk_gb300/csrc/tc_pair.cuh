@@ -666,11 +666,14 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           const int r = 1 - rr;
           const size_t roff =
               (size_t)(f.crow + r * ROW_TILE + row) * (size_t)e + (f.et0 + x) * FU_ET + 64;
+          // a 64-column last e tile has no upper half
+          const bool live = (f.et0 + x) * FU_ET + 64 < e;
           u32x8 uv[4];
 #pragma unroll
-          for (int c = 0; c < 4; ++c) uv[c] = ldg_stream(U + roff + 16 * c);
+          for (int c = 0; c < 4; ++c)
+            if (live) uv[c] = ldg_stream(U + roff + 16 * c);
           const bool w = mbar_wait(&o_full[r], tcnt & 1, kWaitLimitNs);
-          if (w) {
+          if (w && live) {
             tc_fence_after();
             pair_gate64(uv, O, roff, tbase + lane_off + (uint32_t)(r * FU_ET + 64));
             tc_fence_before();

@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   const int G = n / C;
-  const int n_es = (e + WK_ET - 1) / WK_ET;  // the last slice may be 128 columns
+  const int n_es = (e + WK_ET - 1) / WK_ET;  // the last slice may be narrower
   const int n_slices = B * n_es;
   const int n_units = n_slices * S;
   const int W = (int)gridDim.x;
@@ -319,11 +319,10 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
           fence_proxy_async_smem();
           named_bar_sync(2, 128);
           if (mt == 0) {
-            // a 128-column last slice: its upper half is past e (zeros)
-            if (col0 + 128 * h < e) {
-              tma_store_2d(map, stage, col0 + 128 * h, prow);
+            // a narrower last slice: the columns past e (zeros) are not stored
+            if (col0 + 128 * h < e) tma_store_2d(map, stage, col0 + 128 * h, prow);
+            if (col0 + 128 * h + 64 < e)
               tma_store_2d(map, stage + WK_STAGE_TILE, col0 + 128 * h + 64, prow);
-            }
             bulk_commit_group();
           }
         }

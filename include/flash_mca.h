@@ -77,7 +77,7 @@ typedef int32_t fmca_path;
                                else the SIMT path */
 #define FMCA_PATH_SIMT 1    /* CUDA-core fp32 kernels, any supported shape */
 #define FMCA_PATH_TCGEN05 2 /* tcgen05/TMEM + TMA kernels; FMCA_BF16 only,
-                               s == 128, C % 128 == 0, e % 128 == 0
+                               s == 128, C % 128 == 0, e % 64 == 0
                                (e % 256 == 0 without a global term for
                                C > 256, and for the backward pass) */
 
@@ -87,12 +87,12 @@ typedef int32_t fmca_path;
  *
  * Tensor-core coverage of the bf16 shapes: the tcgen05 kernels take s = 128
  * (the pages' attention width), C a multiple of 128 (128, 256, ..., up to
- * C = n for the quadratic-only model) and e a multiple of 128.  Two forms
+ * C = n for the quadratic-only model) and e a multiple of 64.  Two forms
  * need e a multiple of 256: the quadratic-only model with chunks over 256
  * tokens (FMCA_LIN_NORM_NONE, C > 256), whose relu^2 weights go through the
  * workspace, and the backward pass.  Every other bf16 shape in the
  * supported sizes (s = 16 ... 256 other than 128, C = 64 or any C that is
- * not a multiple of 128, e not a multiple of 128) runs the fp32 CUDA-core
+ * not a multiple of 128, e not a multiple of 64) runs the fp32 CUDA-core
  * kernels: correct, to the fp32 bar, but several times slower.
  * FMCA_PATH_AUTO picks the tensor-core path whenever it applies
  * (flash_mca_auto_path answers for the default options). */

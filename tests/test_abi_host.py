@@ -96,9 +96,10 @@ def test_auto_path_choice():
     assert fm.flash_mca_auto_path(2, 8192, 128, 1536, 256, 1, f32) == fm.FMCA_PATH_SIMT
     assert fm.flash_mca_auto_path(1, 256, 32, 64, 64, 1, f32) == fm.FMCA_PATH_SIMT
     assert fm.flash_mca_auto_path(1, 512, 64, 256, 256, 1, bf) == fm.FMCA_PATH_SIMT   # s != 128
-    assert fm.flash_mca_auto_path(1, 512, 128, 320, 256, 1, bf) == fm.FMCA_PATH_SIMT  # e % 128
-    # e a multiple of 128 but not of 256: the forward pass's own forms take it
+    assert fm.flash_mca_auto_path(1, 512, 128, 200, 256, 1, bf) == fm.FMCA_PATH_SIMT  # e % 64
+    # e a multiple of 64 but not of 256: the forward pass's own forms take it
     assert fm.flash_mca_auto_path(1, 512, 128, 640, 256, 1, bf) == fm.FMCA_PATH_TCGEN05
+    assert fm.flash_mca_auto_path(1, 512, 128, 320, 256, 1, bf) == fm.FMCA_PATH_TCGEN05
     assert fm.flash_mca_auto_path(1, 512, 128, 256, 64, 1, bf) == fm.FMCA_PATH_SIMT   # C = 64
     assert fm.flash_mca_auto_path(1, 500, 128, 256, 64, 1, bf) == -1
 
@@ -123,7 +124,7 @@ def test_launch_counts():
                                      lin_norm=fm.FMCA_LIN_NORM_POSITION) == 2
     assert fm.flash_mca_launch_count(2, 8192, 128, 1536, 256, 1, bf, fm.FMCA_PATH_SIMT) == 3
     assert fm.flash_mca_launch_count(1, 512, 64, 256, 256, 1, bf, fm.FMCA_PATH_TCGEN05) == 0
-    # e % 256 == 128: every form but the stored-weights one (no global term,
+    # e % 256 != 0: every form but the stored-weights one (no global term,
     # chunks over 256 tokens), which goes to the CUDA cores
     assert fm.flash_mca_launch_count(2, 2048, 128, 640, 256, 1, bf) == 2
     assert fm.flash_mca_launch_count(2, 2048, 128, 640, 512, 1, bf, fm.FMCA_PATH_TCGEN05,

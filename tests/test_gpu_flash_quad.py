@@ -45,6 +45,7 @@ def test_longer_chunks_on_the_tensor_core_path(B, n, C, s, e, causal):
     (1, 1280, 128, 256, False),
     (2, 256, 128, 384, True),     # e % 256 == 128 (C = n = 256: the fused kernel)
     (2, 256, 128, 384, False),
+    (2, 256, 128, 320, True),     # a 64-column last e tile
 ])
 def test_flash_quad_tensor_core(B, n, s, e, causal):
     m = fm()

@@ -212,6 +212,10 @@ def test_full_size_workload_whole_output(name):
     (4, 2048, 256, 640, True),
     (4, 2048, 256, 640, False),
     (4, 2048, 128, 384, True),
+    # e % 128 == 64: the last e tile is 64 columns, the last slice 64 of 256
+    (4, 2048, 256, 576, True),
+    (4, 2048, 256, 576, False),
+    (4, 2048, 128, 320, True),
 ])
 def test_more_units_than_sms_whole_output(B, n, C, e, causal):
     """Shapes that are not benchmark workloads, with more work units than SMs."""

@@ -52,6 +52,7 @@ def check(B, n, C, s, e, causal, dtype, variant, path, seed):
     (1, 512, 256, 128, 512, False),
     (2, 640, 128, 128, 256, True),   # five chunks of 128
     (1, 512, 256, 128, 640, True),   # e % 256 == 128: a half-wide last walker slice
+    (1, 512, 256, 128, 448, False),  # e % 128 == 64: a 64-column last e tile
 ])
 def test_tensor_core_path(B, n, C, s, e, causal, variant):
     m = fm()
