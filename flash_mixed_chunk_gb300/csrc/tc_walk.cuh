@@ -8,13 +8,18 @@
 // The chunk axis of a sequence is cut into S segments of L chunks.  A walker
 // unit (segment sg, sequence b, 256 e columns) walks its segment's chunks in
 // order:
-//   D_g = T3_g^T V_g[:, slice]      M = 128 (s), N = 256, K = C keys, both
-//                                   operands MN-major, into TMEM
-//   causal: local_g = R, stored as bf16 (not for the segment's first chunk,
-//           where it is zero, when the output kernel is the row-pair one),
-//           then R += D_g (R = the fp32 sum of the segment's states before
-//           g, in TMEM)
+//   R += T3_g^T V_g[:, slice]      M = 128 (s), N = 256, K = C keys, both
+//                                  operands MN-major, accumulated in TMEM
+//                                  (R = the fp32 sum of the segment's states
+//                                  up to g; the first chunk's products start
+//                                  it afresh)
+//   causal: after chunk g, local_{g+1} = R, stored as bf16 (the segment's
+//           first chunk's local sums are zero: stored as zeros only for the
+//           output kernels that read them, not the row-pair one)
 //   after the segment's last chunk: its total R, stored as bf16
+// The epilogue reads R once per chunk and releases it to the next chunk's
+// products as soon as it is read, before its stores; bidirectional walkers
+// read it once per segment.
 // The chunk states are never rounded; the sums are fp32 sums of the fp32
 // products.  seg_carry_group (run by the row-pair kernel's idle warps, or as
 // the launch tc_seg_carry) then turns the segment totals into carries (the
@@ -179,7 +184,9 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t dcol = tbase;
+          // R += T3_g^T V_g: the segment's running sum, fresh at its first chunk
+          const uint32_t rcol = tbase + WK_COL_R;
+          const bool first = g == g0;
           for (int k = 0; k < items; ++k, ++it) {
             const int slot = it % WK_RING;
             if (!mbar_wait(&tready[slot], (it / WK_RING) & 1, kWaitLimitNs)) {
@@ -194,7 +201,7 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
             for (int kk = 0; kk < WK_KEYS / 16; ++kk) {
               const uint64_t ad = smem_desc_sw128(sz + kk * 2048, WK_ATOM, 1024);
               const uint64_t bd = smem_desc_sw128(sz + WK_ITEM_V + kk * 2048, WK_ATOM, 1024);
-              mma_bf16_ss(dcol, ad, bd, idesc, (k | kk) != 0);
+              mma_bf16_ss(rcol, ad, bd, idesc, (!first || (k | kk) != 0) ? 1u : 0u);
             }
             mma_commit(&empty[slot]);
           }
@@ -272,59 +279,49 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     uint8_t *stage = smem + WK_OFF_STAGE;
     const uint32_t rcol = tbase + lane_off + WK_COL_R;
-    const uint32_t dcol = tbase + lane_off;
     int j = 0;
     bool ok = true;
-    // One pass over the 256 columns, 128 at a time through the staging tile
-    // (two [128][64] TMA stores at (col0 + 128 h, prow)): out_r stages R,
-    // out_sum stages R + D, update writes R + D back to R.
-    auto pass = [&](bool out_r, bool out_sum, bool update, const CUtensorMap *map, int col0,
-                    int prow) {
-      const bool out = out_r || out_sum;
+    // R (or zeros) out as bf16: 128 columns at a time through the staging
+    // tile, two [128][64] TMA stores at (col0 + 128 h, prow) each; release:
+    // R goes back to the MMA issuer once every thread has read its last
+    // columns, before their stores
+    auto pass = [&](bool zero, const CUtensorMap *map, int col0, int prow, bool release) {
 #pragma unroll 1
       for (int h = 0; h < 2; ++h) {
-        if (out) {
-          if (mt == 0) bulk_wait_group_read<0>();  // the previous stores have read the tile
-          named_bar_sync(2, 128);
-        }
+        if (mt == 0) bulk_wait_group_read<0>();  // the previous stores have read the tile
+        named_bar_sync(2, 128);
 #pragma unroll 1
         for (int q = 0; q < 4; ++q) {
           const uint32_t c = (uint32_t)(32 * (4 * h + q));
-          uint32_t r[32], d[32];
-          tmem_ld32(rcol + c, r);
-          if (out_sum || update) tmem_ld32(dcol + c, d);
-          tmem_ld_wait();
-          if (out_sum || update) {
+          uint32_t r[32];
+          if (zero) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-              d[i] = __float_as_uint(__uint_as_float(r[i]) + __uint_as_float(d[i]));
+            for (int i = 0; i < 32; ++i) r[i] = 0u;
+          } else {
+            tmem_ld32(rcol + c, r);
+            tmem_ld_wait();
           }
-          if (out) {
-            const uint32_t *src = out_r ? r : d;
-            uint8_t *sb = stage + (q >> 1) * WK_STAGE_TILE;
+          uint8_t *sb = stage + (q >> 1) * WK_STAGE_TILE;
 #pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              const uint32_t *v = src + 8 * c4;
-              *reinterpret_cast<uint4 *>(sb + sw128_offset(row, (q & 1) * 64 + 16 * c4)) =
-                  make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
-                             pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
-                             pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
-                             pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
-            }
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const uint32_t *v = r + 8 * c4;
+            *reinterpret_cast<uint4 *>(sb + sw128_offset(row, (q & 1) * 64 + 16 * c4)) =
+                make_uint4(pack_bf16x2(__uint_as_float(v[0]), __uint_as_float(v[1])),
+                           pack_bf16x2(__uint_as_float(v[2]), __uint_as_float(v[3])),
+                           pack_bf16x2(__uint_as_float(v[4]), __uint_as_float(v[5])),
+                           pack_bf16x2(__uint_as_float(v[6]), __uint_as_float(v[7])));
           }
-          if (update) tmem_st32(rcol + c, d);
         }
-        if (update) tmem_st_wait();
-        if (out) {
-          fence_proxy_async_smem();
-          named_bar_sync(2, 128);
-          if (mt == 0) {
-            // a narrower last slice: the columns past e (zeros) are not stored
-            if (col0 + 128 * h < e) tma_store_2d(map, stage, col0 + 128 * h, prow);
-            if (col0 + 128 * h + 64 < e)
-              tma_store_2d(map, stage + WK_STAGE_TILE, col0 + 128 * h + 64, prow);
-            bulk_commit_group();
-          }
+        fence_proxy_async_smem();
+        if (release && h == 1) tc_fence_before();
+        named_bar_sync(2, 128);
+        if (mt == 0) {
+          if (release && h == 1) mbar_arrive(&acc_empty);
+          // a narrower last slice: the columns past e (zeros) are not stored
+          if (col0 + 128 * h < e) tma_store_2d(map, stage, col0 + 128 * h, prow);
+          if (col0 + 128 * h + 64 < e)
+            tma_store_2d(map, stage + WK_STAGE_TILE, col0 + 128 * h + 64, prow);
+          bulk_commit_group();
         }
       }
     };
@@ -339,27 +336,21 @@ __global__ void __launch_bounds__(WK_THREADS, 1)
           break;
         }
         tc_fence_after();
-        // R = the segment's sum before this chunk: zero at its first
-        if (g == g0) {
-          uint32_t z[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) z[i] = 0u;
-#pragma unroll 1
-          for (int q = 0; q < WK_ET / 32; ++q) tmem_st32(rcol + 32 * q, z);
-          tmem_st_wait();
-        }
-        const bool out_local = causal && (g > g0 || store_first_local);
-        if (g < g1 - 1) {
-          // causal: local_g = R out; R += D_g
-          pass(out_local, false, true, &mapL, es * WK_ET, (b * G + g) * S_DIM);
+        // R = the segment's sum up to and including chunk g: the next chunk's
+        // local sums (causal), or after the segment's last chunk its total.
+        // A segment's first chunk has zero local sums, stored only when the
+        // output kernel reads them (not the row-pair one).
+        if (causal && g == g0 && store_first_local)
+          pass(true, &mapL, es * WK_ET, (b * G + g) * S_DIM, false);
+        if (g == g1 - 1) {
+          pass(false, &mapT, es * WK_ET, (b * S + sg) * S_DIM, true);
+        } else if (causal) {
+          pass(false, &mapL, es * WK_ET, (b * G + g + 1) * S_DIM, true);
         } else {
-          // the segment's last chunk: local_g (causal), then the total R + D_g
-          if (out_local) pass(true, false, false, &mapL, es * WK_ET, (b * G + g) * S_DIM);
-          pass(false, true, false, &mapT, es * WK_ET, (b * S + sg) * S_DIM);
+          // nothing of R read for this chunk
+          named_bar_sync(2, 128);
+          if (mt == 0) mbar_arrive(&acc_empty);
         }
-        tc_fence_before();
-        named_bar_sync(2, 128);
-        if (mt == 0) mbar_arrive(&acc_empty);  // every epilogue thread has read D
       }
     }
     if (mt == 0) bulk_wait_group<0>();
