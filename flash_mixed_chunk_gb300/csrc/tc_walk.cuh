@@ -32,17 +32,18 @@
 // position; 1/(g C) for causal chunk g with the tokens-summed divisor), which
 // the walker of e slice g % ceil(e / 256) writes with T0 and T1.
 //
-// The kernel is bound by the bytes each SM can have in flight (its loads take
-// microseconds to land), so a unit takes 256 e columns: each Z chunk it loads
-// serves twice the columns of a 128-column slice.
+// A unit takes 256 e columns, so each Z chunk it loads serves twice the
+// columns of a 128-column slice.  The MMA issuer waits for the epilogue's read
+// of R between chunks; that read, not the copies, is the kernel's chain.
 // Warp roles (352 threads): 0 and 10 TMA producers (Z and V: one thread
 // issues a copy every few hundred cycles, so the two streams issue in
 // parallel), 1 MMA issuer, 2-5 transform (T3 = Z gamma_3 + beta_3 in place;
-// T rows), 6-9 epilogue (the running sum in TMEM, bf16 sums through a
-// staging tile and TMA stores).
+// T rows), 6-9 epilogue (R out as bf16 sums through a staging tile and TMA
+// stores).
 // Shared memory: a ring of 4 items of 48 KB (64 keys: Z [2][64][64] and V
-// [4][64][64], 128-byte swizzled), one 32 KB staging tile.  TMEM: D [0, 256),
-// R [256, 512); the next chunk's products wait until the epilogue has read D.
+// [4][64][64], 128-byte swizzled), one 32 KB staging tile.  TMEM: R in
+// [256, 512) of the 512 columns allocated; the next chunk's products wait
+// until the epilogue has read R.
 #pragma once
 
 #include "tc_common.cuh"
