@@ -166,6 +166,23 @@ __device__ __forceinline__ void pair_gate64(const u32x8 (&uv)[4], __nv_bfloat16 
   }
 }
 
+// An e tile's carry merged into its local sums, in place in the local-sum
+// item (both items are the same 128-byte swizzled [2][128][64] layout, so the
+// sum is element by element): thread m of the 192 that share it (the merge
+// warps' 64, then the relu^2 warps' 128) takes the 16-byte pieces m, m + 192,
+// ...  A proxy fence follows, as the MMA reads the sum next.
+__device__ __forceinline__ void pair_merge(uint8_t *ring, int il, int icy, int m) {
+  uint4 *lp = reinterpret_cast<uint4 *>(ring + (il % PA_RING) * PA_ITEM);
+  const uint4 *cp = reinterpret_cast<const uint4 *>(ring + (icy % PA_RING) * PA_ITEM);
+#pragma unroll 4
+  for (int i = m; i < (int)(PA_ITEM / 16); i += 192) {
+    const uint4 a = lp[i], c = cp[i];
+    lp[i] = make_uint4(add_bf16x2(a.x, c.x), add_bf16x2(a.y, c.y), add_bf16x2(a.z, c.z),
+                       add_bf16x2(a.w, c.w));
+  }
+  fence_proxy_async_smem();
+}
+
 // kState: a carried-in state or a state out (flash_mca_forward_seq); the
 // plain forward pass compiles without that code.  kCausal: causal chunks
 // (masked scores, prefix sums); otherwise bidirectional (every key, the
@@ -228,7 +245,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     }
     mbar_init(&mma_done, 1);
     mbar_init(&mg_go, 1);
-    mbar_init(&m_full, 1);
+    mbar_init(&m_full, 2);  // the merge warps and the relu^2 warps
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -515,7 +532,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 ok = false;
                 break;
               }
-              if (merge) ++mcnt;
+              if (merge) {
+                ++mcnt;
+                mbar_arrive(&empty[(il + 1) % PA_RING]);  // the carry item is merged in
+              }
             }
             tc_fence_after();
             if (nglob > 0) {
@@ -567,30 +587,13 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
         if (!(f.local && f.carry)) continue;
         const bool w = mbar_wait(&mg_go, mcnt & 1, kWaitLimitNs);
         ++mcnt;
-        if (w) {
-          uint4 *lp = reinterpret_cast<uint4 *>(ring + (il % PA_RING) * PA_ITEM);
-          const uint4 *cp = reinterpret_cast<const uint4 *>(ring + (icy % PA_RING) * PA_ITEM);
-#pragma unroll 4
-          for (int i = mt; i < (int)(PA_ITEM / 16); i += 64) {
-            const uint4 a = lp[i], c = cp[i];
-            const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
-            uint32_t o[4];
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              o[q] = pack_bf16x2(bf16_lo(aw[q]) + bf16_lo(cw[q]), bf16_hi(aw[q]) + bf16_hi(cw[q]));
-            lp[i] = make_uint4(o[0], o[1], o[2], o[3]);
-          }
-          fence_proxy_async_smem();  // read next by the MMA
-        }
+        if (w) pair_merge(ring, il, icy, mt);  // its third of the tile
         ok = named_bar_and(4, 64, w);
         if (!ok) {
           if (mt == 0) record_timeout(861);
           break;
         }
-        if (mt == 0) {
-          mbar_arrive(&m_full);
-          mbar_arrive(&empty[icy % PA_RING]);  // the carry item is no longer needed
-        }
+        if (mt == 0) mbar_arrive(&m_full);
       }
     }
   } else if (warp >= 4 && warp < 8) {
@@ -600,6 +603,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const int row = quad * 32 + lane;  // query row within its row tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     int tcnt = 0;
+    int it = 0, mcnt = 0;  // ring items and merges, as the merge warps count them
     bool ok = true;
     for (int j = 0; ok; ++j) {
       const int qs = j % FU_QUEUE;
@@ -658,10 +662,25 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           if (mt == 0) mbar_arrive(&p_full[ps]);
         }
       }
-      // then columns 64-127 of the unit's output tiles (the epilogue warps
-      // take 0-63)
+      // then, per e tile, two thirds of the merge (the merge warps take the
+      // rest) and columns 64-127 of the output tiles (the epilogue warps take
+      // 0-63)
       const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
+      it += 4;  // the unit's T0 and T1 items
       for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
+        const int il = it + 2, icy = it + 3;
+        it += 2 + (int)f.local + (int)f.carry;
+        if (f.local && f.carry) {
+          const bool w = mbar_wait(&mg_go, mcnt & 1, kWaitLimitNs);
+          ++mcnt;
+          if (w) pair_merge(ring, il, icy, 64 + mt);
+          ok = named_bar_and(2, 128, w);
+          if (!ok) {
+            if (mt == 0) record_timeout(862);
+            break;
+          }
+          if (mt == 0) mbar_arrive(&m_full);
+        }
         for (int rr = 0; rr < 2 && ok; ++rr) {
           const int r = 1 - rr;
           const size_t roff =
