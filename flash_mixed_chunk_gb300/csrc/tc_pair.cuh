@@ -35,9 +35,10 @@
 //                        (causal 2 + 4 slots, bidirectional 4 + 4)
 //   per e tile, r = 1 then 0:
 //     O_r  = sum_k P_rk V_k + T2_r (local_g + carry)   (A of the first from
-//            TMEM; M = 128, N = 128); two merge warps add the carry tile into
-//            the local-sum tile in shared memory first (one product instead
-//            of two, and the carry's slot goes back at once)
+//            TMEM; M = 128, N = 128); the two merge warps and the four
+//            relu^2 warps add the carry tile into the local-sum tile in
+//            shared memory first (packed bf16 adds; one product instead of
+//            two, and the carry's slot goes back once the sum is formed)
 //     out  = U * O_r      eight warps (the epilogue warps columns 0-63, the
 //                         relu^2 warps, idle once a unit's weights are formed,
 //                         columns 64-127); O_1 drains while O_0 forms and the
@@ -73,8 +74,9 @@ template <bool kCausal>
 __host__ __device__ constexpr int pair_pslots() { return kCausal ? 6 : 8; }
 template <bool kCausal>
 __host__ __device__ constexpr uint32_t pair_col_p() { return kCausal ? 320u : 256u; }
-// warps: 0 producer, 1 MMA, 2-3 merge, 4-7 relu^2 then epilogue (columns
-// 64-127), 8-11 epilogue (columns 0-63)
+// warps: 0 producer, 1 MMA, 2-3 merge, 4-7 relu^2 then, per e tile, two
+// thirds of the merge and the epilogue of columns 64-127, 8-11 epilogue
+// (columns 0-63)
 constexpr int PAIR_THREADS = 384;
 static_assert(PAIR_SMEM <= 232448, "tc_chunk_pair exceeds 227 KB of shared memory");
 
@@ -564,8 +566,8 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     }
   } else if (warp == 2 || warp == 3) {
     // =========================== merge warps (64 threads): local += carry
-    // in the local-sum item, in place (both items are the same 128-byte
-    // swizzled [2][128][64] layout, so the sum is element by element)
+    // in the local-sum item, in place (pair_merge), a third of each tile's;
+    // the relu^2 warps take the rest
     const int mt = threadIdx.x - 64;
     int it = 0, mcnt = 0;
     bool ok = true;
