@@ -425,13 +425,6 @@ __device__ __forceinline__ void stg_stream(void *p, const u32x8 &v) {
       : "memory");
 }
 
-// Two bf16 sums in one instruction (each rounded to nearest even).
-__device__ __forceinline__ uint32_t add_bf16x2(uint32_t a, uint32_t b) {
-  uint32_t d;
-  asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
-  return d;
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t *>(&h);

@@ -11,7 +11,8 @@
 //
 // At its start every CTA turns its share of the walkers' segment totals into
 // carries (bidirectional: the total of each sequence, in its first segment's
-// slot; warps 2-3 and 8-11, idle until the first merge and output tile) and
+// slot; warps 2-3, otherwise unused, and 8-11, idle until the first output
+// tile) and
 // counts itself on a grid counter; the producer loads no carry before every
 // CTA is counted.  Causal: a segment's first chunk has no local-sum item (its
 // local sum is zero and the walkers do not store it), a sequence's first
@@ -34,11 +35,11 @@
 //                        keys at a time, bf16 in TMEM, resident for the unit
 //                        (causal 2 + 4 slots, bidirectional 4 + 4)
 //   per e tile, r = 1 then 0:
-//     O_r  = sum_k P_rk V_k + T2_r (local_g + carry)   (A of the first from
-//            TMEM; M = 128, N = 128); the two merge warps and the four
-//            relu^2 warps add the carry tile into the local-sum tile in
-//            shared memory first (packed bf16 adds; one product instead of
-//            two, and the carry's slot goes back once the sum is formed)
+//     O_r  = sum_k P_rk V_k + T2_r local_g + T2_r carry   (A of the first
+//            from TMEM; M = 128, N = 128; the local sums and the carry are
+//            two products into the same accumulator: cheaper than adding the
+//            two tiles in shared memory first, which the MMA issuer would
+//            wait for)
 //     out  = U * O_r      eight warps (the epilogue warps columns 0-63, the
 //                         relu^2 warps, idle once a unit's weights are formed,
 //                         columns 64-127); O_1 drains while O_0 forms and the
@@ -74,9 +75,8 @@ template <bool kCausal>
 __host__ __device__ constexpr int pair_pslots() { return kCausal ? 6 : 8; }
 template <bool kCausal>
 __host__ __device__ constexpr uint32_t pair_col_p() { return kCausal ? 320u : 256u; }
-// warps: 0 producer, 1 MMA, 2-3 merge, 4-7 relu^2 then, per e tile, two
-// thirds of the merge and the epilogue of columns 64-127, 8-11 epilogue
-// (columns 0-63)
+// warps: 0 producer, 1 MMA, 2-3 the start's carries only, 4-7 relu^2 then
+// the epilogue of columns 64-127, 8-11 epilogue (columns 0-63)
 constexpr int PAIR_THREADS = 384;
 static_assert(PAIR_SMEM <= 232448, "tc_chunk_pair exceeds 227 KB of shared memory");
 
@@ -168,23 +168,6 @@ __device__ __forceinline__ void pair_gate64(const u32x8 (&uv)[4], __nv_bfloat16 
   }
 }
 
-// An e tile's carry merged into its local sums, in place in the local-sum
-// item (both items are the same 128-byte swizzled [2][128][64] layout, so the
-// sum is element by element): thread m of the 192 that share it (the merge
-// warps' 64, then the relu^2 warps' 128) takes the 16-byte pieces m, m + 192,
-// ...  A proxy fence follows, as the MMA reads the sum next.
-__device__ __forceinline__ void pair_merge(uint8_t *ring, int il, int icy, int m) {
-  uint4 *lp = reinterpret_cast<uint4 *>(ring + (il % PA_RING) * PA_ITEM);
-  const uint4 *cp = reinterpret_cast<const uint4 *>(ring + (icy % PA_RING) * PA_ITEM);
-#pragma unroll 4
-  for (int i = m; i < (int)(PA_ITEM / 16); i += 192) {
-    const uint4 a = lp[i], c = cp[i];
-    lp[i] = make_uint4(add_bf16x2(a.x, c.x), add_bf16x2(a.y, c.y), add_bf16x2(a.z, c.z),
-                       add_bf16x2(a.w, c.w));
-  }
-  fence_proxy_async_smem();
-}
-
 // kState: a carried-in state or a state out (flash_mca_forward_seq); the
 // plain forward pass compiles without that code.  kCausal: causal chunks
 // (masked scores, prefix sums); otherwise bidirectional (every key, the
@@ -216,10 +199,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   __shared__ __align__(8) uint64_t s_full[kSS];  // stage st's scores are in TMEM
   __shared__ __align__(8) uint64_t p_full[kPS], p_empty[kPS];
   __shared__ __align__(8) uint64_t o_full[2], o_empty[2], mma_done;
-  // the MMA thread, the ring's only in-order consumer, hands an e tile's
-  // local-sum and carry items to the merge warps (mg_go) once they have
-  // landed; the merge warps hand the sum back (m_full)
-  __shared__ __align__(8) uint64_t mg_go, m_full;
   __shared__ int uq_unit[FU_QUEUE], uq_net[FU_QUEUE];
   __shared__ uint32_t tmem_base;
 
@@ -228,7 +207,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < FU_QUEUE; ++i) {
       mbar_init(&uq_full[i], 1);
-      mbar_init(&uq_empty[i], 4);  // MMA issuer, merge, relu^2 and epilogue warps
+      mbar_init(&uq_empty[i], 3);  // MMA issuer, relu^2 and epilogue warps
     }
     mbar_init(&b_full, 1);
     mbar_init(&b_empty, 1);
@@ -246,8 +225,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       mbar_init(&o_empty[i], 2);  // both column halves drained
     }
     mbar_init(&mma_done, 1);
-    mbar_init(&mg_go, 1);
-    mbar_init(&m_full, 2);  // the merge warps and the relu^2 warps
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -262,7 +239,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
   uint8_t *bbuf = smem + PA_OFF_B;
 
   // The segment carries, formed while the unit's rows, scores and weights
-  // come in: warps 2-3 and 8-11 (idle until the first merge and output tile)
+  // come in: warps 2-3 and 8-11 (idle until the first output tile)
   // turn this CTA's share of the column groups' totals into carries, then
   // the CTA is counted; the producer loads no carry before every CTA is.
   if (grid.carries && (warp == 2 || warp == 3 || warp >= 8)) {
@@ -383,7 +360,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       // O += P V (A from TMEM) and O += T2 (local | carry) (A K-major); B MN-major
       constexpr uint32_t idesc_o = idesc_bf16_f32(128, FU_ET, false, true);
       const uint32_t baddr = smem_u32(bbuf);
-      int it = 0, tcnt = 0, mcnt = 0;
+      int it = 0, tcnt = 0;
       bool ok = true;
       auto wait_item = [&](int item) -> bool {
         if (!mbar_wait(&full[item % PA_RING], (item / PA_RING) & 1, kWaitLimitNs)) {
@@ -465,7 +442,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           // il: the local sums, or the carry alone in a segment's first chunk
           const int iv1 = it, iv0 = it + 1, il = it + 2;
           const int nglob = (int)f.local + (int)f.carry;
-          const bool merge = f.local && f.carry;
           it += 2 + nglob;
           for (int rr = 0; rr < 2 && ok; ++rr) {
             const int r = 1 - rr;
@@ -508,17 +484,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
               // keys 128-255 are read last by row tile 1 (causal) or row tile
               // 0 (bidirectional)
               if (k == 3 && r == (kCausal ? 1 : 0)) mma_commit(&empty[iv1 % PA_RING]);
-              if (r == 1 && k == 3) {
-                // the local sums and the carry have landed: merge them while
-                // the keys 0-127 products run
-                if (merge) {
-                  if (!wait_item(il) || !wait_item(il + 1)) {
-                    ok = false;
-                    break;
-                  }
-                  mbar_arrive(&mg_go);
-                }
-              }
             }
             if (!ok) break;
             if (r == 0) mma_commit(&empty[iv0 % PA_RING]);  // row tile 0 read keys 0-127 last
@@ -527,21 +492,17 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
               ok = false;
               break;
             }
-            // the local sums, with the carry added by the merge warps
-            if (r == 1 && nglob > 0) {
-              if (merge ? !mbar_wait(&m_full, mcnt & 1, kWaitLimitNs) : !wait_item(il)) {
-                record_timeout(828);
-                ok = false;
-                break;
-              }
-              if (merge) {
-                ++mcnt;
-                mbar_arrive(&empty[(il + 1) % PA_RING]);  // the carry item is merged in
-              }
+            // the global items (the local sums and the carry, each its own
+            // product into the same accumulator) have landed
+            if (r == 1 && nglob > 0 &&
+                (!wait_item(il) || (nglob == 2 && !wait_item(il + 1)))) {
+              record_timeout(828);
+              ok = false;
+              break;
             }
             tc_fence_after();
-            if (nglob > 0) {
-              const uint32_t pb = slot_addr(il);
+            for (int gi = 0; gi < nglob; ++gi) {
+              const uint32_t pb = slot_addr(il + gi);
               const uint32_t ab = baddr + (uint32_t)r * PA_ITEM;
 #pragma unroll
               for (int kk = 0; kk < S_DIM / 16; ++kk) {
@@ -550,7 +511,7 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
                 const uint64_t bd = smem_desc_sw128(pb + kk * 2048, 16384, 1024);
                 mma_bf16_ss(ocol, ad, bd, idesc_o, 1u);
               }
-              if (r == 0) mma_commit(&empty[il % PA_RING]);
+              if (r == 0) mma_commit(&empty[(il + gi) % PA_RING]);  // its last read
             }
             mma_commit(&o_full[r]);
           }
@@ -564,40 +525,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
       mma_commit(&mma_done);
       if (!mbar_wait(&mma_done, 0, kWaitLimitNs)) record_timeout(829);
     }
-  } else if (warp == 2 || warp == 3) {
-    // =========================== merge warps (64 threads): local += carry
-    // in the local-sum item, in place (pair_merge), a third of each tile's;
-    // the relu^2 warps take the rest
-    const int mt = threadIdx.x - 64;
-    int it = 0, mcnt = 0;
-    bool ok = true;
-    for (int j = 0; ok; ++j) {
-      const int qs = j % FU_QUEUE;
-      const bool got = mbar_wait(&uq_full[qs], (j / FU_QUEUE) & 1, kWaitLimitNs);
-      const int u = got ? uq_unit[qs] : -1, unet = got ? uq_net[qs] : 0;
-      const bool more = named_bar_and(4, 64, u >= 0);
-      if (mt == 0 && got) mbar_arrive(&uq_empty[qs]);
-      if (!more) {
-        if (!got && mt == 0) record_timeout(860);
-        break;
-      }
-      const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
-      it += 4;  // the unit's T0 and T1 items
-      for (int x = 0; x < f.net && ok; ++x) {
-        const int il = it + 2, icy = it + 3;
-        it += 2 + (int)f.local + (int)f.carry;
-        if (!(f.local && f.carry)) continue;
-        const bool w = mbar_wait(&mg_go, mcnt & 1, kWaitLimitNs);
-        ++mcnt;
-        if (w) pair_merge(ring, il, icy, mt);  // its third of the tile
-        ok = named_bar_and(4, 64, w);
-        if (!ok) {
-          if (mt == 0) record_timeout(861);
-          break;
-        }
-        if (mt == 0) mbar_arrive(&m_full);
-      }
-    }
   } else if (warp >= 4 && warp < 8) {
     // =========================== relu^2 warps (128 threads): S -> P in TMEM
     const int mt = threadIdx.x - 128;
@@ -605,7 +532,6 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
     const int row = quad * 32 + lane;  // query row within its row tile (TMEM lane)
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     int tcnt = 0;
-    int it = 0, mcnt = 0;  // ring items and merges, as the merge warps count them
     bool ok = true;
     for (int j = 0; ok; ++j) {
       const int qs = j % FU_QUEUE;
@@ -664,25 +590,10 @@ __global__ void __launch_bounds__(PAIR_THREADS, 1)
           if (mt == 0) mbar_arrive(&p_full[ps]);
         }
       }
-      // then, per e tile, two thirds of the merge (the merge warps take the
-      // rest) and columns 64-127 of the output tiles (the epilogue warps take
-      // 0-63)
+      // then columns 64-127 of the unit's output tiles (the epilogue warps
+      // take 0-63)
       const PairUnit f = decode_pair<kState, kCausal>(u, unet, grid);
-      it += 4;  // the unit's T0 and T1 items
       for (int x = 0; x < f.net && ok; ++x, ++tcnt) {
-        const int il = it + 2, icy = it + 3;
-        it += 2 + (int)f.local + (int)f.carry;
-        if (f.local && f.carry) {
-          const bool w = mbar_wait(&mg_go, mcnt & 1, kWaitLimitNs);
-          ++mcnt;
-          if (w) pair_merge(ring, il, icy, 64 + mt);
-          ok = named_bar_and(2, 128, w);
-          if (!ok) {
-            if (mt == 0) record_timeout(862);
-            break;
-          }
-          if (mt == 0) mbar_arrive(&m_full);
-        }
         for (int rr = 0; rr < 2 && ok; ++rr) {
           const int r = 1 - rr;
           const size_t roff =
